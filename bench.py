@@ -1,0 +1,510 @@
+"""Benchmark: one decode layer step (append + paged decode attention) per step.
+
+Default workload: Llama-3-8B heads (32 query / 8 kv heads x 128), bf16, 256
+sequences with lognormal context lengths (median 1024, sigma 1, cap 8192).
+One step appends one new token per sequence at its explicit position and runs
+decode attention over context + 1 tokens.  The per-layer K/V (about 1.7 GB)
+is far larger than the 129 MB L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs its own
+replica on its own GPU (the path shards by sequence; no collective) and the
+value is the work of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attention achieved HBM GB/s (% of GB300 peak) and decode tokens/s"
+LAYERS = {"llama3-8b_batch256": 32, "llama3-8b_long_context": 32, "llama3-8b_shared_prefix": 32,
+          "qwen2.5-0.5b_gqa": 24, "gpt2_tiny_f32": 12}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing
+# ---------------------------------------------------------------------------
+def dist_init(n_gpus: int):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        if dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[torch.cuda.current_device()])
+        else:
+            dist.barrier()
+
+
+def all_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def all_sum(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes
+# ---------------------------------------------------------------------------
+def decode_bytes(wl) -> int:
+    """Bytes one decode launch must move: each K/V element of every context once,
+    q and out, the block-table entries and lengths, and the split-KV partials
+    (written and read back) of sequences longer than one partition."""
+    e = 2 if wl.dtype == "bf16" else 4
+    L = wl.context_lens.astype(np.int64) + 1
+    kv = int((L * 2 * wl.num_kv_heads * wl.head_dim * e).sum())
+    qo = 2 * wl.num_seqs * wl.num_q_heads * wl.head_dim * e
+    table = int((4 * ((L + 15) // 16)).sum()) + 4 * wl.num_seqs
+    parts = (L + 511) // 512
+    multi = parts[parts > 1]
+    partial = int((multi * wl.num_q_heads * (wl.head_dim + 2) * 4 * 2).sum())
+    return kv + qo + table + partial
+
+
+def append_bytes(wl) -> int:
+    """New rows read and written into the pools, plus start / cu / table reads."""
+    e = 2 if wl.dtype == "bf16" else 4
+    rows = wl.num_seqs * wl.num_kv_heads * wl.head_dim * e * 2   # K and V
+    return 2 * rows + 12 * wl.num_seqs
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            props = torch.cuda.get_device_properties(device_index)
+            uuid = str(props.uuid)
+            self.gpu = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            self.gpu = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "200"]
+            if self.gpu:
+                cmd += ["-i", self.gpu]
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# the CUDA arm
+# ---------------------------------------------------------------------------
+def load_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return None
+
+
+def decode_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("pa_decode.cu", "pa_ptx.cuh", "pa_internal.h"):
+        h.update(open(os.path.join(ROOT, "paged_kv_cache_207_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """dram bytes per decode launch from a committed ncu summary, if it was taken on
+    the current decode source; else None."""
+    path = os.path.join(ROOT, "profiles", f"decode_{workload}_dram.txt")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    for line in open(path):
+        if "=" in line and not line.startswith("#"):
+            k, v = line.split("=", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("decode_source_sha256_16") != decode_source_hash():
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def run_ours(args, rank, world, local):
+    import paged_kv_cache_207_gb300 as pk
+    from paged_kv_cache_207_gb300 import build, workloads as W
+
+    torch.cuda.set_device(local)
+    build.build()
+    pk.lib()
+    wl = W.WORKLOADS[args.workload](device="cuda", **({"seed": 210 + 1000 * rank}
+                                                      if args.workload == "llama3-8b_batch256" else {}))
+    tdt = wl.torch_dtype()
+    S, Hq, Hkv, D = wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
+    shape = pk.pool_shape(wl.num_blocks, Hkv, D, tdt)
+    kp = torch.zeros(shape, dtype=tdt, device="cuda")
+    vp = torch.zeros(shape, dtype=tdt, device="cuda")
+    tables = torch.from_numpy(wl.block_tables).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    # fill the context (untimed set-up), one append call
+    seqs = [f[0] for f in wl.fill]
+    ns = [f[3] for f in wl.fill]
+    first, end = wl.fill[0][2], wl.fill[-1][2] + wl.fill[-1][3]
+    pk.append_kv(kp, vp, wl.k_rows[first:end].contiguous(), wl.v_rows[first:end].contiguous(),
+                 tables[torch.tensor(seqs, device="cuda")].contiguous(),
+                 torch.tensor([f[1] for f in wl.fill], dtype=torch.int32, device="cuda"),
+                 torch.tensor(np.concatenate([[0], np.cumsum(ns)]), dtype=torch.int32, device="cuda"),
+                 err_flag=err)
+    rows = torch.from_numpy(wl.new_rows).cuda()
+    k_new = wl.k_rows[rows].contiguous()
+    v_new = wl.v_rows[rows].contiguous()
+    start = torch.from_numpy(wl.context_lens.astype(np.int32)).cuda()
+    cu = torch.arange(S + 1, dtype=torch.int32, device="cuda")
+    lens = start + 1
+    q = wl.q.contiguous()
+    out = torch.empty_like(q)
+    ws = torch.empty(max(pk.decode_workspace_size(S, Hq, D, wl.max_blocks), 16), dtype=torch.uint8,
+                     device="cuda")
+    hint = int(lens.max().item())
+    del wl.k_rows, wl.v_rows
+    torch.cuda.empty_cache()
+    stream = torch.cuda.current_stream()
+
+    def step(ev_d0=None, ev_d1=None):
+        pk.append_kv(kp, vp, k_new, v_new, tables, start, cu, err_flag=err, stream=stream)
+        if ev_d0 is not None:
+            ev_d0.record(stream)
+        pk.decode_attention(out, q, kp, vp, tables, lens, wl.scale, workspace=ws,
+                            max_context_len_hint=hint, err_flag=err, stream=stream)
+        if ev_d1 is not None:
+            ev_d1.record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error flag {int(err.item())} during warm-up")
+
+    K = args.steps
+    d0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    d1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(K):
+        step(d0[i], d1[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms_total = t0.elapsed_time(t1)
+    dec_ms = sum(a.elapsed_time(b) for a, b in zip(d0, d1)) / K
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error flag {int(err.item())} during the timed steps")
+
+    ms_total_max = all_max(ms_total, world)
+    step_bytes = decode_bytes(wl) + append_bytes(wl)
+    total_bytes = all_sum(float(step_bytes) * K, world)
+    value = total_bytes / (ms_total_max / 1e3) / 1e9
+    ms_per_step = ms_total_max / K
+    layers = LAYERS.get(args.workload, 32)
+    tokens_per_s = all_sum(float(S), world) / (layers * ms_per_step / 1e3)
+
+    # end to end: host buffers in pinned memory, copies inside the timed region
+    h_q = q.cpu().pin_memory()
+    h_k, h_v = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
+    h_start, h_cu, h_lens = start.cpu().pin_memory(), cu.cpu().pin_memory(), lens.cpu().pin_memory()
+    h_tab = tables.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
+    d_start, d_cu, d_lens, d_tab = (torch.empty_like(start), torch.empty_like(cu),
+                                    torch.empty_like(lens), torch.empty_like(tables))
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_start, h_cu, h_lens, h_tab))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        for dst, src in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_start, h_start), (d_cu, h_cu),
+                         (d_lens, h_lens), (d_tab, h_tab)):
+            dst.copy_(src, non_blocking=True)
+        pk.append_kv(kp, vp, d_k, d_v, d_tab, d_start, d_cu, err_flag=err, stream=stream)
+        pk.decode_attention(out, d_q, kp, vp, d_tab, d_lens, wl.scale, workspace=ws,
+                            max_context_len_hint=hint, err_flag=err, stream=stream)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = all_max(e0.elapsed_time(e1), world)
+    e2e_value = total_bytes / (e2e_ms / 1e3) / 1e9
+    # the copied-back result equals the device result
+    assert torch.equal(h_out, out.cpu())
+
+    peaks = load_peaks()
+    if peaks and peaks.get("hbm_gbs"):
+        peak, peak_src = float(peaks["hbm_gbs"]), "measured"
+    else:
+        peak, peak_src = 6800.0, "fallback"
+    dbytes = decode_bytes(wl)
+    achieved = dbytes / (dec_ms / 1e3) / 1e9
+    launches_per_step = 1 + 1 + (1 if int(math.ceil(hint / 512)) > 1 else 0)
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic",
+        "config": {"workload": args.workload, "num_seqs_per_gpu": S, "num_q_heads": Hq,
+                   "num_kv_heads": Hkv, "head_dim": D, "block_size": 16,
+                   "context_tokens_after_append": int((wl.context_lens + 1).sum()),
+                   "max_context": int(hint), "step": "pa_append_kv (1 token/seq) + pa_decode_attention",
+                   "layers_for_tokens_per_s": layers,
+                   "l2": "inputs larger than L2 (K/V pools %.2f GB per GPU vs 129 MB L2), no flush"
+                         % (2 * kp.numel() * kp.element_size() / 1e9),
+                   "parallelism": f"replicas x{world} (sequences sharded by rank, no collective)"},
+        "pct_of_peak_hbm": round(100.0 * value / peak, 2),
+        "tokens_per_s": round(tokens_per_s, 1),
+        "roofline": {"kernel": "pa_decode_attention (main kernel + partition merge)",
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(args.workload),
+                     "algorithmic_bytes_per_launch": dbytes, "avg_launch_ms": round(dec_ms, 5)},
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms / K, 5),
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+    }
+    return result, wl
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (baseline, and the `--impl reference` arm)
+# ---------------------------------------------------------------------------
+class OracleSample:
+    """The oracle's own pools holding the context of the first n sequences."""
+
+    def __init__(self, wl, n):
+        from oracle import oracle as orc
+        self.orc = orc
+        self.wl = wl
+        self.n = n
+        od = orc.BF16 if wl.dtype == "bf16" else orc.F32
+        self.od = od
+        et = np.uint16 if od == orc.BF16 else np.float32
+        shape = orc.pool_shape(wl.num_blocks, wl.num_kv_heads, wl.head_dim, od)
+        self.kp = np.zeros(shape, et)
+        self.vp = np.zeros(shape, et)
+        kr, vr = wl.k_rows_cpu, wl.v_rows_cpu
+        for (s, start, first, cnt) in wl.fill:
+            if s < n:
+                orc.append_kv(self.kp, self.vp, kr[first:first + cnt], vr[first:first + cnt],
+                              wl.block_tables[s:s + 1], np.array([start], np.int32),
+                              np.array([0, cnt], np.int32), num_kv_heads=wl.num_kv_heads,
+                              head_dim=wl.head_dim, num_blocks=wl.num_blocks, dtype=od)
+        rows = torch.from_numpy(wl.new_rows[:n])
+        self.k_new, self.v_new = kr[rows], vr[rows]
+        self.q = wl.q_cpu[:n]
+        self.pairs = [(s, h) for s in range(n) for h in range(wl.num_q_heads)]
+        L = wl.context_lens[:n].astype(np.int64) + 1
+        e = 2 if wl.dtype == "bf16" else 4
+        self.bytes = int((L * 2 * wl.num_kv_heads * wl.head_dim * e).sum()) + \
+            2 * n * wl.num_q_heads * wl.head_dim * e + int((4 * ((L + 15) // 16)).sum()) + \
+            n * wl.num_kv_heads * wl.head_dim * e * 4
+
+    def step(self):
+        wl, orc, n = self.wl, self.orc, self.n
+        orc.append_kv(self.kp, self.vp, self.k_new, self.v_new, wl.block_tables[:n],
+                      wl.context_lens[:n].astype(np.int32), np.arange(n + 1, dtype=np.int32),
+                      num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim, num_blocks=wl.num_blocks,
+                      dtype=self.od)
+        return orc.decode_pairs(self.pairs, self.q, self.kp, self.vp, wl.block_tables,
+                                (wl.context_lens + 1).astype(np.int32), num_q_heads=wl.num_q_heads,
+                                num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim,
+                                num_blocks=wl.num_blocks, scale=wl.scale, dtype=self.od)
+
+
+def cpu_workload(name):
+    """The same workload drawn on the CPU generator only for its shape; the oracle's
+    numbers come from the same generator call on the GPU when one exists."""
+    from paged_kv_cache_207_gb300 import workloads as W
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    wl = W.WORKLOADS[name](device=dev)
+    wl.k_rows_cpu = wl.k_rows.cpu()
+    wl.v_rows_cpu = wl.v_rows.cpu()
+    wl.q_cpu = wl.q.cpu()
+    return wl
+
+
+def pick_sample(wl, target_s: float):
+    """Grow the number of sequences until one oracle step takes about target_s seconds."""
+    n = 1
+    while True:
+        smp = OracleSample(wl, n)
+        t = time.perf_counter()
+        smp.step()
+        dt = time.perf_counter() - t
+        if dt >= target_s or n >= wl.num_seqs:
+            return smp, dt
+        n = min(wl.num_seqs, max(n + 1, int(n * min(8.0, target_s / max(dt, 1e-3)))))
+
+
+def cpu_baseline(wl, target_s=12.0):
+    smp, _ = pick_sample(wl, target_s / 3)
+    t = time.perf_counter()
+    reps = 0
+    while time.perf_counter() - t < target_s or reps == 0:
+        smp.step()
+        reps += 1
+    dt = (time.perf_counter() - t) / reps
+    return {"value": round(smp.bytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"append + decode of the first {smp.n} of {wl.num_seqs} sequences "
+                      f"(all {wl.num_q_heads} query heads), {reps} repetitions, plain C oracle, "
+                      f"one thread, {dt:.2f} s per repetition"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    wl = cpu_workload(args.workload)
+    # size one step so that warm-up plus timed steps take about two minutes
+    smp, dt = pick_sample(wl, max(0.005, min(1.0, 120.0 / (args.steps + args.warmup))))
+    for _ in range(args.warmup):
+        smp.step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        smp.step()
+    el = time.perf_counter() - t
+    value = smp.bytes * args.steps / el / 1e9
+    S = smp.n
+    layers = LAYERS.get(args.workload, 32)
+    ms = el * 1e3 / args.steps
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic",
+        "config": {"workload": args.workload, "num_seqs_per_step": S,
+                   "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads,
+                   "head_dim": wl.head_dim, "block_size": 16,
+                   "step": "oracle append + decode of a bounded sample of the workload"},
+        "tokens_per_s": round(S / (layers * ms / 1e3), 3),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"first {S} of {wl.num_seqs} sequences per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama3-8b_batch256")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local = dist_init(args.gpus)
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        return
+    res, wl = run_ours(args, rank, world, local)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            wl_cpu = cpu_workload(args.workload)
+            res["cpu_baseline"] = cpu_baseline(wl_cpu)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

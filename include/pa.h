@@ -1,0 +1,212 @@
+/*
+ * pa.h -- C ABI of the paged KV-cache decode-attention library (sm_103a).
+ *
+ * The operations follow the engines described on two pages:
+ *   spindle ("A faster engine for running language models"):
+ *     - section "Paging": K/V live in a pool of fixed-size blocks (block size
+ *       16) shared by every sequence; each sequence reaches its blocks through
+ *       a block table; reference counts give copy-on-write forks.
+ *     - section "Two bugs worth recording": append takes an explicit start
+ *       position and the attention read takes an explicit length; the runner,
+ *       not the cache, advances lengths once per step.
+ *     - section "Why write the forward pass": batched decoding must equal
+ *       decoding each sequence alone (no attention across sequences).
+ *   Slipstream, section "The thesis" and Fig. 01: decode is bandwidth-bound,
+ *     so the kernels are built to stream K/V at HBM speed.
+ *   mlsystems topic list, the Flash-Decoding entry: decode (q_len = 1)
+ *     attention split over chunks of the KV sequence, then reduced.
+ *
+ * Conventions for every call
+ *   - All array arguments are DEVICE pointers unless the name says "host";
+ *     the caller owns and allocates every buffer.  Nothing is allocated,
+ *     freed, synchronised or kept between calls by the GPU entry points.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls only enqueue work; they return before it runs.
+ *   - Device arrays must be 16-byte aligned.
+ *   - Host-checkable faults return a status and launch nothing.  Faults that
+ *     depend on device data (a table entry outside [0, num_blocks), a
+ *     position beyond the table) are OR-ed as PA_DEV_ERR_* bits into
+ *     *dev_err_flag (an int32 in device memory, may be NULL) and the
+ *     offending element is skipped; nothing traps.
+ *
+ * Pool layout (the pages fix none; this library's choice):
+ *   k_pool, v_pool: [num_blocks][num_kv_heads][head_dim / X][16][X]
+ *   with X = 16 / sizeof(element) (8 for bf16, 4 for fp32).  Element
+ *   (block b, kv head h, slot t, dim d) is at
+ *     ((((b * Hkv + h) * (D / X) + d / X) * 16 + t) * X + d % X).
+ *   Each (block, kv head) tile is one contiguous 16 * D * sizeof(element)
+ *   byte chunk, and the 16-byte pieces of the 16 slots for the same dims sit
+ *   side by side, so a tile moves as one bulk copy and is read back from
+ *   shared memory without bank conflicts.
+ *   Logical position p of sequence s is slot p % 16 of block
+ *   block_tables[s][p / 16].
+ */
+#ifndef PAGED_KV_PA_H
+#define PAGED_KV_PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_BLOCK_SIZE 16
+#define PA_ABI_VERSION 1
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misalignment, small workspace */
+    PA_ERR_UNSUPPORTED = 2,   /* head_dim not 64/128, more than 8 query heads per kv head */
+    PA_ERR_CUDA = 3,          /* a CUDA launch or runtime call failed */
+    PA_ERR_OUT_OF_BLOCKS = 4  /* block manager: not enough free blocks (nothing changed) */
+} pa_status;
+
+typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Bits OR-ed into *dev_err_flag by the kernels. */
+#define PA_DEV_ERR_BAD_BLOCK 1   /* a table entry read for a live position is outside [0, num_blocks) */
+#define PA_DEV_ERR_BAD_POS 2     /* a position < 0 or >= max_blocks_per_seq * 16 */
+#define PA_DEV_ERR_HINT 4        /* a context is longer than max_context_len_hint */
+#define PA_DEV_ERR_BAD_CU 8      /* cu_new_tokens is not a prefix sum ending at total_new_tokens */
+#define PA_DEV_ERR_TIMEOUT 16    /* a bulk-copy wait gave up after 200 ms; while this bit
+                                    is set in the flag, decode CTAs return at once so a
+                                    broken pipeline cannot hold the GPU; clear it to resume */
+#define PA_DEV_ERR_BAD_PAIR 32   /* a copy pair names a block outside [0, num_blocks) */
+
+/* Tokens per split-KV partition of pa_decode_attention (a multiple of 16). */
+#define PA_PARTITION_TOKENS 512
+
+const char* pa_status_string(pa_status s);
+int32_t pa_abi_version(void);
+
+/*
+ * pa_append_kv -- write new K/V tokens at explicit positions (spindle,
+ * "Two bugs worth recording": append takes an explicit start position).
+ *
+ *   k_new, v_new     [total_new_tokens][num_kv_heads][head_dim], plain row-major,
+ *                    rows of sequence s are cu_new_tokens[s] .. cu_new_tokens[s+1]-1
+ *   block_tables     int32 [num_seqs][max_blocks_per_seq]
+ *   start_pos        int32 [num_seqs]: row cu_new_tokens[s] + i goes to position
+ *                    start_pos[s] + i of sequence s
+ *   cu_new_tokens    int32 [num_seqs + 1], cu_new_tokens[0] = 0,
+ *                    cu_new_tokens[num_seqs] = total_new_tokens (host value)
+ * The pools are written bit for bit.  Positions whose table entry is out of
+ * range are skipped and flagged.  The caller guarantees that no two rows
+ * target the same slot and that no target block is shared (refcount > 1);
+ * the block manager below gives those guarantees.  Nothing is read back.
+ */
+pa_status pa_append_kv(void* k_pool, void* v_pool, const void* k_new, const void* v_new,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* start_pos, const int32_t* cu_new_tokens, int32_t num_seqs,
+                       int32_t total_new_tokens, int32_t num_blocks, int32_t num_kv_heads,
+                       int32_t head_dim, pa_dtype dtype, int32_t* dev_err_flag, void* stream);
+
+/*
+ * pa_copy_block -- materialise copy-on-write forks (spindle, "Paging":
+ * reference counts give copy-on-write forking).
+ *
+ *   src_dst_pairs    int32 [num_pairs][2] (device): every byte of block src is
+ *                    copied to block dst in both pools, all kv heads and slots.
+ * Pairs naming a block outside [0, num_blocks) are skipped and flagged; a pair
+ * with src == dst is a no-op.  Destinations must be distinct and no
+ * destination may be another pair's source.
+ */
+pa_status pa_copy_block(void* k_pool, void* v_pool, const int32_t* src_dst_pairs,
+                        int32_t num_pairs, int32_t num_blocks, int32_t num_kv_heads,
+                        int32_t head_dim, pa_dtype dtype, int32_t* dev_err_flag, void* stream);
+
+/*
+ * pa_decode_workspace_size -- bytes of device workspace pa_decode_attention
+ * needs for these sizes (0 when no sequence can span two partitions).  The
+ * workspace holds per-partition partial results of the split-KV reduce.
+ */
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                int32_t max_blocks_per_seq);
+
+/*
+ * pa_decode_attention -- single-token (q_len = 1) attention over the paged
+ * cache (spindle, "Paging" and "Why write the forward pass"; the split over
+ * KV partitions follows the Flash-Decoding entry of the mlsystems list).
+ *
+ *   out, q           [num_seqs][num_q_heads][head_dim], element type `dtype`
+ *   context_lens     int32 [num_seqs]: sequence s attends over positions
+ *                    0 .. context_lens[s]-1 (an explicit length; never changed)
+ *   block_tables     int32 [num_seqs][max_blocks_per_seq]
+ * For each sequence s and query head h, with kv head g = h / (Hq / Hkv):
+ *   out[s][h] = sum_t softmax_t(scale * <q[s][h], K[s][t][g]>) V[s][t][g]
+ * computed in fp32 (bf16 inputs are exact in fp32) and rounded once to the
+ * output type.  Contexts are cut into fixed PA_PARTITION_TOKENS-token
+ * partitions whose partial results are merged with their log-sum-exp
+ * weights; the partition of a token depends only on its position, so a
+ * sequence's result does not depend on the rest of the batch.  A zero-length
+ * context gives zeros.
+ *   max_context_len_hint  host bound on every context_lens[s] used to size
+ *                    the grid; <= 0 means max_blocks_per_seq * 16.  A longer
+ *                    context sets PA_DEV_ERR_HINT and its output is incomplete.
+ *   workspace        device scratch of at least pa_decode_workspace_size()
+ *                    bytes (may be NULL when that size is 0); its contents on
+ *                    entry do not matter.
+ * head_dim must be 64 or 128 and num_q_heads / num_kv_heads at most 8.
+ */
+pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
+                              const int32_t* block_tables, const int32_t* context_lens,
+                              int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t max_blocks_per_seq,
+                              int32_t max_context_len_hint, int32_t num_blocks, float scale,
+                              pa_dtype dtype, void* workspace, size_t workspace_bytes,
+                              int32_t* dev_err_flag, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Host block manager (no GPU; spindle, "Paging").
+ *
+ * Owns the refcounts of a pool of num_blocks blocks and one block table per
+ * live sequence.  Readings where the page is silent:
+ *   - writing into a block whose refcount is above one first copies it into a
+ *     newly allocated block (one (src, dst) pair for pa_copy_block), drops one
+ *     reference to the old block and points the writer's table at the copy; a
+ *     block held once is written in place;
+ *   - refcounts count live sequences only;
+ *   - free blocks are handed out lowest id first.
+ * Handles are not thread-safe; use one per thread or lock around calls.
+ * ------------------------------------------------------------------------- */
+typedef struct pa_block_manager pa_block_manager;
+
+typedef struct {
+    int64_t physical_blocks;   /* blocks with refcount > 0 */
+    int64_t free_blocks;
+    int64_t logical_tokens;    /* sum of live sequence lengths */
+    int64_t num_seqs;
+} pa_bm_stats_t;
+
+pa_status pa_bm_create(int32_t num_blocks, pa_block_manager** out);
+void pa_bm_destroy(pa_block_manager* bm);
+/* A new empty sequence; its id is written to *seq_out. */
+pa_status pa_bm_add_seq(pa_block_manager* bm, int32_t* seq_out);
+/* A child sharing every block of `parent` (each refcount + 1), same length. */
+pa_status pa_bm_fork(pa_block_manager* bm, int32_t parent, int32_t* child_out);
+/* Drop the sequence and one reference to each of its blocks. */
+pa_status pa_bm_free_seq(pa_block_manager* bm, int32_t seq);
+/* Blocks an append of num_tokens tokens at start_pos would take (host). */
+pa_status pa_bm_blocks_needed(const pa_block_manager* bm, int32_t seq, int32_t start_pos,
+                              int32_t num_tokens, int32_t* blocks_out);
+/* Make positions start_pos .. start_pos+num_tokens-1 writable: allocate missing
+ * blocks and copy shared ones.  Host array pairs_out receives the (src, dst)
+ * copy pairs (at most max_pairs).  start_pos may not leave a hole past the
+ * table's end.  On PA_ERR_OUT_OF_BLOCKS or a too-small max_pairs nothing
+ * changes.  The sequence length becomes max(length, start_pos + num_tokens). */
+pa_status pa_bm_prepare_append(pa_block_manager* bm, int32_t seq, int32_t start_pos,
+                               int32_t num_tokens, int32_t* pairs_out, int32_t max_pairs,
+                               int32_t* num_pairs_out);
+/* Host array row_out (max_blocks entries) receives the block table, -1 padded. */
+pa_status pa_bm_block_table(const pa_block_manager* bm, int32_t seq, int32_t* row_out,
+                            int32_t max_blocks, int32_t* num_blocks_out);
+pa_status pa_bm_seq_len(const pa_block_manager* bm, int32_t seq, int32_t* len_out);
+pa_status pa_bm_refcount(const pa_block_manager* bm, int32_t block, int32_t* refcount_out);
+pa_status pa_bm_stats(const pa_block_manager* bm, pa_bm_stats_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_KV_PA_H */

@@ -1,0 +1,12 @@
+"""Paged KV-cache single-token decode attention for GB300 (sm_103a).
+
+The kernels live in ``libpaged_kv.so`` behind the C ABI of ``include/pa.h``;
+this package is the thin Python binding (``_native``) plus the seeded workload
+generators (``workloads``).
+"""
+from ._native import (  # noqa: F401
+    BLOCK_SIZE, PARTITION_TOKENS, BlockManager, PagedKVError, append_kv, copy_block,
+    decode_attention, decode_workspace_size, lib, pool_shape,
+    DEV_ERR_BAD_BLOCK, DEV_ERR_BAD_POS, DEV_ERR_HINT, DEV_ERR_BAD_CU, DEV_ERR_TIMEOUT,
+    DEV_ERR_BAD_PAIR,
+)

@@ -1,0 +1,242 @@
+"""ctypes binding of ``libpaged_kv.so`` (the C ABI declared in ``include/pa.h``).
+
+Argument marshalling only: tensors become device pointers and sizes, the current
+torch stream becomes the ``void* stream`` argument, and a non-OK status becomes
+an exception.  Every step of the computation runs in the library's kernels;
+there is no fallback, and the import fails loudly if the library was not built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpaged_kv.so")
+
+PA_OK = 0
+PA_F32, PA_BF16 = 0, 1
+BLOCK_SIZE = 16
+PARTITION_TOKENS = 512
+
+DEV_ERR_BAD_BLOCK = 1
+DEV_ERR_BAD_POS = 2
+DEV_ERR_HINT = 4
+DEV_ERR_BAD_CU = 8
+DEV_ERR_TIMEOUT = 16
+DEV_ERR_BAD_PAIR = 32
+
+EXPORTED = [
+    "pa_status_string", "pa_abi_version", "pa_append_kv", "pa_copy_block",
+    "pa_decode_workspace_size", "pa_decode_attention", "pa_bm_create", "pa_bm_destroy",
+    "pa_bm_add_seq", "pa_bm_fork", "pa_bm_free_seq", "pa_bm_blocks_needed",
+    "pa_bm_prepare_append", "pa_bm_block_table", "pa_bm_seq_len", "pa_bm_refcount", "pa_bm_stats",
+]
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed: {msg} (status {status})")
+        self.status = status
+
+
+class BmStats(ctypes.Structure):
+    _fields_ = [("physical_blocks", ctypes.c_int64), ("free_blocks", ctypes.c_int64),
+                ("logical_tokens", ctypes.c_int64), ("num_seqs", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"{_LIB_PATH} is missing: build it with "
+                          "`python -m paged_kv_cache_207_gb300.build` (nvcc, sm_103a)")
+    L = ctypes.CDLL(_LIB_PATH)
+    p, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    ip = ctypes.POINTER(ctypes.c_int32)
+    L.pa_status_string.argtypes = [ctypes.c_int]
+    L.pa_status_string.restype = ctypes.c_char_p
+    L.pa_abi_version.restype = i32
+    L.pa_append_kv.argtypes = [p, p, p, p, p, i32, p, p, i32, i32, i32, i32, i32, ctypes.c_int, p, p]
+    L.pa_append_kv.restype = ctypes.c_int
+    L.pa_copy_block.argtypes = [p, p, p, i32, i32, i32, i32, ctypes.c_int, p, p]
+    L.pa_copy_block.restype = ctypes.c_int
+    L.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32]
+    L.pa_decode_workspace_size.restype = sz
+    L.pa_decode_attention.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32,
+                                      ctypes.c_float, ctypes.c_int, p, sz, p, p]
+    L.pa_decode_attention.restype = ctypes.c_int
+    L.pa_bm_create.argtypes = [i32, ctypes.POINTER(p)]
+    L.pa_bm_destroy.argtypes = [p]
+    L.pa_bm_destroy.restype = None
+    L.pa_bm_add_seq.argtypes = [p, ip]
+    L.pa_bm_fork.argtypes = [p, i32, ip]
+    L.pa_bm_free_seq.argtypes = [p, i32]
+    L.pa_bm_blocks_needed.argtypes = [p, i32, i32, i32, ip]
+    L.pa_bm_prepare_append.argtypes = [p, i32, i32, i32, ip, i32, ip]
+    L.pa_bm_block_table.argtypes = [p, i32, ip, i32, ip]
+    L.pa_bm_seq_len.argtypes = [p, i32, ip]
+    L.pa_bm_refcount.argtypes = [p, i32, ip]
+    L.pa_bm_stats.argtypes = [p, ctypes.POINTER(BmStats)]
+    for n in ("pa_bm_create", "pa_bm_add_seq", "pa_bm_fork", "pa_bm_free_seq",
+              "pa_bm_blocks_needed", "pa_bm_prepare_append", "pa_bm_block_table",
+              "pa_bm_seq_len", "pa_bm_refcount", "pa_bm_stats"):
+        getattr(L, n).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def check(fn: str, status: int) -> None:
+    if status != PA_OK:
+        raise PagedKVError(fn, status, lib().pa_status_string(status).decode())
+
+
+def _ptr(t) -> int:
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch tensor")
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor (device pointer)")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _i32(t, name):
+    if t.dtype != torch.int32:
+        raise TypeError(f"{name} must be int32")
+    return _ptr(t)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return PA_BF16
+    if t.dtype == torch.float32:
+        return PA_F32
+    raise TypeError(f"unsupported element type {t.dtype}")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def pool_shape(num_blocks: int, num_kv_heads: int, head_dim: int, dtype: torch.dtype):
+    """Shape of one K or V pool in the library's layout."""
+    x = 16 // torch.empty((), dtype=dtype).element_size()
+    return (num_blocks, num_kv_heads, head_dim // x, BLOCK_SIZE, x)
+
+
+def _pool_dims(k_pool: torch.Tensor):
+    if k_pool.dim() != 5 or k_pool.shape[3] != BLOCK_SIZE:
+        raise ValueError("pools must have shape [num_blocks][Hkv][D/X][16][X]")
+    return k_pool.shape[0], k_pool.shape[1], k_pool.shape[2] * k_pool.shape[4]
+
+
+def append_kv(k_pool, v_pool, k_new, v_new, block_tables, start_pos, cu_new_tokens,
+              err_flag=None, stream=None) -> None:
+    """Write rows of k_new / v_new ([tokens][Hkv][D]) at explicit positions."""
+    nb, hkv, d = _pool_dims(k_pool)
+    check("pa_append_kv", lib().pa_append_kv(
+        _ptr(k_pool), _ptr(v_pool), _ptr(k_new), _ptr(v_new), _i32(block_tables, "block_tables"),
+        block_tables.shape[1], _i32(start_pos, "start_pos"), _i32(cu_new_tokens, "cu_new_tokens"),
+        start_pos.shape[0], k_new.shape[0], nb, hkv, d, _dtype_code(k_pool),
+        None if err_flag is None else _i32(err_flag, "err_flag"), _stream(stream)))
+
+
+def copy_block(k_pool, v_pool, pairs, err_flag=None, stream=None) -> None:
+    """Copy whole blocks src -> dst (pairs: int32 [n][2] on the device)."""
+    nb, hkv, d = _pool_dims(k_pool)
+    check("pa_copy_block", lib().pa_copy_block(
+        _ptr(k_pool), _ptr(v_pool), _i32(pairs, "pairs"), pairs.shape[0], nb, hkv, d,
+        _dtype_code(k_pool), None if err_flag is None else _i32(err_flag, "err_flag"),
+        _stream(stream)))
+
+
+def decode_workspace_size(num_seqs: int, num_q_heads: int, head_dim: int,
+                          max_blocks_per_seq: int) -> int:
+    return int(lib().pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_blocks_per_seq))
+
+
+def decode_attention(out, q, k_pool, v_pool, block_tables, context_lens, scale, workspace=None,
+                     max_context_len_hint: int = 0, err_flag=None, stream=None) -> None:
+    """Single-token attention of q ([S][Hq][D]) over the paged cache into out."""
+    nb, hkv, d = _pool_dims(k_pool)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    check("pa_decode_attention", lib().pa_decode_attention(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _i32(block_tables, "block_tables"),
+        _i32(context_lens, "context_lens"), q.shape[0], q.shape[1], hkv, d, block_tables.shape[1],
+        int(max_context_len_hint), nb, float(scale), _dtype_code(q),
+        None if workspace is None else _ptr(workspace), ws_bytes,
+        None if err_flag is None else _i32(err_flag, "err_flag"), _stream(stream)))
+
+
+class BlockManager:
+    """Host block manager (refcounts, block tables, copy-on-write pairs)."""
+
+    def __init__(self, num_blocks: int):
+        self._h = ctypes.c_void_p()
+        check("pa_bm_create", lib().pa_bm_create(num_blocks, ctypes.byref(self._h)))
+        self.num_blocks = num_blocks
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.pa_bm_destroy(h)
+            self._h = None
+
+    def add_seq(self) -> int:
+        out = ctypes.c_int32()
+        check("pa_bm_add_seq", lib().pa_bm_add_seq(self._h, ctypes.byref(out)))
+        return out.value
+
+    def fork(self, parent: int) -> int:
+        out = ctypes.c_int32()
+        check("pa_bm_fork", lib().pa_bm_fork(self._h, parent, ctypes.byref(out)))
+        return out.value
+
+    def free(self, seq: int) -> None:
+        check("pa_bm_free_seq", lib().pa_bm_free_seq(self._h, seq))
+
+    def blocks_needed(self, seq: int, start: int, n: int) -> int:
+        out = ctypes.c_int32()
+        check("pa_bm_blocks_needed", lib().pa_bm_blocks_needed(self._h, seq, start, n,
+                                                                 ctypes.byref(out)))
+        return out.value
+
+    def prepare_append(self, seq: int, start: int, n: int) -> list:
+        """Returns the copy-on-write pairs [(src, dst), ...]; raises on out-of-blocks."""
+        cap = n // BLOCK_SIZE + 2
+        buf = (ctypes.c_int32 * (2 * cap))()
+        npairs = ctypes.c_int32()
+        check("pa_bm_prepare_append", lib().pa_bm_prepare_append(
+            self._h, seq, start, n, buf, cap, ctypes.byref(npairs)))
+        return [(buf[2 * i], buf[2 * i + 1]) for i in range(npairs.value)]
+
+    def block_table(self, seq: int, max_blocks: int) -> list:
+        buf = (ctypes.c_int32 * max(max_blocks, 1))()
+        check("pa_bm_block_table", lib().pa_bm_block_table(self._h, seq, buf, max_blocks, None))
+        return list(buf[:max_blocks])
+
+    def seq_len(self, seq: int) -> int:
+        out = ctypes.c_int32()
+        check("pa_bm_seq_len", lib().pa_bm_seq_len(self._h, seq, ctypes.byref(out)))
+        return out.value
+
+    def refcount(self, block: int) -> int:
+        out = ctypes.c_int32()
+        check("pa_bm_refcount", lib().pa_bm_refcount(self._h, block, ctypes.byref(out)))
+        return out.value
+
+    def stats(self) -> dict:
+        st = BmStats()
+        check("pa_bm_stats", lib().pa_bm_stats(self._h, ctypes.byref(st)))
+        return {"physical_blocks": st.physical_blocks, "free_blocks": st.free_blocks,
+                "logical_tokens": st.logical_tokens, "num_seqs": st.num_seqs,
+                "physical_slots": st.physical_blocks * BLOCK_SIZE}

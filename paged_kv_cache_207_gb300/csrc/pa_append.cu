@@ -1,0 +1,147 @@
+// pa_append.cu -- writing new tokens into the paged pools, and copy-on-write
+// block copies.
+//
+// Append (spindle, "Two bugs worth recording": append takes an explicit start
+// position): row i of sequence s goes to position start_pos[s] + i, i.e. slot
+// (pos % 16) of block block_tables[s][pos / 16].  One thread moves one 16-byte
+// piece of one (row, kv head) of K or V; reads are coalesced along the row,
+// writes land on the slot's 16-byte piece inside each chunk of the tile.
+//
+// Copy (spindle, "Paging": refcounted copy-on-write forking): every byte of
+// block src goes to block dst in both pools; 16-byte vector loads and stores.
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+__device__ __forceinline__ void raise_flag(int32_t* err, int bits) {
+    if (err) atomicOr(err, bits);
+}
+
+struct AParams {
+    char* k_pool;
+    char* v_pool;
+    const char* k_new;
+    const char* v_new;
+    const int32_t* tables;
+    const int32_t* start_pos;
+    const int32_t* cu;
+    int32_t* err;
+    int max_blocks, S, total, num_blocks, Hkv, chunks;   // chunks = 16-byte pieces per row and head
+    long long items;                                      // total * Hkv * chunks
+};
+
+__global__ void __launch_bounds__(256) append_kernel(const AParams p) {
+    const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (item == 0) {
+        if (__ldg(p.cu) != 0 || __ldg(p.cu + p.S) != p.total) raise_flag(p.err, PA_DEV_ERR_BAD_CU);
+    }
+    if (item >= p.items) return;
+    const int ch = (int)(item % p.chunks);
+    const long long rh = item / p.chunks;
+    const int h = (int)(rh % p.Hkv);
+    const int row = (int)(rh / p.Hkv);
+
+    // sequence owning this row: largest s with cu[s] <= row
+    int lo = 0, hi = p.S - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(p.cu + mid) <= row) lo = mid;
+        else hi = mid - 1;
+    }
+    const int s = lo;
+    const int first = __ldg(p.cu + s);
+    if (row < first || row >= __ldg(p.cu + s + 1)) {
+        raise_flag(p.err, PA_DEV_ERR_BAD_CU);
+        return;
+    }
+    const long long pos = (long long)__ldg(p.start_pos + s) + (row - first);
+    if (pos < 0 || pos >= (long long)p.max_blocks * kBlockTokens) {
+        raise_flag(p.err, PA_DEV_ERR_BAD_POS);
+        return;
+    }
+    const int32_t blk = __ldg(p.tables + (size_t)s * p.max_blocks + (int)(pos / kBlockTokens));
+    if (blk < 0 || blk >= p.num_blocks) {
+        raise_flag(p.err, PA_DEV_ERR_BAD_BLOCK);
+        return;
+    }
+    const int slot = (int)(pos % kBlockTokens);
+    // pool byte offset: tile (blk, h), chunk ch, slot  -> 16 bytes
+    const size_t dst = ((((size_t)blk * p.Hkv + h) * p.chunks + ch) * kBlockTokens + slot) * 16;
+    const size_t src = (((size_t)row * p.Hkv + h) * p.chunks + ch) * 16;
+    const uint4 kv = __ldg(reinterpret_cast<const uint4*>(p.k_new + src));
+    const uint4 vv = __ldg(reinterpret_cast<const uint4*>(p.v_new + src));
+    *reinterpret_cast<uint4*>(p.k_pool + dst) = kv;
+    *reinterpret_cast<uint4*>(p.v_pool + dst) = vv;
+}
+
+struct CParams {
+    char* k_pool;
+    char* v_pool;
+    const int32_t* pairs;
+    int32_t* err;
+    int num_blocks;
+    size_t block_bytes;   // bytes of one block in one pool (all kv heads)
+};
+
+// grid = (pair, pool half: 0 = K, 1 = V, slice)
+__global__ void __launch_bounds__(256) copy_kernel(const CParams p) {
+    const int pair = blockIdx.x;
+    const int32_t src = __ldg(p.pairs + 2 * pair), dst = __ldg(p.pairs + 2 * pair + 1);
+    if (src < 0 || src >= p.num_blocks || dst < 0 || dst >= p.num_blocks) {
+        if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) raise_flag(p.err, PA_DEV_ERR_BAD_PAIR);
+        return;
+    }
+    if (src == dst) return;
+    char* pool = blockIdx.y == 0 ? p.k_pool : p.v_pool;
+    const uint4* from = reinterpret_cast<const uint4*>(pool + (size_t)src * p.block_bytes);
+    uint4* to = reinterpret_cast<uint4*>(pool + (size_t)dst * p.block_bytes);
+    const size_t n16 = p.block_bytes / 16;
+    for (size_t i = (size_t)blockIdx.z * blockDim.x + threadIdx.x; i < n16;
+         i += (size_t)gridDim.z * blockDim.x)
+        to[i] = from[i];
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
+    AParams p;
+    p.k_pool = static_cast<char*>(a.k_pool);
+    p.v_pool = static_cast<char*>(a.v_pool);
+    p.k_new = static_cast<const char*>(a.k_new);
+    p.v_new = static_cast<const char*>(a.v_new);
+    p.tables = a.block_tables;
+    p.start_pos = a.start_pos;
+    p.cu = a.cu_new;
+    p.err = a.err;
+    p.max_blocks = a.max_blocks;
+    p.S = a.num_seqs;
+    p.total = a.total_new;
+    p.num_blocks = a.num_blocks;
+    p.Hkv = a.num_kv_heads;
+    p.chunks = a.head_dim * elem_bytes(a.dtype) / 16;
+    p.items = (long long)a.total_new * a.num_kv_heads * p.chunks;
+    if (p.items == 0) return cudaSuccess;
+    const long long blocks = (p.items + 255) / 256;
+    append_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy(const CopyArgs& a, cudaStream_t stream) {
+    if (a.num_pairs == 0) return cudaSuccess;
+    CParams p;
+    p.k_pool = static_cast<char*>(a.k_pool);
+    p.v_pool = static_cast<char*>(a.v_pool);
+    p.pairs = a.pairs;
+    p.err = a.err;
+    p.num_blocks = a.num_blocks;
+    p.block_bytes = (size_t)a.num_kv_heads * kBlockTokens * a.head_dim * elem_bytes(a.dtype);
+    const size_t n16 = p.block_bytes / 16;
+    const unsigned slices = (unsigned)((n16 + 256 * 4 - 1) / (256 * 4));   // ~4 vectors per thread
+    const dim3 grid(a.num_pairs, 2, slices > 0 ? (slices < 64 ? slices : 64) : 1);
+    copy_kernel<<<grid, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

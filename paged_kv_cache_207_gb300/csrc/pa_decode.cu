@@ -1,0 +1,614 @@
+// pa_decode.cu -- single-token decode attention over the block-paged KV cache.
+//
+// What is computed (spindle, "Paging" and "Why write the forward pass"): for
+// every sequence s and query head h, attention of q[s][h] over the keys and
+// values of positions 0 .. context_lens[s]-1, found through the sequence's
+// block table; query head h reads kv head h / G (G = Hq / Hkv).
+//
+// How (split-KV after the Flash-Decoding entry of the mlsystems list; the
+// bandwidth bound after Slipstream, "The thesis" / Fig. 01):
+//   grid = (partition j, kv head, sequence).  A CTA owns one partition of
+//   PA_PARTITION_TOKENS tokens of one (sequence, kv head) and serves all G
+//   query heads that read it, so each K/V byte leaves HBM once.
+//   Each warp streams every NW-th block of the partition through a private
+//   ring of NST shared-memory stages: lane 0 issues two 1-D bulk copies (the
+//   TMA engine) per block -- the contiguous K tile and V tile of that
+//   (block, kv head) -- completing on the stage's mbarrier.
+//   bf16: scores S[16 tokens][8 heads] = K_tile (16 x D) * Q^T (D x 8) on the
+//   tensor cores (mma.m16n8k16, tokens on M, the G query heads padded to 8 on
+//   N), fp32 online softmax in registers, P transposed in-register with
+//   movmatrix, then O^T[D][8] += V^T (D x 16) * P (16 x 8).
+//   fp32: the same pipeline with CUDA-core FMAs (no tensor-core path reaches
+//   fp32 accuracy).
+//   At the end the warps of a CTA merge through shared memory; a sequence
+//   with one partition writes `out` directly, otherwise the partition's
+//   unnormalised output and its (max, sum) go to the workspace and a second
+//   kernel merges partitions with log-sum-exp weights in fixed order.
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "pa_internal.h"
+#include "pa_ptx.cuh"
+
+namespace pa {
+
+namespace {
+
+constexpr uint64_t kWaitLimitNs = 200000000ull;   // 200 ms: a real tile copy takes microseconds
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct KParams {
+    void* out;
+    const void* q;
+    const char* k_pool;
+    const char* v_pool;
+    const int32_t* tables;
+    const int32_t* lens;
+    float* part_o;      // [S*Hq][part_stride][D]
+    float2* part_ml;    // [S*Hq][part_stride] : (max in log2 units, sum)
+    int32_t* err;
+    int Hq, Hkv, G, max_blocks, num_blocks, grid_parts, part_stride;
+    float scale_log2;   // scale * log2(e): scores live in log2 units
+};
+
+__device__ __forceinline__ void raise_flag(int32_t* err, int bits) {
+    if (err) atomicOr(err, bits);
+}
+
+// Context length clamped to the table's capacity; flags bad values once per
+// sequence (from the CTA of partition 0, kv head 0).
+__device__ __forceinline__ int clamped_len(const KParams& p, int s) {
+    int L = __ldg(p.lens + s);
+    const int cap = p.max_blocks * kBlockTokens;
+    const bool leader = blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0;
+    if (L < 0 || L > cap) {
+        if (leader) raise_flag(p.err, PA_DEV_ERR_BAD_POS);
+        L = L < 0 ? 0 : cap;
+    }
+    return L;
+}
+
+// True when some CTA has already given up on a copy: later CTAs return at once
+// so that a broken pipeline cannot keep the GPU busy for long.
+__device__ __forceinline__ bool aborted(const int32_t* err) {
+    if (!err) return false;
+    return (*reinterpret_cast<const volatile int32_t*>(err) & PA_DEV_ERR_TIMEOUT) != 0;
+}
+
+__device__ __forceinline__ int num_parts(int L) {
+    return L > 0 ? (L + kPartTokens - 1) / kPartTokens : 1;
+}
+
+// Per-warp ring of NST stages, each holding one K tile and one V tile.
+template <int TILE, int NW, int NST>
+struct Ring {
+    uint32_t stage0;   // shared address of this warp's stage 0
+    uint32_t bar0;     // shared address of this warp's first mbarrier
+    __device__ __forceinline__ uint32_t k(int st) const { return stage0 + st * 2 * TILE; }
+    __device__ __forceinline__ uint32_t v(int st) const { return stage0 + st * 2 * TILE + TILE; }
+    __device__ __forceinline__ uint32_t bar(int st) const { return bar0 + st * 8; }
+};
+
+// Shared-memory bytes of the stage rings plus the barriers.
+template <int TILE, int NW, int NST>
+constexpr int ring_smem_bytes() { return NW * NST * 2 * TILE + NW * NST * 8; }
+
+// Cross-warp merge of one partition (both element types).  Every warp holds,
+// per padded head g < 8: running max m (log2 units), sum l and unnormalised
+// output row o[g][:] already written to shared memory by the caller.
+template <int D, int NW, typename OutT>
+__device__ __forceinline__ void merge_and_store(const KParams& p, const float* sm_o,
+                                                const float* sm_m, const float* sm_l, int s,
+                                                int kvh, int j, int nparts) {
+    constexpr int OS = D + 4;
+    for (int idx = threadIdx.x; idx < p.G * D; idx += NW * 32) {
+        const int g = idx / D, d = idx - (idx / D) * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_m[w * 8 + g]);
+        float acc = 0.f, lsum = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float wt = fast_exp2(sm_m[w * 8 + g] - M);
+                acc += wt * sm_o[(w * 8 + g) * OS + d];
+                lsum += wt * sm_l[w * 8 + g];
+            }
+        }
+        const size_t row = (size_t)s * p.Hq + (size_t)kvh * p.G + g;
+        if (nparts == 1) {
+            const float v = lsum > 0.f ? acc / lsum : 0.f;
+            if constexpr (sizeof(OutT) == 2)
+                reinterpret_cast<__nv_bfloat16*>(p.out)[row * D + d] = __float2bfloat16_rn(v);
+            else
+                reinterpret_cast<float*>(p.out)[row * D + d] = v;
+        } else {
+            p.part_o[(row * p.part_stride + j) * D + d] = acc;
+            if (d == 0) p.part_ml[row * p.part_stride + j] = make_float2(M, lsum);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// bf16 kernel: tensor-core scores and P.V
+// ---------------------------------------------------------------------------
+template <int D, int NW, int NST>
+__global__ void __launch_bounds__(NW * 32)
+decode_bf16_kernel(const KParams p) {
+    constexpr int TILE = kBlockTokens * D * 2;   // bytes of one (block, kv head) tile
+    constexpr int KS = D / 16;                   // k-steps of the score MMA = m-tiles of P.V
+    extern __shared__ __align__(128) uint8_t smem[];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = lane >> 2, c = lane & 3;
+    const int j = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+
+    const int L = clamped_len(p, s);
+    const int nparts = num_parts(L);
+    if (j == 0 && kvh == 0 && threadIdx.x == 0 && nparts > p.grid_parts)
+        raise_flag(p.err, PA_DEV_ERR_HINT);
+    if (j >= nparts || aborted(p.err)) return;
+
+    const int blk0 = j * kPartBlocks;                            // first logical block
+    const int tok_end = min(L, (j + 1) * kPartTokens);           // one past the last token
+    const int nblk = (tok_end - blk0 * kBlockTokens + kBlockTokens - 1) / kBlockTokens;
+    const int nb_w = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;
+
+    Ring<TILE, NW, NST> ring;
+    ring.stage0 = smem_u32(smem) + warp * NST * 2 * TILE;
+    ring.bar0 = smem_u32(smem) + NW * NST * 2 * TILE + warp * NST * 8;
+    if (lane == 0) {
+#pragma unroll
+        for (int st = 0; st < NST; ++st) mbar_init(ring.bar(st), 1);
+        fence_proxy_async_smem();
+    }
+    __syncwarp();
+
+    // Query fragments (B operand, k = dim, n = query head of the group).
+    uint32_t qb[KS][2];
+    {
+        const bool live = r < p.G;
+        const uint16_t* qrow = reinterpret_cast<const uint16_t*>(p.q) +
+                               ((size_t)s * p.Hq + (size_t)kvh * p.G + (live ? r : 0)) * D;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            qb[kk][0] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * c)) : 0u;
+            qb[kk][1] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 8 + 2 * c)) : 0u;
+        }
+    }
+
+    const uint64_t pol = l2_policy_evict_first();
+    const int32_t* trow = p.tables + (size_t)s * p.max_blocks;
+    auto issue = [&](int i, int st) -> bool {
+        const int b = blk0 + warp + i * NW;
+        const int32_t blk = __ldg(trow + b);
+        const bool ok = blk >= 0 && blk < p.num_blocks;
+        if (lane == 0) {
+            if (ok) {
+                const size_t off = ((size_t)blk * p.Hkv + kvh) * (size_t)TILE;
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(ring.bar(st), 2 * TILE);
+                bulk_g2s(ring.k(st), p.k_pool + off, TILE, ring.bar(st), pol);
+                bulk_g2s(ring.v(st), p.v_pool + off, TILE, ring.bar(st), pol);
+            } else {
+                raise_flag(p.err, PA_DEV_ERR_BAD_BLOCK);
+            }
+        }
+        return ok;
+    };
+
+    float m0 = -INFINITY, m1 = -INFINITY;   // running max of heads 2c, 2c+1 (log2 units)
+    float l0 = 0.f, l1 = 0.f;               // this thread's share of the running sums
+    float o[KS][4];
+#pragma unroll
+    for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+    uint32_t issued = 0, phase = 0;
+    bool failed = false;
+    const int npro = nb_w < NST ? nb_w : NST;
+    for (int i = 0; i < npro; ++i)
+        if (issue(i, i)) issued |= 1u << i;
+
+    // ldmatrix row addresses: K tile k-step kk reads 512 contiguous bytes.
+    const uint32_t k_lane = lane * 16;
+    const int vm = lane >> 3;
+    const uint32_t v_lane = (uint32_t)(((vm & 1) * 16 + (vm >> 1) * 8 + (lane & 7)) * 16);
+
+    for (int i = 0; i < nb_w; ++i) {
+        const int st = i % NST;
+        if ((issued >> st) & 1u) {
+            if (!mbar_wait_bounded(ring.bar(st), (phase >> st) & 1u, kWaitLimitNs)) {
+                failed = true;
+                break;
+            }
+            phase ^= 1u << st;
+            issued &= ~(1u << st);
+            const int tok0 = (blk0 + warp + i * NW) * kBlockTokens;
+            // scores: 16 tokens x 8 heads
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint32_t kt = ring.k(st);
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+                uint32_t a0, a1, a2, a3;
+                ldmatrix_x4(kt + kk * 512 + k_lane, a0, a1, a2, a3);
+                mma_bf16_16816(acc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+            }
+            const bool lo_ok = tok0 + r < tok_end, hi_ok = tok0 + r + 8 < tok_end;
+            const float s0 = lo_ok ? acc[0] * p.scale_log2 : -INFINITY;
+            const float s1 = lo_ok ? acc[1] * p.scale_log2 : -INFINITY;
+            const float s2 = hi_ok ? acc[2] * p.scale_log2 : -INFINITY;
+            const float s3 = hi_ok ? acc[3] * p.scale_log2 : -INFINITY;
+            float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
+#pragma unroll
+            for (int x = 4; x < 32; x <<= 1) {
+                bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, x));
+                bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, x));
+            }
+            const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+            const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+            m0 = mn0;
+            m1 = mn1;
+            const uint32_t x0 = pack_bf16x2(fast_exp2(s0 - mn0), fast_exp2(s1 - mn1));   // token r
+            const uint32_t x1 = pack_bf16x2(fast_exp2(s2 - mn0), fast_exp2(s3 - mn1));   // token r+8
+            l0 = l0 * al0 + (bf16_lo_to_f32(x0) + bf16_lo_to_f32(x1));
+            l1 = l1 * al1 + (bf16_hi_to_f32(x0) + bf16_hi_to_f32(x1));
+            const uint32_t pb0 = movmatrix_trans(x0), pb1 = movmatrix_trans(x1);
+
+            // V^T fragments hold tokens 2c, 2c+1 (regs 0,1) and 2c+8, 2c+9 (regs 2,3);
+            // slots past the context may hold anything (even NaN), so zero them.
+            uint32_t mask_a = 0xffffffffu, mask_b = 0xffffffffu;
+            if (tok0 + kBlockTokens > tok_end) {
+                mask_a = (tok0 + 2 * c < tok_end ? 0x0000ffffu : 0u) |
+                         (tok0 + 2 * c + 1 < tok_end ? 0xffff0000u : 0u);
+                mask_b = (tok0 + 2 * c + 8 < tok_end ? 0x0000ffffu : 0u) |
+                         (tok0 + 2 * c + 9 < tok_end ? 0xffff0000u : 0u);
+            }
+            const uint32_t vt = ring.v(st);
+#pragma unroll
+            for (int mi = 0; mi < KS; ++mi) {
+                uint32_t v0, v1, v2, v3;
+                ldmatrix_x4_trans(vt + mi * 512 + v_lane, v0, v1, v2, v3);
+                v0 &= mask_a; v1 &= mask_a; v2 &= mask_b; v3 &= mask_b;
+                o[mi][0] *= al0; o[mi][1] *= al1; o[mi][2] *= al0; o[mi][3] *= al1;
+                mma_bf16_16816(o[mi], v0, v1, v2, v3, pb0, pb1);
+            }
+        }
+        __syncwarp();
+        if (i + NST < nb_w && issue(i + NST, st)) issued |= 1u << st;
+    }
+
+    if (failed) {
+        // Drain every copy still in flight into this warp's stages before the
+        // shared memory is reused or the CTA exits.
+        if (lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
+        for (int st = 0; st < NST; ++st)
+            if ((issued >> st) & 1u) mbar_wait_bounded(ring.bar(st), (phase >> st) & 1u, kWaitLimitNs);
+    }
+
+#pragma unroll
+    for (int x = 4; x < 32; x <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, x);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, x);
+    }
+
+    __syncthreads();   // every warp is done with its stages
+    constexpr int OS = D + 4;
+    float* sm_o = reinterpret_cast<float*>(smem);       // [NW][8][OS]
+    float* sm_m = sm_o + NW * 8 * OS;                    // [NW][8]
+    float* sm_l = sm_m + NW * 8;                         // [NW][8]
+    {
+        float* ow = sm_o + warp * 8 * OS;
+#pragma unroll
+        for (int mi = 0; mi < KS; ++mi) {
+            const int d0 = 16 * mi + r, d1 = d0 + 8;
+            ow[(2 * c) * OS + d0] = o[mi][0];
+            ow[(2 * c + 1) * OS + d0] = o[mi][1];
+            ow[(2 * c) * OS + d1] = o[mi][2];
+            ow[(2 * c + 1) * OS + d1] = o[mi][3];
+        }
+        if (r == 0) {
+            sm_m[warp * 8 + 2 * c] = m0;
+            sm_m[warp * 8 + 2 * c + 1] = m1;
+            sm_l[warp * 8 + 2 * c] = l0;
+            sm_l[warp * 8 + 2 * c + 1] = l1;
+        }
+    }
+    __syncthreads();
+    merge_and_store<D, NW, __nv_bfloat16>(p, sm_o, sm_m, sm_l, s, kvh, j, nparts);
+}
+
+// ---------------------------------------------------------------------------
+// fp32 kernel: CUDA-core FMAs on the same pipeline
+// ---------------------------------------------------------------------------
+template <int D, int NW, int NST>
+__global__ void __launch_bounds__(NW * 32)
+decode_f32_kernel(const KParams p) {
+    constexpr int TILE = kBlockTokens * D * 4;
+    constexpr int NCH = D / 4;          // 16-byte chunks per token row
+    constexpr int DPL = D / 32;         // output dims per lane
+    extern __shared__ __align__(128) uint8_t smem[];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int j = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+    const int L = clamped_len(p, s);
+    const int nparts = num_parts(L);
+    if (j == 0 && kvh == 0 && threadIdx.x == 0 && nparts > p.grid_parts)
+        raise_flag(p.err, PA_DEV_ERR_HINT);
+    if (j >= nparts || aborted(p.err)) return;
+
+    const int blk0 = j * kPartBlocks;
+    const int tok_end = min(L, (j + 1) * kPartTokens);
+    const int nblk = (tok_end - blk0 * kBlockTokens + kBlockTokens - 1) / kBlockTokens;
+    const int nb_w = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;
+
+    constexpr int RING = ring_smem_bytes<TILE, NW, NST>();
+    float* sq = reinterpret_cast<float*>(smem + RING);                 // [8][D] query rows
+    float* sp = sq + 8 * D + warp * 8 * kBlockTokens;                  // [8][16] this warp's P
+
+    Ring<TILE, NW, NST> ring;
+    ring.stage0 = smem_u32(smem) + warp * NST * 2 * TILE;
+    ring.bar0 = smem_u32(smem) + NW * NST * 2 * TILE + warp * NST * 8;
+    if (lane == 0) {
+#pragma unroll
+        for (int st = 0; st < NST; ++st) mbar_init(ring.bar(st), 1);
+        fence_proxy_async_smem();
+    }
+    const float* qbase = reinterpret_cast<const float*>(p.q) + ((size_t)s * p.Hq + (size_t)kvh * p.G) * D;
+    for (int idx = threadIdx.x; idx < 8 * D; idx += NW * 32)
+        sq[idx] = idx < p.G * D ? __ldg(qbase + idx) : 0.f;
+    __syncthreads();
+
+    const uint64_t pol = l2_policy_evict_first();
+    const int32_t* trow = p.tables + (size_t)s * p.max_blocks;
+    auto issue = [&](int i, int st) -> bool {
+        const int b = blk0 + warp + i * NW;
+        const int32_t blk = __ldg(trow + b);
+        const bool ok = blk >= 0 && blk < p.num_blocks;
+        if (lane == 0) {
+            if (ok) {
+                const size_t off = ((size_t)blk * p.Hkv + kvh) * (size_t)TILE;
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(ring.bar(st), 2 * TILE);
+                bulk_g2s(ring.k(st), p.k_pool + off, TILE, ring.bar(st), pol);
+                bulk_g2s(ring.v(st), p.v_pool + off, TILE, ring.bar(st), pol);
+            } else {
+                raise_flag(p.err, PA_DEV_ERR_BAD_BLOCK);
+            }
+        }
+        return ok;
+    };
+
+    float m[8], l[8], o[8][DPL];
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        m[g] = -INFINITY;
+        l[g] = 0.f;
+#pragma unroll
+        for (int k = 0; k < DPL; ++k) o[g][k] = 0.f;
+    }
+
+    uint32_t issued = 0, phase = 0;
+    bool failed = false;
+    const int npro = nb_w < NST ? nb_w : NST;
+    for (int i = 0; i < npro; ++i)
+        if (issue(i, i)) issued |= 1u << i;
+
+    const int t = lane & 15, half = lane >> 4;
+    for (int i = 0; i < nb_w; ++i) {
+        const int st = i % NST;
+        if ((issued >> st) & 1u) {
+            if (!mbar_wait_bounded(ring.bar(st), (phase >> st) & 1u, kWaitLimitNs)) {
+                failed = true;
+                break;
+            }
+            phase ^= 1u << st;
+            issued &= ~(1u << st);
+            const int tok0 = (blk0 + warp + i * NW) * kBlockTokens;
+            const int nvalid = min(kBlockTokens, tok_end - tok0);
+            const float* kt = reinterpret_cast<const float*>(smem + (warp * NST + st) * 2 * TILE);
+            const float* vt = kt + TILE / 4;
+            // lane (t, half): partial dots of token t over the half's chunks
+            float acc[8];
+#pragma unroll
+            for (int g = 0; g < 8; ++g) acc[g] = 0.f;
+#pragma unroll 4
+            for (int ch = half * (NCH / 2); ch < (half + 1) * (NCH / 2); ++ch) {
+                const float4 kv = *reinterpret_cast<const float4*>(kt + (ch * kBlockTokens + t) * 4);
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    if (g < p.G) {
+                        const float4 qv = *reinterpret_cast<const float4*>(sq + g * D + ch * 4);
+                        acc[g] = fmaf(qv.x, kv.x, acc[g]);
+                        acc[g] = fmaf(qv.y, kv.y, acc[g]);
+                        acc[g] = fmaf(qv.z, kv.z, acc[g]);
+                        acc[g] = fmaf(qv.w, kv.w, acc[g]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                if (g < p.G) {
+                    float sc = acc[g] + __shfl_xor_sync(0xffffffffu, acc[g], 16);
+                    sc = t < nvalid ? sc * p.scale_log2 : -INFINITY;
+                    float bm = sc;
+#pragma unroll
+                    for (int x = 1; x < 16; x <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, x));
+                    const float mn = fmaxf(m[g], bm);
+                    const float al = exp2f(m[g] - mn);
+                    const float pr = exp2f(sc - mn);
+                    float bs = pr;
+#pragma unroll
+                    for (int x = 1; x < 16; x <<= 1) bs += __shfl_xor_sync(0xffffffffu, bs, x);
+                    m[g] = mn;
+                    l[g] = l[g] * al + bs;
+#pragma unroll
+                    for (int k = 0; k < DPL; ++k) o[g][k] *= al;
+                    if (half == 0) sp[g * kBlockTokens + t] = pr;
+                }
+            }
+            __syncwarp();
+            for (int tt = 0; tt < nvalid; ++tt) {
+#pragma unroll
+                for (int k = 0; k < DPL; ++k) {
+                    const int d = lane + 32 * k;
+                    const float v = vt[((d >> 2) * kBlockTokens + tt) * 4 + (d & 3)];
+#pragma unroll
+                    for (int g = 0; g < 8; ++g)
+                        if (g < p.G) o[g][k] = fmaf(sp[g * kBlockTokens + tt], v, o[g][k]);
+                }
+            }
+        }
+        __syncwarp();
+        if (i + NST < nb_w && issue(i + NST, st)) issued |= 1u << st;
+    }
+
+    if (failed) {
+        if (lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
+        for (int st = 0; st < NST; ++st)
+            if ((issued >> st) & 1u) mbar_wait_bounded(ring.bar(st), (phase >> st) & 1u, kWaitLimitNs);
+    }
+
+    __syncthreads();
+    constexpr int OS = D + 4;
+    float* sm_o = reinterpret_cast<float*>(smem);
+    float* sm_m = sm_o + NW * 8 * OS;
+    float* sm_l = sm_m + NW * 8;
+    {
+        float* ow = sm_o + warp * 8 * OS;
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+#pragma unroll
+            for (int k = 0; k < DPL; ++k) ow[g * OS + lane + 32 * k] = o[g][k];
+        }
+        if (lane < 8) {
+            float mm = m[0], ll = l[0];
+#pragma unroll
+            for (int g = 1; g < 8; ++g)
+                if (lane == g) { mm = m[g]; ll = l[g]; }
+            sm_m[warp * 8 + lane] = mm;
+            sm_l[warp * 8 + lane] = ll;
+        }
+    }
+    __syncthreads();
+    merge_and_store<D, NW, float>(p, sm_o, sm_m, sm_l, s, kvh, j, nparts);
+}
+
+// ---------------------------------------------------------------------------
+// Partition merge: out = sum_j 2^(m_j - M) o_j / sum_j 2^(m_j - M) l_j
+// ---------------------------------------------------------------------------
+template <int D, typename OutT>
+__global__ void __launch_bounds__(256)
+decode_reduce_kernel(const KParams p) {
+    constexpr int HPB = 256 / D;   // query heads per CTA
+    const int s = blockIdx.y;
+    const int h = blockIdx.x * HPB + threadIdx.y;
+    const int d = threadIdx.x;
+    if (h >= p.Hq) return;
+    int L = __ldg(p.lens + s);
+    const int cap = p.max_blocks * kBlockTokens;
+    L = L < 0 ? 0 : (L > cap ? cap : L);
+    int n = num_parts(L);
+    if (n <= 1) return;                       // written directly by the main kernel
+    if (n > p.grid_parts) n = p.grid_parts;   // flagged by the main kernel
+    const size_t row = (size_t)s * p.Hq + h;
+    const float2* ml = p.part_ml + row * p.part_stride;
+    const float* po = p.part_o + row * p.part_stride * D;
+    float M = -INFINITY;
+    for (int jj = 0; jj < n; ++jj) M = fmaxf(M, ml[jj].x);
+    float acc = 0.f, lsum = 0.f;
+    if (M != -INFINITY) {
+        for (int jj = 0; jj < n; ++jj) {
+            const float2 v = ml[jj];
+            const float wt = fast_exp2(v.x - M);
+            acc += wt * po[(size_t)jj * D + d];
+            lsum += wt * v.y;
+        }
+    }
+    const float val = lsum > 0.f ? acc / lsum : 0.f;
+    if constexpr (sizeof(OutT) == 2)
+        reinterpret_cast<__nv_bfloat16*>(p.out)[row * D + d] = __float2bfloat16_rn(val);
+    else
+        reinterpret_cast<float*>(p.out)[row * D + d] = val;
+}
+
+// Launch configuration of the main kernels.
+constexpr int kWarps = 4;
+constexpr int kStagesBf16 = 3;
+constexpr int kStagesF32 = 2;
+
+template <int D>
+constexpr int bf16_smem() { return ring_smem_bytes<kBlockTokens * D * 2, kWarps, kStagesBf16>(); }
+template <int D>
+constexpr int f32_smem() {
+    return ring_smem_bytes<kBlockTokens * D * 4, kWarps, kStagesF32>() +
+           (8 * D + kWarps * 8 * kBlockTokens) * 4;
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, int bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int D>
+cudaError_t launch_for_dim(const KParams& kp, const DecodeArgs& a, cudaStream_t stream) {
+    const dim3 grid(a.grid_parts, a.num_kv_heads, a.num_seqs);
+    cudaError_t e;
+    if (a.dtype == PA_BF16) {
+        auto k = decode_bf16_kernel<D, kWarps, kStagesBf16>;
+        if ((e = set_smem(k, bf16_smem<D>())) != cudaSuccess) return e;
+        k<<<grid, kWarps * 32, bf16_smem<D>(), stream>>>(kp);
+    } else {
+        auto k = decode_f32_kernel<D, kWarps, kStagesF32>;
+        if ((e = set_smem(k, f32_smem<D>())) != cudaSuccess) return e;
+        k<<<grid, kWarps * 32, f32_smem<D>(), stream>>>(kp);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (a.grid_parts > 1) {
+        const dim3 rgrid((a.num_q_heads + 256 / D - 1) / (256 / D), a.num_seqs);
+        const dim3 rblock(D, 256 / D);
+        if (a.dtype == PA_BF16)
+            decode_reduce_kernel<D, __nv_bfloat16><<<rgrid, rblock, 0, stream>>>(kp);
+        else
+            decode_reduce_kernel<D, float><<<rgrid, rblock, 0, stream>>>(kp);
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
+}  // namespace
+
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_blocks) {
+    const int stride = decode_part_stride(max_blocks);
+    if (stride <= 1) return 0;
+    const size_t rows = (size_t)num_seqs * (size_t)num_q_heads * (size_t)stride;
+    return rows * (size_t)head_dim * sizeof(float) + rows * sizeof(float2);
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+    KParams kp;
+    kp.out = a.out;
+    kp.q = a.q;
+    kp.k_pool = static_cast<const char*>(a.k_pool);
+    kp.v_pool = static_cast<const char*>(a.v_pool);
+    kp.tables = a.block_tables;
+    kp.lens = a.context_lens;
+    const size_t rows = (size_t)a.num_seqs * a.num_q_heads * a.part_stride;
+    kp.part_o = static_cast<float*>(a.workspace);
+    kp.part_ml = a.workspace ? reinterpret_cast<float2*>(static_cast<char*>(a.workspace) +
+                                                         rows * a.head_dim * sizeof(float))
+                             : nullptr;
+    kp.err = a.err;
+    kp.Hq = a.num_q_heads;
+    kp.Hkv = a.num_kv_heads;
+    kp.G = a.num_q_heads / a.num_kv_heads;
+    kp.max_blocks = a.max_blocks;
+    kp.num_blocks = a.num_blocks;
+    kp.grid_parts = a.grid_parts;
+    kp.part_stride = a.part_stride;
+    kp.scale_log2 = a.scale * kLog2e;
+    if (a.head_dim == 64) return launch_for_dim<64>(kp, a, stream);
+    return launch_for_dim<128>(kp, a, stream);
+}
+
+}  // namespace pa

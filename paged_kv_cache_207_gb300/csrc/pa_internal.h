@@ -1,0 +1,69 @@
+// pa_internal.h -- launch interfaces shared by the C ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "pa.h"
+
+namespace pa {
+
+constexpr int kBlockTokens = PA_BLOCK_SIZE;                     // tokens per block
+constexpr int kPartTokens = PA_PARTITION_TOKENS;                // tokens per split-KV partition
+constexpr int kPartBlocks = kPartTokens / kBlockTokens;         // blocks per partition
+static_assert(kPartTokens % kBlockTokens == 0, "partition must be whole blocks");
+
+inline int elem_bytes(pa_dtype t) { return t == PA_BF16 ? 2 : 4; }
+
+struct DecodeArgs {
+    void* out;
+    const void* q;
+    const void* k_pool;
+    const void* v_pool;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    int32_t* err;            // device error flag, may be null
+    void* workspace;
+    int num_seqs, num_q_heads, num_kv_heads, head_dim;
+    int max_blocks, num_blocks;
+    int grid_parts;          // partitions launched per (sequence, kv head)
+    int part_stride;         // partitions reserved per (sequence, query head) in the workspace
+    float scale;
+    pa_dtype dtype;
+};
+
+// Partitions a sequence of up to max_blocks blocks can span.
+inline int decode_part_stride(int max_blocks) {
+    return (max_blocks + kPartBlocks - 1) / kPartBlocks;
+}
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_blocks);
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+struct AppendArgs {
+    void* k_pool;
+    void* v_pool;
+    const void* k_new;
+    const void* v_new;
+    const int32_t* block_tables;
+    const int32_t* start_pos;
+    const int32_t* cu_new;
+    int32_t* err;
+    int max_blocks, num_seqs, total_new, num_blocks, num_kv_heads, head_dim;
+    pa_dtype dtype;
+};
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
+
+struct CopyArgs {
+    void* k_pool;
+    void* v_pool;
+    const int32_t* pairs;
+    int32_t* err;
+    int num_pairs, num_blocks, num_kv_heads, head_dim;
+    pa_dtype dtype;
+};
+cudaError_t launch_copy(const CopyArgs& a, cudaStream_t stream);
+
+}  // namespace pa
