@@ -210,8 +210,12 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     build.build()
     pk.lib()
-    wl = W.WORKLOADS[args.workload](device="cuda", **({"seed": 210 + 1000 * rank}
-                                                      if args.workload == "llama3-8b_batch256" else {}))
+    kw = {}
+    if args.workload == "llama3-8b_batch256":
+        kw["seed"] = 210 + 1000 * rank
+    if args.num_seqs:
+        kw["num_seqs"] = args.num_seqs
+    wl = W.WORKLOADS[args.workload](device="cuda", **kw)
     tdt = wl.torch_dtype()
     S, Hq, Hkv, D = wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
     shape = pk.pool_shape(wl.num_blocks, Hkv, D, tdt)
@@ -486,6 +490,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3-8b_batch256")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--num-seqs", type=int, default=0,
+                    help="override the workload's sequence count (smaller cases for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
