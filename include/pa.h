@@ -59,7 +59,9 @@ typedef enum {
     PA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misalignment, small workspace */
     PA_ERR_UNSUPPORTED = 2,   /* head_dim not 64/128, more than 8 query heads per kv head */
     PA_ERR_CUDA = 3,          /* a CUDA launch or runtime call failed */
-    PA_ERR_OUT_OF_BLOCKS = 4  /* block manager: not enough free blocks (nothing changed) */
+    PA_ERR_OUT_OF_BLOCKS = 4, /* block manager: not enough free blocks (nothing changed) */
+    PA_ERR_SCRATCH_LIMIT = 5  /* pa_decode_attention_noalloc: the call needs more scratch
+                                 than the library's built-in PA_NOALLOC_SCRATCH_BYTES */
 } pa_status;
 
 typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
@@ -156,6 +158,44 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, cons
                               int32_t max_context_len_hint, int32_t num_blocks, float scale,
                               pa_dtype dtype, void* workspace, size_t workspace_bytes,
                               int32_t* dev_err_flag, void* stream);
+
+/*
+ * pa_decode_attention_noalloc -- pa_decode_attention for callers that cannot
+ * allocate device memory.  (The pages have no counterpart; this entry point is
+ * this library's own addition.)
+ *
+ * pa_decode_attention wants a caller-provided scratch workspace.  Some callers
+ * cannot provide one: a plugin inside a host framework that owns all device
+ * memory and gives plugins no scratch buffer, or a latency-critical decode loop
+ * that must never call cudaMalloc because an allocation can synchronise the
+ * whole device.  This entry point takes the same arguments minus the
+ * workspace and runs the same kernels with the library's own scratch: one
+ * file-scope device array of PA_NOALLOC_SCRATCH_BYTES (16 MiB), which every GPU
+ * that loads the library holds until the process exits.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ *   - Limit: a call may need at most PA_NOALLOC_SCRATCH_BYTES, i.e.
+ *     pa_decode_workspace_size(num_seqs, num_q_heads, head_dim,
+ *     max_blocks_per_seq) <= 16 MiB (for head_dim 128: num_seqs * num_q_heads *
+ *     ceil(max_blocks_per_seq / 32) <= 32 263); larger calls return
+ *     PA_ERR_SCRATCH_LIMIT and launch nothing.
+ *   - Set-up: the first call on a device that needs scratch looks up the
+ *     array's device address (cudaGetSymbolAddress) with that device current;
+ *     make that first call before any stream capture.
+ *   - Sharing: every call on a device uses the same array and leaves its
+ *     partial results in it; no call depends on what an earlier call left
+ *     there.  Calls whose kernels overlap on the GPU (other streams, other host
+ *     threads) race on the array: serialise them.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+pa_status pa_decode_attention_noalloc(void* out, const void* q, const void* k_pool,
+                                      const void* v_pool, const int32_t* block_tables,
+                                      const int32_t* context_lens, int32_t num_seqs,
+                                      int32_t num_q_heads, int32_t num_kv_heads,
+                                      int32_t head_dim, int32_t max_blocks_per_seq,
+                                      int32_t max_context_len_hint, int32_t num_blocks,
+                                      float scale, pa_dtype dtype, int32_t* dev_err_flag,
+                                      void* stream);
 
 /* ---------------------------------------------------------------------------
  * Host block manager (no GPU; spindle, "Paging").

@@ -28,7 +28,7 @@ DEV_ERR_BAD_PAIR = 32
 
 EXPORTED = [
     "pa_status_string", "pa_abi_version", "pa_append_kv", "pa_copy_block",
-    "pa_decode_workspace_size", "pa_decode_attention", "pa_bm_create", "pa_bm_destroy",
+    "pa_decode_workspace_size", "pa_decode_attention", "pa_decode_attention_noalloc", "pa_bm_create", "pa_bm_destroy",
     "pa_bm_add_seq", "pa_bm_fork", "pa_bm_free_seq", "pa_bm_blocks_needed",
     "pa_bm_prepare_append", "pa_bm_block_table", "pa_bm_seq_len", "pa_bm_refcount", "pa_bm_stats",
 ]
@@ -70,6 +70,9 @@ def lib() -> ctypes.CDLL:
     L.pa_decode_attention.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32,
                                       ctypes.c_float, ctypes.c_int, p, sz, p, p]
     L.pa_decode_attention.restype = ctypes.c_int
+    L.pa_decode_attention_noalloc.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32,
+                                              ctypes.c_float, ctypes.c_int, p, p]
+    L.pa_decode_attention_noalloc.restype = ctypes.c_int
     L.pa_bm_create.argtypes = [i32, ctypes.POINTER(p)]
     L.pa_bm_destroy.argtypes = [p]
     L.pa_bm_destroy.restype = None
@@ -174,6 +177,22 @@ def decode_attention(out, q, k_pool, v_pool, block_tables, context_lens, scale, 
         _i32(context_lens, "context_lens"), q.shape[0], q.shape[1], hkv, d, block_tables.shape[1],
         int(max_context_len_hint), nb, float(scale), _dtype_code(q),
         None if workspace is None else _ptr(workspace), ws_bytes,
+        None if err_flag is None else _i32(err_flag, "err_flag"), _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
+PA_ERR_SCRATCH_LIMIT = 5
+
+
+def decode_attention_noalloc(out, q, k_pool, v_pool, block_tables, context_lens, scale,
+                             max_context_len_hint: int = 0, err_flag=None, stream=None) -> None:
+    """decode_attention without a caller workspace: the library's built-in 16 MiB device
+    scratch is used instead (for callers that cannot allocate device memory)."""
+    nb, hkv, d = _pool_dims(k_pool)
+    check("pa_decode_attention_noalloc", lib().pa_decode_attention_noalloc(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _i32(block_tables, "block_tables"),
+        _i32(context_lens, "context_lens"), q.shape[0], q.shape[1], hkv, d, block_tables.shape[1],
+        int(max_context_len_hint), nb, float(scale), _dtype_code(q),
         None if err_flag is None else _i32(err_flag, "err_flag"), _stream(stream)))
 
 

@@ -27,6 +27,7 @@ const char* pa_status_string(pa_status s) {
         case PA_ERR_UNSUPPORTED: return "unsupported configuration";
         case PA_ERR_CUDA: return "CUDA error";
         case PA_ERR_OUT_OF_BLOCKS: return "out of free blocks";
+        case PA_ERR_SCRATCH_LIMIT: return "needs more than the built-in no-alloc scratch";
     }
     return "unknown status";
 }
