@@ -482,6 +482,49 @@ def run_reference(args, rank, world):
     }
 
 
+def run_replay(args, rank, world, local):
+    """The spindle-shaped replay: every iteration of continuous batching, 12 layers of
+    append + decode, timed as a whole (wall clock) and on the GPU (events)."""
+    import paged_kv_cache_207_gb300 as pk
+    from paged_kv_cache_207_gb300 import build, workloads as W
+    from paged_kv_cache_207_gb300.replay import Replay
+    torch.cuda.set_device(local)
+    build.build()
+    pk.lib()
+    rw = W.spindle_replay(device="cuda", seed=208 + 1000 * rank)
+    for _ in range(max(1, min(args.warmup, 3))):
+        Replay(rw, device="cuda").run()
+    torch.cuda.synchronize()
+    barrier(world)
+    st = Replay(rw, device="cuda", time_gpu=True).run()
+    barrier(world)
+    wall = all_max(st.wall_s, world)
+    gpu_s = all_max(st.gpu_ms / 1e3, world)
+    tokens = all_sum(float(st.generated_tokens), world)
+    dbytes = all_sum(float(st.decode_bytes), world)
+    peaks = load_peaks() or {}
+    return {
+        "metric": METRIC, "value": round(dbytes / gpu_s / 1e9, 1), "unit": "GB/s",
+        "n_gpus": world, "steps": st.iterations, "warmup": args.warmup,
+        "ms_per_step": round(gpu_s * 1e3 / st.iterations, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "spindle_replay", "requests": rw.num_seqs,
+                   "cow_children": rw.num_children, "layers": rw.num_layers,
+                   "heads": rw.num_heads, "head_dim": rw.head_dim, "pool_slots": rw.num_blocks * 16,
+                   "step": "one continuous-batching iteration: 12 x (append + decode)"},
+        "pct_of_peak_hbm": round(100 * dbytes / gpu_s / 1e9 / peaks.get("hbm_gbs", 6800.0), 2),
+        "tokens_per_s": round(tokens / wall, 1),
+        "tokens_per_s_gpu_time": round(tokens / gpu_s, 1),
+        "replay": {"iterations": st.iterations, "generated_tokens": st.generated_tokens,
+                   "preemptions": st.preemptions, "cow_copies": st.cow_copies,
+                   "prefill_tokens": st.prefill_tokens,
+                   "peak_physical_slots": st.peak_physical_slots,
+                   "mean_slot_utilisation": round(st.mean_slot_utilisation, 4),
+                   "wall_s": round(wall, 3), "gpu_s": round(gpu_s, 4)},
+        "gpu_launches": st.launches,
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -498,6 +541,11 @@ def main():
     rank, world, local = dist_init(args.gpus)
     if args.impl == "reference":
         res = run_reference(args, rank, world)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        return
+    if args.workload == "spindle_replay":
+        res = run_replay(args, rank, world, local)
         if rank == 0:
             print(json.dumps(res), flush=True)
         return

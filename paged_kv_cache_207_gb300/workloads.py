@@ -226,3 +226,79 @@ WORKLOADS = {
     "llama3-8b_long_context": llama8b_long,
     "llama3-8b_shared_prefix": llama8b_shared_prefix,
 }
+
+
+# ---- the spindle-shaped replay ------------------------------------------------
+
+@dataclass
+class ReplayWorkload:
+    """64 requests replayed through continuous batching (spindle, "Paging" and
+    "Continuous batching, and the control"): 60 independent requests plus 4
+    copy-on-write children forked from one 16-token parent prompt.  GPT-2 124M
+    heads (12 x 64), 12 layers, bf16, a pool of 8192 token slots (512 blocks) per
+    layer.  Prompt lengths U[16, 128]; generated lengths lognormal (median 40,
+    sigma 1) capped at 192.  All requests arrive at time 0.
+
+    Values are drawn once for every (sequence, layer, position): ``q/k/v`` are
+    [seqs][layers][max_len][heads][head_dim]; the children's first 16 positions
+    hold the parent's prompt rows, so a recomputed (preempted) sequence gets the
+    same numbers again."""
+
+    prompt_lens: np.ndarray       # int32 [64]; the children's entry is the parent prompt (16)
+    gen_lens: np.ndarray          # int32 [64]
+    num_children: int             # the last num_children sequences are the forks
+    parent_prompt: int
+    num_blocks: int
+    num_layers: int
+    num_heads: int
+    head_dim: int
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.prompt_lens.shape[0])
+
+    @property
+    def max_len(self) -> int:
+        return int(self.q.shape[2])
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / float(np.sqrt(self.head_dim))
+
+
+def spindle_replay(device="cpu", seed=208, num_independent=60, num_children=4, parent_prompt=16,
+                   prompt_lo=16, prompt_hi=128, gen_median=40, gen_sigma=1.0, gen_cap=192,
+                   num_blocks=512, num_layers=12, num_heads=12, head_dim=64,
+                   values: bool = True) -> ReplayWorkload:
+    """``values=False`` draws the lengths only (for host-side schedule checks)."""
+    rng = np.random.default_rng(seed + 1000)
+    prompts = rng.integers(prompt_lo, prompt_hi + 1, size=num_independent).astype(np.int32)
+    prompts = np.concatenate([prompts, np.full(num_children, parent_prompt, np.int32)])
+    n = num_independent + num_children
+    gens = lognormal_lengths(rng, n, gen_median, gen_sigma, gen_cap)
+    max_len = prompt_hi + gen_cap
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    shape = (n, num_layers, max_len, num_heads, head_dim)
+    if not values:
+        empty = torch.empty((n, num_layers, max_len, 0, 0))
+        return ReplayWorkload(prompt_lens=prompts, gen_lens=gens, num_children=num_children,
+                              parent_prompt=parent_prompt, num_blocks=num_blocks,
+                              num_layers=num_layers, num_heads=num_heads, head_dim=head_dim,
+                              q=empty, k=empty, v=empty)
+    vals = []
+    for _ in range(3):
+        t = _values(gen, (n * num_layers * max_len, num_heads, head_dim), device, torch.bfloat16)
+        vals.append(t.view(shape))
+    q, k, v = vals
+    first = num_independent
+    for c in range(first + 1, n):           # every child starts from the same parent prompt
+        k[c, :, :parent_prompt] = k[first, :, :parent_prompt]
+        v[c, :, :parent_prompt] = v[first, :, :parent_prompt]
+    return ReplayWorkload(prompt_lens=prompts, gen_lens=gens, num_children=num_children,
+                          parent_prompt=parent_prompt, num_blocks=num_blocks,
+                          num_layers=num_layers, num_heads=num_heads, head_dim=head_dim,
+                          q=q, k=k, v=v)
