@@ -121,10 +121,10 @@ pa_status pa_copy_block(void* k_pool, void* v_pool, const int32_t* src_dst_pairs
 /*
  * pa_decode_workspace_size -- bytes of device workspace pa_decode_attention
  * needs for these sizes (0 when no sequence can span two partitions).  The
- * workspace holds per-partition partial results of the split-KV reduce.
+ * workspace holds the per-partition partial results of the split-KV merge.
  */
-size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
-                                int32_t max_blocks_per_seq);
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t max_blocks_per_seq);
 
 /*
  * pa_decode_attention -- single-token (q_len = 1) attention over the paged
@@ -148,7 +148,8 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t h
  *                    context sets PA_DEV_ERR_HINT and its output is incomplete.
  *   workspace        device scratch of at least pa_decode_workspace_size()
  *                    bytes (may be NULL when that size is 0); its contents on
- *                    entry do not matter.
+ *                    entry do not matter.  Calls sharing a workspace must not
+ *                    overlap on the GPU.
  * head_dim must be 64 or 128 and num_q_heads / num_kv_heads at most 8.
  */
 pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
@@ -175,10 +176,10 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, cons
  * cudaMalloc, cudaFree or other allocating routine.
  *
  *   - Limit: a call may need at most PA_NOALLOC_SCRATCH_BYTES, i.e.
- *     pa_decode_workspace_size(num_seqs, num_q_heads, head_dim,
- *     max_blocks_per_seq) <= 16 MiB (for head_dim 128: num_seqs * num_q_heads *
- *     ceil(max_blocks_per_seq / 32) <= 32 263); larger calls return
- *     PA_ERR_SCRATCH_LIMIT and launch nothing.
+ *     pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+ *     max_blocks_per_seq) <= 16 MiB (for head_dim 128, about num_seqs *
+ *     num_q_heads * ceil(max_blocks_per_seq / 32) <= 32 000); larger calls
+ *     return PA_ERR_SCRATCH_LIMIT and launch nothing.
  *   - Set-up: the first call on a device that needs scratch looks up the
  *     array's device address (cudaGetSymbolAddress) with that device current;
  *     make that first call before any stream capture.

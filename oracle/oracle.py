@@ -33,31 +33,58 @@ def build(force: bool = False) -> str:
     the oracle gives the same doubles on x86-64 and on aarch64."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
-                               "-o", tmp, _SRC, "-lm"])
+        compile_source(_SRC, tmp)
         os.replace(tmp, _LIB)
     return _LIB
+
+
+def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
+    p = ctypes.c_void_p
+    i = ctypes.c_int
+    L.oracle_decode.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, ctypes.c_double, i]
+    L.oracle_decode_pairs.argtypes = [p, p, i, p, p, p, p, p, i, i, i, i, i, ctypes.c_double, i]
+    L.oracle_decode_one.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, i, ctypes.c_double, i]
+    L.oracle_decode_contig.argtypes = [p, p, p, p, i, i, i, i, ctypes.c_double, i]
+    L.oracle_append_kv.argtypes = [p, p, p, p, p, i, p, p, i, i, i, i, i]
+    L.oracle_copy_block.argtypes = [p, p, p, i, i, i, i, i]
+    L.oracle_round_out.argtypes = [p, p, ctypes.c_int64, i]
+    L.oracle_double_to_bf16.argtypes = [ctypes.c_double]
+    L.oracle_double_to_bf16.restype = ctypes.c_uint16
+    L.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+    L.oracle_bf16_to_double.restype = ctypes.c_double
+    return L
+
+
+def compile_source(src: str, out_path: str) -> str:
+    """Compile a C source file with the oracle's flags into a shared library."""
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
+                           "-o", out_path, src, "-lm"])
+    return out_path
+
+
+class use_library:
+    """Context manager: route every call of this module to another build of the oracle
+    (used by the tests that plant mistakes in a copy of the source)."""
+
+    def __init__(self, path: str):
+        self.L = _bind(ctypes.CDLL(path))
+
+    def __enter__(self):
+        global _lib
+        self.prev = _lib
+        _lib = self.L
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self.prev
+        return False
 
 
 def lib() -> ctypes.CDLL:
     global _lib
     if _lib is None:
-        _lib = ctypes.CDLL(build())
-        p = ctypes.c_void_p
-        i = ctypes.c_int
-        _lib.oracle_decode.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, ctypes.c_double, i]
-        _lib.oracle_decode_pairs.argtypes = [p, p, i, p, p, p, p, p, i, i, i, i, i,
-                                             ctypes.c_double, i]
-        _lib.oracle_decode_one.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, i,
-                                           ctypes.c_double, i]
-        _lib.oracle_decode_contig.argtypes = [p, p, p, p, i, i, i, i, ctypes.c_double, i]
-        _lib.oracle_append_kv.argtypes = [p, p, p, p, p, i, p, p, i, i, i, i, i]
-        _lib.oracle_copy_block.argtypes = [p, p, p, i, i, i, i, i]
-        _lib.oracle_round_out.argtypes = [p, p, ctypes.c_int64, i]
-        _lib.oracle_double_to_bf16.argtypes = [ctypes.c_double]
-        _lib.oracle_double_to_bf16.restype = ctypes.c_uint16
-        _lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
-        _lib.oracle_bf16_to_double.restype = ctypes.c_double
+        _lib = _bind(ctypes.CDLL(build()))
     return _lib
 
 

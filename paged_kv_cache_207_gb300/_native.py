@@ -65,7 +65,7 @@ def lib() -> ctypes.CDLL:
     L.pa_append_kv.restype = ctypes.c_int
     L.pa_copy_block.argtypes = [p, p, p, i32, i32, i32, i32, ctypes.c_int, p, p]
     L.pa_copy_block.restype = ctypes.c_int
-    L.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32]
+    L.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     L.pa_decode_workspace_size.restype = sz
     L.pa_decode_attention.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32,
                                       ctypes.c_float, ctypes.c_int, p, sz, p, p]
@@ -162,9 +162,17 @@ def copy_block(k_pool, v_pool, pairs, err_flag=None, stream=None) -> None:
         _stream(stream)))
 
 
-def decode_workspace_size(num_seqs: int, num_q_heads: int, head_dim: int,
+def decode_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
                           max_blocks_per_seq: int) -> int:
-    return int(lib().pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_blocks_per_seq))
+    return int(lib().pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                              max_blocks_per_seq))
+
+
+def decode_workspace(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                     max_blocks_per_seq: int, device="cuda"):
+    """A zero-filled workspace for decode_attention (None when none is needed)."""
+    n = decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq)
+    return torch.zeros(n, dtype=torch.uint8, device=device) if n else None
 
 
 def decode_attention(out, q, k_pool, v_pool, block_tables, context_lens, scale, workspace=None,

@@ -49,6 +49,8 @@ def _compile(src: str, ptxas_verbose: bool) -> str:
     obj = os.path.join(BUILD, os.path.basename(src) + ".o")
     cmd = [_nvcc(), "-c", src, "-o", obj, "-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
            "-I", INCLUDE, "-I", CSRC] + ARCH
+    # optional extra flags, e.g. -DPA_DECODE_WARPS=8 -DPA_DECODE_STAGES=2 for tuning builds
+    cmd += os.environ.get("PA_EXTRA_NVCC_FLAGS", "").split()
     if src.endswith(".cu"):
         cmd += ["--expt-relaxed-constexpr"]
         if ptxas_verbose:

@@ -94,10 +94,13 @@ pa_status pa_copy_block(void* k_pool, void* v_pool, const int32_t* src_dst_pairs
     return cuda_status(pa::launch_copy(a, static_cast<cudaStream_t>(stream)));
 }
 
-size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
-                                int32_t max_blocks_per_seq) {
-    if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0) return 0;
-    return pa::decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_blocks_per_seq);
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t max_blocks_per_seq) {
+    if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        max_blocks_per_seq <= 0)
+        return 0;
+    return pa::decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                      max_blocks_per_seq);
 }
 
 pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
@@ -121,7 +124,7 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, cons
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
         return PA_ERR_INVALID_ARG;
     const size_t need =
-        pa::decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_blocks_per_seq);
+        pa::decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
         return PA_ERR_INVALID_ARG;
 

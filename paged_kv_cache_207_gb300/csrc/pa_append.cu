@@ -33,6 +33,9 @@ struct AParams {
 };
 
 __global__ void __launch_bounds__(256) append_kernel(const AParams p) {
+    // a decode launched after this kernel may start its set-up now; it waits for this
+    // grid to finish before reading the pools
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (item == 0) {
         if (__ldg(p.cu) != 0 || __ldg(p.cu + p.S) != p.total) raise_flag(p.err, PA_DEV_ERR_BAD_CU);
@@ -43,18 +46,32 @@ __global__ void __launch_bounds__(256) append_kernel(const AParams p) {
     const int h = (int)(rh % p.Hkv);
     const int row = (int)(rh / p.Hkv);
 
-    // sequence owning this row: largest s with cu[s] <= row
-    int lo = 0, hi = p.S - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(p.cu + mid) <= row) lo = mid;
-        else hi = mid - 1;
-    }
-    const int s = lo;
-    const int first = __ldg(p.cu + s);
-    if (row < first || row >= __ldg(p.cu + s + 1)) {
-        raise_flag(p.err, PA_DEV_ERR_BAD_CU);
-        return;
+    // the new data depends only on the row: load it first, the address chain follows
+    const size_t src = (((size_t)row * p.Hkv + h) * p.chunks + ch) * 16;
+    const uint4 kv = __ldg(reinterpret_cast<const uint4*>(p.k_new + src));
+    const uint4 vv = __ldg(reinterpret_cast<const uint4*>(p.v_new + src));
+
+    // sequence owning this row: cu[s] <= row < cu[s+1].  Guess by proportion (exact
+    // when every sequence appends the same number of rows, e.g. one per decode step),
+    // then fall back to a binary search.
+    int s = (int)(((long long)row * p.S) / (p.total > 0 ? p.total : 1));
+    if (s >= p.S) s = p.S - 1;
+    int first = __ldg(p.cu + s);
+    int next = __ldg(p.cu + s + 1);
+    if (!(first <= row && row < next)) {
+        int lo = 0, hi = p.S - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(p.cu + mid) <= row) lo = mid;
+            else hi = mid - 1;
+        }
+        s = lo;
+        first = __ldg(p.cu + s);
+        next = __ldg(p.cu + s + 1);
+        if (row < first || row >= next) {
+            raise_flag(p.err, PA_DEV_ERR_BAD_CU);
+            return;
+        }
     }
     const long long pos = (long long)__ldg(p.start_pos + s) + (row - first);
     if (pos < 0 || pos >= (long long)p.max_blocks * kBlockTokens) {
@@ -69,9 +86,6 @@ __global__ void __launch_bounds__(256) append_kernel(const AParams p) {
     const int slot = (int)(pos % kBlockTokens);
     // pool byte offset: tile (blk, h), chunk ch, slot  -> 16 bytes
     const size_t dst = ((((size_t)blk * p.Hkv + h) * p.chunks + ch) * kBlockTokens + slot) * 16;
-    const size_t src = (((size_t)row * p.Hkv + h) * p.chunks + ch) * 16;
-    const uint4 kv = __ldg(reinterpret_cast<const uint4*>(p.k_new + src));
-    const uint4 vv = __ldg(reinterpret_cast<const uint4*>(p.v_new + src));
     *reinterpret_cast<uint4*>(p.k_pool + dst) = kv;
     *reinterpret_cast<uint4*>(p.v_pool + dst) = vv;
 }

@@ -143,7 +143,16 @@ decode_bf16_kernel(const KParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = lane >> 2, c = lane & 3;
     const int j = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+    const int32_t* trow = p.tables + (size_t)s * p.max_blocks;
 
+    // This warp's first NST table entries are read before the context length is known,
+    // so both loads are in flight together (entries past the table row are not read).
+    int32_t first_blk[NST];
+#pragma unroll
+    for (int i = 0; i < NST; ++i) {
+        const int b = j * kPartBlocks + warp + i * NW;
+        first_blk[i] = b < p.max_blocks ? __ldg(trow + b) : -1;
+    }
     const int L = clamped_len(p, s);
     const int nparts = num_parts(L);
     if (j == 0 && kvh == 0 && threadIdx.x == 0 && nparts > p.grid_parts)
@@ -178,11 +187,13 @@ decode_bf16_kernel(const KParams p) {
         }
     }
 
+    // Everything above reads only the query, the tables and the lengths.  The pools
+    // may still be being written by the previous kernel (an append): wait for it.
+    grid_dependency_wait();
+    grid_launch_dependents();
+
     const uint64_t pol = l2_policy_evict_first();
-    const int32_t* trow = p.tables + (size_t)s * p.max_blocks;
-    auto issue = [&](int i, int st) -> bool {
-        const int b = blk0 + warp + i * NW;
-        const int32_t blk = __ldg(trow + b);
+    auto issue_blk = [&](int32_t blk, int st) -> bool {
         const bool ok = blk >= 0 && blk < p.num_blocks;
         if (lane == 0) {
             if (ok) {
@@ -206,9 +217,9 @@ decode_bf16_kernel(const KParams p) {
 
     uint32_t issued = 0, phase = 0;
     bool failed = false;
-    const int npro = nb_w < NST ? nb_w : NST;
-    for (int i = 0; i < npro; ++i)
-        if (issue(i, i)) issued |= 1u << i;
+#pragma unroll
+    for (int i = 0; i < NST; ++i)
+        if (i < nb_w && issue_blk(first_blk[i], i)) issued |= 1u << i;
 
     // ldmatrix row addresses: K tile k-step kk reads 512 contiguous bytes.
     const uint32_t k_lane = lane * 16;
@@ -275,7 +286,8 @@ decode_bf16_kernel(const KParams p) {
             }
         }
         __syncwarp();
-        if (i + NST < nb_w && issue(i + NST, st)) issued |= 1u << st;
+        if (i + NST < nb_w && issue_blk(__ldg(trow + blk0 + warp + (i + NST) * NW), st))
+            issued |= 1u << st;
     }
 
     if (failed) {
@@ -329,6 +341,8 @@ decode_f32_kernel(const KParams p) {
     constexpr int DPL = D / 32;         // output dims per lane
     extern __shared__ __align__(128) uint8_t smem[];
 
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int j = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
     const int L = clamped_len(p, s);
@@ -495,46 +509,100 @@ decode_f32_kernel(const KParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// Partition merge: out = sum_j 2^(m_j - M) o_j / sum_j 2^(m_j - M) l_j
+// Partition merge: out = sum_j 2^(m_j - M) o_j / sum_j 2^(m_j - M) l_j.
+// RPC rows (sequence, query head) per 256-thread CTA: RPC = 8 gives one warp per
+// row (few partitions); RPC = 1 gives the whole CTA to one row, warp w summing
+// partitions w, w + 8, ... and the warps combined in order through shared memory
+// (many partitions).  Lane k owns D/32 dims.  The order of every sum is fixed.
 // ---------------------------------------------------------------------------
-template <int D, typename OutT>
+template <int D, int RPC, typename OutT>
 __global__ void __launch_bounds__(256)
-decode_reduce_kernel(const KParams p) {
-    constexpr int HPB = 256 / D;   // query heads per CTA
-    const int s = blockIdx.y;
-    const int h = blockIdx.x * HPB + threadIdx.y;
-    const int d = threadIdx.x;
-    if (h >= p.Hq) return;
-    int L = __ldg(p.lens + s);
-    const int cap = p.max_blocks * kBlockTokens;
-    L = L < 0 ? 0 : (L > cap ? cap : L);
-    int n = num_parts(L);
-    if (n <= 1) return;                       // written directly by the main kernel
-    if (n > p.grid_parts) n = p.grid_parts;   // flagged by the main kernel
-    const size_t row = (size_t)s * p.Hq + h;
-    const float2* ml = p.part_ml + row * p.part_stride;
-    const float* po = p.part_o + row * p.part_stride * D;
+decode_reduce_kernel(const KParams p, int num_rows) {
+    constexpr int DPL = D / 32;
+    constexpr int WPR = 8 / RPC;                    // warps per row
+    __shared__ float sm_acc[8][D];
+    __shared__ float sm_l[8];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int row = blockIdx.x * RPC + warp / WPR;  // s * Hq + h
+    const int wr = warp % WPR;                      // this warp's share of the row
+    const bool live = row < num_rows;
+    int n = 0;
+    if (live) {
+        const int s = row / p.Hq;
+        int L = __ldg(p.lens + s);
+        const int cap = p.max_blocks * kBlockTokens;
+        L = L < 0 ? 0 : (L > cap ? cap : L);
+        n = num_parts(L);
+        if (n > p.grid_parts) n = p.grid_parts;     // flagged by the main kernel
+    }
+    // one partition: written directly by the main kernel
+    if (WPR == 1 && (!live || n <= 1)) return;
+    grid_dependency_wait();     // the main kernel's partials are complete and visible
+    const bool work = live && n > 1;
+    const size_t prow = (size_t)(work ? row : 0) * p.part_stride;
+    const float2* ml = p.part_ml + prow;
+    const float* po = p.part_o + prow * D + lane * DPL;
     float M = -INFINITY;
-    for (int jj = 0; jj < n; ++jj) M = fmaxf(M, ml[jj].x);
-    float acc = 0.f, lsum = 0.f;
-    if (M != -INFINITY) {
-        for (int jj = 0; jj < n; ++jj) {
-            const float2 v = ml[jj];
+    if (work)
+        for (int i = lane; i < n; i += 32) M = fmaxf(M, ml[i].x);
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
+    float acc[DPL];
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) acc[k] = 0.f;
+    float lsum = 0.f;
+    if (work && M != -INFINITY) {
+#pragma unroll 8
+        for (int i = wr; i < n; i += WPR) {
+            const float2 v = ml[i];
             const float wt = fast_exp2(v.x - M);
-            acc += wt * po[(size_t)jj * D + d];
             lsum += wt * v.y;
+            if constexpr (DPL == 4) {
+                const float4 o = *reinterpret_cast<const float4*>(po + (size_t)i * D);
+                acc[0] += wt * o.x; acc[1] += wt * o.y; acc[2] += wt * o.z; acc[3] += wt * o.w;
+            } else {
+                const float2 o = *reinterpret_cast<const float2*>(po + (size_t)i * D);
+                acc[0] += wt * o.x; acc[1] += wt * o.y;
+            }
         }
     }
-    const float val = lsum > 0.f ? acc / lsum : 0.f;
-    if constexpr (sizeof(OutT) == 2)
-        reinterpret_cast<__nv_bfloat16*>(p.out)[row * D + d] = __float2bfloat16_rn(val);
-    else
-        reinterpret_cast<float*>(p.out)[row * D + d] = val;
+    if constexpr (WPR > 1) {
+#pragma unroll
+        for (int k = 0; k < DPL; ++k) sm_acc[warp][lane * DPL + k] = acc[k];
+        if (lane == 0) sm_l[warp] = lsum;
+        __syncthreads();
+        if (!work || wr != 0) return;
+        lsum = 0.f;
+#pragma unroll
+        for (int k = 0; k < DPL; ++k) acc[k] = 0.f;
+        for (int w = 0; w < WPR; ++w) {
+            lsum += sm_l[w];
+#pragma unroll
+            for (int k = 0; k < DPL; ++k) acc[k] += sm_acc[w][lane * DPL + k];
+        }
+    }
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) {
+        const size_t idx = (size_t)row * D + lane * DPL + k;
+        if constexpr (sizeof(OutT) == 2)
+            reinterpret_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(acc[k] * inv);
+        else
+            reinterpret_cast<float*>(p.out)[idx] = acc[k] * inv;
+    }
 }
 
 // Launch configuration of the main kernels.
-constexpr int kWarps = 4;
-constexpr int kStagesBf16 = 3;
+// 4 warps x 2 ring stages (64 KB of shared memory for head_dim 128, 3 CTAs per SM)
+// measured fastest on GB300 among 1-8 warps x 2-6 stages.
+#ifndef PA_DECODE_WARPS
+#define PA_DECODE_WARPS 4
+#endif
+#ifndef PA_DECODE_STAGES
+#define PA_DECODE_STAGES 2
+#endif
+constexpr int kWarps = PA_DECODE_WARPS;        // warps per CTA
+constexpr int kStagesBf16 = PA_DECODE_STAGES;  // ring stages per warp (bf16)
 constexpr int kStagesF32 = 2;
 
 template <int D>
@@ -550,6 +618,45 @@ cudaError_t set_smem(K kernel, int bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
+// Launch with programmatic stream serialisation: the kernel may start while the
+// previous kernel of the stream finishes, and waits (griddepcontrol.wait) before
+// reading anything that kernel writes.
+#ifndef PA_USE_PDL
+#define PA_USE_PDL 1
+#endif
+
+template <typename K>
+cudaError_t launch_dependent(K kernel, dim3 grid, dim3 block, int smem, cudaStream_t stream,
+                             const KParams& kp) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = PA_USE_PDL;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, kp);
+}
+
+template <typename K>
+cudaError_t launch_dependent_rows(K kernel, dim3 grid, dim3 block, cudaStream_t stream,
+                                  const KParams& kp, int rows) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = PA_USE_PDL;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, kp, rows);
+}
+
 template <int D>
 cudaError_t launch_for_dim(const KParams& kp, const DecodeArgs& a, cudaStream_t stream) {
     const dim3 grid(a.grid_parts, a.num_kv_heads, a.num_seqs);
@@ -557,28 +664,33 @@ cudaError_t launch_for_dim(const KParams& kp, const DecodeArgs& a, cudaStream_t 
     if (a.dtype == PA_BF16) {
         auto k = decode_bf16_kernel<D, kWarps, kStagesBf16>;
         if ((e = set_smem(k, bf16_smem<D>())) != cudaSuccess) return e;
-        k<<<grid, kWarps * 32, bf16_smem<D>(), stream>>>(kp);
+        e = launch_dependent(k, grid, dim3(kWarps * 32), bf16_smem<D>(), stream, kp);
     } else {
         auto k = decode_f32_kernel<D, kWarps, kStagesF32>;
         if ((e = set_smem(k, f32_smem<D>())) != cudaSuccess) return e;
-        k<<<grid, kWarps * 32, f32_smem<D>(), stream>>>(kp);
+        e = launch_dependent(k, grid, dim3(kWarps * 32), f32_smem<D>(), stream, kp);
     }
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (e != cudaSuccess) return e;
     if (a.grid_parts > 1) {
-        const dim3 rgrid((a.num_q_heads + 256 / D - 1) / (256 / D), a.num_seqs);
-        const dim3 rblock(D, 256 / D);
-        if (a.dtype == PA_BF16)
-            decode_reduce_kernel<D, __nv_bfloat16><<<rgrid, rblock, 0, stream>>>(kp);
-        else
-            decode_reduce_kernel<D, float><<<rgrid, rblock, 0, stream>>>(kp);
-        e = cudaGetLastError();
+        const int rows = a.num_seqs * a.num_q_heads;
+        if (a.grid_parts <= 32) {          // few partitions: a warp per row
+            const dim3 rgrid((rows + 7) / 8);
+            e = a.dtype == PA_BF16
+                    ? launch_dependent_rows(decode_reduce_kernel<D, 8, __nv_bfloat16>, rgrid, dim3(256), stream, kp, rows)
+                    : launch_dependent_rows(decode_reduce_kernel<D, 8, float>, rgrid, dim3(256), stream, kp, rows);
+        } else {                           // many partitions: a CTA per row
+            e = a.dtype == PA_BF16
+                    ? launch_dependent_rows(decode_reduce_kernel<D, 1, __nv_bfloat16>, dim3(rows), dim3(256), stream, kp, rows)
+                    : launch_dependent_rows(decode_reduce_kernel<D, 1, float>, dim3(rows), dim3(256), stream, kp, rows);
+        }
     }
     return e;
 }
 
 }  // namespace
 
-size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_blocks) {
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int /*num_kv_heads*/, int head_dim,
+                              int max_blocks) {
     const int stride = decode_part_stride(max_blocks);
     if (stride <= 1) return 0;
     const size_t rows = (size_t)num_seqs * (size_t)num_q_heads * (size_t)stride;

@@ -38,7 +38,8 @@ struct DecodeArgs {
 inline int decode_part_stride(int max_blocks) {
     return (max_blocks + kPartBlocks - 1) / kPartBlocks;
 }
-size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_blocks);
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                              int max_blocks);
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 

@@ -17,9 +17,10 @@ namespace {
 
 static_assert(PA_NOALLOC_SCRATCH_BYTES % 256 == 0, "scratch size must be a multiple of 256");
 
-// The shared scratch.  Every call uses all of it that it needs; a call leaves
-// its partials behind and the next call overwrites them (the decode kernels
-// never read scratch they did not write in the same call).
+// The shared scratch.  Every call uses as much of it as it needs and leaves its
+// partial results behind; the next call overwrites them (the decode kernels never
+// read partial results they did not write in the same call), so nothing in it
+// needs clearing.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 256;
@@ -49,8 +50,8 @@ extern "C" pa_status pa_decode_attention_noalloc(
     const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
     int32_t head_dim, int32_t max_blocks_per_seq, int32_t max_context_len_hint, int32_t num_blocks,
     float scale, pa_dtype dtype, int32_t* dev_err_flag, void* stream) {
-    const size_t need =
-        pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_blocks_per_seq);
+    const size_t need = pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                 max_blocks_per_seq);
     if (need > (size_t)PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_SCRATCH_LIMIT;
     void* scratch = nullptr;
     if (need > 0) {

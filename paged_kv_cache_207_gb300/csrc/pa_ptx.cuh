@@ -117,6 +117,20 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// ---- programmatic dependent launch ---------------------------------------------
+
+// Wait until the grid this kernel depends on (the previous kernel in the stream)
+// has completed and its memory is visible.  A no-op for ordinary launches.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next kernel in the stream, if launched as a dependent, to start its
+// own set-up now (it still waits for this grid before touching its results).
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- conversions -------------------------------------------------------------
 
 // Pack two fp32 into bf16x2 (round to nearest even): `lo` in bits 0..15.

@@ -92,8 +92,8 @@ class DevicePools:
         q = (wl.q if q is None else q).to(self.k.device).contiguous()
         tables = self.tables if tables is None else tables
         out = torch.empty_like(q)
-        ws_bytes = pk.decode_workspace_size(q.shape[0], wl.num_q_heads, wl.head_dim, tables.shape[1])
-        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=self.k.device)
+        ws = pk.decode_workspace(q.shape[0], wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                 tables.shape[1], device=self.k.device)
         pk.decode_attention(out, q, self.k, self.v, tables, lens, wl.scale, workspace=ws,
                             max_context_len_hint=hint, err_flag=self.err)
         return out

@@ -48,11 +48,11 @@ def test_status_strings(native):
 def test_workspace_size_formula(native):
     L = native.lib()
     # one partition (max 32 blocks = 512 tokens) needs no workspace
-    assert L.pa_decode_workspace_size(4, 12, 64, 7) == 0
-    assert L.pa_decode_workspace_size(4, 12, 64, 32) == 0
+    assert L.pa_decode_workspace_size(4, 12, 12, 64, 7) == 0
+    assert L.pa_decode_workspace_size(4, 12, 12, 64, 32) == 0
     # 33 blocks -> 2 partitions: S*Hq*2 rows of (D floats + (max, sum))
-    assert L.pa_decode_workspace_size(4, 12, 64, 33) == 4 * 12 * 2 * (64 * 4 + 8)
-    assert L.pa_decode_workspace_size(8, 32, 128, 8192) == 8 * 32 * 256 * (128 * 4 + 8)
+    assert L.pa_decode_workspace_size(4, 12, 12, 64, 33) == 4 * 12 * 2 * (64 * 4 + 8)
+    assert L.pa_decode_workspace_size(8, 32, 8, 128, 8192) == 8 * 32 * 256 * (128 * 4 + 8)
 
 
 def _decode(L, **kw):

@@ -233,7 +233,7 @@ def test_device_errors_are_flagged_and_skipped_without_faulting():
     tables = torch.tensor([[0, 1, 2, 3, 4, 5, 6, 7] * 9], dtype=torch.int32, device="cuda")
     q1 = torch.zeros(1, 4, D, dtype=torch.bfloat16, device="cuda")
     out1 = torch.empty_like(q1)
-    ws = torch.empty(pk.decode_workspace_size(1, 4, D, 72), dtype=torch.uint8, device="cuda")
+    ws = pk.decode_workspace(1, 4, Hkv, D, 72)
     pk.decode_attention(out1, q1, kp, vp, tables, torch.tensor([1000], dtype=torch.int32, device="cuda"),
                         0.125, workspace=ws, max_context_len_hint=300, err_flag=err)
     torch.cuda.synchronize()
@@ -249,8 +249,8 @@ def test_output_guard_regions_untouched():
     n = wl.q.numel()
     buf = torch.full((n + 2048,), 7.0, dtype=torch.bfloat16, device="cuda")
     out = buf[1024:1024 + n].view(wl.q.shape)
-    ws_b = pk.decode_workspace_size(2, 8, 128, wl.max_blocks)
-    ws = torch.empty(ws_b + 4096, dtype=torch.uint8, device="cuda")
+    ws_b = pk.decode_workspace_size(2, 8, 2, 128, wl.max_blocks)
+    ws = torch.zeros(ws_b + 4096, dtype=torch.uint8, device="cuda")
     pk.decode_attention(out, wl.q.cuda(), dp.k, dp.v, dp.tables, lens, wl.scale, workspace=ws)
     torch.cuda.synchronize()
     assert torch.all(buf[:1024] == 7.0) and torch.all(buf[1024 + n:] == 7.0)
@@ -282,3 +282,37 @@ def test_named_workload_full_size_sampled(name, nsample):
     got = np.stack([as_f64(out[s, h]) for s, h in pairs])
     assert_close(wl, got, want, name)
     assert torch.isfinite(out.float()).all()
+
+
+def test_group_boundaries_of_the_partition_merge():
+    # 16 partitions fill one merge group; 17 and 33 need a second and third group
+    P = pk.PARTITION_TOKENS
+    lens = [16 * P, 16 * P + 1, 17 * P, 33 * P + 100, 5]
+    wl = W.make_decode_workload("groups", context_lens=np.array(lens) - 1, num_q_heads=8,
+                                num_kv_heads=2, head_dim=128, dtype="bf16", seed=77, device="cuda")
+    dp = DevicePools(wl, canary=False)
+    out = dp.run_step()
+    pairs = _all_pairs(wl)
+    want = oracle_contig(wl, pairs)
+    assert_close(wl, as_f64(out).reshape(len(pairs), 128), want, "merge groups")
+    assert int(dp.err.item()) == 0
+
+
+def test_repeated_calls_on_one_workspace_give_the_same_bits():
+    # whatever an earlier call left in the workspace does not leak into the next one
+    wl = W.make_decode_workload("reuse", context_lens=[3000, 700, 9000], num_q_heads=32,
+                                num_kv_heads=8, head_dim=128, dtype="bf16", seed=9, device="cuda")
+    dp = DevicePools(wl, canary=False)
+    k_new, v_new, start, cu, lens = dp.step_inputs()
+    pk.append_kv(dp.k, dp.v, k_new, v_new, dp.tables, start, cu, err_flag=dp.err)
+    ws = pk.decode_workspace(3, 32, 8, 128, wl.max_blocks)
+    outs = []
+    for _ in range(3):
+        out = torch.empty_like(wl.q)
+        pk.decode_attention(out, wl.q, dp.k, dp.v, dp.tables, lens, wl.scale, workspace=ws,
+                            err_flag=dp.err)
+        torch.cuda.synchronize()
+        outs.append(out)
+        ws.fill_(0x7F)     # garbage for the next call
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+    assert int(dp.err.item()) == 0

@@ -1,0 +1,89 @@
+"""Planted mistakes in the oracle must fail its pins (no GPU needed).
+
+Each case copies the oracle's C source, plants one plausible slip -- a dropped
+term, a flipped sign, a wrong block / slot / head index, a missing
+normalisation, a wrong rounding -- builds the copy, and runs the pins of
+test_oracle_pins.py against it.  At least one pin must fail for every mutant;
+otherwise the pins would not be able to tell that mistake from the right answer.
+The mistakes are planted on the CPU only, in a temporary copy.
+"""
+import os
+
+import pytest
+
+import test_oracle_pins as pins
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+F32, BF16 = 0, 1
+
+MUTANTS = {
+    "no_max_subtraction": ("x[t] = exp(x[t] - xmax);", "x[t] = exp(x[t]);"),
+    "score_sign": ("x[t] = scale * acc;", "x[t] = -scale * acc;"),
+    "scale_dropped": ("x[t] = scale * acc;", "x[t] = acc;"),
+    "no_normalisation": ("double p = x[t] / denom;", "double p = x[t];"),
+    "context_short_by_one": ("    for (int t = 0; t < L; ++t) {\n        int64_t blk;",
+                             "    for (int t = 0; t < L - 1; ++t) {\n        int64_t blk;"),
+    "wrong_slot": ("size_t e = pool_elem(blk, g, t % ORACLE_BLOCK, d, Hkv, D, X);",
+                   "size_t e = pool_elem(blk, g, (t + 1) % ORACLE_BLOCK, d, Hkv, D, X);"),
+    "wrong_block": ("int32_t b = tables[(size_t)s * (size_t)max_blocks + (size_t)lb];",
+                    "int32_t b = tables[(size_t)s * (size_t)max_blocks];"),
+    "gqa_modulo_map": ("int g = h / (Hq / Hkv);", "int g = h % Hkv;"),
+    "query_of_wrong_head": ("qv[d] = load_elem(q, ((size_t)s * Hq + h) * (size_t)D + d, dtype);",
+                            "qv[d] = load_elem(q, ((size_t)s * Hq + g) * (size_t)D + d, dtype);"),
+    "round_down": ("double r = rint(m / ulp) * ulp;", "double r = floor(m / ulp) * ulp;"),
+    "no_subnormal_spacing": ("    if (ex < -126) ex = -126;     /* subnormal range keeps the fixed spacing */\n", ""),
+    "widen_shift": ("uint32_t u = ((uint32_t)b) << 16;", "uint32_t u = ((uint32_t)b) << 15;"),
+    "append_wrong_slot": ("size_t dst = pool_elem(blk, h, p % ORACLE_BLOCK, d, Hkv, D, X);",
+                          "size_t dst = pool_elem(blk, h, (p + 1) % ORACLE_BLOCK, d, Hkv, D, X);"),
+    "append_first_row_only": ("size_t row = (size_t)(cu_new[s] + i);", "size_t row = (size_t)(cu_new[s]);"),
+    "copy_keys_only": ("        memmove((char*)v_pool + (size_t)dst * block_bytes, (char*)v_pool + (size_t)src * block_bytes, block_bytes);\n", ""),
+}
+
+
+def _pins():
+    yield "bf16_cases", lambda o: pins.test_bf16_rounding_hand_worked_cases(o)
+    yield "bf16_torch", lambda o: pins.test_bf16_rounding_matches_torch_on_fp32_values(o)
+    yield "bf16_widen", lambda o: pins.test_bf16_widening_is_exact(o)
+    for dt in (F32, BF16):
+        yield f"single_token_{dt}", lambda o, dt=dt: pins.test_single_token_context_returns_its_value_row(o, dt)
+        yield f"zero_query_{dt}", lambda o, dt=dt: pins.test_zero_query_gives_mean_of_values(o, dt)
+        yield f"paged_contig_{dt}", lambda o, dt=dt: pins.test_paged_equals_contiguous_and_batched_equals_alone(o, dt)
+    yield "two_token", lambda o: pins.test_two_token_closed_form(o)
+    for hot in (0, 37):
+        yield f"dominant_{hot}", lambda o, hot=hot: pins.test_dominant_key_selects_its_value(o, hot)
+    yield "positions", lambda o: pins.test_positions_reach_the_right_block_and_slot(o)
+    yield "gqa", lambda o: pins.test_gqa_query_head_reads_kv_head_h_div_group(o)
+    yield "zero_len", lambda o: pins.test_zero_length_context_is_zero(o)
+    yield "large_scores", lambda o: pins.test_large_scores_do_not_overflow(o)
+    yield "sdpa", lambda o: pins.test_matches_torch_sdpa_on_contiguous_rows(o, BF16, 14, 2, 64)
+    yield "append", lambda o: pins.test_append_writes_only_its_slots_and_reads_back(o)
+    yield "append_bad", lambda o: pins.test_append_rejects_bad_block_and_position(o)
+    yield "copy", lambda o: pins.test_copy_block_copies_every_byte_of_both_pools(o)
+
+
+def test_every_pin_passes_on_the_unmutated_source(oracle_mod, tmp_path):
+    src = open(os.path.join(ROOT, "oracle", "pa_oracle.c")).read()
+    path = tmp_path / "same.c"
+    path.write_text(src)
+    so = oracle_mod.compile_source(str(path), str(tmp_path / "same.so"))
+    with oracle_mod.use_library(so):
+        for name, pin in _pins():
+            pin(oracle_mod)
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS))
+def test_planted_mistake_fails_a_pin(oracle_mod, tmp_path, mutant):
+    old, new = MUTANTS[mutant]
+    src = open(os.path.join(ROOT, "oracle", "pa_oracle.c")).read()
+    assert src.count(old) == 1, f"mutation site for {mutant} not found exactly once"
+    path = tmp_path / f"{mutant}.c"
+    path.write_text(src.replace(old, new))
+    so = oracle_mod.compile_source(str(path), str(tmp_path / f"{mutant}.so"))
+    caught = []
+    with oracle_mod.use_library(so):
+        for name, pin in _pins():
+            try:
+                pin(oracle_mod)
+            except (AssertionError, ValueError):
+                caught.append(name)
+    assert caught, f"no pin fails when the oracle has the mistake '{mutant}'"

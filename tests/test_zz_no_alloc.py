@@ -55,9 +55,9 @@ def test_noalloc_decode_matches_workspace_decode_on_two_calls():
                _batch(W, pk, 32, [900, 2500, 5, 1536])]
     for wl, kp, vp, tables, lens in batches:
         S = wl.num_seqs
-        need = pk.decode_workspace_size(S, 32, 128, wl.max_blocks)
+        need = pk.decode_workspace_size(S, 32, 8, 128, wl.max_blocks)
         assert 0 < need <= pk._native.NOALLOC_SCRATCH_BYTES
-        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
         ref = torch.empty_like(wl.q)
         pk.decode_attention(ref, wl.q, kp, vp, tables, lens, wl.scale, workspace=ws, err_flag=err)
         out = torch.full_like(wl.q, float("nan"))
@@ -73,7 +73,7 @@ def test_noalloc_decode_matches_workspace_decode_on_two_calls():
 
     # a call that would need more than the built-in scratch is refused, nothing launched
     big_blocks = 8192
-    need = pk.decode_workspace_size(256, 32, 128, big_blocks)
+    need = pk.decode_workspace_size(256, 32, 8, 128, big_blocks)
     assert need > pk._native.NOALLOC_SCRATCH_BYTES
     wl, kp, vp, tables, lens = batches[1]
     st = L.pa_decode_attention_noalloc(16, 16, kp.data_ptr(), vp.data_ptr(), 16, 16, 256, 32, 8,
