@@ -508,6 +508,8 @@ def run_replay(args, rank, world, local):
     tokens = all_sum(float(st.generated_tokens), world)
     dbytes = all_sum(float(st.decode_bytes), world)
     peaks = load_peaks() or {}
+    from paged_kv_cache_207_gb300.replay import contiguous_account, paged_account
+    ca, pa_ = contiguous_account(rw, max_new_tokens=192), paged_account(rw)
     return {
         "metric": METRIC, "value": round(dbytes / gpu_s / 1e9, 1), "unit": "GB/s",
         "n_gpus": world, "steps": st.iterations, "warmup": args.warmup,
@@ -526,6 +528,13 @@ def run_replay(args, rank, world, local):
                    "peak_physical_slots": st.peak_physical_slots,
                    "mean_slot_utilisation": round(st.mean_slot_utilisation, 4),
                    "wall_s": round(wall, 3), "gpu_s": round(gpu_s, 4)},
+        "allocators": {
+            "contiguous": {"peak_slots_held": ca.peak_slots_held,
+                           "mean_slot_utilisation": round(ca.mean_slot_utilisation, 4),
+                           "steps_to_drain": ca.steps_to_drain},
+            "paged": {"peak_slots_held": pa_.peak_slots_held,
+                      "mean_slot_utilisation": round(pa_.mean_slot_utilisation, 4),
+                      "steps_to_drain": pa_.steps_to_drain}},
         "gpu_launches": st.launches,
     }
 

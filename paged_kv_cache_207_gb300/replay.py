@@ -260,3 +260,51 @@ class Replay:
         if int(self.err.item()) != 0:
             raise RuntimeError(f"device error flag {int(self.err.item())} during the replay")
         return self.stats
+
+
+# ---- the control: a contiguous per-sequence allocator ------------------------------
+
+@dataclass
+class AllocatorAccount:
+    peak_slots_held: int
+    mean_slot_utilisation: float
+    steps_to_drain: int
+
+
+def contiguous_account(rw, max_new_tokens: int | None = None, slots: int | None = None) -> AllocatorAccount:
+    """Replay the same requests through a contiguous allocator (spindle, "Paging": a
+    contiguous buffer is sized at admission to prompt + max_new_tokens, the only bound
+    known then, and held for the request's whole lifetime).  Same FCFS admission, one
+    token per running request per step; a fork cannot share, so each copy-on-write
+    child holds its own buffer.  Host accounting only."""
+    cap = int(rw.gen_lens.max()) if max_new_tokens is None else max_new_tokens
+    total = rw.num_blocks * BLOCK if slots is None else slots
+    waiting = collections.deque(range(rw.num_seqs))
+    running: list[int] = []
+    done_gen = [0] * rw.num_seqs
+    held = steps = peak = 0
+    util_sum = 0.0
+    while waiting or running:
+        while waiting and held + int(rw.prompt_lens[waiting[0]]) + cap <= total:
+            i = waiting.popleft()
+            held += int(rw.prompt_lens[i]) + cap
+            running.append(i)
+        if not running:
+            raise RuntimeError("a request does not fit the pool")
+        peak = max(peak, held)
+        tokens = sum(int(rw.prompt_lens[i]) + done_gen[i] + 1 for i in running)
+        util_sum += tokens / held
+        steps += 1
+        for i in running:
+            done_gen[i] += 1
+        for i in list(running):
+            if done_gen[i] >= int(rw.gen_lens[i]):
+                running.remove(i)
+                held -= int(rw.prompt_lens[i]) + cap
+    return AllocatorAccount(peak, util_sum / steps, steps)
+
+
+def paged_account(rw) -> AllocatorAccount:
+    """The block-paged schedule of ``Replay`` run on the host alone."""
+    st = Replay(rw, device=None).run()
+    return AllocatorAccount(st.peak_physical_slots, st.mean_slot_utilisation, st.iterations)

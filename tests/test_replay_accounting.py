@@ -1,0 +1,55 @@
+"""Contiguous versus paged slot accounting on the replay trace (no GPU needed).
+
+spindle, "Paging": 64 requests replayed through both allocators with 8192 token
+slots and block size 16 give peak slots 8161 -> 3264 (2.50x less), mean slot
+utilisation 0.574 -> 0.929 and steps to drain 236 -> 192.  The synthetic trace
+here is not the page's trace, so the numbers differ; what must hold is the kind
+of result: paging holds fewer slots at peak, uses them better, and drains in no
+more steps.  The contiguous accounting is also checked against a brute-force
+recount.
+"""
+import numpy as np
+import pytest
+
+
+@pytest.fixture(scope="module")
+def accounts():
+    from paged_kv_cache_207_gb300 import build
+    build.build()
+    from paged_kv_cache_207_gb300 import workloads as W
+    from paged_kv_cache_207_gb300.replay import contiguous_account, paged_account
+    rw = W.spindle_replay(values=False)
+    return rw, contiguous_account(rw, max_new_tokens=192), paged_account(rw)
+
+
+def test_paging_holds_fewer_slots_uses_them_better_and_drains_no_slower(accounts):
+    rw, contig, paged = accounts
+    assert paged.peak_slots_held < contig.peak_slots_held
+    assert paged.mean_slot_utilisation > contig.mean_slot_utilisation
+    assert paged.steps_to_drain <= contig.steps_to_drain
+    assert contig.peak_slots_held <= 8192 and paged.peak_slots_held <= 8192
+    # the waste of a paged sequence is below one block, so utilisation is close to 1
+    assert paged.mean_slot_utilisation > 0.9
+
+
+def test_contiguous_accounting_by_brute_force(accounts):
+    rw, contig, _ = accounts
+    # recount: simulate slot by slot with explicit per-request intervals
+    cap, total = 192, 8192
+    start = {}
+    t = 0
+    queue = list(range(rw.num_seqs))
+    live = {}
+    steps = 0
+    peak = 0
+    while queue or live:
+        while queue and sum(v for v in live.values()) + rw.prompt_lens[queue[0]] + cap <= total:
+            i = queue.pop(0)
+            live[i] = int(rw.prompt_lens[i]) + cap
+            start[i] = steps
+        peak = max(peak, sum(live.values()))
+        steps += 1
+        for i in list(live):
+            if steps - start[i] >= rw.gen_lens[i]:
+                del live[i]
+    assert (peak, steps) == (contig.peak_slots_held, contig.steps_to_drain)
