@@ -98,6 +98,19 @@ def decode_bytes(wl) -> int:
     return kv + qo + table + partial
 
 
+def logical_kv_bytes(wl) -> int:
+    e = 2 if wl.dtype == "bf16" else 4
+    return int(((wl.context_lens.astype(np.int64) + 1) * 2 * wl.num_kv_heads * wl.head_dim * e).sum())
+
+
+def unique_kv_bytes(wl, shared: int) -> int:
+    """K/V bytes when the shared prefix is counted once (the bytes that exist in the pool)."""
+    e = 2 if wl.dtype == "bf16" else 4
+    per_token = 2 * wl.num_kv_heads * wl.head_dim * e
+    private = (wl.context_lens.astype(np.int64) + 1 - shared).clip(min=0).sum()
+    return int((shared + private) * per_token)
+
+
 def append_bytes(wl) -> int:
     """New rows read and written into the pools, plus start / cu / table reads."""
     e = 2 if wl.dtype == "bf16" else 4
@@ -246,12 +259,22 @@ def run_ours(args, rank, world, local):
     torch.cuda.empty_cache()
     stream = torch.cuda.current_stream()
 
+    shared = args.shared_prefix
+
+    def decode(q_, tab_, lens_):
+        if shared:
+            pk.decode_attention_shared_prefix(out, q_, kp, vp, tab_, lens_, wl.scale, shared,
+                                              workspace=ws, max_context_len_hint=hint,
+                                              err_flag=err, stream=stream)
+        else:
+            pk.decode_attention(out, q_, kp, vp, tab_, lens_, wl.scale, workspace=ws,
+                                max_context_len_hint=hint, err_flag=err, stream=stream)
+
     def step(ev_d0=None, ev_d1=None):
         pk.append_kv(kp, vp, k_new, v_new, tables, start, cu, err_flag=err, stream=stream)
         if ev_d0 is not None:
             ev_d0.record(stream)
-        pk.decode_attention(out, q, kp, vp, tables, lens, wl.scale, workspace=ws,
-                            max_context_len_hint=hint, err_flag=err, stream=stream)
+        decode(q, tables, lens)
         if ev_d1 is not None:
             ev_d1.record(stream)
 
@@ -312,8 +335,7 @@ def run_ours(args, rank, world, local):
                          (d_lens, h_lens), (d_tab, h_tab)):
             dst.copy_(src, non_blocking=True)
         pk.append_kv(kp, vp, d_k, d_v, d_tab, d_start, d_cu, err_flag=err, stream=stream)
-        pk.decode_attention(out, d_q, kp, vp, d_tab, d_lens, wl.scale, workspace=ws,
-                            max_context_len_hint=hint, err_flag=err, stream=stream)
+        decode(d_q, d_tab, d_lens)
         h_out.copy_(out, non_blocking=True)
 
     for _ in range(max(3, args.warmup)):
@@ -339,7 +361,8 @@ def run_ours(args, rank, world, local):
         peak, peak_src = 6800.0, "fallback"
     dbytes = decode_bytes(wl)
     achieved = dbytes / (dec_ms / 1e3) / 1e9
-    launches_per_step = 1 + 1 + (1 if int(math.ceil(hint / 512)) > 1 else 0)
+    launches_per_step = 1 + 1 + (1 if int(math.ceil(hint / 512)) > 1 or shared >= 512 else 0) + \
+        (1 if shared >= 512 else 0)
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
@@ -349,12 +372,17 @@ def run_ours(args, rank, world, local):
         "config": {"workload": args.workload, "num_seqs_per_gpu": S, "num_q_heads": Hq,
                    "num_kv_heads": Hkv, "head_dim": D, "block_size": 16,
                    "context_tokens_after_append": int((wl.context_lens + 1).sum()),
-                   "max_context": int(hint), "step": "pa_append_kv (1 token/seq) + pa_decode_attention",
+                   "max_context": int(hint),
+                   "step": "pa_append_kv (1 token/seq) + " + ("pa_decode_attention_shared_prefix"
+                                                               if shared else "pa_decode_attention"),
+                   "shared_prefix_tokens": shared,
                    "layers_for_tokens_per_s": layers,
                    "l2": "inputs larger than L2 (K/V pools %.2f GB per GPU vs 129 MB L2), no flush"
                          % (2 * kp.numel() * kp.element_size() / 1e9),
                    "parallelism": f"replicas x{world} (sequences sharded by rank, no collective)"},
         "pct_of_peak_hbm": round(100.0 * value / peak, 2),
+        **({"unique_kv_bytes_per_step": unique_kv_bytes(wl, shared),
+            "logical_kv_bytes_per_step": logical_kv_bytes(wl)} if shared else {}),
         "tokens_per_s": round(tokens_per_s, 1),
         "roofline": {"kernel": "pa_decode_attention (main kernel + partition merge)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
@@ -547,6 +575,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3-8b_batch256")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shared-prefix", type=int, default=0,
+                    help="decode through pa_decode_attention_shared_prefix with this many shared "
+                         "tokens (the llama3-8b_shared_prefix workload shares 4096)")
     ap.add_argument("--num-seqs", type=int, default=0,
                     help="override the workload's sequence count (smaller cases for profiling)")
     args = ap.parse_args()

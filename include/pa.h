@@ -161,6 +161,34 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, cons
                               int32_t* dev_err_flag, void* stream);
 
 /*
+ * pa_decode_attention_shared_prefix -- pa_decode_attention for a batch whose
+ * sequences all share their first shared_prefix_tokens positions in the same
+ * physical blocks (the layout refcounted copy-on-write forks leave behind;
+ * spindle, "Paging").  The whole 512-token partitions of the prefix are read
+ * once per kv head and applied to the queries of every sequence on the tensor
+ * cores; the rest of each context goes through the ordinary kernel; the two
+ * are merged with their log-sum-exp weights.
+ *   Same arguments as pa_decode_attention plus shared_prefix_tokens (a multiple
+ *   of 16).  The caller guarantees that block_tables[s][b] == block_tables[0][b]
+ *   for every s and every b < shared_prefix_tokens / 16, and that every
+ *   context_lens[s] >= shared_prefix_tokens; the kernels read the prefix through
+ *   sequence 0's table row.  bf16 only (fp32 returns PA_ERR_UNSUPPORTED when a
+ *   whole partition is shared).  A prefix shorter than one partition falls back
+ *   to pa_decode_attention.  The workspace is the one pa_decode_workspace_size
+ *   gives (never 0 here when a partition is shared).
+ */
+pa_status pa_decode_attention_shared_prefix(void* out, const void* q, const void* k_pool,
+                                            const void* v_pool, const int32_t* block_tables,
+                                            const int32_t* context_lens, int32_t num_seqs,
+                                            int32_t num_q_heads, int32_t num_kv_heads,
+                                            int32_t head_dim, int32_t max_blocks_per_seq,
+                                            int32_t max_context_len_hint, int32_t num_blocks,
+                                            float scale, pa_dtype dtype,
+                                            int32_t shared_prefix_tokens, void* workspace,
+                                            size_t workspace_bytes, int32_t* dev_err_flag,
+                                            void* stream);
+
+/*
  * pa_decode_attention_noalloc -- pa_decode_attention for callers that cannot
  * allocate device memory.  (The pages have no counterpart; this entry point is
  * this library's own addition.)

@@ -28,7 +28,8 @@ DEV_ERR_BAD_PAIR = 32
 
 EXPORTED = [
     "pa_status_string", "pa_abi_version", "pa_append_kv", "pa_copy_block",
-    "pa_decode_workspace_size", "pa_decode_attention", "pa_decode_attention_noalloc", "pa_bm_create", "pa_bm_destroy",
+    "pa_decode_workspace_size", "pa_decode_attention", "pa_decode_attention_shared_prefix",
+    "pa_decode_attention_noalloc", "pa_bm_create", "pa_bm_destroy",
     "pa_bm_add_seq", "pa_bm_fork", "pa_bm_free_seq", "pa_bm_blocks_needed",
     "pa_bm_prepare_append", "pa_bm_block_table", "pa_bm_seq_len", "pa_bm_refcount", "pa_bm_stats",
 ]
@@ -70,6 +71,10 @@ def lib() -> ctypes.CDLL:
     L.pa_decode_attention.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32,
                                       ctypes.c_float, ctypes.c_int, p, sz, p, p]
     L.pa_decode_attention.restype = ctypes.c_int
+    L.pa_decode_attention_shared_prefix.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, i32, i32,
+                                                    i32, ctypes.c_float, ctypes.c_int, i32, p, sz,
+                                                    p, p]
+    L.pa_decode_attention_shared_prefix.restype = ctypes.c_int
     L.pa_decode_attention_noalloc.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32,
                                               ctypes.c_float, ctypes.c_int, p, p]
     L.pa_decode_attention_noalloc.restype = ctypes.c_int
@@ -184,6 +189,22 @@ def decode_attention(out, q, k_pool, v_pool, block_tables, context_lens, scale, 
         _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _i32(block_tables, "block_tables"),
         _i32(context_lens, "context_lens"), q.shape[0], q.shape[1], hkv, d, block_tables.shape[1],
         int(max_context_len_hint), nb, float(scale), _dtype_code(q),
+        None if workspace is None else _ptr(workspace), ws_bytes,
+        None if err_flag is None else _i32(err_flag, "err_flag"), _stream(stream)))
+
+
+def decode_attention_shared_prefix(out, q, k_pool, v_pool, block_tables, context_lens, scale,
+                                   shared_prefix_tokens: int, workspace=None,
+                                   max_context_len_hint: int = 0, err_flag=None,
+                                   stream=None) -> None:
+    """decode_attention for a batch whose sequences share their first
+    ``shared_prefix_tokens`` positions in the same physical blocks."""
+    nb, hkv, d = _pool_dims(k_pool)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    check("pa_decode_attention_shared_prefix", lib().pa_decode_attention_shared_prefix(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _i32(block_tables, "block_tables"),
+        _i32(context_lens, "context_lens"), q.shape[0], q.shape[1], hkv, d, block_tables.shape[1],
+        int(max_context_len_hint), nb, float(scale), _dtype_code(q), int(shared_prefix_tokens),
         None if workspace is None else _ptr(workspace), ws_bytes,
         None if err_flag is None else _i32(err_flag, "err_flag"), _stream(stream)))
 

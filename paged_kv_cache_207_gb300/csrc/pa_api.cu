@@ -147,6 +147,66 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, cons
     a.num_blocks = num_blocks;
     a.grid_parts = (bound + pa::kPartTokens - 1) / pa::kPartTokens;
     a.part_stride = pa::decode_part_stride(max_blocks_per_seq);
+    a.first_part = 0;
+    a.scale = scale;
+    a.dtype = dtype;
+    return cuda_status(pa::launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_decode_attention_shared_prefix(
+    void* out, const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
+    const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t max_blocks_per_seq, int32_t max_context_len_hint, int32_t num_blocks,
+    float scale, pa_dtype dtype, int32_t shared_prefix_tokens, void* workspace,
+    size_t workspace_bytes, int32_t* dev_err_flag, void* stream) {
+    if (shared_prefix_tokens < 0 || shared_prefix_tokens % pa::kBlockTokens != 0)
+        return PA_ERR_INVALID_ARG;
+    if ((long long)shared_prefix_tokens > (long long)max_blocks_per_seq * pa::kBlockTokens)
+        return PA_ERR_INVALID_ARG;
+    const int first_part = shared_prefix_tokens / pa::kPartTokens;
+    if (first_part == 0 || num_seqs <= 0)   // nothing whole to share: the ordinary path
+        return pa_decode_attention(out, q, k_pool, v_pool, block_tables, context_lens, num_seqs,
+                                   num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                   max_context_len_hint, num_blocks, scale, dtype, workspace,
+                                   workspace_bytes, dev_err_flag, stream);
+    if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 ||
+        !std::isfinite(scale))
+        return PA_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (num_q_heads / num_kv_heads > 8) return PA_ERR_UNSUPPORTED;
+    if ((long long)max_blocks_per_seq * pa::kBlockTokens > INT32_MAX) return PA_ERR_INVALID_ARG;
+    if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+    if (!out || !q || !k_pool || !v_pool || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
+        return PA_ERR_INVALID_ARG;
+    const size_t need =
+        pa::decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
+    if (need == 0 || !workspace || workspace_bytes < need || !aligned16(workspace))
+        return PA_ERR_INVALID_ARG;
+    const int cap = max_blocks_per_seq * pa::kBlockTokens;
+    int bound = (max_context_len_hint > 0 && max_context_len_hint < cap) ? max_context_len_hint : cap;
+    if (bound < shared_prefix_tokens) bound = shared_prefix_tokens;
+    pa::DecodeArgs a;
+    a.out = out;
+    a.q = q;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.err = dev_err_flag;
+    a.workspace = workspace;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.grid_parts = (bound + pa::kPartTokens - 1) / pa::kPartTokens;
+    if (a.grid_parts < first_part) a.grid_parts = first_part;
+    a.part_stride = pa::decode_part_stride(max_blocks_per_seq);
+    a.first_part = first_part;
     a.scale = scale;
     a.dtype = dtype;
     return cuda_status(pa::launch_decode(a, static_cast<cudaStream_t>(stream)));

@@ -48,7 +48,10 @@ struct KParams {
     float* part_o;      // [S*Hq][part_stride][D]
     float2* part_ml;    // [S*Hq][part_stride] : (max in log2 units, sum)
     int32_t* err;
-    int Hq, Hkv, G, max_blocks, num_blocks, grid_parts, part_stride;
+    int Hq, Hkv, G, max_blocks, num_blocks;
+    int grid_parts;     // partitions covered per (sequence, kv head): first_part + launched
+    int part_stride;
+    int first_part;     // partitions below this are a shared prefix done by the prefix kernel
     float scale_log2;   // scale * log2(e): scores live in log2 units
 };
 
@@ -117,7 +120,7 @@ __device__ __forceinline__ void merge_and_store(const KParams& p, const float* s
             }
         }
         const size_t row = (size_t)s * p.Hq + (size_t)kvh * p.G + g;
-        if (nparts == 1) {
+        if (nparts == 1 && p.first_part == 0) {
             const float v = lsum > 0.f ? acc / lsum : 0.f;
             if constexpr (sizeof(OutT) == 2)
                 reinterpret_cast<__nv_bfloat16*>(p.out)[row * D + d] = __float2bfloat16_rn(v);
@@ -142,7 +145,7 @@ decode_bf16_kernel(const KParams p) {
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = lane >> 2, c = lane & 3;
-    const int j = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+    const int j = blockIdx.x + p.first_part, kvh = blockIdx.y, s = blockIdx.z;
     const int32_t* trow = p.tables + (size_t)s * p.max_blocks;
 
     // This warp's first NST table entries are read before the context length is known,
@@ -155,7 +158,7 @@ decode_bf16_kernel(const KParams p) {
     }
     const int L = clamped_len(p, s);
     const int nparts = num_parts(L);
-    if (j == 0 && kvh == 0 && threadIdx.x == 0 && nparts > p.grid_parts)
+    if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0 && nparts > p.grid_parts)
         raise_flag(p.err, PA_DEV_ERR_HINT);
     if (j >= nparts || aborted(p.err)) return;
 
@@ -344,10 +347,10 @@ decode_f32_kernel(const KParams p) {
     grid_dependency_wait();
     grid_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int j = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+    const int j = blockIdx.x + p.first_part, kvh = blockIdx.y, s = blockIdx.z;
     const int L = clamped_len(p, s);
     const int nparts = num_parts(L);
-    if (j == 0 && kvh == 0 && threadIdx.x == 0 && nparts > p.grid_parts)
+    if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0 && nparts > p.grid_parts)
         raise_flag(p.err, PA_DEV_ERR_HINT);
     if (j >= nparts || aborted(p.err)) return;
 
@@ -535,10 +538,11 @@ decode_reduce_kernel(const KParams p, int num_rows) {
         n = num_parts(L);
         if (n > p.grid_parts) n = p.grid_parts;     // flagged by the main kernel
     }
-    // one partition: written directly by the main kernel
-    if (WPR == 1 && (!live || n <= 1)) return;
-    grid_dependency_wait();     // the main kernel's partials are complete and visible
-    const bool work = live && n > 1;
+    // one partition and no shared prefix: written directly by the main kernel
+    const int min_n = p.first_part > 0 ? 1 : 2;
+    if (WPR == 1 && (!live || n < min_n)) return;
+    grid_dependency_wait();     // the partials of the kernels before are complete and visible
+    const bool work = live && n >= min_n;
     const size_t prow = (size_t)(work ? row : 0) * p.part_stride;
     const float2* ml = p.part_ml + prow;
     const float* po = p.part_o + prow * D + lane * DPL;
@@ -590,6 +594,194 @@ decode_reduce_kernel(const KParams p, int num_rows) {
         else
             reinterpret_cast<float*>(p.out)[idx] = acc[k] * inv;
     }
+}
+
+// ---------------------------------------------------------------------------
+// Shared-prefix kernel (bf16): the partitions that lie inside a prefix shared by
+// every sequence of the batch (the blocks a copy-on-write fork leaves shared,
+// spindle "Paging") are read ONCE per kv head and applied to the queries of all
+// sequences.  Rows are (sequence, query head of this kv head) pairs -- S * G of
+// them -- so the scores form a real matrix product Q[rows x D] K^T[D x 16] per
+// block; FlashAttention-2 style, each consumer warp owns 16 rows, P stays in
+// registers as the A operand of P.V, and V is read with ldmatrix.trans.  A
+// producer warp streams the partition's K/V tiles (through sequence 0's table)
+// into a ring shared by the CTA: `full` barriers complete on the bulk copies,
+// `empty` barriers on the four consumer warps.  Output: the same per-partition
+// partials (o, max, sum) as the main kernel, merged by decode_reduce_kernel.
+// ---------------------------------------------------------------------------
+#ifndef PA_PREFIX_CONSUMERS
+#define PA_PREFIX_CONSUMERS 2
+#endif
+constexpr int kPrefixConsumers = PA_PREFIX_CONSUMERS;  // consumer warps per CTA
+constexpr int kPrefixRows = 16 * kPrefixConsumers;    // rows per CTA
+
+template <int D, int NST>
+constexpr int prefix_smem_bytes() { return NST * 2 * kBlockTokens * D * 2 + 2 * NST * 8; }
+
+template <int D, int NST>
+__global__ void __launch_bounds__((kPrefixConsumers + 1) * 32, 1)
+decode_prefix_bf16_kernel(const KParams p, int num_seqs) {
+    constexpr int TILE = kBlockTokens * D * 2;
+    constexpr int KS = D / 16;     // k-steps of Q.K^T
+    constexpr int NT = D / 8;      // n-tiles of P.V
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = lane >> 2, c = lane & 3;
+    const int kvh = blockIdx.y, j = blockIdx.z;
+    const int rows_total = num_seqs * p.G;
+    const uint32_t ring0 = smem_u32(smem);
+    const uint32_t full0 = ring0 + NST * 2 * TILE, empty0 = full0 + NST * 8;
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int st = 0; st < NST; ++st) {
+            mbar_init(full0 + st * 8, 1);
+            mbar_init(empty0 + st * 8, kPrefixConsumers);
+        }
+        fence_proxy_async_smem();
+    }
+    __syncthreads();
+    const int blk0 = j * kPartBlocks;     // every block of the partition is in the prefix
+
+    if (warp == kPrefixConsumers) {       // ---- producer warp
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            for (int i = 0; i < kPartBlocks; ++i) {
+                const int st = i % NST;
+                // stage st is free once its previous use (i - NST) was consumed
+                if (i >= NST && !mbar_wait_bounded(empty0 + st * 8, ((i / NST) - 1) & 1, kWaitLimitNs)) {
+                    raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
+                    break;
+                }
+                int32_t blk = __ldg(p.tables + blk0 + i);     // sequence 0's row
+                if (blk < 0 || blk >= p.num_blocks) {
+                    raise_flag(p.err, PA_DEV_ERR_BAD_BLOCK);
+                    blk = -1;
+                }
+                const uint32_t bar = full0 + st * 8;
+                if (blk >= 0) {
+                    const size_t off = ((size_t)blk * p.Hkv + kvh) * (size_t)TILE;
+                    fence_proxy_async_smem();
+                    mbar_arrive_expect_tx(bar, 2 * TILE);
+                    bulk_g2s(ring0 + st * 2 * TILE, p.k_pool + off, TILE, bar, pol);
+                    bulk_g2s(ring0 + st * 2 * TILE + TILE, p.v_pool + off, TILE, bar, pol);
+                } else {
+                    // nothing to copy: complete the phase so the consumers move on; they
+                    // see the flag and the stale stage only feeds outputs already flagged
+                    mbar_arrive_expect_tx(bar, 0);
+                }
+            }
+        }
+        grid_dependency_wait();
+        return;
+    }
+
+    // ---- consumer warps: rows rr0 = r and rr1 = r + 8 of this warp's 16
+    const int rbase = blockIdx.x * kPrefixRows + warp * 16;
+    const int rr0 = rbase + r, rr1 = rbase + r + 8;
+    auto qrow = [&](int rr) -> const uint16_t* {
+        const int sq = rr / p.G, g = rr - (rr / p.G) * p.G;
+        return reinterpret_cast<const uint16_t*>(p.q) + ((size_t)sq * p.Hq + (size_t)kvh * p.G + g) * D;
+    };
+    uint32_t qa[KS][4];
+    {
+        const bool v0 = rr0 < rows_total, v1 = rr1 < rows_total;
+        const uint16_t* q0 = qrow(v0 ? rr0 : 0);
+        const uint16_t* q1 = qrow(v1 ? rr1 : 0);
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            qa[kk][0] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(q0 + 16 * kk + 2 * c)) : 0u;
+            qa[kk][1] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(q1 + 16 * kk + 2 * c)) : 0u;
+            qa[kk][2] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(q0 + 16 * kk + 8 + 2 * c)) : 0u;
+            qa[kk][3] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(q1 + 16 * kk + 8 + 2 * c)) : 0u;
+        }
+    }
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float o[NT][4];
+#pragma unroll
+    for (int i = 0; i < NT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    const int km = lane >> 3;
+    const uint32_t k_lane = (uint32_t)((((km & 1) * 16) + (km >> 1) * 8 + (lane & 7)) * 16);
+    const uint32_t v_lane = (uint32_t)((((km >> 1) * 16) + (km & 1) * 8 + (lane & 7)) * 16);
+    bool failed = false;
+    for (int i = 0; i < kPartBlocks; ++i) {
+        const int st = i % NST;
+        if (!mbar_wait_bounded(full0 + st * 8, (i / NST) & 1, kWaitLimitNs)) {
+            failed = true;
+            break;
+        }
+        const uint32_t kt = ring0 + st * 2 * TILE, vt = kt + TILE;
+        // two independent accumulator chains (even / odd k-steps) halve the MMA latency chain
+        float sc[2][4], sx[2][4];
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[t][e] = sx[t][e] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            uint32_t b0, b1, b2, b3;   // (tokens 0-7: dims lo, hi), (tokens 8-15: dims lo, hi)
+            ldmatrix_x4(kt + kk * 512 + k_lane, b0, b1, b2, b3);
+            float (&a)[2][4] = (kk & 1) ? sx : sc;
+            mma_bf16_16816(a[0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+            mma_bf16_16816(a[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+        }
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[t][e] = (sc[t][e] + sx[t][e]) * p.scale_log2;
+        float bm0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+        float bm1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, 1));
+        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, 2));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, 1));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, 2));
+        const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+        const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+        m0 = mn0;
+        m1 = mn1;
+        const uint32_t a0 = pack_bf16x2(fast_exp2(sc[0][0] - mn0), fast_exp2(sc[0][1] - mn0));
+        const uint32_t a1 = pack_bf16x2(fast_exp2(sc[0][2] - mn1), fast_exp2(sc[0][3] - mn1));
+        const uint32_t a2 = pack_bf16x2(fast_exp2(sc[1][0] - mn0), fast_exp2(sc[1][1] - mn0));
+        const uint32_t a3 = pack_bf16x2(fast_exp2(sc[1][2] - mn1), fast_exp2(sc[1][3] - mn1));
+        l0 = l0 * al0 + (bf16_lo_to_f32(a0) + bf16_hi_to_f32(a0) + bf16_lo_to_f32(a2) + bf16_hi_to_f32(a2));
+        l1 = l1 * al1 + (bf16_lo_to_f32(a1) + bf16_hi_to_f32(a1) + bf16_lo_to_f32(a3) + bf16_hi_to_f32(a3));
+        // the running maxima rarely move after the first blocks: rescale only when they do
+        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+            for (int nd = 0; nd < NT; ++nd) {
+                o[nd][0] *= al0; o[nd][1] *= al0; o[nd][2] *= al1; o[nd][3] *= al1;
+            }
+        }
+#pragma unroll
+        for (int nd = 0; nd < NT; nd += 2) {
+            uint32_t b0, b1, b2, b3;   // dims nd: (tokens 0-7, 8-15), dims nd+1: (0-7, 8-15)
+            ldmatrix_x4_trans(vt + nd * 256 + v_lane, b0, b1, b2, b3);
+            mma_bf16_16816(o[nd], a0, a1, a2, a3, b0, b1);
+            mma_bf16_16816(o[nd + 1], a0, a1, a2, a3, b2, b3);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + st * 8);
+    }
+    if (failed && lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    auto store_row = [&](int rr, float m, float l, int half) {
+        if (rr >= rows_total) return;
+        const int sq = rr / p.G, g = rr - (rr / p.G) * p.G;
+        const size_t row = (size_t)sq * p.Hq + (size_t)kvh * p.G + g;
+        float* po = p.part_o + (row * p.part_stride + j) * D;
+#pragma unroll
+        for (int nd = 0; nd < NT; ++nd)
+            *reinterpret_cast<float2*>(po + 8 * nd + 2 * c) =
+                make_float2(o[nd][2 * half], o[nd][2 * half + 1]);
+        if (c == 0) p.part_ml[row * p.part_stride + j] = make_float2(m, l);
+    };
+    store_row(rr0, m0, l0, 0);
+    store_row(rr1, m1, l1, 1);
+    // this grid must not finish before the kernel it overlaps with (the suffix part
+    // launched just before it) has finished: the merge after it waits on this grid only
+    grid_dependency_wait();
 }
 
 // Launch configuration of the main kernels.
@@ -658,20 +850,31 @@ cudaError_t launch_dependent_rows(K kernel, dim3 grid, dim3 block, cudaStream_t 
 }
 
 template <int D>
+cudaError_t launch_prefix_for_dim(const KParams& kp, int num_seqs, int num_kv_heads,
+                                  cudaStream_t stream);
+
+template <int D>
 cudaError_t launch_for_dim(const KParams& kp, const DecodeArgs& a, cudaStream_t stream) {
-    const dim3 grid(a.grid_parts, a.num_kv_heads, a.num_seqs);
-    cudaError_t e;
-    if (a.dtype == PA_BF16) {
-        auto k = decode_bf16_kernel<D, kWarps, kStagesBf16>;
-        if ((e = set_smem(k, bf16_smem<D>())) != cudaSuccess) return e;
-        e = launch_dependent(k, grid, dim3(kWarps * 32), bf16_smem<D>(), stream, kp);
-    } else {
-        auto k = decode_f32_kernel<D, kWarps, kStagesF32>;
-        if ((e = set_smem(k, f32_smem<D>())) != cudaSuccess) return e;
-        e = launch_dependent(k, grid, dim3(kWarps * 32), f32_smem<D>(), stream, kp);
+    cudaError_t e = cudaSuccess;
+    const int launched = a.grid_parts - kp.first_part;   // partitions of the main kernel
+    if (launched > 0) {
+        const dim3 grid(launched, a.num_kv_heads, a.num_seqs);
+        if (a.dtype == PA_BF16) {
+            auto k = decode_bf16_kernel<D, kWarps, kStagesBf16>;
+            if ((e = set_smem(k, bf16_smem<D>())) != cudaSuccess) return e;
+            e = launch_dependent(k, grid, dim3(kWarps * 32), bf16_smem<D>(), stream, kp);
+        } else {
+            auto k = decode_f32_kernel<D, kWarps, kStagesF32>;
+            if ((e = set_smem(k, f32_smem<D>())) != cudaSuccess) return e;
+            e = launch_dependent(k, grid, dim3(kWarps * 32), f32_smem<D>(), stream, kp);
+        }
+        if (e != cudaSuccess) return e;
     }
-    if (e != cudaSuccess) return e;
-    if (a.grid_parts > 1) {
+    if (kp.first_part > 0) {
+        e = launch_prefix_for_dim<D>(kp, a.num_seqs, a.num_kv_heads, stream);
+        if (e != cudaSuccess) return e;
+    }
+    if (a.grid_parts > 1 || kp.first_part > 0) {
         const int rows = a.num_seqs * a.num_q_heads;
         if (a.grid_parts <= 32) {          // few partitions: a warp per row
             const dim3 rgrid((rows + 7) / 8);
@@ -685,6 +888,39 @@ cudaError_t launch_for_dim(const KParams& kp, const DecodeArgs& a, cudaStream_t 
         }
     }
     return e;
+}
+
+// Ring depth of the prefix kernel (48 KB of tiles for head_dim 128, 32 KB for 64) and
+// 2 consumer warps per CTA: with 4 CTAs per SM this was the fastest of 1-4 consumer
+// warps x 4-20 stages measured on GB300 for a 64-sequence, 4096-token shared prefix.
+#ifndef PA_PREFIX_STAGES_128
+#define PA_PREFIX_STAGES_128 6
+#endif
+#ifndef PA_PREFIX_STAGES_64
+#define PA_PREFIX_STAGES_64 8
+#endif
+
+template <int D>
+cudaError_t launch_prefix_for_dim(const KParams& kp, int num_seqs, int num_kv_heads,
+                                  cudaStream_t stream) {
+    constexpr int NST = D == 128 ? PA_PREFIX_STAGES_128 : PA_PREFIX_STAGES_64;
+    auto k = decode_prefix_bf16_kernel<D, NST>;
+    constexpr int smem = prefix_smem_bytes<D, NST>();
+    cudaError_t e = set_smem(k, smem);
+    if (e != cudaSuccess) return e;
+    const int rows = num_seqs * kp.G;
+    const dim3 grid((rows + kPrefixRows - 1) / kPrefixRows, num_kv_heads, kp.first_part);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3((kPrefixConsumers + 1) * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = PA_USE_PDL;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, kp, num_seqs);
 }
 
 }  // namespace
@@ -718,6 +954,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     kp.num_blocks = a.num_blocks;
     kp.grid_parts = a.grid_parts;
     kp.part_stride = a.part_stride;
+    kp.first_part = a.first_part;
     kp.scale_log2 = a.scale * kLog2e;
     if (a.head_dim == 64) return launch_for_dim<64>(kp, a, stream);
     return launch_for_dim<128>(kp, a, stream);

@@ -30,6 +30,8 @@ struct DecodeArgs {
     int max_blocks, num_blocks;
     int grid_parts;          // partitions launched per (sequence, kv head)
     int part_stride;         // partitions reserved per (sequence, query head) in the workspace
+    int first_part;          // leading partitions inside a prefix shared by every sequence
+                             // (0: none); computed once per kv head by the prefix kernel
     float scale;
     pa_dtype dtype;
 };

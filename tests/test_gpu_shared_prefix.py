@@ -1,0 +1,77 @@
+"""GPU parity of prefix-sharing decode (pa_decode_attention_shared_prefix).
+
+Sequences that share their first positions in the same physical blocks (the
+layout refcounted copy-on-write forks leave behind; spindle, "Paging") are
+decoded with the prefix read once per kv head.  Results must match the oracle
+computed on each sequence's logical rows, for prefixes of whole and partial
+partitions, empty suffixes, several query-head groupings and row counts that
+leave the last 64-row tile partly empty.
+"""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_207_gb300 as pk
+from paged_kv_cache_207_gb300 import workloads as W
+from _gpu_common import DevicePools, as_f64, assert_close, oracle_contig
+
+pytestmark = pytest.mark.gpu
+
+
+def _prefix_step(wl, dp, shared, hint=0):
+    k_new, v_new, start, cu, lens = dp.step_inputs()
+    pk.append_kv(dp.k, dp.v, k_new, v_new, dp.tables, start, cu, err_flag=dp.err)
+    out = torch.empty_like(wl.q)
+    ws = pk.decode_workspace(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                             wl.max_blocks)
+    pk.decode_attention_shared_prefix(out, wl.q, dp.k, dp.v, dp.tables, lens, wl.scale, shared,
+                                      workspace=ws, max_context_len_hint=hint, err_flag=dp.err)
+    torch.cuda.synchronize()
+    return out, lens
+
+
+@pytest.mark.parametrize("shared,suffixes,hq,hkv,d", [
+    (512, [1, 16, 17, 600, 1], 32, 8, 128),
+    (1024, [1, 100, 513, 2, 77, 1000, 3], 14, 2, 64),
+    (2048, [5, 40], 12, 12, 64),
+    (528, [1, 30, 700], 8, 1, 128),
+    (4096, [16, 512, 300, 1, 64, 128, 256, 400, 9, 33, 65], 32, 8, 128),
+])
+def test_shared_prefix_against_oracle(shared, suffixes, hq, hkv, d):
+    lens = [shared + n - 1 for n in suffixes]       # context before the step's append
+    wl = W.make_decode_workload("prefix", context_lens=lens, num_q_heads=hq, num_kv_heads=hkv,
+                                head_dim=d, dtype="bf16", seed=shared + hq,
+                                device="cuda", shared_prefix=shared)
+    dp = DevicePools(wl)
+    out, _ = _prefix_step(wl, dp, shared)
+    pairs = [(s, h) for s in range(wl.num_seqs) for h in range(hq)]
+    want = oracle_contig(wl, pairs)
+    assert_close(wl, as_f64(out).reshape(len(pairs), d), want, f"prefix {shared}")
+    assert int(dp.err.item()) == 0
+    # and the ordinary path on the same cache agrees within the same tolerance
+    ref = dp.decode(torch.from_numpy(np.array(lens, np.int32) + 1).cuda())
+    assert_close(wl, as_f64(out), as_f64(ref), "prefix vs ordinary")
+
+
+def test_short_prefix_falls_back_to_the_ordinary_path_bitwise():
+    lens = [300 + n for n in (1, 50, 200)]
+    wl = W.make_decode_workload("short", context_lens=lens, num_q_heads=32, num_kv_heads=8,
+                                head_dim=128, dtype="bf16", seed=3, device="cuda",
+                                shared_prefix=256)
+    dp = DevicePools(wl)
+    out, lens_t = _prefix_step(wl, dp, 256)
+    ref = dp.decode(lens_t)
+    assert torch.equal(out, ref)
+
+
+def test_shared_prefix_workload_full_size_sampled():
+    wl = W.llama8b_shared_prefix(device="cuda")
+    dp = DevicePools(wl, canary=False)
+    out, _ = _prefix_step(wl, dp, 4096, hint=int(wl.context_lens.max()) + 1)
+    assert int(dp.err.item()) == 0
+    rng = np.random.default_rng(5)
+    pairs = [(int(s), int(rng.integers(32))) for s in rng.choice(wl.num_seqs, 16, replace=False)]
+    pairs += [(0, h) for h in range(32)]
+    want = oracle_contig(wl, pairs)
+    got = np.stack([as_f64(out[s, h]) for s, h in pairs])
+    assert_close(wl, got, want, "shared prefix full size")
