@@ -83,13 +83,22 @@ def all_sum(x: float, world: int) -> float:
 # ---------------------------------------------------------------------------
 # algorithmic bytes
 # ---------------------------------------------------------------------------
-def decode_bytes(wl) -> int:
+def kv_bytes_per_token(wl, kv_dtype="bf16") -> int:
+    """K+V bytes of one token (all kv heads): elements, or E4M3 codes + one fp32 scale
+    per (slot, kv head) for the FP8 cache."""
+    if kv_dtype == "fp8":
+        return 2 * wl.num_kv_heads * (wl.head_dim + 4)
+    e = 2 if wl.dtype == "bf16" else 4
+    return 2 * wl.num_kv_heads * wl.head_dim * e
+
+
+def decode_bytes(wl, kv_dtype="bf16") -> int:
     """Bytes one decode launch must move: each K/V element of every context once,
     q and out, the block-table entries and lengths, and the split-KV partials
     (written and read back) of sequences longer than one partition."""
     e = 2 if wl.dtype == "bf16" else 4
     L = wl.context_lens.astype(np.int64) + 1
-    kv = int((L * 2 * wl.num_kv_heads * wl.head_dim * e).sum())
+    kv = int((L * kv_bytes_per_token(wl, kv_dtype)).sum())
     qo = 2 * wl.num_seqs * wl.num_q_heads * wl.head_dim * e
     table = int((4 * ((L + 15) // 16)).sum()) + 4 * wl.num_seqs
     parts = (L + 511) // 512
@@ -111,11 +120,11 @@ def unique_kv_bytes(wl, shared: int) -> int:
     return int((shared + private) * per_token)
 
 
-def append_bytes(wl) -> int:
-    """New rows read and written into the pools, plus start / cu / table reads."""
+def append_bytes(wl, kv_dtype="bf16") -> int:
+    """New rows read, and written into the pools, plus start / cu / table reads."""
     e = 2 if wl.dtype == "bf16" else 4
-    rows = wl.num_seqs * wl.num_kv_heads * wl.head_dim * e * 2   # K and V
-    return 2 * rows + 12 * wl.num_seqs
+    rows = wl.num_seqs * wl.num_kv_heads * wl.head_dim * e * 2   # K and V read
+    return rows + wl.num_seqs * kv_bytes_per_token(wl, kv_dtype) + 12 * wl.num_seqs
 
 
 # ---------------------------------------------------------------------------
@@ -231,16 +240,25 @@ def run_ours(args, rank, world, local):
     wl = W.WORKLOADS[args.workload](device="cuda", **kw)
     tdt = wl.torch_dtype()
     S, Hq, Hkv, D = wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
-    shape = pk.pool_shape(wl.num_blocks, Hkv, D, tdt)
-    kp = torch.zeros(shape, dtype=tdt, device="cuda")
-    vp = torch.zeros(shape, dtype=tdt, device="cuda")
+    fp8 = args.kv_dtype == "fp8"
+    if fp8 and wl.dtype != "bf16":
+        raise SystemExit("the FP8 cache takes bf16 rows")
+    if fp8:
+        shape = pk.fp8_pool_shape(wl.num_blocks, Hkv, D)
+        kp = torch.zeros(shape, dtype=torch.uint8, device="cuda")
+        vp = torch.zeros(shape, dtype=torch.uint8, device="cuda")
+    else:
+        shape = pk.pool_shape(wl.num_blocks, Hkv, D, tdt)
+        kp = torch.zeros(shape, dtype=tdt, device="cuda")
+        vp = torch.zeros(shape, dtype=tdt, device="cuda")
+    append = pk.append_kv_fp8 if fp8 else pk.append_kv
     tables = torch.from_numpy(wl.block_tables).cuda()
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     # fill the context (untimed set-up), one append call
     seqs = [f[0] for f in wl.fill]
     ns = [f[3] for f in wl.fill]
     first, end = wl.fill[0][2], wl.fill[-1][2] + wl.fill[-1][3]
-    pk.append_kv(kp, vp, wl.k_rows[first:end].contiguous(), wl.v_rows[first:end].contiguous(),
+    append(kp, vp, wl.k_rows[first:end].contiguous(), wl.v_rows[first:end].contiguous(),
                  tables[torch.tensor(seqs, device="cuda")].contiguous(),
                  torch.tensor([f[1] for f in wl.fill], dtype=torch.int32, device="cuda"),
                  torch.tensor(np.concatenate([[0], np.cumsum(ns)]), dtype=torch.int32, device="cuda"),
@@ -262,7 +280,10 @@ def run_ours(args, rank, world, local):
     shared = args.shared_prefix
 
     def decode(q_, tab_, lens_):
-        if shared:
+        if fp8:
+            pk.decode_attention_fp8(out, q_, kp, vp, tab_, lens_, wl.scale, workspace=ws,
+                                    max_context_len_hint=hint, err_flag=err, stream=stream)
+        elif shared:
             pk.decode_attention_shared_prefix(out, q_, kp, vp, tab_, lens_, wl.scale, shared,
                                               workspace=ws, max_context_len_hint=hint,
                                               err_flag=err, stream=stream)
@@ -271,7 +292,7 @@ def run_ours(args, rank, world, local):
                                 max_context_len_hint=hint, err_flag=err, stream=stream)
 
     def step(ev_d0=None, ev_d1=None):
-        pk.append_kv(kp, vp, k_new, v_new, tables, start, cu, err_flag=err, stream=stream)
+        append(kp, vp, k_new, v_new, tables, start, cu, err_flag=err, stream=stream)
         if ev_d0 is not None:
             ev_d0.record(stream)
         decode(q, tables, lens)
@@ -311,7 +332,7 @@ def run_ours(args, rank, world, local):
         raise RuntimeError(f"device error flag {int(err.item())} during the timed steps")
 
     ms_total_max = all_max(ms_total, world)
-    step_bytes = decode_bytes(wl) + append_bytes(wl)
+    step_bytes = decode_bytes(wl, args.kv_dtype) + append_bytes(wl, args.kv_dtype)
     total_bytes = all_sum(float(step_bytes) * K, world)
     value = total_bytes / (ms_total_max / 1e3) / 1e9
     ms_per_step = ms_total_max / K
@@ -334,7 +355,7 @@ def run_ours(args, rank, world, local):
         for dst, src in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_start, h_start), (d_cu, h_cu),
                          (d_lens, h_lens), (d_tab, h_tab)):
             dst.copy_(src, non_blocking=True)
-        pk.append_kv(kp, vp, d_k, d_v, d_tab, d_start, d_cu, err_flag=err, stream=stream)
+        append(kp, vp, d_k, d_v, d_tab, d_start, d_cu, err_flag=err, stream=stream)
         decode(d_q, d_tab, d_lens)
         h_out.copy_(out, non_blocking=True)
 
@@ -359,7 +380,7 @@ def run_ours(args, rank, world, local):
         peak, peak_src = float(peaks["hbm_gbs"]), "measured"
     else:
         peak, peak_src = 6800.0, "fallback"
-    dbytes = decode_bytes(wl)
+    dbytes = decode_bytes(wl, args.kv_dtype)
     achieved = dbytes / (dec_ms / 1e3) / 1e9
     launches_per_step = 1 + 1 + (1 if int(math.ceil(hint / 512)) > 1 or shared >= 512 else 0) + \
         (1 if shared >= 512 else 0)
@@ -367,9 +388,11 @@ def run_ours(args, rank, world, local):
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8_e4m3 K/V, bf16 q/out, fp32 softmax" if fp8 else wl.dtype,
         "data": "synthetic",
         "config": {"workload": args.workload, "num_seqs_per_gpu": S, "num_q_heads": Hq,
+                   "kv_cache": "fp8_e4m3 (per-slot fp32 scales)" if fp8 else wl.dtype,
                    "num_kv_heads": Hkv, "head_dim": D, "block_size": 16,
                    "context_tokens_after_append": int((wl.context_lens + 1).sum()),
                    "max_context": int(hint),
@@ -384,10 +407,11 @@ def run_ours(args, rank, world, local):
         **({"unique_kv_bytes_per_step": unique_kv_bytes(wl, shared),
             "logical_kv_bytes_per_step": logical_kv_bytes(wl)} if shared else {}),
         "tokens_per_s": round(tokens_per_s, 1),
-        "roofline": {"kernel": "pa_decode_attention (main kernel + partition merge)",
+        "roofline": {"kernel": ("pa_decode_attention_fp8" if fp8 else "pa_decode_attention") +
+                               " (main kernel + partition merge)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(args.workload),
+                     "frac": round(achieved / peak, 4), "traffic": None if (fp8 or shared) else profiled_traffic(args.workload),
                      "algorithmic_bytes_per_launch": dbytes, "avg_launch_ms": round(dec_ms, 5)},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms / K, 5),
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
@@ -575,6 +599,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3-8b_batch256")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
+                    help="K/V cache element type; fp8 = E4M3 codes with per-slot scales")
     ap.add_argument("--shared-prefix", type=int, default=0,
                     help="decode through pa_decode_attention_shared_prefix with this many shared "
                          "tokens (the llama3-8b_shared_prefix workload shares 4096)")

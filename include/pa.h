@@ -64,7 +64,11 @@ typedef enum {
                                  than the library's built-in PA_NOALLOC_SCRATCH_BYTES */
 } pa_status;
 
-typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
+typedef enum {
+    PA_F32 = 0,
+    PA_BF16 = 1,
+    PA_FP8_E4M3 = 2   /* pools only: E4M3 codes with per-slot fp32 scales (see pa_append_kv_fp8) */
+} pa_dtype;
 
 /* Bits OR-ed into *dev_err_flag by the kernels. */
 #define PA_DEV_ERR_BAD_BLOCK 1   /* a table entry read for a live position is outside [0, num_blocks) */
@@ -159,6 +163,42 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, cons
                               int32_t max_context_len_hint, int32_t num_blocks, float scale,
                               pa_dtype dtype, void* workspace, size_t workspace_bytes,
                               int32_t* dev_err_flag, void* stream);
+
+/*
+ * FP8 (E4M3) KV cache -- half the bytes per token for the bandwidth-bound decode
+ * (Slipstream, "Companion work": a block-scaled low-precision kernel plugs into
+ * the same bandwidth-bound decode path; the per-slot scale is this library's
+ * choice for an 8-bit cache).
+ *
+ * Pools: uint8 [num_blocks][num_kv_heads][PA_FP8_RECORD_BYTES(head_dim)].  A
+ * record holds the 16 slots of one (block, kv head): 16 * head_dim E4M3 codes
+ * -- K as [head_dim / 16][16 slots][16 dims], V as [head_dim][16 slots] -- then
+ * 16 fp32 scales, one per slot; value = code * scale.  pa_copy_block takes
+ * dtype PA_FP8_E4M3 for these pools.
+ */
+#define PA_FP8_RECORD_BYTES(head_dim) (16 * (head_dim) + 64)
+
+/* pa_append_kv_fp8 -- like pa_append_kv, with bf16 rows k_new / v_new that are
+ * quantised on the way in: each (row, kv head) gets scale = max|x| / 448 and
+ * codes = E4M3(x / scale) (fp32 arithmetic, round to nearest even, saturating at
+ * 448; an all-zero row gets scale 0 and zero codes).  head_dim 64 or 128. */
+pa_status pa_append_kv_fp8(void* k_pool, void* v_pool, const void* k_new, const void* v_new,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* start_pos, const int32_t* cu_new_tokens,
+                           int32_t num_seqs, int32_t total_new_tokens, int32_t num_blocks,
+                           int32_t num_kv_heads, int32_t head_dim, int32_t* dev_err_flag,
+                           void* stream);
+
+/* pa_decode_attention_fp8 -- pa_decode_attention over FP8 pools; q and out are
+ * bf16, scores and the softmax in fp32, the products on the tensor cores in f16
+ * (every E4M3 code is exact in f16).  Same workspace, partitions, errors. */
+pa_status pa_decode_attention_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                  const int32_t* block_tables, const int32_t* context_lens,
+                                  int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t max_blocks_per_seq,
+                                  int32_t max_context_len_hint, int32_t num_blocks, float scale,
+                                  void* workspace, size_t workspace_bytes, int32_t* dev_err_flag,
+                                  void* stream);
 
 /*
  * pa_decode_attention_shared_prefix -- pa_decode_attention for a batch whose

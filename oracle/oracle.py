@@ -52,6 +52,12 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.oracle_double_to_bf16.restype = ctypes.c_uint16
     L.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
     L.oracle_bf16_to_double.restype = ctypes.c_double
+    L.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+    L.oracle_f32_to_e4m3.restype = ctypes.c_uint8
+    L.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    L.oracle_e4m3_to_double.restype = ctypes.c_double
+    L.oracle_append_kv_fp8.argtypes = [p, p, p, p, p, i, p, p, i, i, i, i]
+    L.oracle_decode_fp8_pairs.argtypes = [p, p, i, p, p, p, p, p, i, i, i, i, i, ctypes.c_double]
     return L
 
 
@@ -203,6 +209,54 @@ def double_to_bf16(x: float) -> int:
 
 def bf16_to_double(b: int) -> float:
     return float(lib().oracle_bf16_to_double(int(b)))
+
+
+# ---- FP8 (E4M3) cache with per-slot scales --------------------------------------
+
+def f32_to_e4m3(x: float) -> int:
+    return int(lib().oracle_f32_to_e4m3(float(x)))
+
+
+def e4m3_to_double(code: int) -> float:
+    return float(lib().oracle_e4m3_to_double(int(code)))
+
+
+def fp8_pool_shape(num_blocks: int, num_kv_heads: int, head_dim: int):
+    """One FP8 pool: per (block, kv head) a record of 16*D code bytes + 16 fp32 scales."""
+    return (num_blocks, num_kv_heads, 16 * head_dim + 64)
+
+
+def append_kv_fp8(k_pool, v_pool, k_new, v_new, block_tables, start_pos, cu_new_tokens, *,
+                  num_kv_heads, head_dim, num_blocks) -> int:
+    """Quantise bf16 rows (uint16 bits or torch bf16) into numpy uint8 FP8 pools in place."""
+    for p in (k_pool, v_pool):
+        if not (isinstance(p, np.ndarray) and p.dtype == np.uint8 and p.flags.c_contiguous):
+            raise TypeError("FP8 pools must be C-contiguous numpy uint8 arrays")
+    k_new, v_new = _np(k_new, np.uint16), _np(v_new, np.uint16)
+    tables = _np(block_tables, np.int32)
+    start = _np(start_pos, np.int32)
+    cu = _np(cu_new_tokens, np.int32)
+    return lib().oracle_append_kv_fp8(_ptr(k_pool), _ptr(v_pool), _ptr(k_new), _ptr(v_new),
+                                      _ptr(tables), tables.shape[1], _ptr(start), _ptr(cu),
+                                      start.shape[0], num_blocks, num_kv_heads, head_dim)
+
+
+def decode_fp8_pairs(pairs, q, k_pool, v_pool, block_tables, context_lens, *, num_q_heads,
+                     num_kv_heads, head_dim, num_blocks, scale) -> np.ndarray:
+    """Decode attention over FP8 pools for chosen (sequence, query head) pairs: float64 [n][D]."""
+    q = _np(q, np.uint16)
+    k_pool, v_pool = _np(k_pool, np.uint8), _np(v_pool, np.uint8)
+    tables = _np(block_tables, np.int32)
+    lens = _np(context_lens, np.int32)
+    pairs = np.ascontiguousarray(np.asarray(pairs, np.int32).reshape(-1, 2))
+    out = np.zeros((pairs.shape[0], head_dim), np.float64)
+    rc = lib().oracle_decode_fp8_pairs(_ptr(out), _ptr(pairs), pairs.shape[0], _ptr(q),
+                                       _ptr(k_pool), _ptr(v_pool), _ptr(tables), _ptr(lens),
+                                       num_q_heads, num_kv_heads, head_dim, tables.shape[1],
+                                       num_blocks, float(scale))
+    if rc != 0:
+        raise ValueError(f"oracle_decode_fp8_pairs failed with code {rc}")
+    return out
 
 
 def pool_shape(num_blocks: int, num_kv_heads: int, head_dim: int, dtype: int):

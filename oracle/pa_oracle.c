@@ -302,3 +302,166 @@ int oracle_decode_pairs(double* out, const int32_t* pairs, int n, const void* q,
     }
     return rc;
 }
+
+/* ---- FP8 (E4M3) KV cache ------------------------------------------------ *
+ * Quantised pools hold, per (block, kv head), a record of 16 * D code bytes
+ * followed by 16 fp32 scales (one per slot):
+ *   K codes: [D / 16][16 slots][16 dims]   (16-byte pieces per slot, as the
+ *            bf16 layout with X = 16)
+ *   V codes: [D][16 slots]                 (one 16-byte row per dim)
+ *   scales : [16] fp32, value = code * scale
+ * E4M3: 1 sign, 4 exponent (bias 7) and 3 mantissa bits; no infinities; the
+ * code 0x7F / 0xFF is NaN; the largest finite value is 448; below 2^-6 the
+ * spacing is fixed at 2^-9 (subnormals).  (The pages name a block-scaled FP4
+ * GEMM on the Slipstream page, "Companion work", for the same bandwidth-bound
+ * decode; a per-token scale is this library's reading for an 8-bit cache.) */
+
+double oracle_e4m3_to_double(uint8_t c) {
+    int sign = (c >> 7) & 1, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);
+    else v = ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* Nearest E4M3 value (ties to even), magnitudes above 448 saturate to 448. */
+uint8_t oracle_f32_to_e4m3(float x) {
+    if (isnan(x)) return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    double m = fabs((double)x);
+    if (m == 0.0) return sign;
+    int e;
+    frexp(m, &e);
+    int ex = e - 1;               /* m in [2^ex, 2^(ex+1)) */
+    if (ex < -6) ex = -6;         /* subnormal spacing 2^-9 */
+    double ulp = ldexp(1.0, ex - 3);
+    double r = rint(m / ulp) * ulp;
+    if (r > 448.0) r = 448.0;
+    if (r == 0.0) return sign;
+    uint8_t code;
+    if (r < ldexp(1.0, -6)) {
+        code = (uint8_t)(r / ldexp(1.0, -9));           /* subnormal: E = 0 */
+    } else {
+        int re;
+        frexp(r, &re);                                  /* r in [2^(re-1), 2^re) */
+        int E = re - 1 + 7;
+        int M = (int)(r / ldexp(1.0, re - 1) * 8.0) - 8;
+        code = (uint8_t)((E << 3) | M);
+    }
+    return sign | code;
+}
+
+static size_t fp8_record_bytes(int D) { return (size_t)16 * D + 64; }
+
+/* Quantise one row of D values (bf16 bits) with its own scale amax / 448;
+ * the arithmetic is fp32, each step correctly rounded. */
+static float quantise_row(const uint16_t* row, int D, uint8_t* codes) {
+    float amax = 0.0f;
+    for (int d = 0; d < D; ++d) {
+        uint32_t u = ((uint32_t)row[d]) << 16;
+        float f;
+        memcpy(&f, &u, sizeof f);
+        f = fabsf(f);
+        if (f > amax) amax = f;
+    }
+    float scale = amax / 448.0f;
+    for (int d = 0; d < D; ++d) {
+        uint32_t u = ((uint32_t)row[d]) << 16;
+        float f;
+        memcpy(&f, &u, sizeof f);
+        codes[d] = scale > 0.0f ? oracle_f32_to_e4m3(f / scale) : 0;
+    }
+    return scale;
+}
+
+/* Append with quantisation: rows of bf16 k_new / v_new ([sum n][Hkv][D]) go
+ * to explicit positions like oracle_append_kv, as codes plus per-slot scales. */
+int oracle_append_kv_fp8(void* k_pool, void* v_pool, const void* k_new, const void* v_new,
+                         const int32_t* tables, int max_blocks, const int32_t* start_pos,
+                         const int32_t* cu_new, int num_seqs, int num_blocks, int Hkv, int D) {
+    if (Hkv <= 0 || D <= 0 || D % 16 != 0 || num_seqs < 0) return OR_BAD_ARG;
+    size_t rec = fp8_record_bytes(D);
+    uint8_t* codes = (uint8_t*)malloc((size_t)D);
+    if (!codes) return OR_BAD_ARG;
+    int rc = OR_OK;
+    for (int s = 0; s < num_seqs; ++s) {
+        int n = cu_new[s + 1] - cu_new[s];
+        for (int i = 0; i < n; ++i) {
+            int p = start_pos[s] + i;
+            int64_t blk;
+            int r = lookup_block(tables, max_blocks, s, p, num_blocks, &blk);
+            if (r != OR_OK) { rc = r; continue; }
+            int t = p % ORACLE_BLOCK;
+            size_t row = (size_t)(cu_new[s] + i);
+            for (int h = 0; h < Hkv; ++h) {
+                uint8_t* krec = (uint8_t*)k_pool + ((size_t)blk * Hkv + h) * rec;
+                uint8_t* vrec = (uint8_t*)v_pool + ((size_t)blk * Hkv + h) * rec;
+                const uint16_t* krow = (const uint16_t*)k_new + (row * Hkv + h) * (size_t)D;
+                const uint16_t* vrow = (const uint16_t*)v_new + (row * Hkv + h) * (size_t)D;
+                float ks = quantise_row(krow, D, codes);
+                for (int d = 0; d < D; ++d) krec[((size_t)(d / 16) * 16 + t) * 16 + d % 16] = codes[d];
+                memcpy(krec + (size_t)16 * D + 4 * t, &ks, 4);
+                float vs = quantise_row(vrow, D, codes);
+                for (int d = 0; d < D; ++d) vrec[(size_t)d * 16 + t] = codes[d];
+                memcpy(vrec + (size_t)16 * D + 4 * t, &vs, 4);
+            }
+        }
+    }
+    free(codes);
+    return rc;
+}
+
+/* Decode over FP8 pools: gather each position's codes through the table,
+ * dequantise (code * scale, exact in double) and attend; q is bf16. */
+int oracle_decode_fp8_one(double* out_row, const void* q, const void* k_pool, const void* v_pool,
+                          const int32_t* tables, const int32_t* context_lens, int s, int h,
+                          int Hq, int Hkv, int D, int max_blocks, int num_blocks, double scale) {
+    if (Hkv <= 0 || D <= 0 || D % 16 != 0 || Hq <= 0 || Hq % Hkv != 0) return OR_BAD_ARG;
+    int g = h / (Hq / Hkv);
+    int L = context_lens[s];
+    for (int d = 0; d < D; ++d) out_row[d] = 0.0;
+    if (L <= 0) return L < 0 ? OR_BAD_POS : OR_OK;
+    if (L > max_blocks * ORACLE_BLOCK) return OR_BAD_POS;
+    size_t rec = fp8_record_bytes(D);
+    double* Kc = (double*)malloc(sizeof(double) * (size_t)L * (size_t)D);
+    double* Vc = (double*)malloc(sizeof(double) * (size_t)L * (size_t)D);
+    double* x = (double*)malloc(sizeof(double) * (size_t)L);
+    double* qv = (double*)malloc(sizeof(double) * (size_t)D);
+    int rc = OR_OK;
+    if (!Kc || !Vc || !x || !qv) { rc = OR_BAD_ARG; goto done; }
+    for (int t = 0; t < L; ++t) {
+        int64_t blk;
+        rc = lookup_block(tables, max_blocks, s, t, num_blocks, &blk);
+        if (rc != OR_OK) goto done;
+        int slot = t % ORACLE_BLOCK;
+        const uint8_t* krec = (const uint8_t*)k_pool + ((size_t)blk * Hkv + g) * rec;
+        const uint8_t* vrec = (const uint8_t*)v_pool + ((size_t)blk * Hkv + g) * rec;
+        float ks, vs;
+        memcpy(&ks, krec + (size_t)16 * D + 4 * slot, 4);
+        memcpy(&vs, vrec + (size_t)16 * D + 4 * slot, 4);
+        for (int d = 0; d < D; ++d) {
+            Kc[(size_t)t * D + d] = oracle_e4m3_to_double(krec[((size_t)(d / 16) * 16 + slot) * 16 + d % 16]) * ks;
+            Vc[(size_t)t * D + d] = oracle_e4m3_to_double(vrec[(size_t)d * 16 + slot]) * vs;
+        }
+    }
+    for (int d = 0; d < D; ++d) qv[d] = load_elem(q, ((size_t)s * Hq + h) * (size_t)D + d, 1);
+    attend(out_row, qv, Kc, Vc, x, L, D, scale);
+done:
+    free(Kc); free(Vc); free(x); free(qv);
+    return rc;
+}
+
+int oracle_decode_fp8_pairs(double* out, const int32_t* pairs, int n, const void* q,
+                            const void* k_pool, const void* v_pool, const int32_t* tables,
+                            const int32_t* context_lens, int Hq, int Hkv, int D, int max_blocks,
+                            int num_blocks, double scale) {
+    int rc = OR_OK;
+    for (int i = 0; i < n; ++i) {
+        int r = oracle_decode_fp8_one(out + (size_t)i * D, q, k_pool, v_pool, tables, context_lens,
+                                      pairs[2 * i], pairs[2 * i + 1], Hq, Hkv, D, max_blocks,
+                                      num_blocks, scale);
+        if (r != OR_OK) rc = r;
+    }
+    return rc;
+}

@@ -10,6 +10,7 @@
 // Copy (spindle, "Paging": refcounted copy-on-write forking): every byte of
 // block src goes to block dst in both pools; 16-byte vector loads and stores.
 #include "pa_internal.h"
+#include "pa_ptx.cuh"
 
 namespace pa {
 
@@ -90,6 +91,108 @@ __global__ void __launch_bounds__(256) append_kernel(const AParams p) {
     *reinterpret_cast<uint4*>(p.v_pool + dst) = vv;
 }
 
+// FP8 append: one warp per (row, kv head).  The row's D bf16 values get one
+// scale amax / 448 and E4M3 codes x / scale (fp32, each step correctly rounded,
+// then round to nearest even with saturation); K codes go to the slot's 16-byte
+// pieces of the record, V codes to byte `slot` of each dim's 16-byte row, and
+// the two scales after the codes.
+template <int D>
+__global__ void __launch_bounds__(256) append_fp8_kernel(const AParams p) {
+    constexpr int VPL = D / 32;   // values per lane: 4 (D = 128) or 2 (D = 64)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        if (__ldg(p.cu) != 0 || __ldg(p.cu + p.S) != p.total) raise_flag(p.err, PA_DEV_ERR_BAD_CU);
+    }
+    if (wid >= (long long)p.total * p.Hkv) return;
+    const int h = (int)(wid % p.Hkv);
+    const int row = (int)(wid / p.Hkv);
+    const size_t src = ((size_t)row * p.Hkv + h) * D + (size_t)lane * VPL;
+    float kx[VPL], vx[VPL];
+    if constexpr (VPL == 4) {
+        const uint2 kr = __ldg(reinterpret_cast<const uint2*>(p.k_new) + src / 4);
+        const uint2 vr = __ldg(reinterpret_cast<const uint2*>(p.v_new) + src / 4);
+        kx[0] = __uint_as_float(kr.x << 16); kx[1] = __uint_as_float(kr.x & 0xffff0000u);
+        kx[2] = __uint_as_float(kr.y << 16); kx[3] = __uint_as_float(kr.y & 0xffff0000u);
+        vx[0] = __uint_as_float(vr.x << 16); vx[1] = __uint_as_float(vr.x & 0xffff0000u);
+        vx[2] = __uint_as_float(vr.y << 16); vx[3] = __uint_as_float(vr.y & 0xffff0000u);
+    } else {
+        const uint32_t kr = __ldg(reinterpret_cast<const uint32_t*>(p.k_new) + src / 2);
+        const uint32_t vr = __ldg(reinterpret_cast<const uint32_t*>(p.v_new) + src / 2);
+        kx[0] = __uint_as_float(kr << 16); kx[1] = __uint_as_float(kr & 0xffff0000u);
+        vx[0] = __uint_as_float(vr << 16); vx[1] = __uint_as_float(vr & 0xffff0000u);
+    }
+    float ka = 0.f, va = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) {
+        ka = fmaxf(ka, fabsf(kx[k]));
+        va = fmaxf(va, fabsf(vx[k]));
+    }
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) {
+        ka = fmaxf(ka, __shfl_xor_sync(0xffffffffu, ka, x));
+        va = fmaxf(va, __shfl_xor_sync(0xffffffffu, va, x));
+    }
+    const float ks = __fdiv_rn(ka, 448.f), vs = __fdiv_rn(va, 448.f);
+
+    int s = (int)(((long long)row * p.S) / (p.total > 0 ? p.total : 1));
+    if (s >= p.S) s = p.S - 1;
+    int first = __ldg(p.cu + s);
+    int next = __ldg(p.cu + s + 1);
+    if (!(first <= row && row < next)) {
+        int lo = 0, hi = p.S - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(p.cu + mid) <= row) lo = mid;
+            else hi = mid - 1;
+        }
+        s = lo;
+        first = __ldg(p.cu + s);
+        next = __ldg(p.cu + s + 1);
+        if (row < first || row >= next) {
+            if (lane == 0) raise_flag(p.err, PA_DEV_ERR_BAD_CU);
+            return;
+        }
+    }
+    const long long pos = (long long)__ldg(p.start_pos + s) + (row - first);
+    if (pos < 0 || pos >= (long long)p.max_blocks * kBlockTokens) {
+        if (lane == 0) raise_flag(p.err, PA_DEV_ERR_BAD_POS);
+        return;
+    }
+    const int32_t blk = __ldg(p.tables + (size_t)s * p.max_blocks + (int)(pos / kBlockTokens));
+    if (blk < 0 || blk >= p.num_blocks) {
+        if (lane == 0) raise_flag(p.err, PA_DEV_ERR_BAD_BLOCK);
+        return;
+    }
+    const int slot = (int)(pos % kBlockTokens);
+    const size_t rec = fp8_record_bytes(D);
+    char* krec = p.k_pool + ((size_t)blk * p.Hkv + h) * rec;
+    char* vrec = p.v_pool + ((size_t)blk * p.Hkv + h) * rec;
+    uint8_t kc[VPL], vc[VPL];
+#pragma unroll
+    for (int k = 0; k < VPL; k += 2) {
+        const uint16_t k2 = ks > 0.f ? pack_e4m3x2(__fdiv_rn(kx[k], ks), __fdiv_rn(kx[k + 1], ks)) : 0;
+        const uint16_t v2 = vs > 0.f ? pack_e4m3x2(__fdiv_rn(vx[k], vs), __fdiv_rn(vx[k + 1], vs)) : 0;
+        kc[k] = (uint8_t)(k2 & 0xff); kc[k + 1] = (uint8_t)(k2 >> 8);
+        vc[k] = (uint8_t)(v2 & 0xff); vc[k + 1] = (uint8_t)(v2 >> 8);
+    }
+    // K: dims d = lane*VPL .. +VPL-1 lie in one 16-dim piece
+    const int d0 = lane * VPL;
+    char* kdst = krec + ((size_t)(d0 / 16) * kBlockTokens + slot) * 16 + (d0 % 16);
+    if constexpr (VPL == 4)
+        *reinterpret_cast<uint32_t*>(kdst) = (uint32_t)kc[0] | ((uint32_t)kc[1] << 8) |
+                                             ((uint32_t)kc[2] << 16) | ((uint32_t)kc[3] << 24);
+    else
+        *reinterpret_cast<uint16_t*>(kdst) = (uint16_t)(kc[0] | (kc[1] << 8));
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) vrec[(size_t)(d0 + k) * kBlockTokens + slot] = (char)vc[k];
+    if (lane == 0) {
+        *reinterpret_cast<float*>(krec + (size_t)16 * D + 4 * slot) = ks;
+        *reinterpret_cast<float*>(vrec + (size_t)16 * D + 4 * slot) = vs;
+    }
+}
+
 struct CParams {
     char* k_pool;
     char* v_pool;
@@ -142,6 +245,32 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+cudaError_t launch_append_fp8(const AppendArgs& a, cudaStream_t stream) {
+    AParams p;
+    p.k_pool = static_cast<char*>(a.k_pool);
+    p.v_pool = static_cast<char*>(a.v_pool);
+    p.k_new = static_cast<const char*>(a.k_new);
+    p.v_new = static_cast<const char*>(a.v_new);
+    p.tables = a.block_tables;
+    p.start_pos = a.start_pos;
+    p.cu = a.cu_new;
+    p.err = a.err;
+    p.max_blocks = a.max_blocks;
+    p.S = a.num_seqs;
+    p.total = a.total_new;
+    p.num_blocks = a.num_blocks;
+    p.Hkv = a.num_kv_heads;
+    p.chunks = 0;
+    p.items = (long long)a.total_new * a.num_kv_heads;   // warps
+    if (p.items == 0) return cudaSuccess;
+    const long long blocks = (p.items * 32 + 255) / 256;
+    if (a.head_dim == 64)
+        append_fp8_kernel<64><<<(unsigned)blocks, 256, 0, stream>>>(p);
+    else
+        append_fp8_kernel<128><<<(unsigned)blocks, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_copy(const CopyArgs& a, cudaStream_t stream) {
     if (a.num_pairs == 0) return cudaSuccess;
     CParams p;
@@ -150,7 +279,9 @@ cudaError_t launch_copy(const CopyArgs& a, cudaStream_t stream) {
     p.pairs = a.pairs;
     p.err = a.err;
     p.num_blocks = a.num_blocks;
-    p.block_bytes = (size_t)a.num_kv_heads * kBlockTokens * a.head_dim * elem_bytes(a.dtype);
+    p.block_bytes = a.dtype == PA_FP8_E4M3
+                        ? (size_t)a.num_kv_heads * fp8_record_bytes(a.head_dim)
+                        : (size_t)a.num_kv_heads * kBlockTokens * a.head_dim * elem_bytes(a.dtype);
     const size_t n16 = p.block_bytes / 16;
     const unsigned slices = (unsigned)((n16 + 256 * 4 - 1) / (256 * 4));   // ~4 vectors per thread
     const dim3 grid(a.num_pairs, 2, slices > 0 ? (slices < 64 ? slices : 64) : 1);

@@ -334,6 +334,242 @@ decode_bf16_kernel(const KParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// FP8 kernel: E4M3 K/V records (codes + per-slot fp32 scales), bf16 q and out.
+// Same pipeline as the bf16 kernel; the codes are converted to f16 in registers
+// (exact) and the tensor cores run f16 x f16 -> fp32.
+//   K: ldmatrix of a tile's 16-byte rows gives each thread 4 consecutive dims of
+//      one token; the dot product's index is permuted (logical k 2c+e <-> dim
+//      4c+e, 2c+8+e <-> 4c+2+e) identically in the query fragment.  The A rows
+//      are gathered in the token order pi(m) = 4(m/2) + m%2, pi(8+m) = pi(m) + 2,
+//      which makes the transposed probabilities line up with V below.
+//   V: each dim's 16 tokens form one 16-byte row, so ldmatrix of V^T rows gives
+//      each thread 4 consecutive tokens of one dim: logical k 2c+e <-> token
+//      4c+e, 2c+8+e <-> token 4c+2+e, which is what movmatrix of the score tile
+//      in the pi order delivers.
+//   Scales: scores are multiplied by the key's slot scale; probabilities by the
+//   value's slot scale (and 2^8, to stay in f16's normal range; the sum gets the
+//   same 2^8) before the P.V product.
+// ---------------------------------------------------------------------------
+template <int D, int NW, int NST>
+__global__ void __launch_bounds__(NW * 32)
+decode_fp8_kernel(const KParams p) {
+    constexpr int REC = 16 * D + 64;            // bytes of one (block, kv head) record
+    constexpr int KS = D / 16;                  // k-steps (one 16-dim piece each) = m-tiles of P.V
+    constexpr float kPScale = 256.f;
+    extern __shared__ __align__(128) uint8_t smem[];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = lane >> 2, c = lane & 3;
+    const int j = blockIdx.x + p.first_part, kvh = blockIdx.y, s = blockIdx.z;
+    const int32_t* trow = p.tables + (size_t)s * p.max_blocks;
+    int32_t first_blk[NST];
+#pragma unroll
+    for (int i = 0; i < NST; ++i) {
+        const int b = j * kPartBlocks + warp + i * NW;
+        first_blk[i] = b < p.max_blocks ? __ldg(trow + b) : -1;
+    }
+    const int L = clamped_len(p, s);
+    const int nparts = num_parts(L);
+    if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0 && nparts > p.grid_parts)
+        raise_flag(p.err, PA_DEV_ERR_HINT);
+    if (j >= nparts || aborted(p.err)) return;
+
+    const int blk0 = j * kPartBlocks;
+    const int tok_end = min(L, (j + 1) * kPartTokens);
+    const int nblk = (tok_end - blk0 * kBlockTokens + kBlockTokens - 1) / kBlockTokens;
+    const int nb_w = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;
+
+    const uint32_t stage0 = smem_u32(smem) + warp * NST * 2 * REC;
+    const uint32_t bar0 = smem_u32(smem) + NW * NST * 2 * REC + warp * NST * 8;
+    if (lane == 0) {
+#pragma unroll
+        for (int st = 0; st < NST; ++st) mbar_init(bar0 + st * 8, 1);
+        fence_proxy_async_smem();
+    }
+    __syncwarp();
+
+    // query fragments in f16 with the permuted dims: b0 <- dims 16kk+4c, +1; b1 <- +2, +3
+    uint32_t qb[KS][2];
+    {
+        const bool live = r < p.G;
+        const uint16_t* qrow = reinterpret_cast<const uint16_t*>(p.q) +
+                               ((size_t)s * p.Hq + (size_t)kvh * p.G + (live ? r : 0)) * D;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            if (live) {
+                const uint2 u = __ldg(reinterpret_cast<const uint2*>(qrow + 16 * kk + 4 * c));
+                qb[kk][0] = pack_f16x2(bf16_lo_to_f32(u.x), bf16_hi_to_f32(u.x));
+                qb[kk][1] = pack_f16x2(bf16_lo_to_f32(u.y), bf16_hi_to_f32(u.y));
+            } else {
+                qb[kk][0] = qb[kk][1] = 0u;
+            }
+        }
+    }
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    const uint64_t pol = l2_policy_evict_first();
+    auto issue_blk = [&](int32_t blk, int st) -> bool {
+        const bool ok = blk >= 0 && blk < p.num_blocks;
+        if (lane == 0) {
+            if (ok) {
+                const size_t off = ((size_t)blk * p.Hkv + kvh) * (size_t)REC;
+                const uint32_t bar = bar0 + st * 8;
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(bar, 2 * REC);
+                bulk_g2s(stage0 + st * 2 * REC, p.k_pool + off, REC, bar, pol);
+                bulk_g2s(stage0 + st * 2 * REC + REC, p.v_pool + off, REC, bar, pol);
+            } else {
+                raise_flag(p.err, PA_DEV_ERR_BAD_BLOCK);
+            }
+        }
+        return ok;
+    };
+
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float o[KS][4];
+#pragma unroll
+    for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    uint32_t issued = 0, phase = 0;
+    bool failed = false;
+#pragma unroll
+    for (int i = 0; i < NST; ++i)
+        if (i < nb_w && issue_blk(first_blk[i], i)) issued |= 1u << i;
+
+    // K rows gathered in the pi order; lane l addresses row l%8 of matrix l/8:
+    // matrices 0 / 1 = rows 0-7 / 8-15 of piece kk, 2 / 3 = the same of piece kk+1
+    const int km = lane >> 3, kr = lane & 7;
+    const int ktok = 4 * (kr >> 1) + (kr & 1) + ((km & 1) ? 2 : 0);
+    const uint32_t k_lane = (uint32_t)(((km >> 1) * kBlockTokens + ktok) * 16);
+    const int tr0 = 4 * (r >> 1) + (r & 1), tr1 = tr0 + 2;     // tokens of score rows r, r+8
+
+    for (int i = 0; i < nb_w; ++i) {
+        const int st = i % NST;
+        if ((issued >> st) & 1u) {
+            if (!mbar_wait_bounded(bar0 + st * 8, (phase >> st) & 1u, kWaitLimitNs)) {
+                failed = true;
+                break;
+            }
+            phase ^= 1u << st;
+            issued &= ~(1u << st);
+            const int tok0 = (blk0 + warp + i * NW) * kBlockTokens;
+            const uint32_t kt = stage0 + st * 2 * REC, vt = kt + REC;
+            const float* kscale = reinterpret_cast<const float*>(smem + (kt - smem_u32(smem)) + 16 * D);
+            const float* vscale = reinterpret_cast<const float*>(smem + (vt - smem_u32(smem)) + 16 * D);
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < KS; kk += 2) {
+                uint32_t x0, x1, x2, x3;
+                ldmatrix_x4(kt + kk * 256 + k_lane, x0, x1, x2, x3);
+                mma_f16_16816(acc, e4m3x2_to_f16x2((uint16_t)(x0 & 0xffffu)),
+                              e4m3x2_to_f16x2((uint16_t)(x1 & 0xffffu)),
+                              e4m3x2_to_f16x2((uint16_t)(x0 >> 16)),
+                              e4m3x2_to_f16x2((uint16_t)(x1 >> 16)), qb[kk][0], qb[kk][1]);
+                if (kk + 1 < KS)
+                    mma_f16_16816(acc, e4m3x2_to_f16x2((uint16_t)(x2 & 0xffffu)),
+                                  e4m3x2_to_f16x2((uint16_t)(x3 & 0xffffu)),
+                                  e4m3x2_to_f16x2((uint16_t)(x2 >> 16)),
+                                  e4m3x2_to_f16x2((uint16_t)(x3 >> 16)), qb[kk + 1][0], qb[kk + 1][1]);
+            }
+            const bool ok0 = tok0 + tr0 < tok_end, ok1 = tok0 + tr1 < tok_end;
+            const float sk0 = kscale[tr0] * p.scale_log2, sk1 = kscale[tr1] * p.scale_log2;
+            const float s0 = ok0 ? acc[0] * sk0 : -INFINITY;
+            const float s1 = ok0 ? acc[1] * sk0 : -INFINITY;
+            const float s2 = ok1 ? acc[2] * sk1 : -INFINITY;
+            const float s3 = ok1 ? acc[3] * sk1 : -INFINITY;
+            float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
+#pragma unroll
+            for (int x = 4; x < 32; x <<= 1) {
+                bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, x));
+                bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, x));
+            }
+            const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+            const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+            m0 = mn0;
+            m1 = mn1;
+            const float p0 = fast_exp2(s0 - mn0), p1 = fast_exp2(s1 - mn1);
+            const float p2 = fast_exp2(s2 - mn0), p3 = fast_exp2(s3 - mn1);
+            l0 = l0 * al0 + (p0 + p2);
+            l1 = l1 * al1 + (p1 + p3);
+            // slots past the context carry arbitrary scales (even inf after the 2^8): their
+            // probabilities are zero and must stay zero, so select rather than multiply
+            const float sv0 = vscale[tr0] * kPScale, sv1 = vscale[tr1] * kPScale;
+            const uint32_t pb0 = movmatrix_trans(
+                pack_f16x2(ok0 ? p0 * sv0 : 0.f, ok0 ? p1 * sv0 : 0.f));
+            const uint32_t pb1 = movmatrix_trans(
+                pack_f16x2(ok1 ? p2 * sv1 : 0.f, ok1 ? p3 * sv1 : 0.f));
+            // V^T rows: thread holds tokens 4c..4c+3 of one dim; past the context the
+            // codes may be anything, so zero them
+            uint32_t vmask = 0xffffffffu;
+            if (tok0 + kBlockTokens > tok_end) {
+                vmask = 0u;
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+                    if (tok0 + 4 * c + b < tok_end) vmask |= 0xffu << (8 * b);
+            }
+#pragma unroll
+            for (int mi = 0; mi < KS; mi += 2) {
+                uint32_t y0, y1, y2, y3;   // dims 16mi+0..7, 16mi+8..15, 16(mi+1)+0..7, +8..15
+                ldmatrix_x4(vt + mi * 256 + lane * 16, y0, y1, y2, y3);
+                y0 &= vmask; y1 &= vmask; y2 &= vmask; y3 &= vmask;
+                o[mi][0] *= al0; o[mi][1] *= al1; o[mi][2] *= al0; o[mi][3] *= al1;
+                mma_f16_16816(o[mi], e4m3x2_to_f16x2((uint16_t)(y0 & 0xffffu)),
+                              e4m3x2_to_f16x2((uint16_t)(y1 & 0xffffu)),
+                              e4m3x2_to_f16x2((uint16_t)(y0 >> 16)),
+                              e4m3x2_to_f16x2((uint16_t)(y1 >> 16)), pb0, pb1);
+                if (mi + 1 < KS) {
+                    o[mi + 1][0] *= al0; o[mi + 1][1] *= al1; o[mi + 1][2] *= al0; o[mi + 1][3] *= al1;
+                    mma_f16_16816(o[mi + 1], e4m3x2_to_f16x2((uint16_t)(y2 & 0xffffu)),
+                                  e4m3x2_to_f16x2((uint16_t)(y3 & 0xffffu)),
+                                  e4m3x2_to_f16x2((uint16_t)(y2 >> 16)),
+                                  e4m3x2_to_f16x2((uint16_t)(y3 >> 16)), pb0, pb1);
+                }
+            }
+        }
+        __syncwarp();
+        if (i + NST < nb_w && issue_blk(__ldg(trow + blk0 + warp + (i + NST) * NW), st))
+            issued |= 1u << st;
+    }
+    if (failed) {
+        if (lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
+        for (int st = 0; st < NST; ++st)
+            if ((issued >> st) & 1u) mbar_wait_bounded(bar0 + st * 8, (phase >> st) & 1u, kWaitLimitNs);
+    }
+#pragma unroll
+    for (int x = 4; x < 32; x <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, x);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, x);
+    }
+    l0 *= kPScale;   // the P.V products carry the same factor
+    l1 *= kPScale;
+
+    __syncthreads();
+    constexpr int OS = D + 4;
+    float* sm_o = reinterpret_cast<float*>(smem);
+    float* sm_m = sm_o + NW * 8 * OS;
+    float* sm_l = sm_m + NW * 8;
+    {
+        float* ow = sm_o + warp * 8 * OS;
+#pragma unroll
+        for (int mi = 0; mi < KS; ++mi) {
+            const int d0 = 16 * mi + r, d1 = d0 + 8;
+            ow[(2 * c) * OS + d0] = o[mi][0];
+            ow[(2 * c + 1) * OS + d0] = o[mi][1];
+            ow[(2 * c) * OS + d1] = o[mi][2];
+            ow[(2 * c + 1) * OS + d1] = o[mi][3];
+        }
+        if (r == 0) {
+            sm_m[warp * 8 + 2 * c] = m0;
+            sm_m[warp * 8 + 2 * c + 1] = m1;
+            sm_l[warp * 8 + 2 * c] = l0;
+            sm_l[warp * 8 + 2 * c + 1] = l1;
+        }
+    }
+    __syncthreads();
+    merge_and_store<D, NW, __nv_bfloat16>(p, sm_o, sm_m, sm_l, s, kvh, j, nparts);
+}
+
+// ---------------------------------------------------------------------------
 // fp32 kernel: CUDA-core FMAs on the same pipeline
 // ---------------------------------------------------------------------------
 template <int D, int NW, int NST>
@@ -849,6 +1085,14 @@ cudaError_t launch_dependent_rows(K kernel, dim3 grid, dim3 block, cudaStream_t 
     return cudaLaunchKernelEx(&cfg, kernel, kp, rows);
 }
 
+constexpr int kStagesFp8 = 3;
+
+template <int D>
+constexpr int fp8_smem() { return kWarps * kStagesFp8 * 2 * (16 * D + 64) + kWarps * kStagesFp8 * 8; }
+
+template <int D>
+cudaError_t launch_fp8_for_dim(const KParams& kp, const DecodeArgs& a, cudaStream_t stream);
+
 template <int D>
 cudaError_t launch_prefix_for_dim(const KParams& kp, int num_seqs, int num_kv_heads,
                                   cudaStream_t stream);
@@ -923,6 +1167,26 @@ cudaError_t launch_prefix_for_dim(const KParams& kp, int num_seqs, int num_kv_he
     return cudaLaunchKernelEx(&cfg, k, kp, num_seqs);
 }
 
+template <int D>
+cudaError_t launch_fp8_for_dim(const KParams& kp, const DecodeArgs& a, cudaStream_t stream) {
+    cudaError_t e;
+    const dim3 grid(a.grid_parts, a.num_kv_heads, a.num_seqs);
+    auto k = decode_fp8_kernel<D, kWarps, kStagesFp8>;
+    if ((e = set_smem(k, fp8_smem<D>())) != cudaSuccess) return e;
+    if ((e = launch_dependent(k, grid, dim3(kWarps * 32), fp8_smem<D>(), stream, kp)) != cudaSuccess)
+        return e;
+    if (a.grid_parts > 1) {
+        const int rows = a.num_seqs * a.num_q_heads;
+        if (a.grid_parts <= 32)
+            e = launch_dependent_rows(decode_reduce_kernel<D, 8, __nv_bfloat16>, dim3((rows + 7) / 8),
+                                      dim3(256), stream, kp, rows);
+        else
+            e = launch_dependent_rows(decode_reduce_kernel<D, 1, __nv_bfloat16>, dim3(rows), dim3(256),
+                                      stream, kp, rows);
+    }
+    return e;
+}
+
 }  // namespace
 
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int /*num_kv_heads*/, int head_dim,
@@ -933,7 +1197,18 @@ size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int /*num_kv_heads*
     return rows * (size_t)head_dim * sizeof(float) + rows * sizeof(float2);
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+namespace {
+KParams make_params(const DecodeArgs& a);
+}
+
+cudaError_t launch_decode_fp8(const DecodeArgs& a, cudaStream_t stream) {
+    const KParams kp = make_params(a);
+    if (a.head_dim == 64) return launch_fp8_for_dim<64>(kp, a, stream);
+    return launch_fp8_for_dim<128>(kp, a, stream);
+}
+
+namespace {
+KParams make_params(const DecodeArgs& a) {
     KParams kp;
     kp.out = a.out;
     kp.q = a.q;
@@ -956,6 +1231,12 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     kp.part_stride = a.part_stride;
     kp.first_part = a.first_part;
     kp.scale_log2 = a.scale * kLog2e;
+    return kp;
+}
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+    const KParams kp = make_params(a);
     if (a.head_dim == 64) return launch_for_dim<64>(kp, a, stream);
     return launch_for_dim<128>(kp, a, stream);
 }

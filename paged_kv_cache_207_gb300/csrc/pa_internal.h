@@ -15,7 +15,7 @@ constexpr int kPartTokens = PA_PARTITION_TOKENS;                // tokens per sp
 constexpr int kPartBlocks = kPartTokens / kBlockTokens;         // blocks per partition
 static_assert(kPartTokens % kBlockTokens == 0, "partition must be whole blocks");
 
-inline int elem_bytes(pa_dtype t) { return t == PA_BF16 ? 2 : 4; }
+inline int elem_bytes(pa_dtype t) { return t == PA_BF16 ? 2 : (t == PA_FP8_E4M3 ? 1 : 4); }
 
 struct DecodeArgs {
     void* out;
@@ -68,5 +68,16 @@ struct CopyArgs {
     pa_dtype dtype;
 };
 cudaError_t launch_copy(const CopyArgs& a, cudaStream_t stream);
+
+}  // namespace pa
+
+namespace pa {
+
+// FP8 (E4M3) cache: per (block, kv head) a record of 16 * D code bytes
+// (K: [D/16][16 slots][16]; V: [D][16 slots]) followed by 16 fp32 slot scales.
+__host__ __device__ inline size_t fp8_record_bytes(int head_dim) { return (size_t)16 * head_dim + 64; }
+
+cudaError_t launch_append_fp8(const AppendArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_fp8(const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace pa

@@ -11,6 +11,7 @@ import os
 
 import pytest
 
+import test_oracle_fp8_pins as fp8
 import test_oracle_pins as pins
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -21,21 +22,37 @@ MUTANTS = {
     "score_sign": ("x[t] = scale * acc;", "x[t] = -scale * acc;"),
     "scale_dropped": ("x[t] = scale * acc;", "x[t] = acc;"),
     "no_normalisation": ("double p = x[t] / denom;", "double p = x[t];"),
-    "context_short_by_one": ("    for (int t = 0; t < L; ++t) {\n        int64_t blk;",
-                             "    for (int t = 0; t < L - 1; ++t) {\n        int64_t blk;"),
+    "context_short_by_one": ("    for (int t = 0; t < L; ++t) {\n        int64_t blk;\n        rc = lookup_block(tables, max_blocks, s, t, num_blocks, &blk);\n        if (rc != OR_OK) goto done;\n        for (int d",
+                             "    for (int t = 0; t < L - 1; ++t) {\n        int64_t blk;\n        rc = lookup_block(tables, max_blocks, s, t, num_blocks, &blk);\n        if (rc != OR_OK) goto done;\n        for (int d"),
+    "fp8_context_short_by_one": ("    for (int t = 0; t < L; ++t) {\n        int64_t blk;\n        rc = lookup_block(tables, max_blocks, s, t, num_blocks, &blk);\n        if (rc != OR_OK) goto done;\n        int slot",
+                                 "    for (int t = 0; t < L - 1; ++t) {\n        int64_t blk;\n        rc = lookup_block(tables, max_blocks, s, t, num_blocks, &blk);\n        if (rc != OR_OK) goto done;\n        int slot"),
     "wrong_slot": ("size_t e = pool_elem(blk, g, t % ORACLE_BLOCK, d, Hkv, D, X);",
                    "size_t e = pool_elem(blk, g, (t + 1) % ORACLE_BLOCK, d, Hkv, D, X);"),
     "wrong_block": ("int32_t b = tables[(size_t)s * (size_t)max_blocks + (size_t)lb];",
                     "int32_t b = tables[(size_t)s * (size_t)max_blocks];"),
-    "gqa_modulo_map": ("int g = h / (Hq / Hkv);", "int g = h % Hkv;"),
+    "gqa_modulo_map": ("int X = 16 / elem_bytes_of(dtype);\n    int g = h / (Hq / Hkv);",
+                       "int X = 16 / elem_bytes_of(dtype);\n    int g = h % Hkv;"),
+    "fp8_gqa_modulo_map": ("return OR_BAD_ARG;\n    int g = h / (Hq / Hkv);",
+                           "return OR_BAD_ARG;\n    int g = h % Hkv;"),
     "query_of_wrong_head": ("qv[d] = load_elem(q, ((size_t)s * Hq + h) * (size_t)D + d, dtype);",
                             "qv[d] = load_elem(q, ((size_t)s * Hq + g) * (size_t)D + d, dtype);"),
-    "round_down": ("double r = rint(m / ulp) * ulp;", "double r = floor(m / ulp) * ulp;"),
+    "round_down": ("double r = rint(m / ulp) * ulp;\n    if (r >= ldexp(1.0, 128))",
+                   "double r = floor(m / ulp) * ulp;\n    if (r >= ldexp(1.0, 128))"),
     "no_subnormal_spacing": ("    if (ex < -126) ex = -126;     /* subnormal range keeps the fixed spacing */\n", ""),
     "widen_shift": ("uint32_t u = ((uint32_t)b) << 16;", "uint32_t u = ((uint32_t)b) << 15;"),
     "append_wrong_slot": ("size_t dst = pool_elem(blk, h, p % ORACLE_BLOCK, d, Hkv, D, X);",
                           "size_t dst = pool_elem(blk, h, (p + 1) % ORACLE_BLOCK, d, Hkv, D, X);"),
-    "append_first_row_only": ("size_t row = (size_t)(cu_new[s] + i);", "size_t row = (size_t)(cu_new[s]);"),
+    "append_first_row_only": ("size_t row = (size_t)(cu_new[s] + i);\n            for (int h = 0; h < Hkv; ++h) {\n                for (int d",
+                              "size_t row = (size_t)(cu_new[s]);\n            for (int h = 0; h < Hkv; ++h) {\n                for (int d"),
+    "e4m3_round_down": ("    double r = rint(m / ulp) * ulp;\n    if (r > 448.0) r = 448.0;",
+                        "    double r = floor(m / ulp) * ulp;\n    if (r > 448.0) r = 448.0;"),
+    "e4m3_no_saturation": ("    if (r > 448.0) r = 448.0;\n", ""),
+    "e4m3_exponent_bias": ("int E = re - 1 + 7;", "int E = re - 1 + 8;"),
+    "fp8_scale_not_applied": ("Kc[(size_t)t * D + d] = oracle_e4m3_to_double(krec[((size_t)(d / 16) * 16 + slot) * 16 + d % 16]) * ks;",
+                              "Kc[(size_t)t * D + d] = oracle_e4m3_to_double(krec[((size_t)(d / 16) * 16 + slot) * 16 + d % 16]);"),
+    "fp8_v_layout_untransposed": ("for (int d = 0; d < D; ++d) vrec[(size_t)d * 16 + t] = codes[d];",
+                                  "for (int d = 0; d < D; ++d) vrec[((size_t)(d / 16) * 16 + t) * 16 + d % 16] = codes[d];"),
+    "fp8_scale_from_first_value": ("        if (f > amax) amax = f;\n", "        if (d == 0) amax = f;\n"),
     "copy_keys_only": ("        memmove((char*)v_pool + (size_t)dst * block_bytes, (char*)v_pool + (size_t)src * block_bytes, block_bytes);\n", ""),
 }
 
@@ -59,6 +76,11 @@ def _pins():
     yield "append", lambda o: pins.test_append_writes_only_its_slots_and_reads_back(o)
     yield "append_bad", lambda o: pins.test_append_rejects_bad_block_and_position(o)
     yield "copy", lambda o: pins.test_copy_block_copies_every_byte_of_both_pools(o)
+    yield "e4m3_cases", lambda o: fp8.test_e4m3_hand_worked_cases(o)
+    yield "e4m3_torch", lambda o: fp8.test_e4m3_matches_torch_in_range(o)
+    yield "e4m3_bijection", lambda o: fp8.test_e4m3_codes_and_values_are_a_bijection(o)
+    yield "fp8_append", lambda o: fp8.test_quantised_append_scales_and_codes(o)
+    yield "fp8_decode", lambda o: fp8.test_fp8_decode_closed_forms_and_library_routine(o)
 
 
 def test_every_pin_passes_on_the_unmutated_source(oracle_mod, tmp_path):
