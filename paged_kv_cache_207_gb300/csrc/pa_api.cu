@@ -147,6 +147,7 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, cons
     a.num_blocks = num_blocks;
     a.grid_parts = (bound + pa::kPartTokens - 1) / pa::kPartTokens;
     a.part_stride = pa::decode_part_stride(max_blocks_per_seq);
+    a.part_blocks = pa::kPartBlocks;
     a.first_part = 0;
     a.scale = scale;
     a.dtype = dtype;
@@ -206,6 +207,7 @@ pa_status pa_decode_attention_shared_prefix(
     a.grid_parts = (bound + pa::kPartTokens - 1) / pa::kPartTokens;
     if (a.grid_parts < first_part) a.grid_parts = first_part;
     a.part_stride = pa::decode_part_stride(max_blocks_per_seq);
+    a.part_blocks = pa::kPartBlocks;
     a.first_part = first_part;
     a.scale = scale;
     a.dtype = dtype;
@@ -289,8 +291,10 @@ pa_status pa_decode_attention_fp8(void* out, const void* q, const void* k_pool, 
     a.head_dim = head_dim;
     a.max_blocks = max_blocks_per_seq;
     a.num_blocks = num_blocks;
-    a.grid_parts = (bound + pa::kPartTokens - 1) / pa::kPartTokens;
-    a.part_stride = pa::decode_part_stride(max_blocks_per_seq);
+    const int fp8_part_tokens = pa::kFp8PartBlocks * pa::kBlockTokens;
+    a.grid_parts = (bound + fp8_part_tokens - 1) / fp8_part_tokens;
+    a.part_stride = pa::decode_part_stride(max_blocks_per_seq);   // >= the FP8 partitions used
+    a.part_blocks = pa::kFp8PartBlocks;
     a.first_part = 0;
     a.scale = scale;
     a.dtype = PA_FP8_E4M3;

@@ -52,8 +52,16 @@ struct KParams {
     int grid_parts;     // partitions covered per (sequence, kv head): first_part + launched
     int part_stride;
     int first_part;     // partitions below this are a shared prefix done by the prefix kernel
+    int part_blocks;    // blocks per split-KV partition (a fixed constant of each path)
     float scale_log2;   // scale * log2(e): scores live in log2 units
 };
+
+// Rescale the output accumulators only in blocks where a running maximum moved
+// (any lane of the warp); after the first blocks of a partition it rarely does.
+#ifndef PA_LAZY_RESCALE
+#define PA_LAZY_RESCALE 1
+#endif
+constexpr bool kLazyRescale = PA_LAZY_RESCALE != 0;
 
 __device__ __forceinline__ void raise_flag(int32_t* err, int bits) {
     if (err) atomicOr(err, bits);
@@ -79,8 +87,9 @@ __device__ __forceinline__ bool aborted(const int32_t* err) {
     return (*reinterpret_cast<const volatile int32_t*>(err) & PA_DEV_ERR_TIMEOUT) != 0;
 }
 
-__device__ __forceinline__ int num_parts(int L) {
-    return L > 0 ? (L + kPartTokens - 1) / kPartTokens : 1;
+__device__ __forceinline__ int num_parts(int L, int part_blocks) {
+    const int pt = part_blocks * kBlockTokens;
+    return L > 0 ? (L + pt - 1) / pt : 1;
 }
 
 // Per-warp ring of NST stages, each holding one K tile and one V tile.
@@ -153,17 +162,17 @@ decode_bf16_kernel(const KParams p) {
     int32_t first_blk[NST];
 #pragma unroll
     for (int i = 0; i < NST; ++i) {
-        const int b = j * kPartBlocks + warp + i * NW;
+        const int b = j * p.part_blocks + warp + i * NW;
         first_blk[i] = b < p.max_blocks ? __ldg(trow + b) : -1;
     }
     const int L = clamped_len(p, s);
-    const int nparts = num_parts(L);
+    const int nparts = num_parts(L, p.part_blocks);
     if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0 && nparts > p.grid_parts)
         raise_flag(p.err, PA_DEV_ERR_HINT);
     if (j >= nparts || aborted(p.err)) return;
 
-    const int blk0 = j * kPartBlocks;                            // first logical block
-    const int tok_end = min(L, (j + 1) * kPartTokens);           // one past the last token
+    const int blk0 = j * p.part_blocks;                            // first logical block
+    const int tok_end = min(L, (j + 1) * p.part_blocks * kBlockTokens);           // one past the last token
     const int nblk = (tok_end - blk0 * kBlockTokens + kBlockTokens - 1) / kBlockTokens;
     const int nb_w = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;
 
@@ -268,6 +277,7 @@ decode_bf16_kernel(const KParams p) {
             l0 = l0 * al0 + (bf16_lo_to_f32(x0) + bf16_lo_to_f32(x1));
             l1 = l1 * al1 + (bf16_hi_to_f32(x0) + bf16_hi_to_f32(x1));
             const uint32_t pb0 = movmatrix_trans(x0), pb1 = movmatrix_trans(x1);
+            const bool rescale = !kLazyRescale || __any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f);
 
             // V^T fragments hold tokens 2c, 2c+1 (regs 0,1) and 2c+8, 2c+9 (regs 2,3);
             // slots past the context may hold anything (even NaN), so zero them.
@@ -284,7 +294,9 @@ decode_bf16_kernel(const KParams p) {
                 uint32_t v0, v1, v2, v3;
                 ldmatrix_x4_trans(vt + mi * 512 + v_lane, v0, v1, v2, v3);
                 v0 &= mask_a; v1 &= mask_a; v2 &= mask_b; v3 &= mask_b;
-                o[mi][0] *= al0; o[mi][1] *= al1; o[mi][2] *= al0; o[mi][3] *= al1;
+                if (rescale) {
+                    o[mi][0] *= al0; o[mi][1] *= al1; o[mi][2] *= al0; o[mi][3] *= al1;
+                }
                 mma_bf16_16816(o[mi], v0, v1, v2, v3, pb0, pb1);
             }
         }
@@ -365,17 +377,17 @@ decode_fp8_kernel(const KParams p) {
     int32_t first_blk[NST];
 #pragma unroll
     for (int i = 0; i < NST; ++i) {
-        const int b = j * kPartBlocks + warp + i * NW;
+        const int b = j * p.part_blocks + warp + i * NW;
         first_blk[i] = b < p.max_blocks ? __ldg(trow + b) : -1;
     }
     const int L = clamped_len(p, s);
-    const int nparts = num_parts(L);
+    const int nparts = num_parts(L, p.part_blocks);
     if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0 && nparts > p.grid_parts)
         raise_flag(p.err, PA_DEV_ERR_HINT);
     if (j >= nparts || aborted(p.err)) return;
 
-    const int blk0 = j * kPartBlocks;
-    const int tok_end = min(L, (j + 1) * kPartTokens);
+    const int blk0 = j * p.part_blocks;
+    const int tok_end = min(L, (j + 1) * p.part_blocks * kBlockTokens);
     const int nblk = (tok_end - blk0 * kBlockTokens + kBlockTokens - 1) / kBlockTokens;
     const int nb_w = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;
 
@@ -500,6 +512,7 @@ decode_fp8_kernel(const KParams p) {
                 pack_f16x2(ok1 ? p2 * sv1 : 0.f, ok1 ? p3 * sv1 : 0.f));
             // V^T rows: thread holds tokens 4c..4c+3 of one dim; past the context the
             // codes may be anything, so zero them
+            const bool rescale = !kLazyRescale || __any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f);
             uint32_t vmask = 0xffffffffu;
             if (tok0 + kBlockTokens > tok_end) {
                 vmask = 0u;
@@ -512,13 +525,18 @@ decode_fp8_kernel(const KParams p) {
                 uint32_t y0, y1, y2, y3;   // dims 16mi+0..7, 16mi+8..15, 16(mi+1)+0..7, +8..15
                 ldmatrix_x4(vt + mi * 256 + lane * 16, y0, y1, y2, y3);
                 y0 &= vmask; y1 &= vmask; y2 &= vmask; y3 &= vmask;
-                o[mi][0] *= al0; o[mi][1] *= al1; o[mi][2] *= al0; o[mi][3] *= al1;
+                if (rescale) {
+                    o[mi][0] *= al0; o[mi][1] *= al1; o[mi][2] *= al0; o[mi][3] *= al1;
+                }
                 mma_f16_16816(o[mi], e4m3x2_to_f16x2((uint16_t)(y0 & 0xffffu)),
                               e4m3x2_to_f16x2((uint16_t)(y1 & 0xffffu)),
                               e4m3x2_to_f16x2((uint16_t)(y0 >> 16)),
                               e4m3x2_to_f16x2((uint16_t)(y1 >> 16)), pb0, pb1);
                 if (mi + 1 < KS) {
-                    o[mi + 1][0] *= al0; o[mi + 1][1] *= al1; o[mi + 1][2] *= al0; o[mi + 1][3] *= al1;
+                    if (rescale) {
+                        o[mi + 1][0] *= al0; o[mi + 1][1] *= al1; o[mi + 1][2] *= al0;
+                        o[mi + 1][3] *= al1;
+                    }
                     mma_f16_16816(o[mi + 1], e4m3x2_to_f16x2((uint16_t)(y2 & 0xffffu)),
                                   e4m3x2_to_f16x2((uint16_t)(y3 & 0xffffu)),
                                   e4m3x2_to_f16x2((uint16_t)(y2 >> 16)),
@@ -585,13 +603,13 @@ decode_f32_kernel(const KParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int j = blockIdx.x + p.first_part, kvh = blockIdx.y, s = blockIdx.z;
     const int L = clamped_len(p, s);
-    const int nparts = num_parts(L);
+    const int nparts = num_parts(L, p.part_blocks);
     if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0 && nparts > p.grid_parts)
         raise_flag(p.err, PA_DEV_ERR_HINT);
     if (j >= nparts || aborted(p.err)) return;
 
-    const int blk0 = j * kPartBlocks;
-    const int tok_end = min(L, (j + 1) * kPartTokens);
+    const int blk0 = j * p.part_blocks;
+    const int tok_end = min(L, (j + 1) * p.part_blocks * kBlockTokens);
     const int nblk = (tok_end - blk0 * kBlockTokens + kBlockTokens - 1) / kBlockTokens;
     const int nb_w = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;
 
@@ -771,7 +789,7 @@ decode_reduce_kernel(const KParams p, int num_rows) {
         int L = __ldg(p.lens + s);
         const int cap = p.max_blocks * kBlockTokens;
         L = L < 0 ? 0 : (L > cap ? cap : L);
-        n = num_parts(L);
+        n = num_parts(L, p.part_blocks);
         if (n > p.grid_parts) n = p.grid_parts;     // flagged by the main kernel
     }
     // one partition and no shared prefix: written directly by the main kernel
@@ -876,12 +894,12 @@ decode_prefix_bf16_kernel(const KParams p, int num_seqs) {
         fence_proxy_async_smem();
     }
     __syncthreads();
-    const int blk0 = j * kPartBlocks;     // every block of the partition is in the prefix
+    const int blk0 = j * p.part_blocks;     // every block of the partition is in the prefix
 
     if (warp == kPrefixConsumers) {       // ---- producer warp
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
-            for (int i = 0; i < kPartBlocks; ++i) {
+            for (int i = 0; i < p.part_blocks; ++i) {
                 const int st = i % NST;
                 // stage st is free once its previous use (i - NST) was consumed
                 if (i >= NST && !mbar_wait_bounded(empty0 + st * 8, ((i / NST) - 1) & 1, kWaitLimitNs)) {
@@ -939,7 +957,7 @@ decode_prefix_bf16_kernel(const KParams p, int num_seqs) {
     const uint32_t k_lane = (uint32_t)((((km & 1) * 16) + (km >> 1) * 8 + (lane & 7)) * 16);
     const uint32_t v_lane = (uint32_t)((((km >> 1) * 16) + (km & 1) * 8 + (lane & 7)) * 16);
     bool failed = false;
-    for (int i = 0; i < kPartBlocks; ++i) {
+    for (int i = 0; i < p.part_blocks; ++i) {
         const int st = i % NST;
         if (!mbar_wait_bounded(full0 + st * 8, (i / NST) & 1, kWaitLimitNs)) {
             failed = true;
@@ -1085,10 +1103,21 @@ cudaError_t launch_dependent_rows(K kernel, dim3 grid, dim3 block, cudaStream_t 
     return cudaLaunchKernelEx(&cfg, kernel, kp, rows);
 }
 
-constexpr int kStagesFp8 = 3;
+// FP8 launch shape: 4 warps x 2 stages of 4.2 KB records (34 KB, 6 CTAs per SM) and
+// 1024-token partitions measured fastest on GB300 (of 2-6 stages, 512-2048 tokens).
+#ifndef PA_FP8_STAGES
+#define PA_FP8_STAGES 2
+#endif
+#ifndef PA_FP8_WARPS
+#define PA_FP8_WARPS 4
+#endif
+constexpr int kStagesFp8 = PA_FP8_STAGES;
+constexpr int kWarpsFp8 = PA_FP8_WARPS;
 
 template <int D>
-constexpr int fp8_smem() { return kWarps * kStagesFp8 * 2 * (16 * D + 64) + kWarps * kStagesFp8 * 8; }
+constexpr int fp8_smem() {
+    return kWarpsFp8 * kStagesFp8 * 2 * (16 * D + 64) + kWarpsFp8 * kStagesFp8 * 8;
+}
 
 template <int D>
 cudaError_t launch_fp8_for_dim(const KParams& kp, const DecodeArgs& a, cudaStream_t stream);
@@ -1171,9 +1200,9 @@ template <int D>
 cudaError_t launch_fp8_for_dim(const KParams& kp, const DecodeArgs& a, cudaStream_t stream) {
     cudaError_t e;
     const dim3 grid(a.grid_parts, a.num_kv_heads, a.num_seqs);
-    auto k = decode_fp8_kernel<D, kWarps, kStagesFp8>;
+    auto k = decode_fp8_kernel<D, kWarpsFp8, kStagesFp8>;
     if ((e = set_smem(k, fp8_smem<D>())) != cudaSuccess) return e;
-    if ((e = launch_dependent(k, grid, dim3(kWarps * 32), fp8_smem<D>(), stream, kp)) != cudaSuccess)
+    if ((e = launch_dependent(k, grid, dim3(kWarpsFp8 * 32), fp8_smem<D>(), stream, kp)) != cudaSuccess)
         return e;
     if (a.grid_parts > 1) {
         const int rows = a.num_seqs * a.num_q_heads;
@@ -1230,6 +1259,7 @@ KParams make_params(const DecodeArgs& a) {
     kp.grid_parts = a.grid_parts;
     kp.part_stride = a.part_stride;
     kp.first_part = a.first_part;
+    kp.part_blocks = a.part_blocks;
     kp.scale_log2 = a.scale * kLog2e;
     return kp;
 }

@@ -30,6 +30,7 @@ struct DecodeArgs {
     int max_blocks, num_blocks;
     int grid_parts;          // partitions launched per (sequence, kv head)
     int part_stride;         // partitions reserved per (sequence, query head) in the workspace
+    int part_blocks;         // blocks per split-KV partition of this path
     int first_part;          // leading partitions inside a prefix shared by every sequence
                              // (0: none); computed once per kv head by the prefix kernel
     float scale;
@@ -40,6 +41,14 @@ struct DecodeArgs {
 inline int decode_part_stride(int max_blocks) {
     return (max_blocks + kPartBlocks - 1) / kPartBlocks;
 }
+
+// Blocks per split-KV partition of the FP8 path: its tiles are half the bytes of
+// bf16 ones, so a partition covers twice the tokens for the same bytes per CTA.
+#ifndef PA_FP8_PARTITION_BLOCKS
+#define PA_FP8_PARTITION_BLOCKS 64
+#endif
+constexpr int kFp8PartBlocks = PA_FP8_PARTITION_BLOCKS;
+static_assert(kFp8PartBlocks % kPartBlocks == 0, "FP8 partitions are whole bf16 partitions");
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                               int max_blocks);
 
