@@ -165,6 +165,30 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, cons
                               int32_t* dev_err_flag, void* stream);
 
 /*
+ * pa_prefill_attention -- causal attention of chunks of new tokens over the
+ * paged cache (chunked prefill; Slipstream, "Horizon", lists chunked prefill
+ * among the engine's parts; spindle, "Two bugs worth recording": positions are
+ * explicit, never inferred).
+ *
+ *   q, out           [total_q][num_q_heads][head_dim] bf16; rows of sequence s
+ *                    are cu_q[s] .. cu_q[s+1]-1
+ *   start_pos        int32 [num_seqs]: row cu_q[s] + i is the token at position
+ *                    start_pos[s] + i, whose K/V the caller has already appended
+ *   max_chunk        host bound on cu_q[s+1] - cu_q[s] (sizes the grid)
+ * Row (s, i, h) attends over positions 0 .. start_pos[s] + i of sequence s
+ * (query head h reads kv head h / G), i.e. it equals pa_decode_attention of
+ * that query with context length start_pos[s] + i + 1.  bf16 only; head_dim 64
+ * or 128; at most 8 query heads per kv head.  Positions past the table set
+ * PA_DEV_ERR_BAD_POS and the tile is skipped.
+ */
+pa_status pa_prefill_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
+                               const int32_t* block_tables, int32_t max_blocks_per_seq,
+                               const int32_t* start_pos, const int32_t* cu_q, int32_t num_seqs,
+                               int32_t total_q, int32_t max_chunk, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                               float scale, pa_dtype dtype, int32_t* dev_err_flag, void* stream);
+
+/*
  * FP8 (E4M3) KV cache -- half the bytes per token for the bandwidth-bound decode
  * (Slipstream, "Companion work": a block-scaled low-precision kernel plugs into
  * the same bandwidth-bound decode path; the per-slot scale is this library's

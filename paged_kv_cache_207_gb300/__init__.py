@@ -8,6 +8,7 @@ from ._native import (  # noqa: F401
     BLOCK_SIZE, PARTITION_TOKENS, BlockManager, PagedKVError, append_kv, copy_block,
     decode_attention, decode_attention_shared_prefix, decode_workspace, decode_workspace_size, lib,
     pool_shape, fp8_pool_shape, append_kv_fp8, decode_attention_fp8, copy_block_fp8,
+    prefill_attention,
     DEV_ERR_BAD_BLOCK, DEV_ERR_BAD_POS, DEV_ERR_HINT, DEV_ERR_BAD_CU, DEV_ERR_TIMEOUT,
     DEV_ERR_BAD_PAIR,
 )

@@ -29,7 +29,8 @@ DEV_ERR_BAD_PAIR = 32
 EXPORTED = [
     "pa_status_string", "pa_abi_version", "pa_append_kv", "pa_copy_block",
     "pa_decode_workspace_size", "pa_decode_attention", "pa_decode_attention_shared_prefix",
-    "pa_decode_attention_noalloc", "pa_append_kv_fp8", "pa_decode_attention_fp8", "pa_bm_create", "pa_bm_destroy",
+    "pa_decode_attention_noalloc", "pa_append_kv_fp8", "pa_decode_attention_fp8",
+    "pa_prefill_attention", "pa_bm_create", "pa_bm_destroy",
     "pa_bm_add_seq", "pa_bm_fork", "pa_bm_free_seq", "pa_bm_blocks_needed",
     "pa_bm_prepare_append", "pa_bm_block_table", "pa_bm_seq_len", "pa_bm_refcount", "pa_bm_stats",
 ]
@@ -80,6 +81,9 @@ def lib() -> ctypes.CDLL:
     L.pa_decode_attention_fp8.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32,
                                           ctypes.c_float, p, sz, p, p]
     L.pa_decode_attention_fp8.restype = ctypes.c_int
+    L.pa_prefill_attention.argtypes = [p, p, p, p, p, i32, p, p, i32, i32, i32, i32, i32, i32, i32,
+                                       ctypes.c_float, ctypes.c_int, p, p]
+    L.pa_prefill_attention.restype = ctypes.c_int
     L.pa_decode_attention_noalloc.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32,
                                               ctypes.c_float, ctypes.c_int, p, p]
     L.pa_decode_attention_noalloc.restype = ctypes.c_int
@@ -259,6 +263,17 @@ def decode_attention_shared_prefix(out, q, k_pool, v_pool, block_tables, context
         int(max_context_len_hint), nb, float(scale), _dtype_code(q), int(shared_prefix_tokens),
         None if workspace is None else _ptr(workspace), ws_bytes,
         None if err_flag is None else _i32(err_flag, "err_flag"), _stream(stream)))
+
+
+def prefill_attention(out, q, k_pool, v_pool, block_tables, start_pos, cu_q, scale,
+                      max_chunk: int, err_flag=None, stream=None) -> None:
+    """Causal attention of chunk rows q ([total][Hq][D]) over the paged cache."""
+    nb, hkv, d = _pool_dims(k_pool)
+    check("pa_prefill_attention", lib().pa_prefill_attention(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _i32(block_tables, "block_tables"),
+        block_tables.shape[1], _i32(start_pos, "start_pos"), _i32(cu_q, "cu_q"),
+        start_pos.shape[0], q.shape[0], int(max_chunk), q.shape[1], hkv, d, nb, float(scale),
+        _dtype_code(q), None if err_flag is None else _i32(err_flag, "err_flag"), _stream(stream)))
 
 
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024

@@ -20,7 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libpaged_kv.so")
 
-SOURCES = ["pa_api.cu", "pa_decode.cu", "pa_append.cu", "pa_noalloc.cu", "pa_block_manager.cpp"]
+SOURCES = ["pa_api.cu", "pa_decode.cu", "pa_append.cu", "pa_prefill.cu", "pa_noalloc.cu",
+           "pa_block_manager.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

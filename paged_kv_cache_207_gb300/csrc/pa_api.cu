@@ -301,4 +301,44 @@ pa_status pa_decode_attention_fp8(void* out, const void* q, const void* k_pool, 
     return cuda_status(pa::launch_decode_fp8(a, static_cast<cudaStream_t>(stream)));
 }
 
+pa_status pa_prefill_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
+                               const int32_t* block_tables, int32_t max_blocks_per_seq,
+                               const int32_t* start_pos, const int32_t* cu_q, int32_t num_seqs,
+                               int32_t total_q, int32_t max_chunk, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                               float scale, pa_dtype dtype, int32_t* dev_err_flag, void* stream) {
+    if (num_seqs < 0 || total_q < 0 || max_chunk < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        num_blocks <= 0 || max_blocks_per_seq <= 0 || !std::isfinite(scale))
+        return PA_ERR_INVALID_ARG;
+    if (dtype != PA_BF16) return dtype_ok(dtype) ? PA_ERR_UNSUPPORTED : PA_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (num_q_heads / num_kv_heads > 8) return PA_ERR_UNSUPPORTED;
+    if ((long long)max_blocks_per_seq * pa::kBlockTokens > INT32_MAX) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0 || total_q == 0 || max_chunk == 0) return PA_OK;
+    if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+    if (!out || !q || !k_pool || !v_pool || !block_tables || !start_pos || !cu_q)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
+        return PA_ERR_INVALID_ARG;
+    pa::PrefillArgs a;
+    a.out = out;
+    a.q = q;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.block_tables = block_tables;
+    a.start_pos = start_pos;
+    a.cu_q = cu_q;
+    a.err = dev_err_flag;
+    a.num_seqs = num_seqs;
+    a.max_chunk = max_chunk;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.scale = scale;
+    return cuda_status(pa::launch_prefill(a, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -87,6 +87,20 @@ namespace pa {
 __host__ __device__ inline size_t fp8_record_bytes(int head_dim) { return (size_t)16 * head_dim + 64; }
 
 cudaError_t launch_append_fp8(const AppendArgs& a, cudaStream_t stream);
+
+struct PrefillArgs {
+    void* out;
+    const void* q;
+    const void* k_pool;
+    const void* v_pool;
+    const int32_t* block_tables;
+    const int32_t* start_pos;
+    const int32_t* cu_q;
+    int32_t* err;
+    int num_seqs, max_chunk, num_q_heads, num_kv_heads, head_dim, max_blocks, num_blocks;
+    float scale;
+};
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_fp8(const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace pa
