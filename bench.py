@@ -549,11 +549,12 @@ def run_replay(args, rank, world, local):
     build.build()
     pk.lib()
     rw = W.spindle_replay(device="cuda", seed=208 + 1000 * rank)
-    for _ in range(max(1, min(args.warmup, 3))):
-        Replay(rw, device="cuda").run()
-    torch.cuda.synchronize()
     barrier(world)
-    st = Replay(rw, device="cuda", time_gpu=True).run()
+    graphs = not args.no_graphs
+    for _ in range(max(1, min(args.warmup, 3))):
+        Replay(rw, device="cuda", use_graphs=graphs).run()
+    torch.cuda.synchronize()
+    st = Replay(rw, device="cuda", time_gpu=True, use_graphs=graphs).run()
     barrier(world)
     wall = all_max(st.wall_s, world)
     gpu_s = all_max(st.gpu_ms / 1e3, world)
@@ -570,7 +571,8 @@ def run_replay(args, rank, world, local):
         "config": {"workload": "spindle_replay", "requests": rw.num_seqs,
                    "cow_children": rw.num_children, "layers": rw.num_layers,
                    "heads": rw.num_heads, "head_dim": rw.head_dim, "pool_slots": rw.num_blocks * 16,
-                   "step": "one continuous-batching iteration: 12 x (append + decode)"},
+                   "step": "one continuous-batching iteration: 12 x (append + decode)",
+                   "cuda_graphs": graphs},
         "pct_of_peak_hbm": round(100 * dbytes / gpu_s / 1e9 / peaks.get("hbm_gbs", 6800.0), 2),
         "tokens_per_s": round(tokens / wall, 1),
         "tokens_per_s_gpu_time": round(tokens / gpu_s, 1),
@@ -673,6 +675,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3-8b_batch256")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graphs", action="store_true",
+                    help="replay: launch every kernel directly instead of one CUDA graph per step")
     ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
                     help="K/V cache element type; fp8 = E4M3 codes with per-slot scales")
     ap.add_argument("--shared-prefix", type=int, default=0,

@@ -56,10 +56,11 @@ class Replay:
     kernels): the same admissions, preemptions and copy pairs as a device run."""
 
     def __init__(self, rw, device="cuda", time_gpu: bool = False, block_manager=None,
-                 on_schedule=None):
+                 on_schedule=None, use_graphs: bool = False):
         self.rw = rw
         self.dev = device
         self.time_gpu = time_gpu and device is not None
+        self.use_graphs = use_graphs and device is not None
         self.bm = block_manager if block_manager is not None else pk.BlockManager(rw.num_blocks)
         self.on_schedule = on_schedule
         self.max_blocks = (rw.max_len + BLOCK - 1) // BLOCK
@@ -71,6 +72,22 @@ class Replay:
             self.v = [torch.full(shape, float("nan"), dtype=torch.bfloat16, device=device)
                       for _ in range(rw.num_layers)]
             self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        if self.use_graphs:
+            n = rw.num_seqs
+            # fixed device buffers the captured steps read; host staging in pinned memory
+            self.g_tables = torch.full((n, self.max_blocks), -1, dtype=torch.int32, device=device)
+            self.g_start = torch.zeros(n, dtype=torch.int32, device=device)
+            self.g_lens = torch.zeros(n, dtype=torch.int32, device=device)
+            self.g_seq = torch.zeros(n, dtype=torch.long, device=device)
+            self.g_pos = torch.zeros(n, dtype=torch.long, device=device)
+            self.g_cu = torch.arange(n + 1, dtype=torch.int32, device=device)
+            self.h_tables = torch.empty_like(self.g_tables, device="cpu").pin_memory()
+            self.h_start = torch.empty_like(self.g_start, device="cpu").pin_memory()
+            self.h_lens = torch.empty_like(self.g_lens, device="cpu").pin_memory()
+            self.h_seq = torch.empty_like(self.g_seq, device="cpu").pin_memory()
+            self.h_pos = torch.empty_like(self.g_pos, device="cpu").pin_memory()
+            self.graphs = {}          # running-batch size -> (graph, per-layer outputs)
+            self.h_free = None        # event: the last staging copy has been read
         n = rw.num_seqs
         self.gen_done = [0] * n
         self.bm_id = [-1] * n
@@ -176,7 +193,31 @@ class Replay:
         self._finish_iteration(run, ctx)
         return True
 
+    def _capture(self, S: int):
+        """One CUDA graph for an iteration with S running sequences: per layer the
+        gather of the new rows, pa_append_kv and pa_decode_attention, all reading
+        the fixed buffers above."""
+        rw = self.rw
+        g = torch.cuda.CUDAGraph()
+        tables, start, lens = self.g_tables[:S], self.g_start[:S], self.g_lens[:S]
+        seq, pos, cu = self.g_seq[:S], self.g_pos[:S], self.g_cu[:S + 1]
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            outs = []
+            for l in range(rw.num_layers):
+                k_new = rw.k[seq, l, pos]
+                v_new = rw.v[seq, l, pos]
+                q = rw.q[seq, l, pos]
+                out = torch.empty_like(q)
+                pk.append_kv(self.k[l], self.v[l], k_new, v_new, tables, start, cu,
+                             err_flag=self.err)
+                pk.decode_attention(out, q, self.k[l], self.v[l], tables, lens, rw.scale,
+                                    max_context_len_hint=rw.max_len, err_flag=self.err)
+                outs.append(out)
+        return g, outs
+
     def _device_work(self, run, ctx, prefill, pairs, observer) -> None:
+        if self.use_graphs:
+            return self._device_work_graph(run, ctx, prefill, pairs, observer)
         rw = self.rw
         S = len(run)
         tables = self._i32([self.bm.block_table(self.bm_id[s], self.max_blocks) for s in run])
@@ -221,6 +262,57 @@ class Replay:
             ev1.record()
         if observer is not None:
             observer(self, run, ctx, outs)
+        if ev0 is not None:
+            ev1.synchronize()
+            self.stats.gpu_ms += ev0.elapsed_time(ev1)
+
+    def _device_work_graph(self, run, ctx, prefill, pairs, observer) -> None:
+        rw = self.rw
+        S = len(run)
+        ev0 = ev1 = None
+        if self.time_gpu:
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record()
+        if prefill or pairs:       # admissions and copy-on-write copies: ordinary launches
+            pf_tables = pf_start = pf_cu = pf_seq = pf_pos = None
+            if prefill:
+                pf_tables = self._i32([p[1] for p in prefill])
+                pf_start = self._i32([0] * len(prefill))
+                pf_cu = self._i32(np.concatenate([[0], np.cumsum([p[2] for p in prefill])]))
+                pf_seq = torch.cat([torch.full((p[2],), p[0], dtype=torch.long) for p in prefill]).to(self.dev)
+                pf_pos = torch.cat([torch.arange(p[2]) for p in prefill]).to(self.dev)
+            pairs_t = self._i32(pairs).reshape(-1, 2) if pairs else None
+            for l in range(rw.num_layers):
+                if prefill:
+                    pk.append_kv(self.k[l], self.v[l], rw.k[pf_seq, l, pf_pos].contiguous(),
+                                 rw.v[pf_seq, l, pf_pos].contiguous(), pf_tables, pf_start, pf_cu,
+                                 err_flag=self.err)
+                    self.stats.launches += 1
+                if pairs_t is not None:
+                    pk.copy_block(self.k[l], self.v[l], pairs_t, err_flag=self.err)
+                    self.stats.launches += 1
+        if self.h_free is not None:      # the previous copy out of the staging must be done
+            self.h_free.synchronize()
+        self.h_tables[:S].numpy()[:] = np.asarray([self.bm.block_table(self.bm_id[s], self.max_blocks)
+                                                   for s in run], np.int32)
+        self.h_start[:S].numpy()[:] = ctx
+        self.h_lens[:S].numpy()[:] = ctx + 1
+        self.h_seq[:S].numpy()[:] = np.asarray(run, np.int64)
+        self.h_pos[:S].numpy()[:] = ctx.astype(np.int64)
+        for d, h in ((self.g_tables, self.h_tables), (self.g_start, self.h_start),
+                     (self.g_lens, self.h_lens), (self.g_seq, self.h_seq), (self.g_pos, self.h_pos)):
+            d[:S].copy_(h[:S], non_blocking=True)
+        self.h_free = torch.cuda.Event()
+        self.h_free.record()
+        if S not in self.graphs:
+            self.graphs[S] = self._capture(S)
+        g, outs = self.graphs[S]
+        g.replay()
+        self.stats.launches += 2 * rw.num_layers
+        if ev1 is not None:
+            ev1.record()
+        if observer is not None:
+            observer(self, run, ctx, [o.clone() for o in outs])
         if ev0 is not None:
             ev1.synchronize()
             self.stats.gpu_ms += ev0.elapsed_time(ev1)

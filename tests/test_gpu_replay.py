@@ -60,6 +60,13 @@ def test_spindle_replay_tight_pool_preempts_and_recomputes():
     assert stats.preemptions > 0
 
 
+def test_spindle_replay_with_cuda_graphs():
+    from paged_kv_cache_207_gb300 import workloads as W
+    rw = W.spindle_replay(device="cuda", num_blocks=150)
+    stats = _run_checked(rw, use_graphs=True)
+    assert stats.preemptions > 0
+
+
 def test_spindle_replay_partial_parent_copies_on_write():
     from paged_kv_cache_207_gb300 import workloads as W
     rw = W.spindle_replay(device="cuda", parent_prompt=20, num_independent=8, num_blocks=64)
