@@ -22,6 +22,7 @@
 
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
+#include "pa_tc.cuh"
 
 namespace pa {
 
@@ -247,20 +248,424 @@ prefill_bf16_kernel(const PParams p) {
     store_row(v1, tl1, g1, l1, 1);
 }
 
+// ============================================================================
+// tcgen05 kernel: the same computation with the 5th-generation tensor cores.
+//
+// CTA = (query tile, kv head, sequence) with 128 rows (M = 128), one row per
+// thread of the four softmax warps.  Warp 4 streams K and V tiles of 8 blocks
+// (128 tokens) through separate two-stage rings with bulk copies; warp 5 owns
+// the tensor memory and one of its threads issues the MMAs:
+//   S_j = Q K_j^T  -> TMEM columns [128 (j % 2), +128)  (one M128 N16 K16 MMA per
+//                    block and 16 dims, B read straight from the block tile)
+//   O  += P_j V_j  -> TMEM columns [256, 256 + D)      (one M128 N=D K16 MMA per
+//                    block; V's block tile is an MN-major B operand)
+// in the order S_0, S_1, PV_0, S_2, PV_1, ..., so the scores of tile j + 1 are
+// computed while the softmax warps work on tile j.  Each softmax thread reads
+// its row of S_j from TMEM, applies the causal mask, keeps a running maximum
+// that is only raised when a tile exceeds it by more than 2^8 (the output is
+// then rescaled in TMEM), writes its bf16 probabilities into the shared P tile
+// in the core-matrix layout of an A operand, and at the end reads its row of O,
+// divides by the row sum and stores it.
+// ============================================================================
+
+namespace tc {
+
+constexpr int kRowsTC = 128;
+constexpr int kKeyBlocks = 8;
+constexpr int kKeyTok = kKeyBlocks * kBlockTokens;
+constexpr int kSoftWarps = 4;
+constexpr int kProducerWarp = kSoftWarps;
+constexpr int kMmaWarp = kSoftWarps + 1;
+constexpr int kThreadsTC = (kSoftWarps + 2) * 32;
+constexpr int kTmemCols = 512;
+constexpr uint32_t kColO = 256;
+constexpr float kRescaleLog2 = 8.f;
+
+template <int D>
+struct Smem {
+    static constexpr int TILE = kBlockTokens * D * 2;          // one (block, kv head) tile
+    static constexpr int KTILE = kKeyBlocks * TILE;            // one ring stage
+    static constexpr int Q = 0;                                // [D/8][16][8 rows][16 B]
+    static constexpr int P = Q + kRowsTC * D * 2;              // [16][16][8 rows][16 B]
+    static constexpr int K = P + kRowsTC * kKeyTok * 2;
+    static constexpr int V = K + 2 * KTILE;
+    static constexpr int BAR = V + 2 * KTILE;
+    static constexpr int NBAR = 15;
+    static constexpr int SLOT = BAR + NBAR * 8;
+    // at least 120 KB so that one CTA (and its 512 TMEM columns) owns an SM
+    static constexpr int BYTES = SLOT + 16 < 122880 ? 122880 : SLOT + 16;
+};
+
+// barrier indices
+constexpr int kKFull = 0, kKEmpty = 2, kVFull = 4, kVEmpty = 6, kSFull = 8, kSFree = 10,
+              kPFull = 12, kPVDone = 13, kDone = 14;
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// All lanes wait; the result is made uniform across the warp.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+    const bool ok = mbar_wait_bounded(bar, parity, kWaitLimitNs);
+    return __all_sync(0xffffffffu, ok);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams p) {
+    using L = Smem<D>;
+    constexpr int TILE = L::TILE, KTILE = L::KTILE;
+    constexpr int KSTEPS = D / 16;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qt = gridDim.x - 1 - blockIdx.x;            // later (longer) tiles first
+    const int kvh = blockIdx.y, s = blockIdx.z;
+    const int q0 = __ldg(p.cu_q + s);
+    const int n = __ldg(p.cu_q + s + 1) - q0;
+    const int i0 = qt * p.TQ;
+    if (i0 >= n) return;
+    const int start = __ldg(p.start_pos + s);
+    const int i_end = min(n, i0 + p.TQ);
+    const int p_last = start + i_end - 1;                 // last position this tile attends to
+    if (start < 0 || p_last >= p.max_blocks * kBlockTokens) {
+        if (threadIdx.x == 0 && kvh == 0) raise_flag(p.err, PA_DEV_ERR_BAD_POS);
+        return;
+    }
+    const int nblk = p_last / kBlockTokens + 1;
+    const int ntiles = (nblk + kKeyBlocks - 1) / kKeyBlocks;
+    const int32_t* trow = p.tables + (size_t)s * p.max_blocks;
+
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sQ = sbase + L::Q, sP = sbase + L::P, sK = sbase + L::K, sV = sbase + L::V;
+    const uint32_t bar0 = sbase + L::BAR;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int st = 0; st < 2; ++st) {
+            mbar_init(bar(kKFull + st), 1);
+            mbar_init(bar(kKEmpty + st), 1);
+            mbar_init(bar(kVFull + st), 1);
+            mbar_init(bar(kVEmpty + st), 1);
+            mbar_init(bar(kSFull + st), 1);
+            mbar_init(bar(kSFree + st), kSoftWarps);
+        }
+        mbar_init(bar(kPFull), kSoftWarps);
+        mbar_init(bar(kPVDone), 1);
+        mbar_init(bar(kDone), 1);
+        fence_proxy_async_smem();
+    }
+    if (warp == kMmaWarp) tmem_alloc<kTmemCols>(sbase + L::SLOT);
+
+    // rows: (chunk token, query head of this kv head), token-major
+    const int row = threadIdx.x;                          // meaningful for the softmax warps
+    int pos = p_last;                                     // rows outside the chunk see all (finite)
+    bool row_valid = false;
+    size_t orow = 0;
+    if (warp < kSoftWarps) {
+        const int tl = row / p.G, g = row - tl * p.G;
+        row_valid = tl < p.TQ && i0 + tl < n;
+        if (row_valid) {
+            pos = start + i0 + tl;
+            orow = ((size_t)(q0 + i0 + tl) * p.Hq + (size_t)kvh * p.G + g) * D;
+        }
+        grid_dependency_wait();
+        const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + orow);
+#pragma unroll 4
+        for (int kg = 0; kg < D / 8; ++kg) {
+            const uint4 v = row_valid ? __ldg(qsrc + kg) : make_uint4(0u, 0u, 0u, 0u);
+            st_shared_v4(sQ + (uint32_t)((kg * 16 + (row >> 3)) * 128 + (row & 7) * 16), v.x, v.y,
+                         v.z, v.w);
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::SLOT);
+
+    if (warp == kProducerWarp) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0) {
+            grid_dependency_wait();        // the chunk's own K/V come from the append before
+            grid_launch_dependents();
+            const uint64_t pol = l2_policy_evict_last();   // tiles are re-read by other query tiles
+            int issued = 0;
+            bool ok = true;
+            auto load = [&](const char* pool, uint32_t dst, uint32_t full, int b0, int nb) {
+                int32_t blks[kKeyBlocks];
+                uint32_t bytes = 0;
+#pragma unroll
+                for (int b = 0; b < kKeyBlocks; ++b) {
+                    int32_t blk = -1;
+                    if (b < nb) {
+                        blk = __ldg(trow + b0 + b);
+                        if (blk < 0 || blk >= p.num_blocks) {
+                            raise_flag(p.err, PA_DEV_ERR_BAD_BLOCK);
+                            blk = -1;
+                        } else {
+                            bytes += TILE;
+                        }
+                    }
+                    blks[b] = blk;
+                }
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(full, bytes);
+#pragma unroll
+                for (int b = 0; b < kKeyBlocks; ++b)
+                    if (blks[b] >= 0)
+                        bulk_g2s(dst + b * TILE, pool + ((size_t)blks[b] * p.Hkv + kvh) * (size_t)TILE,
+                                 TILE, full, pol);
+            };
+            for (int j = 0; j < ntiles; ++j) {
+                const int st = j & 1;
+                const int b0 = j * kKeyBlocks, nb = min(kKeyBlocks, nblk - b0);
+                if (j >= 2 && !mbar_wait_bounded(bar(kKEmpty + st), ((j >> 1) - 1) & 1, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                load(p.k_pool, sK + st * KTILE, bar(kKFull + st), b0, nb);
+                if (j >= 2 && !mbar_wait_bounded(bar(kVEmpty + st), ((j >> 1) - 1) & 1, kWaitLimitNs)) {
+                    // K of tile j is in flight: wait for it below
+                    issued = j + 1;
+                    ok = false;
+                    break;
+                }
+                load(p.v_pool, sV + st * KTILE, bar(kVFull + st), b0, nb);
+                issued = j + 1;
+            }
+            if (!ok) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
+            // no copy may still be landing in shared memory when the CTA exits
+            for (int j = max(0, issued - 2); j < issued; ++j) {
+                const int st = j & 1;
+                mbar_wait_bounded(bar(kKFull + st), (j >> 1) & 1, kWaitLimitNs);
+                mbar_wait_bounded(bar(kVFull + st), (j >> 1) & 1, kWaitLimitNs);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ---------------------------------------------------------------- MMA issue
+        constexpr uint32_t idS = umma_idesc_bf16(128, 16, 0);
+        constexpr uint32_t idO = umma_idesc_bf16(128, D, 1);
+        const uint64_t qdesc = umma_desc(sQ, 2048, 128);
+        const uint64_t pdesc = umma_desc(sP, 2048, 128);
+        bool ok = true;
+        auto issue_s = [&](int j) {
+            const int st = j & 1;
+            ok = warp_wait(bar(kKFull + st), (j >> 1) & 1);
+            if (ok && j >= 2) ok = warp_wait(bar(kSFree + st), ((j >> 1) - 1) & 1);
+            if (!ok) return;
+            tc_fence_after();
+            if (lane == 0) {
+                const int nb = min(kKeyBlocks, nblk - j * kKeyBlocks);
+                const uint64_t kdesc = umma_desc(sK + st * KTILE, 256, 128);
+                const uint32_t dcol = tmem + (uint32_t)(st * kKeyTok);
+                for (int b = 0; b < nb; ++b)
+#pragma unroll
+                    for (int ks = 0; ks < KSTEPS; ++ks)
+                        umma_ss(dcol + 16 * b, qdesc + (uint64_t)(ks * 256),
+                                kdesc + (uint64_t)((b * TILE + ks * 512) >> 4), idS, ks > 0);
+                umma_commit(bar(kSFull + st));
+                umma_commit(bar(kKEmpty + st));
+            }
+            __syncwarp();
+        };
+        auto issue_pv = [&](int j) {
+            const int st = j & 1;
+            ok = warp_wait(bar(kPFull), j & 1);
+            if (ok) ok = warp_wait(bar(kVFull + st), (j >> 1) & 1);
+            if (!ok) return;
+            const int nb = min(kKeyBlocks, nblk - j * kKeyBlocks);
+            if (j == ntiles - 1) {
+                // V rows past the last attended position may hold anything (even NaN)
+                const int first_stale = p_last - (nblk - 1) * kBlockTokens + 1;
+                if (first_stale < kBlockTokens) {
+                    const int nst = kBlockTokens - first_stale;
+                    uint8_t* vt = smem + L::V + st * KTILE + (nb - 1) * TILE;
+                    for (int idx = lane; idx < (D / 8) * nst; idx += 32) {
+                        const int c = idx / nst, sl = first_stale + (idx - c * nst);
+                        *reinterpret_cast<uint4*>(vt + c * 256 + sl * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                }
+                __syncwarp();
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint64_t vdesc = umma_desc(sV + st * KTILE, 128, 256);
+                for (int b = 0; b < nb; ++b)
+                    umma_ss(tmem + kColO, pdesc + (uint64_t)(b * 256),
+                            vdesc + (uint64_t)((b * TILE) >> 4), idO, (j > 0 || b > 0) ? 1u : 0u);
+                umma_commit(bar(kPVDone));
+                umma_commit(bar(kVEmpty + st));
+            }
+            __syncwarp();
+        };
+        issue_s(0);
+        for (int j = 0; ok && j < ntiles; ++j) {
+            if (j + 1 < ntiles) issue_s(j + 1);
+            if (ok) issue_pv(j);
+        }
+        if (!ok && lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
+        // nothing may still be running on the tensor cores when TMEM is freed
+        if (lane == 0) umma_commit(bar(kDone));
+        __syncwarp();
+        mbar_wait_bounded(bar(kDone), 0, kWaitLimitNs);
+    } else {
+        // ---------------------------------------------------------------- softmax rows
+        const uint32_t tl_addr = tmem + ((uint32_t)(32 * warp) << 16);
+        const uint32_t prow = sP + (uint32_t)((row >> 3) * 128 + (row & 7) * 16);
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+            const int st = j & 1;
+            ok = warp_wait(bar(kSFull + st), (j >> 1) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tl_addr + (uint32_t)(st * kKeyTok + 32 * c), sr[c]);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kSFree + st));
+            // scale, causal mask (select: unread or stale columns may hold NaN)
+            const int tok0 = j * kKeyTok;
+            float mx = -INFINITY;
+            if (tok0 + kKeyTok - 1 <= pos) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float x = __uint_as_float(sr[c][i]) * p.scale_log2;
+                        sr[c][i] = __float_as_uint(x);
+                        mx = fmaxf(mx, x);
+                    }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float x = tok0 + 32 * c + i <= pos
+                                            ? __uint_as_float(sr[c][i]) * p.scale_log2
+                                            : -INFINITY;
+                        sr[c][i] = __float_as_uint(x);
+                        mx = fmaxf(mx, x);
+                    }
+            }
+            float alpha = 1.f;
+            bool resc = false;
+            if (mx > m_used + kRescaleLog2) {              // first tile: m_used = -inf
+                alpha = fast_exp2(m_used - mx);
+                resc = j > 0;
+                m_used = mx;
+            }
+            float sum = 0.f;
+            uint32_t pk[64];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const float e0 = fast_exp2(__uint_as_float(sr[c][i]) - m_used);
+                    const float e1 = fast_exp2(__uint_as_float(sr[c][i + 1]) - m_used);
+                    sum += e0 + e1;
+                    pk[(32 * c + i) >> 1] = pack_bf16x2(e0, e1);
+                }
+            l = l * alpha + sum;
+            // PV_{j-1} done: the P tile is free and O is not being written
+            if (j > 0) {
+                ok = warp_wait(bar(kPVDone), (j - 1) & 1);
+                if (!ok) break;
+                tc_fence_after();
+            }
+            if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tl_addr + kColO + 32 * c, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(tl_addr + kColO + 32 * c, o);
+                }
+                tmem_wait_st();
+            }
+#pragma unroll
+            for (int kg = 0; kg < kKeyTok / 8; ++kg)
+                st_shared_v4(prow + kg * 2048, pk[4 * kg], pk[4 * kg + 1], pk[4 * kg + 2], pk[4 * kg + 3]);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kPFull));
+        }
+        if (ok) ok = warp_wait(bar(kPVDone), (ntiles - 1) & 1);
+        if (ok) {
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow);
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tl_addr + kColO + 32 * c, o);
+                tmem_wait_ld();
+                if (row_valid) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+                        dst[4 * c + v] = w;
+                    }
+                }
+            }
+        } else if (lane == 0) {
+            raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc<kTmemCols>(tmem);
+    }
+}
+
+}  // namespace tc
+
 template <typename K>
 cudaError_t set_smem(K kernel, int bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
+#ifndef PA_PREFILL_TC
+#define PA_PREFILL_TC 1
+#endif
+
 template <int D>
 cudaError_t launch_for_dim(const PParams& pp, int num_seqs, int max_chunk, cudaStream_t stream) {
+#if PA_PREFILL_TC
+    auto k = tc::prefill_tc_kernel<D>;
+    constexpr int smem = tc::Smem<D>::BYTES;
+    constexpr int threads = tc::kThreadsTC;
+#else
     auto k = prefill_bf16_kernel<D>;
     constexpr int smem = prefill_smem<D>();
+    constexpr int threads = (kConsumers + 1) * 32;
+#endif
     cudaError_t e = set_smem(k, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((max_chunk + pp.TQ - 1) / pp.TQ, pp.Hkv, num_seqs);
-    cfg.blockDim = dim3((kConsumers + 1) * 32);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -286,7 +691,11 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     pp.Hq = a.num_q_heads;
     pp.Hkv = a.num_kv_heads;
     pp.G = a.num_q_heads / a.num_kv_heads;
+#if PA_PREFILL_TC
+    pp.TQ = tc::kRowsTC / pp.G;
+#else
     pp.TQ = kRows / pp.G;
+#endif
     pp.max_blocks = a.max_blocks;
     pp.num_blocks = a.num_blocks;
     pp.scale_log2 = a.scale * kLog2e;
