@@ -274,43 +274,46 @@ constexpr int kRowsTC = 128;
 constexpr int kKeyBlocks = 8;
 constexpr int kKeyTok = kKeyBlocks * kBlockTokens;
 constexpr int kSoftWarps = 4;
-constexpr int kProducerWarp = kSoftWarps;
-constexpr int kMmaWarp = kSoftWarps + 1;
-constexpr int kThreadsTC = (kSoftWarps + 2) * 32;
+constexpr int kProducerWarp = kSoftWarps;       // V tiles
+constexpr int kMmaWarp = kSoftWarps + 1;        // TMEM owner, MMA issue
+constexpr int kRepackWarp = kSoftWarps + 2;     // K tiles: copy in, repack chunk-major
+constexpr int kThreadsTC = (kSoftWarps + 3) * 32;
 constexpr int kTmemCols = 512;
-constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.f;
+
+// TMEM columns: S double buffer, then O (D columns), P (bf16 pairs of a 128-token
+// tile), Q (bf16 pairs of D dims).  D = 128 uses all 512.
+template <int D>
+struct Tmem {
+    static constexpr uint32_t S = 0;
+    static constexpr uint32_t O = 2 * kKeyTok;
+    static constexpr uint32_t P = O + D;
+    static constexpr uint32_t Q = P + kKeyTok / 2;
+    static_assert(Q + D / 2 <= kTmemCols, "TMEM budget");
+};
 
 template <int D>
 struct Smem {
     static constexpr int TILE = kBlockTokens * D * 2;          // one (block, kv head) tile
     static constexpr int KTILE = kKeyBlocks * TILE;            // one ring stage
-    static constexpr int Q = 0;                                // [D/8][16][8 rows][16 B]
-    static constexpr int P = Q + kRowsTC * D * 2;              // [16][16][8 rows][16 B]
-    static constexpr int K = P + kRowsTC * kKeyTok * 2;
-    static constexpr int V = K + 2 * KTILE;
-    static constexpr int BAR = V + 2 * KTILE;
-    static constexpr int NBAR = 15;
+    static constexpr int K = 0;                                // K tiles as copied, 2 stages
+    static constexpr int V = K + 2 * KTILE;                    // V tiles, 2 stages
+    static constexpr int CM = V + 2 * KTILE;                   // K tiles chunk-major, 2 stages
+    static constexpr int BAR = CM + 2 * KTILE;
+    static constexpr int NBAR = 17;
     static constexpr int SLOT = BAR + NBAR * 8;
     // at least 120 KB so that one CTA (and its 512 TMEM columns) owns an SM
     static constexpr int BYTES = SLOT + 16 < 122880 ? 122880 : SLOT + 16;
 };
 
-// barrier indices
-constexpr int kKFull = 0, kKEmpty = 2, kVFull = 4, kVEmpty = 6, kSFull = 8, kSFree = 10,
-              kPFull = 12, kPVDone = 13, kDone = 14;
+// barrier indices (pairs are per ring stage)
+constexpr int kKFull = 0, kVFull = 2, kVEmpty = 4, kSFull = 6, kSFree = 8, kCmFull = 10,
+              kCmFree = 12, kPFull = 14, kPVDone = 15, kDone = 16;
 
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
     return pol;
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
 }
 
 // All lanes wait; the result is made uniform across the warp.
@@ -319,9 +322,27 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
     return __all_sync(0xffffffffu, ok);
 }
 
+// Lane b < nb of the warp resolves block b0 + b of the sequence's table (-1: missing or
+// invalid, flagged); returns this lane's block and the bytes of the valid tiles.
+__device__ __forceinline__ int32_t resolve_block(const PParams& p, const int32_t* trow, int b0,
+                                                 int nb, int lane, uint32_t tile,
+                                                 uint32_t& bytes) {
+    int32_t blk = -1;
+    if (lane < nb) {
+        blk = __ldg(trow + b0 + lane);
+        if (blk < 0 || blk >= p.num_blocks) {
+            raise_flag(p.err, PA_DEV_ERR_BAD_BLOCK);
+            blk = -1;
+        }
+    }
+    bytes = (uint32_t)__popc(__ballot_sync(0xffffffffu, blk >= 0)) * tile;
+    return blk;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams p) {
     using L = Smem<D>;
+    using T = Tmem<D>;
     constexpr int TILE = L::TILE, KTILE = L::KTILE;
     constexpr int KSTEPS = D / 16;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -344,7 +365,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
     const int32_t* trow = p.tables + (size_t)s * p.max_blocks;
 
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sQ = sbase + L::Q, sP = sbase + L::P, sK = sbase + L::K, sV = sbase + L::V;
+    const uint32_t sK = sbase + L::K, sV = sbase + L::V, sCM = sbase + L::CM;
     const uint32_t bar0 = sbase + L::BAR;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
 
@@ -352,11 +373,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
 #pragma unroll
         for (int st = 0; st < 2; ++st) {
             mbar_init(bar(kKFull + st), 1);
-            mbar_init(bar(kKEmpty + st), 1);
             mbar_init(bar(kVFull + st), 1);
             mbar_init(bar(kVEmpty + st), 1);
             mbar_init(bar(kSFull + st), 1);
             mbar_init(bar(kSFree + st), kSoftWarps);
+            mbar_init(bar(kCmFull + st), 1);
+            mbar_init(bar(kCmFree + st), 1);
         }
         mbar_init(bar(kPFull), kSoftWarps);
         mbar_init(bar(kPVDone), 1);
@@ -364,9 +386,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         fence_proxy_async_smem();
     }
     if (warp == kMmaWarp) tmem_alloc<kTmemCols>(sbase + L::SLOT);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::SLOT);
 
-    // rows: (chunk token, query head of this kv head), token-major
-    const int row = threadIdx.x;                          // meaningful for the softmax warps
+    // rows: (chunk token, query head of this kv head), token-major; one per softmax thread
+    const int row = threadIdx.x;
     int pos = p_last;                                     // rows outside the chunk see all (finite)
     bool row_valid = false;
     size_t orow = 0;
@@ -378,102 +404,154 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
             orow = ((size_t)(q0 + i0 + tl) * p.Hq + (size_t)kvh * p.G + g) * D;
         }
         grid_dependency_wait();
+        // this row of Q into its TMEM lane: columns T::Q .. + D/2, two dims per column
         const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + orow);
-#pragma unroll 4
-        for (int kg = 0; kg < D / 8; ++kg) {
-            const uint4 v = row_valid ? __ldg(qsrc + kg) : make_uint4(0u, 0u, 0u, 0u);
-            st_shared_v4(sQ + (uint32_t)((kg * 16 + (row >> 3)) * 128 + (row & 7) * 16), v.x, v.y,
-                         v.z, v.w);
+        const uint32_t qaddr = tmem + ((uint32_t)(32 * warp) << 16) + T::Q;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+            uint32_t w[32];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const uint4 x = row_valid ? __ldg(qsrc + 8 * c + v) : make_uint4(0u, 0u, 0u, 0u);
+                w[4 * v] = x.x;
+                w[4 * v + 1] = x.y;
+                w[4 * v + 2] = x.z;
+                w[4 * v + 3] = x.w;
+            }
+            tmem_st32(qaddr + 32 * c, w);
         }
-        fence_proxy_async_smem();
+        tmem_wait_st();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::SLOT);
 
     if (warp == kProducerWarp) {
-        // ---------------------------------------------------------------- producer
-        if (lane == 0) {
-            grid_dependency_wait();        // the chunk's own K/V come from the append before
-            grid_launch_dependents();
-            const uint64_t pol = l2_policy_evict_last();   // tiles are re-read by other query tiles
-            int issued = 0;
-            bool ok = true;
-            auto load = [&](const char* pool, uint32_t dst, uint32_t full, int b0, int nb) {
-                int32_t blks[kKeyBlocks];
-                uint32_t bytes = 0;
-#pragma unroll
-                for (int b = 0; b < kKeyBlocks; ++b) {
-                    int32_t blk = -1;
-                    if (b < nb) {
-                        blk = __ldg(trow + b0 + b);
-                        if (blk < 0 || blk >= p.num_blocks) {
-                            raise_flag(p.err, PA_DEV_ERR_BAD_BLOCK);
-                            blk = -1;
-                        } else {
-                            bytes += TILE;
-                        }
-                    }
-                    blks[b] = blk;
-                }
+        // ---------------------------------------------------------------- V tiles
+        // one bulk copy per (block, kv head) tile, lane b handles block b
+        grid_dependency_wait();               // the chunk's own K/V come from the append before
+        __syncwarp();
+        if (lane == 0) grid_launch_dependents();
+        const uint64_t pol = l2_policy_evict_last();   // tiles are re-read by other query tiles
+        int issued = 0;
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+            const int st = j & 1;
+            const int b0 = j * kKeyBlocks, nb = min(kKeyBlocks, nblk - b0);
+            uint32_t bytes;
+            const int32_t blk = resolve_block(p, trow, b0, nb, lane, TILE, bytes);
+            if (j >= 2) {
+                ok = warp_wait(bar(kVEmpty + st), ((j >> 1) - 1) & 1);
+                if (!ok) break;
+            }
+            if (lane == 0) {
                 fence_proxy_async_smem();
-                mbar_arrive_expect_tx(full, bytes);
-#pragma unroll
-                for (int b = 0; b < kKeyBlocks; ++b)
-                    if (blks[b] >= 0)
-                        bulk_g2s(dst + b * TILE, pool + ((size_t)blks[b] * p.Hkv + kvh) * (size_t)TILE,
-                                 TILE, full, pol);
-            };
-            for (int j = 0; j < ntiles; ++j) {
-                const int st = j & 1;
-                const int b0 = j * kKeyBlocks, nb = min(kKeyBlocks, nblk - b0);
-                if (j >= 2 && !mbar_wait_bounded(bar(kKEmpty + st), ((j >> 1) - 1) & 1, kWaitLimitNs)) {
-                    ok = false;
-                    break;
-                }
-                load(p.k_pool, sK + st * KTILE, bar(kKFull + st), b0, nb);
-                if (j >= 2 && !mbar_wait_bounded(bar(kVEmpty + st), ((j >> 1) - 1) & 1, kWaitLimitNs)) {
-                    // K of tile j is in flight: wait for it below
-                    issued = j + 1;
-                    ok = false;
-                    break;
-                }
-                load(p.v_pool, sV + st * KTILE, bar(kVFull + st), b0, nb);
-                issued = j + 1;
+                mbar_arrive_expect_tx(bar(kVFull + st), bytes);
             }
-            if (!ok) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
-            // no copy may still be landing in shared memory when the CTA exits
-            for (int j = max(0, issued - 2); j < issued; ++j) {
-                const int st = j & 1;
-                mbar_wait_bounded(bar(kKFull + st), (j >> 1) & 1, kWaitLimitNs);
-                mbar_wait_bounded(bar(kVFull + st), (j >> 1) & 1, kWaitLimitNs);
-            }
+            __syncwarp();
+            if (lane < kKeyBlocks && blk >= 0)
+                bulk_g2s(sV + st * KTILE + lane * TILE, p.v_pool + ((size_t)blk * p.Hkv + kvh) * (size_t)TILE,
+                         TILE, bar(kVFull + st), pol);
+            issued = j + 1;
         }
+        if (!ok && lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
+        // no copy may still be landing when the CTA exits (a stage's earlier tile
+        // completed before the stage was refilled)
+        if (lane == 0)
+            for (int jj = max(0, issued - 2); jj < issued; ++jj)
+                mbar_wait_bounded(bar(kVFull + (jj & 1)), (jj >> 1) & 1, kWaitLimitNs);
+    } else if (warp == kRepackWarp) {
+        // ---------------------------------------------------------------- K tiles
+        // Copied in per (block, kv head) tile, [8 blocks][D/8][16 slots][16 B], then moved
+        // chunk-major, [D/8][8 blocks][16 slots][16 B]: every 8-token group of the tile is
+        // then 128 B after the previous one, so Q K^T over the tile's 128 tokens is one
+        // MMA per 16 dims.  Each (block, 8-dim chunk) run of 256 B moves whole.
+        grid_dependency_wait();
+        __syncwarp();
+        const uint64_t pol = l2_policy_evict_last();
+        int issued = 0, consumed = 0;
+        bool ok = true;
+        auto load_k = [&](int j) {
+            const int st = j & 1;
+            const int b0 = j * kKeyBlocks, nb = min(kKeyBlocks, nblk - b0);
+            uint32_t bytes;
+            const int32_t blk = resolve_block(p, trow, b0, nb, lane, TILE, bytes);
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(bar(kKFull + st), bytes);
+            }
+            __syncwarp();
+            if (lane < kKeyBlocks && blk >= 0)
+                bulk_g2s(sK + st * KTILE + lane * TILE, p.k_pool + ((size_t)blk * p.Hkv + kvh) * (size_t)TILE,
+                         TILE, bar(kKFull + st), pol);
+            issued = j + 1;
+        };
+        for (int j = 0; j < min(2, ntiles); ++j) load_k(j);
+        for (int j = 0; j < ntiles; ++j) {
+            const int st = j & 1;
+            ok = warp_wait(bar(kKFull + st), (j >> 1) & 1);
+            if (!ok) break;
+            consumed = j + 1;
+            if (j >= 2) {
+                ok = warp_wait(bar(kCmFree + st), ((j >> 1) - 1) & 1);
+                if (!ok) break;
+            }
+            const int nb = min(kKeyBlocks, nblk - j * kKeyBlocks);
+            const uint8_t* src = smem + L::K + st * KTILE;
+            uint8_t* dst = smem + L::CM + st * KTILE;
+            const int piece = (lane & 15) * 16;
+            // eight loads in flight before their stores (a store could alias a later load,
+            // so the compiler would otherwise keep each load behind the previous store)
+            constexpr int kPerLane = kKeyBlocks * (D / 8) / 2;
+#pragma unroll 1
+            for (int u0 = 0; u0 < kPerLane; u0 += 8) {
+                uint4 v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int r = (lane >> 4) + 2 * (u0 + u);
+                    const int b = r / (D / 8), c = r % (D / 8);
+                    if (b < nb) v[u] = *reinterpret_cast<const uint4*>(src + b * TILE + c * 256 + piece);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int r = (lane >> 4) + 2 * (u0 + u);
+                    const int b = r / (D / 8), c = r % (D / 8);
+                    if (b < nb) *reinterpret_cast<uint4*>(dst + c * (kKeyBlocks * 256) + b * 256 + piece) = v[u];
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kCmFull + st));
+            // the copy stage is free again: fetch tile j + 2 into it
+            if (j + 2 < ntiles) load_k(j + 2);
+        }
+        if (!ok && lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
+        if (lane == 0)
+            for (int jj = consumed; jj < issued; ++jj)
+                mbar_wait_bounded(bar(kKFull + (jj & 1)), (jj >> 1) & 1, kWaitLimitNs);
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issue
-        constexpr uint32_t idS = umma_idesc_bf16(128, 16, 0);
+        // S_j = Q K_j^T: A = Q from TMEM, B = the chunk-major K tile, N = 128 tokens.
+        // O += P_j V_j: A = P from TMEM, B = one V block tile (MN-major), K = 16 tokens.
+        constexpr uint32_t idS = umma_idesc_bf16(128, kKeyTok, 0);
         constexpr uint32_t idO = umma_idesc_bf16(128, D, 1);
-        const uint64_t qdesc = umma_desc(sQ, 2048, 128);
-        const uint64_t pdesc = umma_desc(sP, 2048, 128);
         bool ok = true;
         auto issue_s = [&](int j) {
             const int st = j & 1;
-            ok = warp_wait(bar(kKFull + st), (j >> 1) & 1);
+            ok = warp_wait(bar(kCmFull + st), (j >> 1) & 1);
             if (ok && j >= 2) ok = warp_wait(bar(kSFree + st), ((j >> 1) - 1) & 1);
             if (!ok) return;
             tc_fence_after();
             if (lane == 0) {
-                const int nb = min(kKeyBlocks, nblk - j * kKeyBlocks);
-                const uint64_t kdesc = umma_desc(sK + st * KTILE, 256, 128);
-                const uint32_t dcol = tmem + (uint32_t)(st * kKeyTok);
-                for (int b = 0; b < nb; ++b)
+                // columns of blocks past the tile's last one hold stale products (masked)
+                const uint64_t kdesc = umma_desc(sCM + st * KTILE, kKeyBlocks * 256, 128);
+                const uint32_t dcol = tmem + T::S + (uint32_t)(st * kKeyTok);
 #pragma unroll
-                    for (int ks = 0; ks < KSTEPS; ++ks)
-                        umma_ss(dcol + 16 * b, qdesc + (uint64_t)(ks * 256),
-                                kdesc + (uint64_t)((b * TILE + ks * 512) >> 4), idS, ks > 0);
+                for (int ks = 0; ks < KSTEPS; ++ks)
+                    umma_ts(dcol, tmem + T::Q + 8 * ks,
+                            kdesc + (uint64_t)((ks * 2 * kKeyBlocks * 256) >> 4), idS, ks > 0);
                 umma_commit(bar(kSFull + st));
-                umma_commit(bar(kKEmpty + st));
+                umma_commit(bar(kCmFree + st));
             }
             __syncwarp();
         };
@@ -501,8 +579,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
             if (lane == 0) {
                 const uint64_t vdesc = umma_desc(sV + st * KTILE, 128, 256);
                 for (int b = 0; b < nb; ++b)
-                    umma_ss(tmem + kColO, pdesc + (uint64_t)(b * 256),
-                            vdesc + (uint64_t)((b * TILE) >> 4), idO, (j > 0 || b > 0) ? 1u : 0u);
+                    umma_ts(tmem + T::O, tmem + T::P + 8 * b, vdesc + (uint64_t)((b * TILE) >> 4), idO,
+                            (j > 0 || b > 0) ? 1u : 0u);
                 umma_commit(bar(kPVDone));
                 umma_commit(bar(kVEmpty + st));
             }
@@ -521,7 +599,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
     } else {
         // ---------------------------------------------------------------- softmax rows
         const uint32_t tl_addr = tmem + ((uint32_t)(32 * warp) << 16);
-        const uint32_t prow = sP + (uint32_t)((row >> 3) * 128 + (row & 7) * 16);
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
@@ -531,7 +608,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
             tc_fence_after();
             uint32_t sr[4][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(tl_addr + (uint32_t)(st * kKeyTok + 32 * c), sr[c]);
+            for (int c = 0; c < 4; ++c) tmem_ld32(tl_addr + T::S + (uint32_t)(st * kKeyTok + 32 * c), sr[c]);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
@@ -568,7 +645,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
                 m_used = mx;
             }
             float sum = 0.f;
-            uint32_t pk[64];
+            uint32_t pk[2][32];
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -576,10 +653,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
                     const float e0 = fast_exp2(__uint_as_float(sr[c][i]) - m_used);
                     const float e1 = fast_exp2(__uint_as_float(sr[c][i + 1]) - m_used);
                     sum += e0 + e1;
-                    pk[(32 * c + i) >> 1] = pack_bf16x2(e0, e1);
+                    pk[c >> 1][((c & 1) * 32 + i) >> 1] = pack_bf16x2(e0, e1);
                 }
             l = l * alpha + sum;
-            // PV_{j-1} done: the P tile is free and O is not being written
+            // PV_{j-1} done: P's columns are free and O is not being written
             if (j > 0) {
                 ok = warp_wait(bar(kPVDone), (j - 1) & 1);
                 if (!ok) break;
@@ -589,18 +666,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
-                    tmem_ld32(tl_addr + kColO + 32 * c, o);
+                    tmem_ld32(tl_addr + T::O + 32 * c, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(tl_addr + kColO + 32 * c, o);
+                    tmem_st32(tl_addr + T::O + 32 * c, o);
                 }
-                tmem_wait_st();
             }
-#pragma unroll
-            for (int kg = 0; kg < kKeyTok / 8; ++kg)
-                st_shared_v4(prow + kg * 2048, pk[4 * kg], pk[4 * kg + 1], pk[4 * kg + 2], pk[4 * kg + 3]);
-            fence_proxy_async_smem();
+            tmem_st32(tl_addr + T::P, pk[0]);
+            tmem_st32(tl_addr + T::P + 32, pk[1]);
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kPFull));
@@ -613,7 +688,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
-                tmem_ld32(tl_addr + kColO + 32 * c, o);
+                tmem_ld32(tl_addr + T::O + 32 * c, o);
                 tmem_wait_ld();
                 if (row_valid) {
 #pragma unroll

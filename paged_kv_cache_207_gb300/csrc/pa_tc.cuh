@@ -76,6 +76,19 @@ __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc]^T.  A (M = 128 rows) sits one row per TMEM
+// lane, K elements packed two per 32-bit column (element 2w in the low half of
+// column w), so a K = 16 step reads 8 columns.
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
 // Arrive once on the mbarrier when every MMA this thread issued so far is done.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile(
