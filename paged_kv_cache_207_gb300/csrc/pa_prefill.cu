@@ -270,10 +270,15 @@ prefill_bf16_kernel(const PParams p) {
 
 namespace tc {
 
-constexpr int kRowsTC = 128;
+// Two Q tiles of 128 rows (a, b) per CTA share every K/V tile; each has its own softmax
+// warpgroup, S and O in TMEM.  The MMA thread interleaves them so that one tile's
+// softmax runs while the tensor cores work for the other:
+//   S_a(0) S_b(0) | PV_a(0) S_a(1) PV_b(0) S_b(1) | PV_a(1) S_a(2) ...
+constexpr int kHalfRows = 128;
+constexpr int kRowsTC = 2 * kHalfRows;
 constexpr int kKeyBlocks = 8;
 constexpr int kKeyTok = kKeyBlocks * kBlockTokens;
-constexpr int kSoftWarps = 4;
+constexpr int kSoftWarps = 8;                   // warps 0-3: tile a, 4-7: tile b
 constexpr int kProducerWarp = kSoftWarps;       // V tiles
 constexpr int kMmaWarp = kSoftWarps + 1;        // TMEM owner, MMA issue
 constexpr int kRepackWarp = kSoftWarps + 2;     // K tiles: copy in, repack chunk-major
@@ -281,39 +286,41 @@ constexpr int kThreadsTC = (kSoftWarps + 3) * 32;
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;
 
-// TMEM columns: S double buffer, then O (D columns), P (bf16 pairs of a 128-token
-// tile), Q (bf16 pairs of D dims).  D = 128 uses all 512.
-template <int D>
-struct Tmem {
-    static constexpr uint32_t S = 0;
-    static constexpr uint32_t O = 2 * kKeyTok;
-    static constexpr uint32_t P = O + D;
-    static constexpr uint32_t Q = P + kKeyTok / 2;
-    static_assert(Q + D / 2 <= kTmemCols, "TMEM budget");
-};
+// TMEM columns: S of tile h at 128 h (its bf16 P over the first 64 once S is read), O of
+// tile h at 256 + 128 h.
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColO = 2 * kKeyTok;
 
 template <int D>
 struct Smem {
     static constexpr int TILE = kBlockTokens * D * 2;          // one (block, kv head) tile
     static constexpr int KTILE = kKeyBlocks * TILE;            // one ring stage
-    static constexpr int K = 0;                                // K tiles as copied, 2 stages
+    static constexpr int QTILE = kHalfRows * D * 2;            // [D/8][16][8 rows][16 B]
+    static constexpr int Q = 0;                                // tiles a, b
+    static constexpr int K = Q + 2 * QTILE;                    // K tiles as copied, 2 stages
     static constexpr int V = K + 2 * KTILE;                    // V tiles, 2 stages
-    static constexpr int CM = V + 2 * KTILE;                   // K tiles chunk-major, 2 stages
-    static constexpr int BAR = CM + 2 * KTILE;
-    static constexpr int NBAR = 17;
+    static constexpr int CM = V + 2 * KTILE;                   // K tile chunk-major
+    static constexpr int BAR = CM + KTILE;
+    static constexpr int NBAR = 15;
     static constexpr int SLOT = BAR + NBAR * 8;
     // at least 120 KB so that one CTA (and its 512 TMEM columns) owns an SM
     static constexpr int BYTES = SLOT + 16 < 122880 ? 122880 : SLOT + 16;
 };
 
-// barrier indices (pairs are per ring stage)
-constexpr int kKFull = 0, kVFull = 2, kVEmpty = 4, kSFull = 6, kSFree = 8, kCmFull = 10,
-              kCmFree = 12, kPFull = 14, kPVDone = 15, kDone = 16;
+// barrier indices
+constexpr int kKFull = 0, kVFull = 2, kVEmpty = 4, kCmFull = 6, kCmFree = 7, kSFull = 8,
+              kPFull = 10, kODone = 12, kDone = 14;
 
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
     return pol;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
 }
 
 // All lanes wait; the result is made uniform across the warp.
@@ -322,27 +329,29 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
     return __all_sync(0xffffffffu, ok);
 }
 
-// Lane b < nb of the warp resolves block b0 + b of the sequence's table (-1: missing or
-// invalid, flagged); returns this lane's block and the bytes of the valid tiles.
-__device__ __forceinline__ int32_t resolve_block(const PParams& p, const int32_t* trow, int b0,
-                                                 int nb, int lane, uint32_t tile,
-                                                 uint32_t& bytes) {
-    int32_t blk = -1;
-    if (lane < nb) {
-        blk = __ldg(trow + b0 + lane);
-        if (blk < 0 || blk >= p.num_blocks) {
-            raise_flag(p.err, PA_DEV_ERR_BAD_BLOCK);
-            blk = -1;
-        }
+// Table entry of block b of key tile j for lane b of a warp (-1 for lanes past the
+// tile's or the sequence's last block).
+__device__ __forceinline__ int32_t fetch_block(const int32_t* trow, int j, int nblk, int ntiles,
+                                               int lane) {
+    const int b = j * kKeyBlocks + lane;
+    return (j < ntiles && lane < kKeyBlocks && b < nblk) ? __ldg(trow + b) : -1;
+}
+
+// Flags a needed block whose entry is not a block of the pool (its tile is skipped) and
+// returns the bytes of the tile's valid block tiles.
+__device__ __forceinline__ uint32_t check_blocks(const PParams& p, int32_t& blk, int j, int nblk,
+                                                 int lane, uint32_t tile) {
+    const bool needed = lane < kKeyBlocks && j * kKeyBlocks + lane < nblk;
+    if (needed && (blk < 0 || blk >= p.num_blocks)) {
+        raise_flag(p.err, PA_DEV_ERR_BAD_BLOCK);
+        blk = -1;
     }
-    bytes = (uint32_t)__popc(__ballot_sync(0xffffffffu, blk >= 0)) * tile;
-    return blk;
+    return (uint32_t)__popc(__ballot_sync(0xffffffffu, blk >= 0)) * tile;
 }
 
 template <int D>
 __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams p) {
     using L = Smem<D>;
-    using T = Tmem<D>;
     constexpr int TILE = L::TILE, KTILE = L::KTILE;
     constexpr int KSTEPS = D / 16;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -355,7 +364,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
     if (i0 >= n) return;
     const int start = __ldg(p.start_pos + s);
     const int i_end = min(n, i0 + p.TQ);
-    const int p_last = start + i_end - 1;                 // last position this tile attends to
+    const int p_last = start + i_end - 1;                 // last position this CTA attends to
     if (start < 0 || p_last >= p.max_blocks * kBlockTokens) {
         if (threadIdx.x == 0 && kvh == 0) raise_flag(p.err, PA_DEV_ERR_BAD_POS);
         return;
@@ -363,36 +372,35 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
     const int nblk = p_last / kBlockTokens + 1;
     const int ntiles = (nblk + kKeyBlocks - 1) / kKeyBlocks;
     const int32_t* trow = p.tables + (size_t)s * p.max_blocks;
+    // tile b holds rows 128 .. 255; it is skipped when none of them is a chunk row
+    const int tl_b = kHalfRows / p.G;
+    const bool has_b = tl_b < p.TQ && i0 + tl_b < n;
 
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sK = sbase + L::K, sV = sbase + L::V, sCM = sbase + L::CM;
+    const uint32_t sQ = sbase + L::Q, sK = sbase + L::K, sV = sbase + L::V, sCM = sbase + L::CM;
     const uint32_t bar0 = sbase + L::BAR;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
 
     if (threadIdx.x == 0) {
 #pragma unroll
-        for (int st = 0; st < 2; ++st) {
-            mbar_init(bar(kKFull + st), 1);
-            mbar_init(bar(kVFull + st), 1);
-            mbar_init(bar(kVEmpty + st), 1);
-            mbar_init(bar(kSFull + st), 1);
-            mbar_init(bar(kSFree + st), kSoftWarps);
-            mbar_init(bar(kCmFull + st), 1);
-            mbar_init(bar(kCmFree + st), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(kKFull + i), 1);
+            mbar_init(bar(kVFull + i), 1);
+            mbar_init(bar(kVEmpty + i), 1);
+            mbar_init(bar(kSFull + i), 1);
+            mbar_init(bar(kPFull + i), 4);
+            mbar_init(bar(kODone + i), 1);
         }
-        mbar_init(bar(kPFull), kSoftWarps);
-        mbar_init(bar(kPVDone), 1);
+        mbar_init(bar(kCmFull), 1);
+        mbar_init(bar(kCmFree), 1);
         mbar_init(bar(kDone), 1);
         fence_proxy_async_smem();
     }
     if (warp == kMmaWarp) tmem_alloc<kTmemCols>(sbase + L::SLOT);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::SLOT);
 
     // rows: (chunk token, query head of this kv head), token-major; one per softmax thread
-    const int row = threadIdx.x;
+    const int row = threadIdx.x;                          // 0 .. 255 for the softmax warps
+    const int h = warp >> 2;                              // Q tile of a softmax warp
     int pos = p_last;                                     // rows outside the chunk see all (finite)
     bool row_valid = false;
     size_t orow = 0;
@@ -404,27 +412,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
             orow = ((size_t)(q0 + i0 + tl) * p.Hq + (size_t)kvh * p.G + g) * D;
         }
         grid_dependency_wait();
-        // this row of Q into its TMEM lane: columns T::Q .. + D/2, two dims per column
         const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + orow);
-        const uint32_t qaddr = tmem + ((uint32_t)(32 * warp) << 16) + T::Q;
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-            uint32_t w[32];
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-                const uint4 x = row_valid ? __ldg(qsrc + 8 * c + v) : make_uint4(0u, 0u, 0u, 0u);
-                w[4 * v] = x.x;
-                w[4 * v + 1] = x.y;
-                w[4 * v + 2] = x.z;
-                w[4 * v + 3] = x.w;
-            }
-            tmem_st32(qaddr + 32 * c, w);
-        }
-        tmem_wait_st();
+        const int lr = row & (kHalfRows - 1);
+        const uint32_t qdst = sQ + h * L::QTILE + (uint32_t)((lr >> 3) * 128 + (lr & 7) * 16);
+#pragma unroll 4
+        for (int kg = 0; kg < D / 8; ++kg)
+            st_shared_v4(qdst + kg * 2048, row_valid ? __ldg(qsrc + kg) : make_uint4(0u, 0u, 0u, 0u));
+        fence_proxy_async_smem();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::SLOT);
 
     if (warp == kProducerWarp) {
         // ---------------------------------------------------------------- V tiles
@@ -435,11 +434,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         const uint64_t pol = l2_policy_evict_last();   // tiles are re-read by other query tiles
         int issued = 0;
         bool ok = true;
+        int32_t next_blk = fetch_block(trow, 0, nblk, ntiles, lane);
         for (int j = 0; j < ntiles; ++j) {
             const int st = j & 1;
-            const int b0 = j * kKeyBlocks, nb = min(kKeyBlocks, nblk - b0);
-            uint32_t bytes;
-            const int32_t blk = resolve_block(p, trow, b0, nb, lane, TILE, bytes);
+            int32_t blk = next_blk;
+            next_blk = fetch_block(trow, j + 1, nblk, ntiles, lane);   // in flight during the wait
+            const uint32_t bytes = check_blocks(p, blk, j, nblk, lane, TILE);
             if (j >= 2) {
                 ok = warp_wait(bar(kVEmpty + st), ((j >> 1) - 1) & 1);
                 if (!ok) break;
@@ -471,11 +471,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         const uint64_t pol = l2_policy_evict_last();
         int issued = 0, consumed = 0;
         bool ok = true;
-        auto load_k = [&](int j) {
+        auto load_k = [&](int j, int32_t blk) {
             const int st = j & 1;
-            const int b0 = j * kKeyBlocks, nb = min(kKeyBlocks, nblk - b0);
-            uint32_t bytes;
-            const int32_t blk = resolve_block(p, trow, b0, nb, lane, TILE, bytes);
+            const uint32_t bytes = check_blocks(p, blk, j, nblk, lane, TILE);
             if (lane == 0) {
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(bar(kKFull + st), bytes);
@@ -486,34 +484,35 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
                          TILE, bar(kKFull + st), pol);
             issued = j + 1;
         };
-        for (int j = 0; j < min(2, ntiles); ++j) load_k(j);
+        for (int j = 0; j < min(2, ntiles); ++j) load_k(j, fetch_block(trow, j, nblk, ntiles, lane));
         for (int j = 0; j < ntiles; ++j) {
             const int st = j & 1;
+            const int32_t next_blk = fetch_block(trow, j + 2, nblk, ntiles, lane);   // in flight
             ok = warp_wait(bar(kKFull + st), (j >> 1) & 1);
             if (!ok) break;
             consumed = j + 1;
-            if (j >= 2) {
-                ok = warp_wait(bar(kCmFree + st), ((j >> 1) - 1) & 1);
+            if (j >= 1) {                     // the S MMAs of tile j - 1 have read the buffer
+                ok = warp_wait(bar(kCmFree), (j - 1) & 1);
                 if (!ok) break;
             }
             const int nb = min(kKeyBlocks, nblk - j * kKeyBlocks);
             const uint8_t* src = smem + L::K + st * KTILE;
-            uint8_t* dst = smem + L::CM + st * KTILE;
+            uint8_t* dst = smem + L::CM;
             const int piece = (lane & 15) * 16;
-            // eight loads in flight before their stores (a store could alias a later load,
-            // so the compiler would otherwise keep each load behind the previous store)
+            // sixteen loads in flight before their stores (a store could alias a later
+            // load, so the compiler would otherwise keep each load behind the previous store)
             constexpr int kPerLane = kKeyBlocks * (D / 8) / 2;
 #pragma unroll 1
-            for (int u0 = 0; u0 < kPerLane; u0 += 8) {
-                uint4 v[8];
+            for (int u0 = 0; u0 < kPerLane; u0 += 16) {
+                uint4 v[16];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
+                for (int u = 0; u < 16; ++u) {
                     const int r = (lane >> 4) + 2 * (u0 + u);
                     const int b = r / (D / 8), c = r % (D / 8);
                     if (b < nb) v[u] = *reinterpret_cast<const uint4*>(src + b * TILE + c * 256 + piece);
                 }
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
+                for (int u = 0; u < 16; ++u) {
                     const int r = (lane >> 4) + 2 * (u0 + u);
                     const int b = r / (D / 8), c = r % (D / 8);
                     if (b < nb) *reinterpret_cast<uint4*>(dst + c * (kKeyBlocks * 256) + b * 256 + piece) = v[u];
@@ -521,9 +520,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kCmFull + st));
+            if (lane == 0) mbar_arrive(bar(kCmFull));
             // the copy stage is free again: fetch tile j + 2 into it
-            if (j + 2 < ntiles) load_k(j + 2);
+            if (j + 2 < ntiles) load_k(j + 2, next_blk);
         }
         if (!ok && lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
         if (lane == 0)
@@ -531,88 +530,114 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
                 mbar_wait_bounded(bar(kKFull + (jj & 1)), (jj >> 1) & 1, kWaitLimitNs);
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issue
-        // S_j = Q K_j^T: A = Q from TMEM, B = the chunk-major K tile, N = 128 tokens.
-        // O += P_j V_j: A = P from TMEM, B = one V block tile (MN-major), K = 16 tokens.
+        // S_h(j) = Q_h K_j^T: A = Q_h (shared), B = the chunk-major K tile, N = 128 tokens.
+        // O_h += P_h(j) V_j: A = P_h(j) in TMEM (over S_h's first columns), B = one V block
+        // tile (MN-major), K = 16 tokens.  MMAs of this thread execute in issue order, so
+        // S_h(j + 1) overwrites P_h(j) only after PV_h(j) has read it, and a commit after
+        // S_h(j + 1) also covers PV_h(j).
         constexpr uint32_t idS = umma_idesc_bf16(128, kKeyTok, 0);
         constexpr uint32_t idO = umma_idesc_bf16(128, D, 1);
+        const uint64_t kdesc = umma_desc(sCM, kKeyBlocks * 256, 128);
         bool ok = true;
-        auto issue_s = [&](int j) {
-            const int st = j & 1;
-            ok = warp_wait(bar(kCmFull + st), (j >> 1) & 1);
-            if (ok && j >= 2) ok = warp_wait(bar(kSFree + st), ((j >> 1) - 1) & 1);
-            if (!ok) return;
+        auto issue_s = [&](int hh) {
             tc_fence_after();
             if (lane == 0) {
                 // columns of blocks past the tile's last one hold stale products (masked)
-                const uint64_t kdesc = umma_desc(sCM + st * KTILE, kKeyBlocks * 256, 128);
-                const uint32_t dcol = tmem + T::S + (uint32_t)(st * kKeyTok);
+                const uint64_t qdesc = umma_desc(sQ + hh * L::QTILE, 2048, 128);
+                const uint32_t dcol = tmem + kColS + (uint32_t)(hh * kKeyTok);
 #pragma unroll
                 for (int ks = 0; ks < KSTEPS; ++ks)
-                    umma_ts(dcol, tmem + T::Q + 8 * ks,
+                    umma_ss(dcol, qdesc + (uint64_t)(ks * 256),
                             kdesc + (uint64_t)((ks * 2 * kKeyBlocks * 256) >> 4), idS, ks > 0);
-                umma_commit(bar(kSFull + st));
-                umma_commit(bar(kCmFree + st));
+                umma_commit(bar(kSFull + hh));
             }
             __syncwarp();
         };
-        auto issue_pv = [&](int j) {
+        auto issue_pv = [&](int hh, int j) {
             const int st = j & 1;
-            ok = warp_wait(bar(kPFull), j & 1);
-            if (ok) ok = warp_wait(bar(kVFull + st), (j >> 1) & 1);
+            ok = warp_wait(bar(kPFull + hh), j & 1);
             if (!ok) return;
             const int nb = min(kKeyBlocks, nblk - j * kKeyBlocks);
-            if (j == ntiles - 1) {
-                // V rows past the last attended position may hold anything (even NaN)
-                const int first_stale = p_last - (nblk - 1) * kBlockTokens + 1;
-                if (first_stale < kBlockTokens) {
-                    const int nst = kBlockTokens - first_stale;
-                    uint8_t* vt = smem + L::V + st * KTILE + (nb - 1) * TILE;
-                    for (int idx = lane; idx < (D / 8) * nst; idx += 32) {
-                        const int c = idx / nst, sl = first_stale + (idx - c * nst);
-                        *reinterpret_cast<uint4*>(vt + c * 256 + sl * 16) = make_uint4(0u, 0u, 0u, 0u);
+            if (hh == 0) {
+                ok = warp_wait(bar(kVFull + st), (j >> 1) & 1);
+                if (!ok) return;
+                if (j == ntiles - 1) {
+                    // V rows past the last attended position may hold anything (even NaN)
+                    const int first_stale = p_last - (nblk - 1) * kBlockTokens + 1;
+                    if (first_stale < kBlockTokens) {
+                        const int nst = kBlockTokens - first_stale;
+                        uint8_t* vt = smem + L::V + st * KTILE + (nb - 1) * TILE;
+                        for (int idx = lane; idx < (D / 8) * nst; idx += 32) {
+                            const int c = idx / nst, sl = first_stale + (idx - c * nst);
+                            *reinterpret_cast<uint4*>(vt + c * 256 + sl * 16) = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        fence_proxy_async_smem();
                     }
-                    fence_proxy_async_smem();
+                    __syncwarp();
                 }
-                __syncwarp();
             }
             tc_fence_after();
             if (lane == 0) {
                 const uint64_t vdesc = umma_desc(sV + st * KTILE, 128, 256);
+                const uint32_t pcol = tmem + kColS + (uint32_t)(hh * kKeyTok);
+                const uint32_t ocol = tmem + kColO + (uint32_t)(hh * kKeyTok);
                 for (int b = 0; b < nb; ++b)
-                    umma_ts(tmem + T::O, tmem + T::P + 8 * b, vdesc + (uint64_t)((b * TILE) >> 4), idO,
+                    umma_ts(ocol, pcol + 8 * b, vdesc + (uint64_t)((b * TILE) >> 4), idO,
                             (j > 0 || b > 0) ? 1u : 0u);
-                umma_commit(bar(kPVDone));
-                umma_commit(bar(kVEmpty + st));
+                if (j == ntiles - 1) umma_commit(bar(kODone + hh));
+                if (hh == 1 || !has_b) umma_commit(bar(kVEmpty + st));
             }
             __syncwarp();
         };
-        issue_s(0);
+        ok = warp_wait(bar(kCmFull), 0);
+        if (ok) {
+            issue_s(0);
+            if (has_b) issue_s(1);
+            if (lane == 0) umma_commit(bar(kCmFree));
+            __syncwarp();
+        }
         for (int j = 0; ok && j < ntiles; ++j) {
-            if (j + 1 < ntiles) issue_s(j + 1);
-            if (ok) issue_pv(j);
+            const bool more = j + 1 < ntiles;
+            issue_pv(0, j);
+            if (!ok) break;
+            if (more) {
+                ok = warp_wait(bar(kCmFull), (j + 1) & 1);
+                if (!ok) break;
+                issue_s(0);
+            }
+            if (has_b) {
+                issue_pv(1, j);
+                if (!ok) break;
+                if (more) issue_s(1);
+            }
+            if (more) {
+                if (lane == 0) umma_commit(bar(kCmFree));
+                __syncwarp();
+            }
         }
         if (!ok && lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
         // nothing may still be running on the tensor cores when TMEM is freed
         if (lane == 0) umma_commit(bar(kDone));
         __syncwarp();
         mbar_wait_bounded(bar(kDone), 0, kWaitLimitNs);
-    } else {
+    } else if (h == 0 || has_b) {
         // ---------------------------------------------------------------- softmax rows
-        const uint32_t tl_addr = tmem + ((uint32_t)(32 * warp) << 16);
+        // Warp w reaches TMEM lanes 32 (w % 4) ..; this thread's row of tile h is lane
+        // row % 128.  A commit after S_h(j) covers every earlier MMA, so when S_h(j) is
+        // seen complete, PV_h(j - 1) is too: O_h may be rescaled and P_h(j) written at once.
+        const uint32_t tl_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        const uint32_t scol = kColS + (uint32_t)(h * kKeyTok);
+        const uint32_t ocol = kColO + (uint32_t)(h * kKeyTok);
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
-            const int st = j & 1;
-            ok = warp_wait(bar(kSFull + st), (j >> 1) & 1);
+            ok = warp_wait(bar(kSFull + h), j & 1);
             if (!ok) break;
             tc_fence_after();
             uint32_t sr[4][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(tl_addr + T::S + (uint32_t)(st * kKeyTok + 32 * c), sr[c]);
+            for (int c = 0; c < 4; ++c) tmem_ld32(tl_addr + scol + 32 * c, sr[c]);
             tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kSFree + st));
             // scale, causal mask (select: unread or stale columns may hold NaN)
             const int tok0 = j * kKeyTok;
             float mx = -INFINITY;
@@ -644,43 +669,41 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
                 resc = j > 0;
                 m_used = mx;
             }
-            float sum = 0.f;
-            uint32_t pk[2][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const float e0 = fast_exp2(__uint_as_float(sr[c][i]) - m_used);
-                    const float e1 = fast_exp2(__uint_as_float(sr[c][i + 1]) - m_used);
-                    sum += e0 + e1;
-                    pk[c >> 1][((c & 1) * 32 + i) >> 1] = pack_bf16x2(e0, e1);
-                }
-            l = l * alpha + sum;
-            // PV_{j-1} done: P's columns are free and O is not being written
-            if (j > 0) {
-                ok = warp_wait(bar(kPVDone), (j - 1) & 1);
-                if (!ok) break;
-                tc_fence_after();
-            }
             if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
-                    tmem_ld32(tl_addr + T::O + 32 * c, o);
+                    tmem_ld32(tl_addr + ocol + 32 * c, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(tl_addr + T::O + 32 * c, o);
+                    tmem_st32(tl_addr + ocol + 32 * c, o);
                 }
             }
-            tmem_st32(tl_addr + T::P, pk[0]);
-            tmem_st32(tl_addr + T::P + 32, pk[1]);
+            // probabilities, bf16 pairs, over the first 64 columns of S_h (already read)
+            float sum = 0.f;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const int c = 2 * half + cc;
+                        const float e0 = fast_exp2(__uint_as_float(sr[c][i]) - m_used);
+                        const float e1 = fast_exp2(__uint_as_float(sr[c][i + 1]) - m_used);
+                        sum += e0 + e1;
+                        pk[16 * cc + (i >> 1)] = pack_bf16x2(e0, e1);
+                    }
+                tmem_st32(tl_addr + scol + 32 * half, pk);
+            }
+            l = l * alpha + sum;
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kPFull));
+            if (lane == 0) mbar_arrive(bar(kPFull + h));
         }
-        if (ok) ok = warp_wait(bar(kPVDone), (ntiles - 1) & 1);
+        if (ok) ok = warp_wait(bar(kODone + h), 0);
         if (ok) {
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -688,7 +711,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
-                tmem_ld32(tl_addr + T::O + 32 * c, o);
+                tmem_ld32(tl_addr + ocol + 32 * c, o);
                 tmem_wait_ld();
                 if (row_valid) {
 #pragma unroll
