@@ -282,7 +282,8 @@ constexpr int kSoftWarps = 8;                   // warps 0-3: tile a, 4-7: tile 
 constexpr int kProducerWarp = kSoftWarps;       // V tiles
 constexpr int kMmaWarp = kSoftWarps + 1;        // TMEM owner, MMA issue
 constexpr int kRepackWarp = kSoftWarps + 2;     // K tiles: copy in, repack chunk-major
-constexpr int kThreadsTC = (kSoftWarps + 3) * 32;
+constexpr int kRepackWarps = 2;
+constexpr int kThreadsTC = (kSoftWarps + 2 + kRepackWarps) * 32;
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;
 
@@ -391,7 +392,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
             mbar_init(bar(kPFull + i), 4);
             mbar_init(bar(kODone + i), 1);
         }
-        mbar_init(bar(kCmFull), 1);
+        mbar_init(bar(kCmFull), kRepackWarps);
         mbar_init(bar(kCmFree), 1);
         mbar_init(bar(kDone), 1);
         fence_proxy_async_smem();
@@ -460,12 +461,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         if (lane == 0)
             for (int jj = max(0, issued - 2); jj < issued; ++jj)
                 mbar_wait_bounded(bar(kVFull + (jj & 1)), (jj >> 1) & 1, kWaitLimitNs);
-    } else if (warp == kRepackWarp) {
+    } else if (warp >= kRepackWarp) {
         // ---------------------------------------------------------------- K tiles
         // Copied in per (block, kv head) tile, [8 blocks][D/8][16 slots][16 B], then moved
         // chunk-major, [D/8][8 blocks][16 slots][16 B]: every 8-token group of the tile is
         // then 128 B after the previous one, so Q K^T over the tile's 128 tokens is one
-        // MMA per 16 dims.  Each (block, 8-dim chunk) run of 256 B moves whole.
+        // MMA per 16 dims.  Each (block, 8-dim chunk) run of 256 B moves whole; the two
+        // repack warps take half of the runs each, and the first also issues the copies.
+        const int rw = warp - kRepackWarp;
         grid_dependency_wait();
         __syncwarp();
         const uint64_t pol = l2_policy_evict_last();
@@ -484,10 +487,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
                          TILE, bar(kKFull + st), pol);
             issued = j + 1;
         };
-        for (int j = 0; j < min(2, ntiles); ++j) load_k(j, fetch_block(trow, j, nblk, ntiles, lane));
+        if (rw == 0)
+            for (int j = 0; j < min(2, ntiles); ++j) load_k(j, fetch_block(trow, j, nblk, ntiles, lane));
         for (int j = 0; j < ntiles; ++j) {
             const int st = j & 1;
-            const int32_t next_blk = fetch_block(trow, j + 2, nblk, ntiles, lane);   // in flight
+            const int32_t next_blk = rw == 0 ? fetch_block(trow, j + 2, nblk, ntiles, lane) : -1;
             ok = warp_wait(bar(kKFull + st), (j >> 1) & 1);
             if (!ok) break;
             consumed = j + 1;
@@ -501,19 +505,21 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
             const int piece = (lane & 15) * 16;
             // sixteen loads in flight before their stores (a store could alias a later
             // load, so the compiler would otherwise keep each load behind the previous store)
-            constexpr int kPerLane = kKeyBlocks * (D / 8) / 2;
+            constexpr int kRuns = kKeyBlocks * (D / 8);
+            constexpr int kPerLane = kRuns / (2 * kRepackWarps);
+            const int r0 = rw * (kRuns / kRepackWarps) + (lane >> 4);
 #pragma unroll 1
             for (int u0 = 0; u0 < kPerLane; u0 += 16) {
                 uint4 v[16];
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
-                    const int r = (lane >> 4) + 2 * (u0 + u);
+                    const int r = r0 + 2 * (u0 + u);
                     const int b = r / (D / 8), c = r % (D / 8);
                     if (b < nb) v[u] = *reinterpret_cast<const uint4*>(src + b * TILE + c * 256 + piece);
                 }
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
-                    const int r = (lane >> 4) + 2 * (u0 + u);
+                    const int r = r0 + 2 * (u0 + u);
                     const int b = r / (D / 8), c = r % (D / 8);
                     if (b < nb) *reinterpret_cast<uint4*>(dst + c * (kKeyBlocks * 256) + b * 256 + piece) = v[u];
                 }
@@ -521,8 +527,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kCmFull));
-            // the copy stage is free again: fetch tile j + 2 into it
-            if (j + 2 < ntiles) load_k(j + 2, next_blk);
+            if (rw == 0 && j + 2 < ntiles) {
+                // both warps are done with the copy stage: fetch tile j + 2 into it
+                ok = warp_wait(bar(kCmFull), j & 1);
+                if (!ok) break;
+                load_k(j + 2, next_blk);
+            }
         }
         if (!ok && lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
         if (lane == 0)
