@@ -850,194 +850,6 @@ decode_reduce_kernel(const KParams p, int num_rows) {
     }
 }
 
-// ---------------------------------------------------------------------------
-// Shared-prefix kernel (bf16): the partitions that lie inside a prefix shared by
-// every sequence of the batch (the blocks a copy-on-write fork leaves shared,
-// spindle "Paging") are read ONCE per kv head and applied to the queries of all
-// sequences.  Rows are (sequence, query head of this kv head) pairs -- S * G of
-// them -- so the scores form a real matrix product Q[rows x D] K^T[D x 16] per
-// block; FlashAttention-2 style, each consumer warp owns 16 rows, P stays in
-// registers as the A operand of P.V, and V is read with ldmatrix.trans.  A
-// producer warp streams the partition's K/V tiles (through sequence 0's table)
-// into a ring shared by the CTA: `full` barriers complete on the bulk copies,
-// `empty` barriers on the four consumer warps.  Output: the same per-partition
-// partials (o, max, sum) as the main kernel, merged by decode_reduce_kernel.
-// ---------------------------------------------------------------------------
-#ifndef PA_PREFIX_CONSUMERS
-#define PA_PREFIX_CONSUMERS 2
-#endif
-constexpr int kPrefixConsumers = PA_PREFIX_CONSUMERS;  // consumer warps per CTA
-constexpr int kPrefixRows = 16 * kPrefixConsumers;    // rows per CTA
-
-template <int D, int NST>
-constexpr int prefix_smem_bytes() { return NST * 2 * kBlockTokens * D * 2 + 2 * NST * 8; }
-
-template <int D, int NST>
-__global__ void __launch_bounds__((kPrefixConsumers + 1) * 32, 1)
-decode_prefix_bf16_kernel(const KParams p, int num_seqs) {
-    constexpr int TILE = kBlockTokens * D * 2;
-    constexpr int KS = D / 16;     // k-steps of Q.K^T
-    constexpr int NT = D / 8;      // n-tiles of P.V
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = lane >> 2, c = lane & 3;
-    const int kvh = blockIdx.y, j = blockIdx.z;
-    const int rows_total = num_seqs * p.G;
-    const uint32_t ring0 = smem_u32(smem);
-    const uint32_t full0 = ring0 + NST * 2 * TILE, empty0 = full0 + NST * 8;
-    if (threadIdx.x == 0) {
-#pragma unroll
-        for (int st = 0; st < NST; ++st) {
-            mbar_init(full0 + st * 8, 1);
-            mbar_init(empty0 + st * 8, kPrefixConsumers);
-        }
-        fence_proxy_async_smem();
-    }
-    __syncthreads();
-    const int blk0 = j * p.part_blocks;     // every block of the partition is in the prefix
-
-    if (warp == kPrefixConsumers) {       // ---- producer warp
-        if (lane == 0) {
-            const uint64_t pol = l2_policy_evict_first();
-            for (int i = 0; i < p.part_blocks; ++i) {
-                const int st = i % NST;
-                // stage st is free once its previous use (i - NST) was consumed
-                if (i >= NST && !mbar_wait_bounded(empty0 + st * 8, ((i / NST) - 1) & 1, kWaitLimitNs)) {
-                    raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
-                    break;
-                }
-                int32_t blk = __ldg(p.tables + blk0 + i);     // sequence 0's row
-                if (blk < 0 || blk >= p.num_blocks) {
-                    raise_flag(p.err, PA_DEV_ERR_BAD_BLOCK);
-                    blk = -1;
-                }
-                const uint32_t bar = full0 + st * 8;
-                if (blk >= 0) {
-                    const size_t off = ((size_t)blk * p.Hkv + kvh) * (size_t)TILE;
-                    fence_proxy_async_smem();
-                    mbar_arrive_expect_tx(bar, 2 * TILE);
-                    bulk_g2s(ring0 + st * 2 * TILE, p.k_pool + off, TILE, bar, pol);
-                    bulk_g2s(ring0 + st * 2 * TILE + TILE, p.v_pool + off, TILE, bar, pol);
-                } else {
-                    // nothing to copy: complete the phase so the consumers move on; they
-                    // see the flag and the stale stage only feeds outputs already flagged
-                    mbar_arrive_expect_tx(bar, 0);
-                }
-            }
-        }
-        grid_dependency_wait();
-        return;
-    }
-
-    // ---- consumer warps: rows rr0 = r and rr1 = r + 8 of this warp's 16
-    const int rbase = blockIdx.x * kPrefixRows + warp * 16;
-    const int rr0 = rbase + r, rr1 = rbase + r + 8;
-    auto qrow = [&](int rr) -> const uint16_t* {
-        const int sq = rr / p.G, g = rr - (rr / p.G) * p.G;
-        return reinterpret_cast<const uint16_t*>(p.q) + ((size_t)sq * p.Hq + (size_t)kvh * p.G + g) * D;
-    };
-    uint32_t qa[KS][4];
-    {
-        const bool v0 = rr0 < rows_total, v1 = rr1 < rows_total;
-        const uint16_t* q0 = qrow(v0 ? rr0 : 0);
-        const uint16_t* q1 = qrow(v1 ? rr1 : 0);
-#pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-            qa[kk][0] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(q0 + 16 * kk + 2 * c)) : 0u;
-            qa[kk][1] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(q1 + 16 * kk + 2 * c)) : 0u;
-            qa[kk][2] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(q0 + 16 * kk + 8 + 2 * c)) : 0u;
-            qa[kk][3] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(q1 + 16 * kk + 8 + 2 * c)) : 0u;
-        }
-    }
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    float o[NT][4];
-#pragma unroll
-    for (int i = 0; i < NT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    const int km = lane >> 3;
-    const uint32_t k_lane = (uint32_t)((((km & 1) * 16) + (km >> 1) * 8 + (lane & 7)) * 16);
-    const uint32_t v_lane = (uint32_t)((((km >> 1) * 16) + (km & 1) * 8 + (lane & 7)) * 16);
-    bool failed = false;
-    for (int i = 0; i < p.part_blocks; ++i) {
-        const int st = i % NST;
-        if (!mbar_wait_bounded(full0 + st * 8, (i / NST) & 1, kWaitLimitNs)) {
-            failed = true;
-            break;
-        }
-        const uint32_t kt = ring0 + st * 2 * TILE, vt = kt + TILE;
-        // two independent accumulator chains (even / odd k-steps) halve the MMA latency chain
-        float sc[2][4], sx[2][4];
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sc[t][e] = sx[t][e] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-            uint32_t b0, b1, b2, b3;   // (tokens 0-7: dims lo, hi), (tokens 8-15: dims lo, hi)
-            ldmatrix_x4(kt + kk * 512 + k_lane, b0, b1, b2, b3);
-            float (&a)[2][4] = (kk & 1) ? sx : sc;
-            mma_bf16_16816(a[0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-            mma_bf16_16816(a[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
-        }
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sc[t][e] = (sc[t][e] + sx[t][e]) * p.scale_log2;
-        float bm0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-        float bm1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
-        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, 1));
-        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, 2));
-        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, 1));
-        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, 2));
-        const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-        const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
-        m0 = mn0;
-        m1 = mn1;
-        const uint32_t a0 = pack_bf16x2(fast_exp2(sc[0][0] - mn0), fast_exp2(sc[0][1] - mn0));
-        const uint32_t a1 = pack_bf16x2(fast_exp2(sc[0][2] - mn1), fast_exp2(sc[0][3] - mn1));
-        const uint32_t a2 = pack_bf16x2(fast_exp2(sc[1][0] - mn0), fast_exp2(sc[1][1] - mn0));
-        const uint32_t a3 = pack_bf16x2(fast_exp2(sc[1][2] - mn1), fast_exp2(sc[1][3] - mn1));
-        l0 = l0 * al0 + (bf16_lo_to_f32(a0) + bf16_hi_to_f32(a0) + bf16_lo_to_f32(a2) + bf16_hi_to_f32(a2));
-        l1 = l1 * al1 + (bf16_lo_to_f32(a1) + bf16_hi_to_f32(a1) + bf16_lo_to_f32(a3) + bf16_hi_to_f32(a3));
-        // the running maxima rarely move after the first blocks: rescale only when they do
-        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-            for (int nd = 0; nd < NT; ++nd) {
-                o[nd][0] *= al0; o[nd][1] *= al0; o[nd][2] *= al1; o[nd][3] *= al1;
-            }
-        }
-#pragma unroll
-        for (int nd = 0; nd < NT; nd += 2) {
-            uint32_t b0, b1, b2, b3;   // dims nd: (tokens 0-7, 8-15), dims nd+1: (0-7, 8-15)
-            ldmatrix_x4_trans(vt + nd * 256 + v_lane, b0, b1, b2, b3);
-            mma_bf16_16816(o[nd], a0, a1, a2, a3, b0, b1);
-            mma_bf16_16816(o[nd + 1], a0, a1, a2, a3, b2, b3);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + st * 8);
-    }
-    if (failed && lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    auto store_row = [&](int rr, float m, float l, int half) {
-        if (rr >= rows_total) return;
-        const int sq = rr / p.G, g = rr - (rr / p.G) * p.G;
-        const size_t row = (size_t)sq * p.Hq + (size_t)kvh * p.G + g;
-        float* po = p.part_o + (row * p.part_stride + j) * D;
-#pragma unroll
-        for (int nd = 0; nd < NT; ++nd)
-            *reinterpret_cast<float2*>(po + 8 * nd + 2 * c) =
-                make_float2(o[nd][2 * half], o[nd][2 * half + 1]);
-        if (c == 0) p.part_ml[row * p.part_stride + j] = make_float2(m, l);
-    };
-    store_row(rr0, m0, l0, 0);
-    store_row(rr1, m1, l1, 1);
-    // this grid must not finish before the kernel it overlaps with (the suffix part
-    // launched just before it) has finished: the merge after it waits on this grid only
-    grid_dependency_wait();
-}
-
 // Launch configuration of the main kernels.
 // 4 warps x 2 ring stages (64 KB of shared memory for head_dim 128, 3 CTAs per SM)
 // measured fastest on GB300 among 1-8 warps x 2-6 stages.
@@ -1123,10 +935,6 @@ template <int D>
 cudaError_t launch_fp8_for_dim(const KParams& kp, const DecodeArgs& a, cudaStream_t stream);
 
 template <int D>
-cudaError_t launch_prefix_for_dim(const KParams& kp, int num_seqs, int num_kv_heads,
-                                  cudaStream_t stream);
-
-template <int D>
 cudaError_t launch_for_dim(const KParams& kp, const DecodeArgs& a, cudaStream_t stream) {
     cudaError_t e = cudaSuccess;
     const int launched = a.grid_parts - kp.first_part;   // partitions of the main kernel
@@ -1144,7 +952,7 @@ cudaError_t launch_for_dim(const KParams& kp, const DecodeArgs& a, cudaStream_t 
         if (e != cudaSuccess) return e;
     }
     if (kp.first_part > 0) {
-        e = launch_prefix_for_dim<D>(kp, a.num_seqs, a.num_kv_heads, stream);
+        e = launch_prefix_tc(a, stream);
         if (e != cudaSuccess) return e;
     }
     if (a.grid_parts > 1 || kp.first_part > 0) {
@@ -1161,39 +969,6 @@ cudaError_t launch_for_dim(const KParams& kp, const DecodeArgs& a, cudaStream_t 
         }
     }
     return e;
-}
-
-// Ring depth of the prefix kernel (48 KB of tiles for head_dim 128, 32 KB for 64) and
-// 2 consumer warps per CTA: with 4 CTAs per SM this was the fastest of 1-4 consumer
-// warps x 4-20 stages measured on GB300 for a 64-sequence, 4096-token shared prefix.
-#ifndef PA_PREFIX_STAGES_128
-#define PA_PREFIX_STAGES_128 6
-#endif
-#ifndef PA_PREFIX_STAGES_64
-#define PA_PREFIX_STAGES_64 8
-#endif
-
-template <int D>
-cudaError_t launch_prefix_for_dim(const KParams& kp, int num_seqs, int num_kv_heads,
-                                  cudaStream_t stream) {
-    constexpr int NST = D == 128 ? PA_PREFIX_STAGES_128 : PA_PREFIX_STAGES_64;
-    auto k = decode_prefix_bf16_kernel<D, NST>;
-    constexpr int smem = prefix_smem_bytes<D, NST>();
-    cudaError_t e = set_smem(k, smem);
-    if (e != cudaSuccess) return e;
-    const int rows = num_seqs * kp.G;
-    const dim3 grid((rows + kPrefixRows - 1) / kPrefixRows, num_kv_heads, kp.first_part);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3((kPrefixConsumers + 1) * 32);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = PA_USE_PDL;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k, kp, num_seqs);
 }
 
 template <int D>

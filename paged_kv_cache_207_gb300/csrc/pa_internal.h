@@ -101,6 +101,9 @@ struct PrefillArgs {
     float scale;
 };
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+// The prefix partitions [0, first_part) of a decode with a shared prefix, on tcgen05:
+// writes their (o, max, sum) partials into the decode workspace for the merge.
+cudaError_t launch_prefix_tc(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_fp8(const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace pa

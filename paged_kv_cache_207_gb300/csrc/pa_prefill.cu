@@ -43,6 +43,10 @@ struct PParams {
     int32_t* err;
     int Hq, Hkv, G, TQ, max_blocks, num_blocks;
     float scale_log2;
+    // shared-prefix mode: partials of one partition per (sequence, query head) row
+    float* part_o;
+    float2* part_ml;
+    int part_stride, part_blocks, num_seqs, rows_per_cta;
 };
 
 __device__ __forceinline__ void raise_flag(int32_t* err, int bits) {
@@ -144,32 +148,50 @@ __device__ __forceinline__ uint32_t check_blocks(const PParams& p, int32_t& blk,
     return (uint32_t)__popc(__ballot_sync(0xffffffffu, blk >= 0)) * tile;
 }
 
-template <int D>
+// PREFIX = false: causal prefill of chunk rows (CTA = query tile, kv head, sequence).
+// PREFIX = true: rows are (sequence, query head) pairs of the kv head (CTA = row group,
+// kv head, partition j of a prefix shared by every sequence, read through table row 0);
+// every key is visible and the CTA writes unnormalised partials (o, max, sum) of
+// partition j for the split-KV merge instead of outputs.
+template <int D, bool PREFIX>
 __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams p) {
     using L = Smem<D>;
     constexpr int TILE = L::TILE, KTILE = L::KTILE;
     constexpr int KSTEPS = D / 16;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qt = gridDim.x - 1 - blockIdx.x;            // later (longer) tiles first
-    const int kvh = blockIdx.y, s = blockIdx.z;
-    const int q0 = __ldg(p.cu_q + s);
-    const int n = __ldg(p.cu_q + s + 1) - q0;
-    const int i0 = qt * p.TQ;
-    if (i0 >= n) return;
-    const int start = __ldg(p.start_pos + s);
-    const int i_end = min(n, i0 + p.TQ);
-    const int p_last = start + i_end - 1;                 // last position this CTA attends to
-    if (start < 0 || p_last >= p.max_blocks * kBlockTokens) {
-        if (threadIdx.x == 0 && kvh == 0) raise_flag(p.err, PA_DEV_ERR_BAD_POS);
-        return;
+    const int kvh = blockIdx.y;
+    int q0 = 0, n = 0, i0 = 0, start = 0, p_last, nblk, row_base = 0, rows_total = 0;
+    const int32_t* trow;
+    bool has_b;
+    if constexpr (PREFIX) {
+        rows_total = p.num_seqs * p.G;
+        row_base = blockIdx.x * p.rows_per_cta;
+        nblk = p.part_blocks;
+        p_last = nblk * kBlockTokens - 1;                 // positions relative to the partition
+        trow = p.tables + (size_t)blockIdx.z * p.part_blocks;
+        has_b = p.rows_per_cta > kHalfRows && row_base + kHalfRows < rows_total;
+    } else {
+        const int qt = gridDim.x - 1 - blockIdx.x;        // later (longer) tiles first
+        const int s = blockIdx.z;
+        q0 = __ldg(p.cu_q + s);
+        n = __ldg(p.cu_q + s + 1) - q0;
+        i0 = qt * p.TQ;
+        if (i0 >= n) return;
+        start = __ldg(p.start_pos + s);
+        const int i_end = min(n, i0 + p.TQ);
+        p_last = start + i_end - 1;                       // last position this CTA attends to
+        if (start < 0 || p_last >= p.max_blocks * kBlockTokens) {
+            if (threadIdx.x == 0 && kvh == 0) raise_flag(p.err, PA_DEV_ERR_BAD_POS);
+            return;
+        }
+        nblk = p_last / kBlockTokens + 1;
+        trow = p.tables + (size_t)s * p.max_blocks;
+        // tile b holds rows 128 .. 255; it is skipped when none of them is a chunk row
+        const int tl_b = kHalfRows / p.G;
+        has_b = tl_b < p.TQ && i0 + tl_b < n;
     }
-    const int nblk = p_last / kBlockTokens + 1;
     const int ntiles = (nblk + kKeyBlocks - 1) / kKeyBlocks;
-    const int32_t* trow = p.tables + (size_t)s * p.max_blocks;
-    // tile b holds rows 128 .. 255; it is skipped when none of them is a chunk row
-    const int tl_b = kHalfRows / p.G;
-    const bool has_b = tl_b < p.TQ && i0 + tl_b < n;
 
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sQ = sbase + L::Q, sK = sbase + L::K, sV = sbase + L::V, sCM = sbase + L::CM;
@@ -200,14 +222,21 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
     bool row_valid = false;
     size_t orow = 0;
     if (warp < kSoftWarps) {
-        const int tl = row / p.G, g = row - tl * p.G;
-        row_valid = tl < p.TQ && i0 + tl < n;
-        if (row_valid) {
-            pos = start + i0 + tl;
-            orow = ((size_t)(q0 + i0 + tl) * p.Hq + (size_t)kvh * p.G + g) * D;
+        if constexpr (PREFIX) {
+            const int r = row_base + row, sq = r / p.G, g = r - sq * p.G;
+            row_valid = row < p.rows_per_cta && r < rows_total;
+            if (row_valid) orow = (size_t)sq * p.Hq + (size_t)kvh * p.G + g;   // partial row
+        } else {
+            const int tl = row / p.G, g = row - tl * p.G;
+            row_valid = tl < p.TQ && i0 + tl < n;
+            if (row_valid) {
+                pos = start + i0 + tl;
+                orow = ((size_t)(q0 + i0 + tl) * p.Hq + (size_t)kvh * p.G + g) * D;
+            }
+            grid_dependency_wait();
         }
-        grid_dependency_wait();
-        const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + orow);
+        const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
+                                                           (PREFIX ? orow * D : orow));
         const int lr = row & (kHalfRows - 1);
         const uint32_t qdst = sQ + h * L::QTILE + (uint32_t)((lr >> 3) * 128 + (lr & 7) * 16);
 #pragma unroll 4
@@ -223,7 +252,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
     if (warp == kProducerWarp) {
         // ---------------------------------------------------------------- V tiles
         // one bulk copy per (block, kv head) tile, lane b handles block b
-        grid_dependency_wait();               // the chunk's own K/V come from the append before
+        if (!PREFIX) grid_dependency_wait();  // the chunk's own K/V come from the append before
         __syncwarp();
         if (lane == 0) grid_launch_dependents();
         const uint64_t pol = l2_policy_evict_last();   // tiles are re-read by other query tiles
@@ -263,7 +292,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         // MMA per 16 dims.  Each (block, 8-dim chunk) run of 256 B moves whole; the two
         // repack warps take half of the runs each, and the first also issues the copies.
         const int rw = warp - kRepackWarp;
-        grid_dependency_wait();
+        if (!PREFIX) grid_dependency_wait();
         __syncwarp();
         const uint64_t pol = l2_policy_evict_last();
         int issued = 0, consumed = 0;
@@ -508,7 +537,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
             if (lane == 0) mbar_arrive(bar(kPFull + h));
         }
         if (ok) ok = warp_wait(bar(kODone + h), 0);
-        if (ok) {
+        if (ok && PREFIX) {
+            tc_fence_after();
+            float4* po = reinterpret_cast<float4*>(p.part_o + (orow * p.part_stride + blockIdx.z) * D);
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tl_addr + ocol + 32 * c, o);
+                tmem_wait_ld();
+                if (row_valid) {
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        po[8 * c + v] = make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
+                                                    __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
+                }
+            }
+            if (row_valid) p.part_ml[orow * p.part_stride + blockIdx.z] = make_float2(m_used, l);
+        } else if (ok) {
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow);
@@ -539,6 +584,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         tc_fence_after();
         tmem_dealloc<kTmemCols>(tmem);
     }
+    // prefix mode: this grid overlaps the suffix kernel launched before it, and the merge
+    // after it waits on this grid only, so it must not finish before that kernel has
+    if (PREFIX) grid_dependency_wait();
 }
 
 }  // namespace tc
@@ -548,16 +596,15 @@ cudaError_t set_smem(K kernel, int bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-template <int D>
-cudaError_t launch_for_dim(const PParams& pp, int num_seqs, int max_chunk, cudaStream_t stream) {
-    auto k = tc::prefill_tc_kernel<D>;
+template <int D, bool PREFIX>
+cudaError_t launch_tc(const PParams& pp, dim3 grid, cudaStream_t stream) {
+    auto k = tc::prefill_tc_kernel<D, PREFIX>;
     constexpr int smem = tc::Smem<D>::BYTES;
-    constexpr int threads = tc::kThreadsTC;
     cudaError_t e = set_smem(k, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((max_chunk + pp.TQ - 1) / pp.TQ, pp.Hkv, num_seqs);
-    cfg.blockDim = dim3(threads);
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(tc::kThreadsTC);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -568,27 +615,61 @@ cudaError_t launch_for_dim(const PParams& pp, int num_seqs, int max_chunk, cudaS
     return cudaLaunchKernelEx(&cfg, k, pp);
 }
 
+PParams common_params(const void* q, const void* k_pool, const void* v_pool, const int32_t* tables,
+                      int32_t* err, int Hq, int Hkv, int max_blocks, int num_blocks, float scale) {
+    PParams pp = {};
+    pp.q = q;
+    pp.k_pool = static_cast<const char*>(k_pool);
+    pp.v_pool = static_cast<const char*>(v_pool);
+    pp.tables = tables;
+    pp.err = err;
+    pp.Hq = Hq;
+    pp.Hkv = Hkv;
+    pp.G = Hq / Hkv;
+    pp.max_blocks = max_blocks;
+    pp.num_blocks = num_blocks;
+    pp.scale_log2 = scale * kLog2e;
+    return pp;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 148;
+    return n;
+}
+
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
-    PParams pp;
+    PParams pp = common_params(a.q, a.k_pool, a.v_pool, a.block_tables, a.err, a.num_q_heads,
+                               a.num_kv_heads, a.max_blocks, a.num_blocks, a.scale);
     pp.out = a.out;
-    pp.q = a.q;
-    pp.k_pool = static_cast<const char*>(a.k_pool);
-    pp.v_pool = static_cast<const char*>(a.v_pool);
-    pp.tables = a.block_tables;
     pp.start_pos = a.start_pos;
     pp.cu_q = a.cu_q;
-    pp.err = a.err;
-    pp.Hq = a.num_q_heads;
-    pp.Hkv = a.num_kv_heads;
-    pp.G = a.num_q_heads / a.num_kv_heads;
     pp.TQ = tc::kRowsTC / pp.G;
-    pp.max_blocks = a.max_blocks;
-    pp.num_blocks = a.num_blocks;
-    pp.scale_log2 = a.scale * kLog2e;
-    if (a.head_dim == 64) return launch_for_dim<64>(pp, a.num_seqs, a.max_chunk, stream);
-    return launch_for_dim<128>(pp, a.num_seqs, a.max_chunk, stream);
+    const dim3 grid((a.max_chunk + pp.TQ - 1) / pp.TQ, pp.Hkv, a.num_seqs);
+    if (a.head_dim == 64) return launch_tc<64, false>(pp, grid, stream);
+    return launch_tc<128, false>(pp, grid, stream);
+}
+
+cudaError_t launch_prefix_tc(const DecodeArgs& a, cudaStream_t stream) {
+    PParams pp = common_params(a.q, a.k_pool, a.v_pool, a.block_tables, a.err, a.num_q_heads,
+                               a.num_kv_heads, a.max_blocks, a.num_blocks, a.scale);
+    const size_t prow = (size_t)a.num_seqs * a.num_q_heads * a.part_stride;
+    pp.part_o = static_cast<float*>(a.workspace);
+    pp.part_ml = reinterpret_cast<float2*>(static_cast<char*>(a.workspace) + prow * a.head_dim * sizeof(float));
+    pp.part_stride = a.part_stride;
+    pp.part_blocks = a.part_blocks;
+    pp.num_seqs = a.num_seqs;
+    // 256 rows (two Q tiles) per CTA when that still gives every SM a CTA, else 128
+    const int rows = a.num_seqs * pp.G;
+    const long long ctas256 = (long long)((rows + tc::kRowsTC - 1) / tc::kRowsTC) * a.num_kv_heads * a.first_part;
+    pp.rows_per_cta = ctas256 >= sm_count() ? tc::kRowsTC : tc::kHalfRows;
+    const dim3 grid((rows + pp.rows_per_cta - 1) / pp.rows_per_cta, a.num_kv_heads, a.first_part);
+    if (a.head_dim == 64) return launch_tc<64, true>(pp, grid, stream);
+    return launch_tc<128, true>(pp, grid, stream);
 }
 
 }  // namespace pa
