@@ -128,6 +128,39 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
     return __all_sync(0xffffffffu, ok);
 }
 
+// Three-input maximum and packed two-lane fp32 arithmetic (one instruction for two
+// values); a packed pair holds its first value in the low 32 bits.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float lo_f32(uint64_t x) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+    return lo;
+}
+__device__ __forceinline__ float hi_f32(uint64_t x) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+    return hi;
+}
+__device__ __forceinline__ uint64_t ffma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t fadd_f32x2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 // Table entry of block b of key tile j for lane b of a warp (-1 for lanes past the
 // tile's or the sequence's last block).
 __device__ __forceinline__ int32_t fetch_block(const int32_t* trow, int j, int nblk, int ntiles,
@@ -239,9 +272,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
                                                            (PREFIX ? orow * D : orow));
         const int lr = row & (kHalfRows - 1);
         const uint32_t qdst = sQ + h * L::QTILE + (uint32_t)((lr >> 3) * 128 + (lr & 7) * 16);
+        // a negative scale is applied as |scale| to -q (exact), so that the softmax can
+        // take the row maximum of the unscaled scores
+        const uint32_t flip = p.scale_log2 < 0.f ? 0x80008000u : 0u;
 #pragma unroll 4
-        for (int kg = 0; kg < D / 8; ++kg)
-            st_shared_v4(qdst + kg * 2048, row_valid ? __ldg(qsrc + kg) : make_uint4(0u, 0u, 0u, 0u));
+        for (int kg = 0; kg < D / 8; ++kg) {
+            uint4 v = row_valid ? __ldg(qsrc + kg) : make_uint4(0u, 0u, 0u, 0u);
+            v.x ^= flip;
+            v.y ^= flip;
+            v.z ^= flip;
+            v.w ^= flip;
+            st_shared_v4(qdst + kg * 2048, v);
+        }
         fence_proxy_async_smem();
     }
     tc_fence_before();
@@ -461,6 +503,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         const uint32_t tl_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
         const uint32_t scol = kColS + (uint32_t)(h * kKeyTok);
         const uint32_t ocol = kColO + (uint32_t)(h * kKeyTok);
+        const float cs = fabsf(p.scale_log2);          // a negative scale was moved into Q
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
@@ -471,26 +514,28 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
 #pragma unroll
             for (int c = 0; c < 4; ++c) tmem_ld32(tl_addr + scol + 32 * c, sr[c]);
             tmem_wait_ld();
-            // scale, causal mask (select: unread or stale columns may hold NaN)
             const int tok0 = j * kKeyTok;
-            float mx = -INFINITY;
-            if (tok0 + kKeyTok - 1 <= pos) {
+            // every key of the tile is visible to every row of the warp: warp-uniform, so
+            // that the warp-collective TMEM stores below run with all 32 lanes
+            const bool full = __all_sync(0xffffffffu, tok0 + kKeyTok - 1 <= pos);
+            float mx;
+            if (full) {
+                // the row maximum of the unscaled scores (c >= 0), four independent chains
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float x = __uint_as_float(sr[c][i]) * p.scale_log2;
-                        sr[c][i] = __float_as_uint(x);
-                        mx = fmaxf(mx, x);
-                    }
+                    for (int i = 0; i < 32; i += 2)
+                        m4[c] = max3f(m4[c], __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
+                mx = max3f(m4[0], m4[1], fmaxf(m4[2], m4[3])) * cs;
             } else {
+                // scale and causal mask (select: unread or stale columns may hold NaN)
+                mx = -INFINITY;
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const float x = tok0 + 32 * c + i <= pos
-                                            ? __uint_as_float(sr[c][i]) * p.scale_log2
-                                            : -INFINITY;
+                        const float x = tok0 + 32 * c + i <= pos ? __uint_as_float(sr[c][i]) * cs : -INFINITY;
                         sr[c][i] = __float_as_uint(x);
                         mx = fmaxf(mx, x);
                     }
@@ -513,22 +558,46 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
                     tmem_st32(tl_addr + ocol + 32 * c, o);
                 }
             }
-            // probabilities, bf16 pairs, over the first 64 columns of S_h (already read)
-            float sum = 0.f;
+            // probabilities, bf16 pairs, over the first 64 columns of S_h (already read);
+            // a full tile takes s c - m for two keys in one packed FFMA and sums in pairs
+            float sum;
+            if (full) {
+                const uint64_t c2 = pack_f32x2(cs, cs), nm2 = pack_f32x2(-m_used, -m_used);
+                uint64_t sum2[2] = {pack_f32x2(0.f, 0.f), pack_f32x2(0.f, 0.f)};
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t pk[32];
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t pk[32];
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc)
+                    for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const int c = 2 * half + cc;
-                        const float e0 = fast_exp2(__uint_as_float(sr[c][i]) - m_used);
-                        const float e1 = fast_exp2(__uint_as_float(sr[c][i + 1]) - m_used);
-                        sum += e0 + e1;
-                        pk[16 * cc + (i >> 1)] = pack_bf16x2(e0, e1);
-                    }
-                tmem_st32(tl_addr + scol + 32 * half, pk);
+                        for (int i = 0; i < 32; i += 2) {
+                            const int c = 2 * half + cc;
+                            const uint64_t x2 = ffma_f32x2(pack_f32x2(__uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1])), c2, nm2);
+                            const float e0 = fast_exp2(lo_f32(x2)), e1 = fast_exp2(hi_f32(x2));
+                            sum2[(i >> 1) & 1] = fadd_f32x2(sum2[(i >> 1) & 1], pack_f32x2(e0, e1));
+                            pk[16 * cc + (i >> 1)] = pack_bf16x2(e0, e1);
+                        }
+                    tmem_st32(tl_addr + scol + 32 * half, pk);
+                }
+                const uint64_t t = fadd_f32x2(sum2[0], sum2[1]);
+                sum = lo_f32(t) + hi_f32(t);
+            } else {
+                sum = 0.f;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            const int c = 2 * half + cc;
+                            const float e0 = fast_exp2(__uint_as_float(sr[c][i]) - m_used);
+                            const float e1 = fast_exp2(__uint_as_float(sr[c][i + 1]) - m_used);
+                            sum += e0 + e1;
+                            pk[16 * cc + (i >> 1)] = pack_bf16x2(e0, e1);
+                        }
+                    tmem_st32(tl_addr + scol + 32 * half, pk);
+                }
             }
             l = l * alpha + sum;
             tmem_wait_st();
