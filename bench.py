@@ -332,7 +332,12 @@ def run_ours(args, rank, world, local):
         raise RuntimeError(f"device error flag {int(err.item())} during the timed steps")
 
     ms_total_max = all_max(ms_total, world)
-    step_bytes = decode_bytes(wl, args.kv_dtype) + append_bytes(wl, args.kv_dtype)
+    # with a shared prefix the bytes that must move count the prefix once (it exists once in
+    # the pool); the logical figure (every sequence's whole context) is reported beside it
+    dbytes = decode_bytes(wl, args.kv_dtype)
+    if shared:
+        dbytes += unique_kv_bytes(wl, shared) - logical_kv_bytes(wl)
+    step_bytes = dbytes + append_bytes(wl, args.kv_dtype)
     total_bytes = all_sum(float(step_bytes) * K, world)
     value = total_bytes / (ms_total_max / 1e3) / 1e9
     ms_per_step = ms_total_max / K
@@ -380,7 +385,6 @@ def run_ours(args, rank, world, local):
         peak, peak_src = float(peaks["hbm_gbs"]), "measured"
     else:
         peak, peak_src = 6800.0, "fallback"
-    dbytes = decode_bytes(wl, args.kv_dtype)
     achieved = dbytes / (dec_ms / 1e3) / 1e9
     launches_per_step = 1 + 1 + (1 if int(math.ceil(hint / 512)) > 1 or shared >= 512 else 0) + \
         (1 if shared >= 512 else 0)
@@ -405,7 +409,9 @@ def run_ours(args, rank, world, local):
                    "parallelism": f"replicas x{world} (sequences sharded by rank, no collective)"},
         "pct_of_peak_hbm": round(100.0 * value / peak, 2),
         **({"unique_kv_bytes_per_step": unique_kv_bytes(wl, shared),
-            "logical_kv_bytes_per_step": logical_kv_bytes(wl)} if shared else {}),
+            "logical_kv_bytes_per_step": logical_kv_bytes(wl),
+            "logical_gbs": round(value * (step_bytes - unique_kv_bytes(wl, shared) +
+                                          logical_kv_bytes(wl)) / step_bytes, 1)} if shared else {}),
         "tokens_per_s": round(tokens_per_s, 1),
         "roofline": {"kernel": ("pa_decode_attention_fp8" if fp8 else "pa_decode_attention") +
                                " (main kernel + partition merge)",

@@ -75,3 +75,24 @@ def test_shared_prefix_workload_full_size_sampled():
     want = oracle_contig(wl, pairs)
     got = np.stack([as_f64(out[s, h]) for s, h in pairs])
     assert_close(wl, got, want, "shared prefix full size")
+
+
+def test_shared_prefix_two_q_tiles_per_cta():
+    # 120 sequences x 4 query heads per kv head = 480 rows in two groups of 256 (the second
+    # group's second Q tile partly empty); with 16 prefix partitions and 8 kv heads there are
+    # enough CTAs to hold 256 rows each
+    lens = [8192 + n - 1 for n in np.random.default_rng(11).integers(1, 300, 120)]
+    wl = W.make_decode_workload("prefix2", context_lens=lens, num_q_heads=32, num_kv_heads=8,
+                                head_dim=128, dtype="bf16", seed=12, device="cuda",
+                                shared_prefix=8192)
+    dp = DevicePools(wl, canary=False)
+    out, lens_t = _prefix_step(wl, dp, 8192, hint=int(max(lens)) + 1)
+    assert int(dp.err.item()) == 0
+    rng = np.random.default_rng(13)
+    seqs = sorted(set(rng.choice(120, 10, replace=False).tolist()) | {0, 31, 32, 63, 64, 95, 96, 119})
+    pairs = [(s, int(rng.integers(32))) for s in seqs]
+    want = oracle_contig(wl, pairs)
+    got = np.stack([as_f64(out[s, h]) for s, h in pairs])
+    assert_close(wl, got, want, "two Q tiles per CTA")
+    ref = dp.decode(lens_t)
+    assert_close(wl, as_f64(out), as_f64(ref), "prefix vs ordinary, two Q tiles per CTA")
