@@ -736,6 +736,9 @@ cudaError_t launch_prefix_tc(const DecodeArgs& a, cudaStream_t stream) {
     const int rows = a.num_seqs * pp.G;
     const long long ctas256 = (long long)((rows + tc::kRowsTC - 1) / tc::kRowsTC) * a.num_kv_heads * a.first_part;
     pp.rows_per_cta = ctas256 >= sm_count() ? tc::kRowsTC : tc::kHalfRows;
+#ifdef PA_PREFIX_TC_ROWS
+    pp.rows_per_cta = PA_PREFIX_TC_ROWS;              // tuning builds: 128 or 256
+#endif
     const dim3 grid((rows + pp.rows_per_cta - 1) / pp.rows_per_cta, a.num_kv_heads, a.first_part);
     if (a.head_dim == 64) return launch_tc<64, true>(pp, grid, stream);
     return launch_tc<128, true>(pp, grid, stream);

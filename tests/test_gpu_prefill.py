@@ -40,7 +40,7 @@ def _prefill_case(chunks, hq, hkv, d, seed):
     return wl, dp, q, out, starts, ns
 
 
-def _check(wl, q, out, starts, ns, rows_per_seq=None):
+def _check(wl, q, out, starts, ns, rows_per_seq=None, only=None):
     kr, vr = wl.k_rows.cpu(), wl.v_rows.cpu()
     qc, oc = q.cpu(), out.float().cpu().double().numpy()
     G = wl.num_q_heads // wl.num_kv_heads
@@ -48,6 +48,9 @@ def _check(wl, q, out, starts, ns, rows_per_seq=None):
     worst = 0.0
     base = 0
     for s, (st, n) in enumerate(zip(starts, ns)):
+        if only is not None and s not in only:
+            base += n
+            continue
         logical = torch.from_numpy(wl.logical_rows(s))
         idx = range(n) if rows_per_seq is None else sorted(set(rng.integers(0, n, rows_per_seq).tolist()) | {0, n - 1})
         for i in idx:
@@ -102,3 +105,47 @@ def test_twelve_layers_prefill_at_the_same_explicit_start():
     for layer in range(12):
         wl, dp, q, out, starts, ns = _prefill_case([(64, 32), (0, 20)], 12, 12, 64, seed=300 + layer)
         _check(wl, q, out, starts, ns)
+
+
+def _prefill_with(chunks, hq, hkv, d, seed, edit):
+    """Append as _prefill_case does, then run the prefill on inputs changed by `edit`."""
+    totals = [s + n for s, n in chunks]
+    wl = W.make_decode_workload("prefill_err", context_lens=np.array(totals) - 1, num_q_heads=hq,
+                                num_kv_heads=hkv, head_dim=d, dtype="bf16", seed=seed,
+                                device="cuda")
+    dp = DevicePools(wl)
+    k_new, v_new, start, cu, _ = dp.step_inputs()
+    pk.append_kv(dp.k, dp.v, k_new, v_new, dp.tables, start, cu, err_flag=dp.err)
+    torch.cuda.synchronize()
+    assert int(dp.err.item()) == 0
+    ns = [n for _, n in chunks]
+    starts = [s for s, _ in chunks]
+    g = torch.Generator(device="cuda").manual_seed(seed + 1)
+    q = torch.randn(sum(ns), hq, d, generator=g, device="cuda").to(torch.bfloat16)
+    out = torch.zeros_like(q)
+    tables = dp.tables.clone()
+    st = torch.tensor(starts, dtype=torch.int32, device="cuda")
+    edit(wl, tables, st)
+    cu_q = torch.tensor(np.concatenate([[0], np.cumsum(ns)]), dtype=torch.int32, device="cuda")
+    pk.prefill_attention(out, q, dp.k, dp.v, tables, st, cu_q, wl.scale, max_chunk=max(ns),
+                         err_flag=dp.err)
+    torch.cuda.synchronize()
+    return wl, dp, q, out, starts, ns
+
+
+def test_prefill_block_outside_the_pool_is_flagged_and_others_are_exact():
+    # sequence 1's first block points past the pool: its tiles are skipped and flagged, the
+    # barrier accounting still completes (no timeout bit), other sequences are unaffected
+    def edit(wl, tables, st):
+        tables[1, 0] = wl.num_blocks
+    wl, dp, q, out, starts, ns = _prefill_with([(100, 64), (300, 40), (0, 90)], 32, 8, 128, 41, edit)
+    assert int(dp.err.item()) == pk.DEV_ERR_BAD_BLOCK
+    _check(wl, q, out, starts, ns, only={0, 2})
+
+
+def test_prefill_negative_start_is_flagged_and_others_are_exact():
+    def edit(wl, tables, st):
+        st[0] = -1
+    wl, dp, q, out, starts, ns = _prefill_with([(50, 30), (200, 70)], 14, 2, 64, 43, edit)
+    assert int(dp.err.item()) == pk.DEV_ERR_BAD_POS
+    _check(wl, q, out, starts, ns, only={1})
