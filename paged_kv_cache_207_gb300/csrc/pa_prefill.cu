@@ -100,7 +100,7 @@ struct Smem {
     static constexpr int V = K + 2 * KTILE;                    // V tiles, 2 stages
     static constexpr int CM = V + 2 * KTILE;                   // K tile chunk-major
     static constexpr int BAR = CM + KTILE;
-    static constexpr int NBAR = 15;
+    static constexpr int NBAR = 16;
     static constexpr int SLOT = BAR + NBAR * 8;
     // at least 120 KB so that one CTA (and its 512 TMEM columns) owns an SM
     static constexpr int BYTES = SLOT + 16 < 122880 ? 122880 : SLOT + 16;
@@ -108,7 +108,7 @@ struct Smem {
 
 // barrier indices
 constexpr int kKFull = 0, kVFull = 2, kVEmpty = 4, kCmFull = 6, kCmFree = 7, kSFull = 8,
-              kPFull = 10, kODone = 12, kDone = 14;
+              kPFull = 10, kODone = 12, kDone = 14, kPVDone = 15;
 
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     uint64_t pol;
@@ -244,6 +244,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         mbar_init(bar(kCmFull), kRepackWarps);
         mbar_init(bar(kCmFree), 1);
         mbar_init(bar(kDone), 1);
+        mbar_init(bar(kPVDone), 1);
         fence_proxy_async_smem();
     }
     if (warp == kMmaWarp) tmem_alloc<kTmemCols>(sbase + L::SLOT);
@@ -409,26 +410,28 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         // O_h += P_h(j) V_j: A = P_h(j) in TMEM (over S_h's first columns), B = one V block
         // tile (MN-major), K = 16 tokens.  MMAs of this thread execute in issue order, so
         // S_h(j + 1) overwrites P_h(j) only after PV_h(j) has read it, and a commit after
-        // S_h(j + 1) also covers PV_h(j).
+        // S_h(j + 1) also covers PV_h(j).  Without a tile b its S columns are a second S
+        // buffer for tile a: S(j) goes to buffer j % 2 and S(j + 2) is issued right after
+        // PV(j), so the scores of the next tile are ready when the softmax finishes.
         constexpr uint32_t idS = umma_idesc_bf16(128, kKeyTok, 0);
         constexpr uint32_t idO = umma_idesc_bf16(128, D, 1);
         const uint64_t kdesc = umma_desc(sCM, kKeyBlocks * 256, 128);
         bool ok = true;
-        auto issue_s = [&](int hh) {
+        auto issue_s = [&](int hh, int buf) {
             tc_fence_after();
             if (lane == 0) {
                 // columns of blocks past the tile's last one hold stale products (masked)
                 const uint64_t qdesc = umma_desc(sQ + hh * L::QTILE, 2048, 128);
-                const uint32_t dcol = tmem + kColS + (uint32_t)(hh * kKeyTok);
+                const uint32_t dcol = tmem + kColS + (uint32_t)(buf * kKeyTok);
 #pragma unroll
                 for (int ks = 0; ks < KSTEPS; ++ks)
                     umma_ss(dcol, qdesc + (uint64_t)(ks * 256),
                             kdesc + (uint64_t)((ks * 2 * kKeyBlocks * 256) >> 4), idS, ks > 0);
-                umma_commit(bar(kSFull + hh));
+                umma_commit(bar(kSFull + buf));
             }
             __syncwarp();
         };
-        auto issue_pv = [&](int hh, int j) {
+        auto issue_pv = [&](int hh, int j, int buf) {
             const int st = j & 1;
             ok = warp_wait(bar(kPFull + hh), j & 1);
             if (!ok) return;
@@ -454,40 +457,57 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
             tc_fence_after();
             if (lane == 0) {
                 const uint64_t vdesc = umma_desc(sV + st * KTILE, 128, 256);
-                const uint32_t pcol = tmem + kColS + (uint32_t)(hh * kKeyTok);
+                const uint32_t pcol = tmem + kColS + (uint32_t)(buf * kKeyTok);
                 const uint32_t ocol = tmem + kColO + (uint32_t)(hh * kKeyTok);
                 for (int b = 0; b < nb; ++b)
                     umma_ts(ocol, pcol + 8 * b, vdesc + (uint64_t)((b * TILE) >> 4), idO,
                             (j > 0 || b > 0) ? 1u : 0u);
                 if (j == ntiles - 1) umma_commit(bar(kODone + hh));
                 if (hh == 1 || !has_b) umma_commit(bar(kVEmpty + st));
+                if (!has_b) umma_commit(bar(kPVDone));
             }
             __syncwarp();
         };
-        ok = warp_wait(bar(kCmFull), 0);
-        if (ok) {
-            issue_s(0);
-            if (has_b) issue_s(1);
+        auto next_s = [&](int j, int buf) {       // S of tile j for tile a, then free the K tile
+            ok = warp_wait(bar(kCmFull), j & 1);
+            if (!ok) return;
+            issue_s(0, buf);
             if (lane == 0) umma_commit(bar(kCmFree));
             __syncwarp();
-        }
-        for (int j = 0; ok && j < ntiles; ++j) {
-            const bool more = j + 1 < ntiles;
-            issue_pv(0, j);
-            if (!ok) break;
-            if (more) {
-                ok = warp_wait(bar(kCmFull), (j + 1) & 1);
-                if (!ok) break;
-                issue_s(0);
+        };
+        if (!has_b) {
+            // one Q tile, S double-buffered: S(0) S(1) | PV(0) S(2) | PV(1) S(3) ...
+            next_s(0, 0);
+            if (ok && ntiles > 1) next_s(1, 1);
+            for (int j = 0; ok && j < ntiles; ++j) {
+                issue_pv(0, j, j & 1);
+                if (ok && j + 2 < ntiles) next_s(j + 2, j & 1);
             }
-            if (has_b) {
-                issue_pv(1, j);
-                if (!ok) break;
-                if (more) issue_s(1);
-            }
-            if (more) {
+        } else {
+            // two Q tiles: S_a(0) S_b(0) | PV_a(0) S_a(1) PV_b(0) S_b(1) | ...
+            ok = warp_wait(bar(kCmFull), 0);
+            if (ok) {
+                issue_s(0, 0);
+                issue_s(1, 1);
                 if (lane == 0) umma_commit(bar(kCmFree));
                 __syncwarp();
+            }
+            for (int j = 0; ok && j < ntiles; ++j) {
+                const bool more = j + 1 < ntiles;
+                issue_pv(0, j, 0);
+                if (!ok) break;
+                if (more) {
+                    ok = warp_wait(bar(kCmFull), (j + 1) & 1);
+                    if (!ok) break;
+                    issue_s(0, 0);
+                }
+                issue_pv(1, j, 1);
+                if (!ok) break;
+                if (more) {
+                    issue_s(1, 1);
+                    if (lane == 0) umma_commit(bar(kCmFree));
+                    __syncwarp();
+                }
             }
         }
         if (!ok && lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
@@ -498,16 +518,19 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
     } else if (h == 0 || has_b) {
         // ---------------------------------------------------------------- softmax rows
         // Warp w reaches TMEM lanes 32 (w % 4) ..; this thread's row of tile h is lane
-        // row % 128.  A commit after S_h(j) covers every earlier MMA, so when S_h(j) is
-        // seen complete, PV_h(j - 1) is too: O_h may be rescaled and P_h(j) written at once.
+        // row % 128.  With two tiles a commit after S_h(j) covers every earlier MMA, so when
+        // S_h(j) is seen complete, PV_h(j - 1) is too: O_h may be rescaled and P_h(j)
+        // written at once.
         const uint32_t tl_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        const uint32_t scol = kColS + (uint32_t)(h * kKeyTok);
+        // without a tile b, tile a's S alternates between both S buffers (see the MMA warp)
         const uint32_t ocol = kColO + (uint32_t)(h * kKeyTok);
         const float cs = fabsf(p.scale_log2);          // a negative scale was moved into Q
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
-            ok = warp_wait(bar(kSFull + h), j & 1);
+            const int sb = has_b ? h : (j & 1);
+            const uint32_t scol = kColS + (uint32_t)(sb * kKeyTok);
+            ok = warp_wait(bar(kSFull + sb), has_b ? (j & 1) : ((j >> 1) & 1));
             if (!ok) break;
             tc_fence_after();
             uint32_t sr[4][32];
@@ -548,6 +571,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
                 m_used = mx;
             }
             if (__any_sync(0xffffffffu, resc)) {
+                // with S double-buffered, S(j) complete does not imply PV(j - 1) complete:
+                // wait for it before O changes (the barrier is at most one phase ahead)
+                if (!has_b) {
+                    ok = warp_wait(bar(kPVDone), (j - 1) & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
