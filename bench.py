@@ -33,6 +33,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "paged decode-attention achieved HBM GB/s (% of GB300 peak) and decode tokens/s"
+# workloads whose pool is near L2's size: the timed step runs every layer, each on a pool of its
+# own, so L2 cannot serve one layer's cache to the next
+ROTATE_LAYERS = {"qwen2.5-0.5b_gqa": 24}
 LAYERS = {"llama3-8b_batch256": 32, "llama3-8b_long_context": 32, "llama3-8b_shared_prefix": 32,
           "qwen2.5-0.5b_gqa": 24, "gpt2_tiny_f32": 12}
 
@@ -276,10 +279,13 @@ def run_ours(args, rank, world, local):
     del wl.k_rows, wl.v_rows
     torch.cuda.empty_cache()
     stream = torch.cuda.current_stream()
+    rot = ROTATE_LAYERS.get(args.workload, 1)
+    pools = [(kp, vp)] + [(kp.clone(), vp.clone()) for _ in range(rot - 1)]
 
     shared = args.shared_prefix
 
-    def decode(q_, tab_, lens_):
+    def decode(q_, tab_, lens_, layer=0):
+        kp, vp = pools[layer]
         if fp8:
             pk.decode_attention_fp8(out, q_, kp, vp, tab_, lens_, wl.scale, workspace=ws,
                                     max_context_len_hint=hint, err_flag=err, stream=stream)
@@ -292,12 +298,13 @@ def run_ours(args, rank, world, local):
                                 max_context_len_hint=hint, err_flag=err, stream=stream)
 
     def step(ev_d0=None, ev_d1=None):
-        append(kp, vp, k_new, v_new, tables, start, cu, err_flag=err, stream=stream)
-        if ev_d0 is not None:
-            ev_d0.record(stream)
-        decode(q, tables, lens)
-        if ev_d1 is not None:
-            ev_d1.record(stream)
+        for layer in range(rot):
+            append(*pools[layer], k_new, v_new, tables, start, cu, err_flag=err, stream=stream)
+            if ev_d0 is not None:
+                ev_d0[layer].record(stream)
+            decode(q, tables, lens, layer)
+            if ev_d1 is not None:
+                ev_d1[layer].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -320,14 +327,14 @@ def run_ours(args, rank, world, local):
     # The decode call alone, for the roofline: the same K steps again with events
     # around each decode (events between the launches stop the append -> decode
     # overlap, so the step time above is taken without them).
-    d0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    d1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    d0 = [[torch.cuda.Event(enable_timing=True) for _ in range(rot)] for _ in range(K)]
+    d1 = [[torch.cuda.Event(enable_timing=True) for _ in range(rot)] for _ in range(K)]
     for i in range(K):
         step(d0[i], d1[i])
     torch.cuda.synchronize()
     clk = clocks.stop()
     ms_total = t0.elapsed_time(t1)
-    dec_ms = sum(a.elapsed_time(b) for a, b in zip(d0, d1)) / K
+    dec_ms = sum(a.elapsed_time(b) for ea, eb in zip(d0, d1) for a, b in zip(ea, eb)) / (K * rot)
     if int(err.item()) != 0:
         raise RuntimeError(f"device error flag {int(err.item())} during the timed steps")
 
@@ -337,12 +344,13 @@ def run_ours(args, rank, world, local):
     dbytes = decode_bytes(wl, args.kv_dtype)
     if shared:
         dbytes += unique_kv_bytes(wl, shared) - logical_kv_bytes(wl)
-    step_bytes = dbytes + append_bytes(wl, args.kv_dtype)
+    step_bytes = (dbytes + append_bytes(wl, args.kv_dtype)) * rot
     total_bytes = all_sum(float(step_bytes) * K, world)
     value = total_bytes / (ms_total_max / 1e3) / 1e9
     ms_per_step = ms_total_max / K
     layers = LAYERS.get(args.workload, 32)
-    tokens_per_s = all_sum(float(S), world) / (layers * ms_per_step / 1e3)
+    # a step covers `rot` of the model's `layers` layers
+    tokens_per_s = all_sum(float(S), world) / ((layers / rot) * ms_per_step / 1e3)
 
     # end to end: host buffers in pinned memory, copies inside the timed region
     h_q = q.cpu().pin_memory()
@@ -360,8 +368,9 @@ def run_ours(args, rank, world, local):
         for dst, src in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_start, h_start), (d_cu, h_cu),
                          (d_lens, h_lens), (d_tab, h_tab)):
             dst.copy_(src, non_blocking=True)
-        append(kp, vp, d_k, d_v, d_tab, d_start, d_cu, err_flag=err, stream=stream)
-        decode(d_q, d_tab, d_lens)
+        for layer in range(rot):
+            append(*pools[layer], d_k, d_v, d_tab, d_start, d_cu, err_flag=err, stream=stream)
+            decode(d_q, d_tab, d_lens, layer)
         h_out.copy_(out, non_blocking=True)
 
     for _ in range(max(3, args.warmup)):
@@ -386,8 +395,8 @@ def run_ours(args, rank, world, local):
     else:
         peak, peak_src = 6800.0, "fallback"
     achieved = dbytes / (dec_ms / 1e3) / 1e9
-    launches_per_step = 1 + 1 + (1 if int(math.ceil(hint / 512)) > 1 or shared >= 512 else 0) + \
-        (1 if shared >= 512 else 0)
+    launches_per_step = (1 + 1 + (1 if int(math.ceil(hint / 512)) > 1 or shared >= 512 else 0) +
+                         (1 if shared >= 512 else 0)) * rot
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
@@ -400,12 +409,15 @@ def run_ours(args, rank, world, local):
                    "num_kv_heads": Hkv, "head_dim": D, "block_size": 16,
                    "context_tokens_after_append": int((wl.context_lens + 1).sum()),
                    "max_context": int(hint),
-                   "step": "pa_append_kv (1 token/seq) + " + ("pa_decode_attention_shared_prefix"
-                                                               if shared else "pa_decode_attention"),
+                   "step": ("%d layers x (" % rot if rot > 1 else "") + "pa_append_kv (1 token/seq) + " +
+                           ("pa_decode_attention_shared_prefix" if shared else "pa_decode_attention") +
+                           (")" if rot > 1 else ""),
                    "shared_prefix_tokens": shared,
                    "layers_for_tokens_per_s": layers,
-                   "l2": "inputs larger than L2 (K/V pools %.2f GB per GPU vs 129 MB L2), no flush"
-                         % (2 * kp.numel() * kp.element_size() / 1e9),
+                   "layer_pools": rot,
+                   "l2": "inputs larger than L2 (K/V pools %.2f GB per GPU vs 129 MB L2%s), no flush"
+                         % (2 * rot * kp.numel() * kp.element_size() / 1e9,
+                            ", a distinct pool per layer of the step" if rot > 1 else ""),
                    "parallelism": f"replicas x{world} (sequences sharded by rank, no collective)"},
         "pct_of_peak_hbm": round(100.0 * value / peak, 2),
         **({"unique_kv_bytes_per_step": unique_kv_bytes(wl, shared),
