@@ -229,9 +229,10 @@ pa_status pa_decode_attention_fp8(void* out, const void* q, const void* k_pool, 
  * sequences all share their first shared_prefix_tokens positions in the same
  * physical blocks (the layout refcounted copy-on-write forks leave behind;
  * spindle, "Paging").  The whole 512-token partitions of the prefix are read
- * once per kv head and applied to the queries of every sequence on the tensor
- * cores; the rest of each context goes through the ordinary kernel; the two
- * are merged with their log-sum-exp weights.
+ * once per kv head and group of 128 or 256 query rows (not once per sequence)
+ * and applied to the queries of every sequence on the tensor cores; the rest
+ * of each context goes through the ordinary kernel; the two are merged with
+ * their log-sum-exp weights.
  *   Same arguments as pa_decode_attention plus shared_prefix_tokens (a multiple
  *   of 16).  The caller guarantees that block_tables[s][b] == block_tables[0][b]
  *   for every s and every b < shared_prefix_tokens / 16, and that every
