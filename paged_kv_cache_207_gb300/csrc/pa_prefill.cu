@@ -63,7 +63,9 @@ __device__ __forceinline__ void raise_flag(int32_t* err, int bits) {
 // keeps a running maximum that is raised only when a tile exceeds it by more than
 // 2^8 (O_h is then rescaled in TMEM), writes its bf16 probabilities over the
 // first half of S_h's columns, and at the end reads its row of O_h, divides by
-// the row sum and stores it.
+// the row sum and stores it (the prefix mode stores the unnormalised partial and
+// its maximum and sum instead).  A CTA with a single Q tile uses tile b's S
+// columns as a second S buffer for tile a.
 // ============================================================================
 
 namespace tc {
