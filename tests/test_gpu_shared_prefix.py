@@ -96,3 +96,20 @@ def test_shared_prefix_two_q_tiles_per_cta():
     assert_close(wl, got, want, "two Q tiles per CTA")
     ref = dp.decode(lens_t)
     assert_close(wl, as_f64(out), as_f64(ref), "prefix vs ordinary, two Q tiles per CTA")
+
+
+def test_repeated_shared_prefix_calls_give_the_same_bits():
+    lens = [2048 + n - 1 for n in (1, 100, 513, 7, 300, 64)]
+    wl = W.make_decode_workload("prefix_rep", context_lens=lens, num_q_heads=32, num_kv_heads=8,
+                                head_dim=128, dtype="bf16", seed=21, device="cuda",
+                                shared_prefix=2048)
+    dp = DevicePools(wl)
+    out, lens_t = _prefix_step(wl, dp, 2048)
+    ws = pk.decode_workspace(wl.num_seqs, 32, 8, 128, wl.max_blocks)
+    for _ in range(20):
+        again = torch.full_like(out, float("nan"))
+        pk.decode_attention_shared_prefix(again, wl.q, dp.k, dp.v, dp.tables, lens_t, wl.scale, 2048,
+                                          workspace=ws, err_flag=dp.err)
+        torch.cuda.synchronize()
+        assert torch.equal(again, out)
+    assert int(dp.err.item()) == 0
