@@ -210,10 +210,10 @@ def decode_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
+def profiled_traffic(workload: str, fp8: bool = False):
     """dram bytes per decode launch from a committed ncu summary, if it was taken on
     the current decode source; else None."""
-    path = os.path.join(ROOT, "profiles", f"decode_{workload}_dram.txt")
+    path = os.path.join(ROOT, "profiles", f"decode_{'fp8_' if fp8 else ''}{workload}_dram.txt")
     if not os.path.exists(path):
         return None
     kv = {}
@@ -468,7 +468,7 @@ def run_ours(args, rank, world, local):
                                " (main kernel + partition merge)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None if (fp8 or shared) else profiled_traffic(args.workload),
+                     "frac": round(achieved / peak, 4), "traffic": None if shared else profiled_traffic(args.workload, fp8),
                      "algorithmic_bytes_per_launch": dbytes, "avg_launch_ms": round(dec_ms, 5)},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms / K, 5),
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
