@@ -756,6 +756,69 @@ def run_prefill(args, rank, world, local):
     e1.record(stream)
     torch.cuda.synchronize()
     kernel_ms = e0.elapsed_time(e1) / K
+
+    # end to end: each step copies its chunk rows, q, positions and tables in from one pinned
+    # buffer and its output back, on a stream per direction with two sets of device buffers
+    srcs = (q, k_chunk, v_chunk, start_t, cu_q, tables)
+    offs, total = [], 0
+    for t in srcs:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+
+    def views(buf):
+        return tuple(buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                     for o, t in zip(offs, srcs))
+    h_in = torch.empty(total, dtype=torch.uint8).pin_memory()
+    for dst, src in zip(views(h_in), srcs):
+        dst.copy_(src.cpu())
+    d_in = [torch.empty(total, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    bufs = [views(b) for b in d_in]
+    outs = [torch.empty_like(out) for _ in range(2)]
+    h_outs = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    in_stream, back_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    loaded = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    returned = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
+
+    def e2e_step(i):
+        b = i & 1
+        d_q, d_k, d_v, d_st, d_cu, d_tab = bufs[b]
+        with torch.cuda.stream(in_stream):
+            if used[b]:
+                in_stream.wait_event(computed[b])
+            d_in[b].copy_(h_in, non_blocking=True)
+            loaded[b].record(in_stream)
+        stream.wait_event(loaded[b])
+        if used[b]:
+            stream.wait_event(returned[b])
+        pk.append_kv(kp, vp, d_k, d_v, d_tab, d_st, d_cu, err_flag=err, stream=stream)
+        pk.prefill_attention(outs[b], d_q, kp, vp, d_tab, d_st, d_cu, wl.scale, max_chunk=n,
+                             err_flag=err, stream=stream)
+        computed[b].record(stream)
+        with torch.cuda.stream(back_stream):
+            back_stream.wait_event(computed[b])
+            h_outs[b].copy_(outs[b], non_blocking=True)
+            returned[b].record(back_stream)
+        used[b] = True
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(in_stream)
+    stream.wait_event(g0)
+    back_stream.wait_event(g0)
+    for i in range(K):
+        e2e_step(i)
+    in_stream.wait_stream(stream)
+    in_stream.wait_stream(back_stream)
+    g1.record(in_stream)
+    torch.cuda.synchronize()
+    e2e_ms = g0.elapsed_time(g1) / K
+    assert torch.equal(h_outs[(K - 1) & 1], out.cpu())
+    h2d = sum(t.numel() * t.element_size() for t in srcs)
+    d2h = out.numel() * out.element_size()
     pos = (starts[:, None] + np.arange(n)[None, :]).astype(np.int64)   # positions of chunk rows
     flops = float(4 * 128 * 32 * (pos + 1).sum())                       # QK and PV, all heads
     peaks = load_peaks() or {}
@@ -773,7 +836,11 @@ def run_prefill(args, rank, world, local):
                          "peak_source": "measured bf16_tflops", "unit": "TFLOP/s",
                          "frac": round(flops / (kernel_ms / 1e3) / 1e12 / peak, 4),
                          "avg_launch_ms": round(kernel_ms, 4), "flops_per_launch": flops, "traffic": None},
-            "tokens_per_s": round(S * n / (ms / 1e3), 1), "clocks": clk}
+            "tokens_per_s": round(S * n / (ms / 1e3), 1),
+            "e2e": {"value": round(flops / (e2e_ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+                    "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h)},
+            "gpu_launches": 2 * K, "clocks": clk}
 
 
 def main():
