@@ -59,6 +59,8 @@ __device__ __forceinline__ void raise_flag(int32_t* err, int bits) {
 // Warp roles: 0-7 softmax (0-3 for Q tile a, 4-7 for tile b; a warp reaches the
 // TMEM lanes 32 (warp % 4) ..), 8 streams V tiles with bulk copies, 9 owns the
 // TMEM and issues the MMAs, 10-11 copy K tiles in and repack them chunk-major.
+// setmaxnreg moves registers from warps 8-11 (104 each) to the softmax warps (200
+// each), which hold a 128-column row of S.
 // Each softmax thread reads its row of S_h from TMEM, applies the causal mask,
 // keeps a running maximum that is raised only when a tile exceeds it by more than
 // 2^8 (O_h is then rescaled in TMEM), writes its bf16 probabilities over the
@@ -83,6 +85,12 @@ constexpr int kProducerWarp = kSoftWarps;       // V tiles
 constexpr int kMmaWarp = kSoftWarps + 1;        // TMEM owner, MMA issue
 constexpr int kRepackWarp = kSoftWarps + 2;     // K tiles: copy in, repack chunk-major
 constexpr int kRepackWarps = 2;
+// 16-byte loads in flight per lane of a repack warp (8 fits in the 104 registers the
+// copy warpgroup keeps; 16 would spill there)
+#ifndef PA_REPACK_BATCH
+#define PA_REPACK_BATCH 8
+#endif
+constexpr int kRepackBatch = PA_REPACK_BATCH;
 constexpr int kThreadsTC = (kSoftWarps + 2 + kRepackWarps) * 32;
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;
@@ -293,7 +301,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::SLOT);
-
+    // Registers move from the copy / MMA warpgroup (warps 8-11) to the two softmax
+    // warpgroups: 2 x 128 x 200 + 128 x 104 = 384 x 168, the launch's allocation.  Each
+    // warpgroup adjusts at the top of its own branch, so that each branch is compiled for
+    // its own budget.
+    if (warp >= kSoftWarps) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 104;" ::: "memory");
     if (warp == kProducerWarp) {
         // ---------------------------------------------------------------- V tiles
         // one bulk copy per (block, kv head) tile, lane b handles block b
@@ -371,22 +384,22 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
             const uint8_t* src = smem + L::K + st * KTILE;
             uint8_t* dst = smem + L::CM;
             const int piece = (lane & 15) * 16;
-            // sixteen loads in flight before their stores (a store could alias a later
+            // a batch of loads in flight before their stores (a store could alias a later
             // load, so the compiler would otherwise keep each load behind the previous store)
             constexpr int kRuns = kKeyBlocks * (D / 8);
             constexpr int kPerLane = kRuns / (2 * kRepackWarps);
             const int r0 = rw * (kRuns / kRepackWarps) + (lane >> 4);
 #pragma unroll 1
-            for (int u0 = 0; u0 < kPerLane; u0 += 16) {
-                uint4 v[16];
+            for (int u0 = 0; u0 < kPerLane; u0 += kRepackBatch) {
+                uint4 v[kRepackBatch];
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
+                for (int u = 0; u < kRepackBatch; ++u) {
                     const int r = r0 + 2 * (u0 + u);
                     const int b = r / (D / 8), c = r % (D / 8);
                     if (b < nb) v[u] = *reinterpret_cast<const uint4*>(src + b * TILE + c * 256 + piece);
                 }
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
+                for (int u = 0; u < kRepackBatch; ++u) {
                     const int r = r0 + 2 * (u0 + u);
                     const int b = r / (D / 8), c = r % (D / 8);
                     if (b < nb) *reinterpret_cast<uint4*>(dst + c * (kKeyBlocks * 256) + b * 256 + piece) = v[u];
@@ -517,7 +530,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         if (lane == 0) umma_commit(bar(kDone));
         __syncwarp();
         mbar_wait_bounded(bar(kDone), 0, kWaitLimitNs);
-    } else if (h == 0 || has_b) {
+    }
+    } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 200;" ::: "memory");
+    if (h == 0 || has_b) {
         // ---------------------------------------------------------------- softmax rows
         // Warp w reaches TMEM lanes 32 (w % 4) ..; this thread's row of tile h is lane
         // row % 128.  With two tiles a commit after S_h(j) covers every earlier MMA, so when
@@ -678,6 +694,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         } else if (lane == 0) {
             raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
         }
+    }
     }
     tc_fence_before();
     __syncthreads();
