@@ -388,6 +388,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
             // load, so the compiler would otherwise keep each load behind the previous store)
             constexpr int kRuns = kKeyBlocks * (D / 8);
             constexpr int kPerLane = kRuns / (2 * kRepackWarps);
+            static_assert(kPerLane % kRepackBatch == 0, "repack batch must divide a lane's runs");
             const int r0 = rw * (kRuns / kRepackWarps) + (lane >> 4);
 #pragma unroll 1
             for (int u0 = 0; u0 < kPerLane; u0 += kRepackBatch) {
