@@ -113,3 +113,23 @@ def test_repeated_shared_prefix_calls_give_the_same_bits():
         torch.cuda.synchronize()
         assert torch.equal(again, out)
     assert int(dp.err.item()) == 0
+
+
+def test_shared_prefix_two_q_tiles_per_cta_head_dim_64():
+    # 300 sequences x 1 query head per kv head = 300 rows (the second group's tile b partly
+    # empty), 12 kv heads, 8 prefix partitions: 192 CTAs of 256 rows at head_dim 64
+    lens = [4096 + n - 1 for n in np.random.default_rng(17).integers(1, 200, 300)]
+    wl = W.make_decode_workload("prefix64", context_lens=lens, num_q_heads=12, num_kv_heads=12,
+                                head_dim=64, dtype="bf16", seed=18, device="cuda",
+                                shared_prefix=4096)
+    dp = DevicePools(wl, canary=False)
+    out, lens_t = _prefix_step(wl, dp, 4096, hint=int(max(lens)) + 1)
+    assert int(dp.err.item()) == 0
+    rng = np.random.default_rng(19)
+    seqs = sorted(set(rng.choice(300, 10, replace=False).tolist()) | {0, 127, 128, 255, 256, 299})
+    pairs = [(s, int(rng.integers(12))) for s in seqs]
+    want = oracle_contig(wl, pairs)
+    got = np.stack([as_f64(out[s, h]) for s, h in pairs])
+    assert_close(wl, got, want, "two Q tiles per CTA, head_dim 64")
+    ref = dp.decode(lens_t)
+    assert_close(wl, as_f64(out), as_f64(ref), "prefix vs ordinary, head_dim 64")
