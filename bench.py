@@ -229,6 +229,81 @@ def profiled_traffic(workload: str, fp8: bool = False):
         return None
 
 
+class PipelinedE2E:
+    """End-to-end steps through the public API.  Every step copies its inputs in from pinned
+    host memory and its result back, both inside the timed region.  The inputs sit in one
+    pinned buffer (256-byte aligned segments) and go over in one copy.  The copies run on a
+    stream per direction into two sets of device buffers, so step i + 1's inputs load while
+    step i computes and step i's result returns while step i + 1 runs (a copy in queued
+    behind a copy back would wait for the compute); events order each buffer's reuse."""
+
+    def __init__(self, srcs, out, stream):
+        self.stream = stream
+        offs, total = [], 0
+        for t in srcs:
+            offs.append(total)
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+
+        def views(buf):
+            return tuple(buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                         for o, t in zip(offs, srcs))
+        self.h_in = torch.empty(total, dtype=torch.uint8).pin_memory()
+        for dst, src in zip(views(self.h_in), srcs):
+            dst.copy_(src.cpu())
+        self.d_in = [torch.empty(total, dtype=torch.uint8, device="cuda") for _ in range(2)]
+        self.bufs = [views(b) for b in self.d_in]
+        self.outs = [torch.empty_like(out) for _ in range(2)]
+        self.h_outs = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+        self.h2d = sum(t.numel() * t.element_size() for t in srcs)
+        self.d2h = out.numel() * out.element_size()
+        self.in_stream, self.back_stream = torch.cuda.Stream(), torch.cuda.Stream()
+        self.loaded = [torch.cuda.Event() for _ in range(2)]     # inputs of set b are in
+        self.computed = [torch.cuda.Event() for _ in range(2)]   # the step using set b is done
+        self.returned = [torch.cuda.Event() for _ in range(2)]   # output b is back on the host
+        self.used = [False, False]
+
+    def step(self, i, compute):
+        """compute(device_inputs, device_out) enqueues the step's kernels on self.stream."""
+        b = i & 1
+        with torch.cuda.stream(self.in_stream):
+            if self.used[b]:
+                self.in_stream.wait_event(self.computed[b])      # step i - 2 is done with set b
+            self.d_in[b].copy_(self.h_in, non_blocking=True)
+            self.loaded[b].record(self.in_stream)
+        self.stream.wait_event(self.loaded[b])
+        if self.used[b]:
+            self.stream.wait_event(self.returned[b])             # output b of step i - 2 is home
+        compute(self.bufs[b], self.outs[b])
+        self.computed[b].record(self.stream)
+        with torch.cuda.stream(self.back_stream):
+            self.back_stream.wait_event(self.computed[b])
+            self.h_outs[b].copy_(self.outs[b], non_blocking=True)
+            self.returned[b].record(self.back_stream)
+        self.used[b] = True
+
+    def run(self, compute, warmup, steps, world=1):
+        """Returns (device ms per step, max over ranks; the host's enqueue ms per step; the
+        last step's output as copied back)."""
+        for i in range(warmup):
+            self.step(i, compute)
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.in_stream)
+        self.stream.wait_event(e0)
+        self.back_stream.wait_event(e0)
+        th = time.perf_counter()
+        for i in range(steps):
+            self.step(i, compute)
+        host_ms = (time.perf_counter() - th) * 1e3 / steps
+        self.in_stream.wait_stream(self.stream)
+        self.in_stream.wait_stream(self.back_stream)
+        e1.record(self.in_stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return all_max(e0.elapsed_time(e1), world) / steps, host_ms, self.h_outs[(steps - 1) & 1]
+
+
 def run_ours(args, rank, world, local):
     import paged_kv_cache_207_gb300 as pk
     from paged_kv_cache_207_gb300 import build, workloads as W
@@ -353,80 +428,19 @@ def run_ours(args, rank, world, local):
     # a step covers `rot` of the model's `layers` layers
     tokens_per_s = all_sum(float(S), world) / ((layers / rot) * ms_per_step / 1e3)
 
-    # end to end: host buffers in pinned memory; every step copies its inputs in and its
-    # result back inside the timed region.  The copies run on streams of their own (one per
-    # direction) into two sets of device buffers, so step i + 1's inputs load while step i
-    # computes and step i's result returns while step i + 1 runs; events order each buffer's
-    # reuse.
-    # A step's inputs sit in one pinned host buffer (256-byte aligned segments) and go over
-    # in one copy into one of two device buffers of the same layout.
-    srcs = (q, k_new, v_new, start, cu, lens, tables)
-    offs, total = [], 0
-    for t in srcs:
-        offs.append(total)
-        total += (t.numel() * t.element_size() + 255) // 256 * 256
-    def views(buf):
-        return tuple(buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
-                     for o, t in zip(offs, srcs))
-    h_in = torch.empty(total, dtype=torch.uint8).pin_memory()
-    for dst, src in zip(views(h_in), srcs):
-        dst.copy_(src.cpu())
-    d_in = [torch.empty(total, dtype=torch.uint8, device="cuda") for _ in range(2)]
-    bufs = [views(b) for b in d_in]
-    outs = [torch.empty_like(out) for _ in range(2)]
-    h_outs = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
-    h2d = sum(t.numel() * t.element_size() for t in srcs)
-    d2h = h_outs[0].numel() * h_outs[0].element_size()
-    # one stream per direction: a copy in queued behind a copy back would wait for the compute
-    copy_stream, back_stream = torch.cuda.Stream(), torch.cuda.Stream()
-    loaded = [torch.cuda.Event() for _ in range(2)]      # inputs of buffer set b are in
-    computed = [torch.cuda.Event() for _ in range(2)]    # the step using set b has finished
-    returned = [torch.cuda.Event() for _ in range(2)]    # output b is back on the host
-    used = [False, False]
+    # end to end through the public API, host copies in the timed region every step
+    e2e = PipelinedE2E((q, k_new, v_new, start, cu, lens, tables), out, stream)
 
-    def e2e_step(i):
-        b = i & 1
-        d_q, d_k, d_v, d_start, d_cu, d_lens, d_tab = bufs[b]
-        with torch.cuda.stream(copy_stream):
-            if used[b]:
-                copy_stream.wait_event(computed[b])          # step i - 2 is done with set b
-            d_in[b].copy_(h_in, non_blocking=True)
-            loaded[b].record(copy_stream)
-        stream.wait_event(loaded[b])
-        if used[b]:
-            stream.wait_event(returned[b])                 # output b of step i - 2 is home
+    def e2e_compute(inp, o):
+        d_q, d_k, d_v, d_start, d_cu, d_lens, d_tab = inp
         for layer in range(rot):
             append(*pools[layer], d_k, d_v, d_tab, d_start, d_cu, err_flag=err, stream=stream)
-            decode(d_q, d_tab, d_lens, layer, outs[b])
-        computed[b].record(stream)
-        with torch.cuda.stream(back_stream):
-            back_stream.wait_event(computed[b])
-            h_outs[b].copy_(outs[b], non_blocking=True)
-            returned[b].record(back_stream)
-        used[b] = True
-
-    for i in range(max(3, args.warmup)):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(copy_stream)
-    stream.wait_event(e0)
-    back_stream.wait_event(e0)
-    th = time.perf_counter()
-    for i in range(K):
-        e2e_step(i)
-    host_ms = (time.perf_counter() - th) * 1e3 / K     # the host's enqueue time per step
-    copy_stream.wait_stream(stream)
-    copy_stream.wait_stream(back_stream)
-    e1.record(copy_stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    e2e_ms = all_max(e0.elapsed_time(e1), world)
+            decode(d_q, d_tab, d_lens, layer, o)
+    e2e_step_ms, host_ms, h_last = e2e.run(e2e_compute, max(3, args.warmup), K, world)
+    e2e_ms = e2e_step_ms * K
     e2e_value = total_bytes / (e2e_ms / 1e3) / 1e9
-    # the copied-back result equals the device result
-    assert torch.equal(h_outs[(K - 1) & 1], outs[(K - 1) & 1].cpu())
-    assert torch.equal(h_outs[(K - 1) & 1], out.cpu())
+    h2d, d2h = e2e.h2d, e2e.d2h
+    assert torch.equal(h_last, out.cpu())       # the copied-back result is the device result
 
     peaks = load_peaks()
     if peaks and peaks.get("hbm_gbs"):
@@ -757,68 +771,17 @@ def run_prefill(args, rank, world, local):
     torch.cuda.synchronize()
     kernel_ms = e0.elapsed_time(e1) / K
 
-    # end to end: each step copies its chunk rows, q, positions and tables in from one pinned
-    # buffer and its output back, on a stream per direction with two sets of device buffers
-    srcs = (q, k_chunk, v_chunk, start_t, cu_q, tables)
-    offs, total = [], 0
-    for t in srcs:
-        offs.append(total)
-        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    # end to end through the public API, host copies in the timed region every step
+    e2e = PipelinedE2E((q, k_chunk, v_chunk, start_t, cu_q, tables), out, stream)
 
-    def views(buf):
-        return tuple(buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
-                     for o, t in zip(offs, srcs))
-    h_in = torch.empty(total, dtype=torch.uint8).pin_memory()
-    for dst, src in zip(views(h_in), srcs):
-        dst.copy_(src.cpu())
-    d_in = [torch.empty(total, dtype=torch.uint8, device="cuda") for _ in range(2)]
-    bufs = [views(b) for b in d_in]
-    outs = [torch.empty_like(out) for _ in range(2)]
-    h_outs = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
-    in_stream, back_stream = torch.cuda.Stream(), torch.cuda.Stream()
-    loaded = [torch.cuda.Event() for _ in range(2)]
-    computed = [torch.cuda.Event() for _ in range(2)]
-    returned = [torch.cuda.Event() for _ in range(2)]
-    used = [False, False]
-
-    def e2e_step(i):
-        b = i & 1
-        d_q, d_k, d_v, d_st, d_cu, d_tab = bufs[b]
-        with torch.cuda.stream(in_stream):
-            if used[b]:
-                in_stream.wait_event(computed[b])
-            d_in[b].copy_(h_in, non_blocking=True)
-            loaded[b].record(in_stream)
-        stream.wait_event(loaded[b])
-        if used[b]:
-            stream.wait_event(returned[b])
+    def e2e_compute(inp, o):
+        d_q, d_k, d_v, d_st, d_cu, d_tab = inp
         pk.append_kv(kp, vp, d_k, d_v, d_tab, d_st, d_cu, err_flag=err, stream=stream)
-        pk.prefill_attention(outs[b], d_q, kp, vp, d_tab, d_st, d_cu, wl.scale, max_chunk=n,
+        pk.prefill_attention(o, d_q, kp, vp, d_tab, d_st, d_cu, wl.scale, max_chunk=n,
                              err_flag=err, stream=stream)
-        computed[b].record(stream)
-        with torch.cuda.stream(back_stream):
-            back_stream.wait_event(computed[b])
-            h_outs[b].copy_(outs[b], non_blocking=True)
-            returned[b].record(back_stream)
-        used[b] = True
-
-    for i in range(args.warmup):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    g0.record(in_stream)
-    stream.wait_event(g0)
-    back_stream.wait_event(g0)
-    for i in range(K):
-        e2e_step(i)
-    in_stream.wait_stream(stream)
-    in_stream.wait_stream(back_stream)
-    g1.record(in_stream)
-    torch.cuda.synchronize()
-    e2e_ms = g0.elapsed_time(g1) / K
-    assert torch.equal(h_outs[(K - 1) & 1], out.cpu())
-    h2d = sum(t.numel() * t.element_size() for t in srcs)
-    d2h = out.numel() * out.element_size()
+    e2e_ms, _, h_last = e2e.run(e2e_compute, args.warmup, K)
+    assert torch.equal(h_last, out.cpu())
+    h2d, d2h = e2e.h2d, e2e.d2h
     pos = (starts[:, None] + np.arange(n)[None, :]).astype(np.int64)   # positions of chunk rows
     flops = float(4 * 128 * 32 * (pos + 1).sum())                       # QK and PV, all heads
     peaks = load_peaks() or {}
