@@ -146,20 +146,10 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
     return r;
 }
 __device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
+    return ((uint64_t)__float_as_uint(hi) << 32) | __float_as_uint(lo);
 }
-__device__ __forceinline__ float lo_f32(uint64_t x) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
-    return lo;
-}
-__device__ __forceinline__ float hi_f32(uint64_t x) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
-    return hi;
-}
+__device__ __forceinline__ float lo_f32(uint64_t x) { return __uint_as_float((uint32_t)x); }
+__device__ __forceinline__ float hi_f32(uint64_t x) { return __uint_as_float((uint32_t)(x >> 32)); }
 __device__ __forceinline__ uint64_t ffma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
     uint64_t r;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
