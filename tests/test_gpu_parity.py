@@ -10,8 +10,8 @@ import torch
 
 import paged_kv_cache_207_gb300 as pk
 from paged_kv_cache_207_gb300 import workloads as W
-from _gpu_common import (DevicePools, as_f64, assert_close, np_bits, odtype, oracle_contig,
-                         oracle_pools, oracle_step_append, pool_bits)
+from _gpu_common import (DevicePools, as_f64, assert_close, np_bits, oracle_contig, oracle_pools,
+                         oracle_step_append, pool_bits)
 from oracle import oracle as orc
 
 pytestmark = pytest.mark.gpu

@@ -8,7 +8,6 @@ recomputation -- must leave every sequence with exactly its own context.
 """
 import numpy as np
 import pytest
-import torch
 
 from _gpu_common import BF16_ATOL
 from oracle import oracle as orc

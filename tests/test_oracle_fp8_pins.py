@@ -11,7 +11,6 @@ import math
 import os
 
 import numpy as np
-import pytest
 import torch
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")

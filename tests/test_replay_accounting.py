@@ -8,7 +8,6 @@ of result: paging holds fewer slots at peak, uses them better, and drains in no
 more steps.  The contiguous accounting is also checked against a brute-force
 recount.
 """
-import numpy as np
 import pytest
 
 

@@ -6,7 +6,6 @@ waste under one block, share the parent's block among the children, and drive
 the product block manager and the oracle's plain model to identical tables,
 copy pairs and counts, iteration by iteration.
 """
-import numpy as np
 import pytest
 
 from oracle.block_manager import OracleBlockManager, OutOfBlocks
