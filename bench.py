@@ -34,9 +34,14 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "paged decode-attention achieved HBM GB/s (% of GB300 peak) and decode tokens/s"
+NOMINAL_HBM_GBS = 7900.0      # GB300 HBM3e nominal bandwidth (the measured copy peak is lower)
+L2_BYTES = 129e6
 # workloads whose pool is near L2's size: the timed step runs every layer, each on a pool of its
 # own, so L2 cannot serve one layer's cache to the next
 ROTATE_LAYERS = {"qwen2.5-0.5b_gqa": 24}
+# workloads whose unique K/V fit in L2: consecutive steps cycle through this many copies of the
+# pools (as consecutive layers of a model would), so no step finds the previous one's data in L2
+STEP_POOLS = {"llama3-8b_shared_prefix": 4}
 LAYERS = {"llama3-8b_batch256": 32, "llama3-8b_long_context": 32, "llama3-8b_shared_prefix": 32,
           "qwen2.5-0.5b_gqa": 24, "gpt2_tiny_f32": 12}
 
@@ -356,12 +361,15 @@ def run_ours(args, rank, world, local):
     torch.cuda.empty_cache()
     stream = torch.cuda.current_stream()
     rot = ROTATE_LAYERS.get(args.workload, 1)
-    pools = [(kp, vp)] + [(kp.clone(), vp.clone()) for _ in range(rot - 1)]
+    npools = rot * STEP_POOLS.get(args.workload, 1)
+    pools = [(kp, vp)] + [(kp.clone(), vp.clone()) for _ in range(npools - 1)]
+    pool_bytes = 2 * npools * kp.numel() * kp.element_size()
+    counter = [0]          # steps issued so far: step i, layer l uses pool (i rot + l) % npools
 
     shared = args.shared_prefix
 
-    def decode(q_, tab_, lens_, layer=0, out=out):
-        kp, vp = pools[layer]
+    def decode(q_, tab_, lens_, pool, out=out):
+        kp, vp = pools[pool]
         if fp8:
             pk.decode_attention_fp8(out, q_, kp, vp, tab_, lens_, wl.scale, workspace=ws,
                                     max_context_len_hint=hint, err_flag=err, stream=stream)
@@ -374,11 +382,14 @@ def run_ours(args, rank, world, local):
                                 max_context_len_hint=hint, err_flag=err, stream=stream)
 
     def step(ev_d0=None, ev_d1=None):
+        base = counter[0] * rot
+        counter[0] += 1
         for layer in range(rot):
-            append(*pools[layer], k_new, v_new, tables, start, cu, err_flag=err, stream=stream)
+            pool = (base + layer) % npools
+            append(*pools[pool], k_new, v_new, tables, start, cu, err_flag=err, stream=stream)
             if ev_d0 is not None:
                 ev_d0[layer].record(stream)
-            decode(q, tables, lens, layer)
+            decode(q, tables, lens, pool)
             if ev_d1 is not None:
                 ev_d1[layer].record(stream)
 
@@ -433,9 +444,12 @@ def run_ours(args, rank, world, local):
 
     def e2e_compute(inp, o):
         d_q, d_k, d_v, d_start, d_cu, d_lens, d_tab = inp
+        base = counter[0] * rot
+        counter[0] += 1
         for layer in range(rot):
-            append(*pools[layer], d_k, d_v, d_tab, d_start, d_cu, err_flag=err, stream=stream)
-            decode(d_q, d_tab, d_lens, layer, o)
+            pool = (base + layer) % npools
+            append(*pools[pool], d_k, d_v, d_tab, d_start, d_cu, err_flag=err, stream=stream)
+            decode(d_q, d_tab, d_lens, pool, o)
     e2e_step_ms, host_ms, h_last = e2e.run(e2e_compute, max(3, args.warmup), K, world)
     e2e_ms = e2e_step_ms * K
     e2e_value = total_bytes / (e2e_ms / 1e3) / 1e9
@@ -468,11 +482,17 @@ def run_ours(args, rank, world, local):
                    "shared_prefix_tokens": shared,
                    "layers_for_tokens_per_s": layers,
                    "layer_pools": rot,
-                   "l2": "inputs larger than L2 (K/V pools %.2f GB per GPU vs 129 MB L2%s), no flush"
-                         % (2 * rot * kp.numel() * kp.element_size() / 1e9,
-                            ", a distinct pool per layer of the step" if rot > 1 else ""),
+                   "pool_sets": npools,
+                   "l2": ("inputs larger than L2 (K/V pools %.2f GB per GPU vs 129 MB L2%s), no flush"
+                          if pool_bytes > L2_BYTES else
+                          "K/V pools %.2f GB fit in the 129 MB L2%s")
+                         % (pool_bytes / 1e9,
+                            ", a distinct pool per layer of the step" if rot > 1 else
+                            (", %d pool copies cycled over consecutive steps" % npools
+                             if npools > 1 else "")),
                    "parallelism": f"replicas x{world} (sequences sharded by rank, no collective)"},
         "pct_of_peak_hbm": round(100.0 * value / peak, 2),
+        "pct_of_nominal_hbm": round(100.0 * value / NOMINAL_HBM_GBS, 2),
         **({"unique_kv_bytes_per_step": unique_kv_bytes(wl, shared),
             "logical_kv_bytes_per_step": logical_kv_bytes(wl),
             "logical_gbs": round(value * (step_bytes - unique_kv_bytes(wl, shared) +
@@ -685,7 +705,14 @@ def run_replay(args, rank, world, local):
                    "step": "one continuous-batching iteration: 12 x (append + decode)",
                    "cuda_graphs": graphs},
         "pct_of_peak_hbm": round(100 * dbytes / gpu_s / 1e9 / peaks.get("hbm_gbs", 6800.0), 2),
+        "pct_of_nominal_hbm": round(100 * dbytes / gpu_s / 1e9 / NOMINAL_HBM_GBS, 2),
         "tokens_per_s": round(tokens / wall, 1),
+        # the whole replay on the wall clock: host scheduling, block manager, the per-iteration
+        # copies of tables and positions, and every launch through the public API
+        "e2e": {"value": round(dbytes / wall / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(wall * 1e3 / st.iterations, 4),
+                "h2d_bytes_per_step": int(st.h2d_bytes // max(1, st.iterations)),
+                "d2h_bytes_per_step": 0},
         "tokens_per_s_gpu_time": round(tokens / gpu_s, 1),
         "replay": {"iterations": st.iterations, "generated_tokens": st.generated_tokens,
                    "preemptions": st.preemptions, "cow_copies": st.cow_copies,
@@ -732,6 +759,11 @@ def run_prefill(args, rank, world, local):
                  torch.zeros(S, dtype=torch.int32, device="cuda"), cu_ctx, err_flag=err)
     k_chunk, v_chunk = wl.k_rows[chunk].contiguous(), wl.v_rows[chunk].contiguous()
     del wl.k_rows, wl.v_rows
+    # consecutive steps alternate between two copies of the pools (as consecutive layers
+    # would), so no step finds the previous step's K/V in L2
+    pools = [(kp, vp), (kp.clone(), vp.clone())]
+    pool_bytes = 2 * len(pools) * kp.numel() * kp.element_size()
+    counter = [0]
     g = torch.Generator(device="cuda").manual_seed(7)
     q = torch.randn(S * n, 32, 128, generator=g, device="cuda").to(torch.bfloat16)
     out = torch.empty_like(q)
@@ -739,7 +771,12 @@ def run_prefill(args, rank, world, local):
     cu_q = torch.arange(0, S * n + 1, n, dtype=torch.int32, device="cuda")
     stream = torch.cuda.current_stream()
 
+    def next_pools():
+        counter[0] += 1
+        return pools[counter[0] % len(pools)]
+
     def step():
+        kp, vp = next_pools()
         pk.append_kv(kp, vp, k_chunk, v_chunk, tables, start_t, cu_q, err_flag=err, stream=stream)
         pk.prefill_attention(out, q, kp, vp, tables, start_t, cu_q, wl.scale, max_chunk=n,
                              err_flag=err, stream=stream)
@@ -765,6 +802,7 @@ def run_prefill(args, rank, world, local):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(K):
+        kp, vp = next_pools()
         pk.prefill_attention(out, q, kp, vp, tables, start_t, cu_q, wl.scale, max_chunk=n,
                              err_flag=err, stream=stream)
     e1.record(stream)
@@ -776,6 +814,7 @@ def run_prefill(args, rank, world, local):
 
     def e2e_compute(inp, o):
         d_q, d_k, d_v, d_st, d_cu, d_tab = inp
+        kp, vp = next_pools()
         pk.append_kv(kp, vp, d_k, d_v, d_tab, d_st, d_cu, err_flag=err, stream=stream)
         pk.prefill_attention(o, d_q, kp, vp, d_tab, d_st, d_cu, wl.scale, max_chunk=n,
                              err_flag=err, stream=stream)
@@ -793,7 +832,10 @@ def run_prefill(args, rank, world, local):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "llama3-8b_prefill", "num_seqs": S, "chunk_tokens": n,
                        "start_positions": "U[0, 3584]", "num_q_heads": 32, "num_kv_heads": 8,
-                       "head_dim": 128, "step": "pa_append_kv (512 rows/seq) + pa_prefill_attention"},
+                       "head_dim": 128, "step": "pa_append_kv (512 rows/seq) + pa_prefill_attention",
+                       "l2": "two copies of the K/V pools (%.2f GB in all) alternate over consecutive "
+                             "steps; the chunk's K/V tiles are re-read from L2 within a step by design"
+                             % (pool_bytes / 1e9)},
             "roofline": {"kernel": "prefill_tc_kernel (tcgen05, TMEM accumulators)", "bound": "tensor",
                          "achieved": round(flops / (kernel_ms / 1e3) / 1e12, 2), "peak": peak,
                          "peak_source": "measured bf16_tflops", "unit": "TFLOP/s",
@@ -804,6 +846,53 @@ def run_prefill(args, rank, world, local):
                     "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h)},
             "gpu_launches": 2 * K, "clocks": clk}
+
+
+# Workloads measured after the headline in the same process (one GPU; each with its own timed
+# region, CUDA-event roofline and clock record).  The first is the long-context split-KV case,
+# the second workload the 70 %-of-HBM target names.
+EXTRA_CONFIGS = [
+    ("llama3-8b_long_context", {"workload": "llama3-8b_long_context"}),
+    ("qwen2.5-0.5b_gqa", {"workload": "qwen2.5-0.5b_gqa"}),
+    ("llama3-8b_shared_prefix", {"workload": "llama3-8b_shared_prefix"}),
+    ("llama3-8b_shared_prefix+sharing", {"workload": "llama3-8b_shared_prefix",
+                                          "shared_prefix": 4096}),
+    ("llama3-8b_batch256+fp8", {"workload": "llama3-8b_batch256", "kv_dtype": "fp8"}),
+    ("llama3-8b_long_context+fp8", {"workload": "llama3-8b_long_context", "kv_dtype": "fp8"}),
+    ("spindle_replay", {"workload": "spindle_replay"}),
+    ("llama3-8b_prefill", {"workload": "llama3-8b_prefill"}),
+]
+DROP_KEYS = ("metric", "n_gpus", "higher_is_better", "scaling", "vs_baseline", "data")
+
+
+def run_one(args, rank, world, local):
+    if args.workload == "llama3-8b_prefill":
+        return run_prefill(args, rank, world, local)
+    if args.workload == "spindle_replay":
+        return run_replay(args, rank, world, local)
+    return run_ours(args, rank, world, local)[0]
+
+
+def run_extra_configs(args, rank, world, local) -> dict:
+    """Every other workload, one after the other, each freed before the next.  Steps are
+    capped so that the extra configs add a minute or two to the run."""
+    out = {}
+    for name, over in EXTRA_CONFIGS:
+        sub = argparse.Namespace(**vars(args))
+        sub.kv_dtype, sub.shared_prefix, sub.num_seqs = "bf16", 0, 0
+        for k, v in over.items():
+            setattr(sub, k, v)
+        sub.steps = max(1, min(args.steps, 50))
+        sub.warmup = max(3, min(args.warmup, 5))
+        try:
+            res = run_one(sub, rank, world, local)
+            out[name] = {k: v for k, v in res.items() if k not in DROP_KEYS}
+            out[name]["metric"] = res.get("metric")
+        except Exception as e:       # one workload failing must not hide the others
+            out[name] = {"error": f"{type(e).__name__}: {e}"}
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
 
 
 def main():
@@ -823,6 +912,8 @@ def main():
                          "tokens (the llama3-8b_shared_prefix workload shares 4096)")
     ap.add_argument("--num-seqs", type=int, default=0,
                     help="override the workload's sequence count (smaller cases for profiling)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="measure the headline workload only (no `configs` entries)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -832,17 +923,19 @@ def main():
         if rank == 0:
             print(json.dumps(res), flush=True)
         return
-    if args.workload == "llama3-8b_prefill":
-        res = run_prefill(args, rank, world, local)
-        if rank == 0:
-            print(json.dumps(res), flush=True)
-        return
-    if args.workload == "spindle_replay":
-        res = run_replay(args, rank, world, local)
+    if args.workload in ("llama3-8b_prefill", "spindle_replay"):
+        res = run_one(args, rank, world, local)
         if rank == 0:
             print(json.dumps(res), flush=True)
         return
     res, wl = run_ours(args, rank, world, local)
+    del wl
+    torch.cuda.empty_cache()
+    # the default run (one GPU, the headline workload) also measures every other workload
+    default_run = (args.workload == "llama3-8b_batch256" and args.kv_dtype == "bf16" and
+                   not args.shared_prefix and not args.num_seqs)
+    if world == 1 and default_run and not args.no_configs:
+        res["configs"] = run_extra_configs(args, rank, world, local)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             wl_cpu = cpu_workload(args.workload)

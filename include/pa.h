@@ -75,10 +75,17 @@ typedef enum {
 #define PA_DEV_ERR_BAD_POS 2     /* a position < 0 or >= max_blocks_per_seq * 16 */
 #define PA_DEV_ERR_HINT 4        /* a context is longer than max_context_len_hint */
 #define PA_DEV_ERR_BAD_CU 8      /* cu_new_tokens is not a prefix sum ending at total_new_tokens */
-#define PA_DEV_ERR_TIMEOUT 16    /* a bulk-copy wait gave up after 200 ms; while this bit
-                                    is set in the flag, decode CTAs return at once so a
-                                    broken pipeline cannot hold the GPU; clear it to resume */
+#define PA_DEV_ERR_TIMEOUT 16    /* a bulk-copy or tensor-core wait gave up after 200 ms.  The
+                                    outputs of the work that gave up are written as NaN.
+                                    While this bit is set in the flag, every decode, prefill
+                                    and partition-merge kernel given the flag returns without
+                                    writing anything (so a broken pipeline cannot hold the GPU
+                                    or overwrite results); clear the bit to resume.  Without a
+                                    flag (NULL) the NaN outputs are the only sign. */
 #define PA_DEV_ERR_BAD_PAIR 32   /* a copy pair names a block outside [0, num_blocks) */
+#define PA_DEV_ERR_BAD_PREFIX 64 /* pa_decode_attention_shared_prefix: a sequence's table does
+                                    not hold sequence 0's prefix blocks, or its context is
+                                    shorter than the shared prefix (its output is wrong) */
 
 /* Tokens per split-KV partition of pa_decode_attention (a multiple of 16). */
 #define PA_PARTITION_TOKENS 512
@@ -237,10 +244,12 @@ pa_status pa_decode_attention_fp8(void* out, const void* q, const void* k_pool, 
  *   of 16).  The caller guarantees that block_tables[s][b] == block_tables[0][b]
  *   for every s and every b < shared_prefix_tokens / 16, and that every
  *   context_lens[s] >= shared_prefix_tokens; the kernels read the prefix through
- *   sequence 0's table row.  bf16 only (fp32 returns PA_ERR_UNSUPPORTED when a
- *   whole partition is shared).  A prefix shorter than one partition falls back
- *   to pa_decode_attention.  The workspace is the one pa_decode_workspace_size
- *   gives (never 0 here when a partition is shared).
+ *   sequence 0's table row, and a sequence that breaks the promise within the
+ *   shared partitions sets PA_DEV_ERR_BAD_PREFIX.  bf16 only (fp32 returns
+ *   PA_ERR_UNSUPPORTED when a whole partition is shared).  A prefix shorter than
+ *   one partition, or a table of at most one partition (max_blocks_per_seq <=
+ *   32), falls back to pa_decode_attention.  The workspace is the one
+ *   pa_decode_workspace_size gives.
  */
 pa_status pa_decode_attention_shared_prefix(void* out, const void* q, const void* k_pool,
                                             const void* v_pool, const int32_t* block_tables,

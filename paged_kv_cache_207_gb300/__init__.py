@@ -10,5 +10,5 @@ from ._native import (  # noqa: F401
     pool_shape, fp8_pool_shape, append_kv_fp8, decode_attention_fp8, copy_block_fp8,
     prefill_attention,
     DEV_ERR_BAD_BLOCK, DEV_ERR_BAD_POS, DEV_ERR_HINT, DEV_ERR_BAD_CU, DEV_ERR_TIMEOUT,
-    DEV_ERR_BAD_PAIR,
+    DEV_ERR_BAD_PAIR, DEV_ERR_BAD_PREFIX,
 )

@@ -25,6 +25,7 @@ DEV_ERR_HINT = 4
 DEV_ERR_BAD_CU = 8
 DEV_ERR_TIMEOUT = 16
 DEV_ERR_BAD_PAIR = 32
+DEV_ERR_BAD_PREFIX = 64
 
 EXPORTED = [
     "pa_status_string", "pa_abi_version", "pa_append_kv", "pa_copy_block",

@@ -165,7 +165,8 @@ pa_status pa_decode_attention_shared_prefix(
     if ((long long)shared_prefix_tokens > (long long)max_blocks_per_seq * pa::kBlockTokens)
         return PA_ERR_INVALID_ARG;
     const int first_part = shared_prefix_tokens / pa::kPartTokens;
-    if (first_part == 0 || num_seqs <= 0)   // nothing whole to share: the ordinary path
+    // nothing whole to share, or every context fits one partition: the ordinary path
+    if (first_part == 0 || num_seqs <= 0 || max_blocks_per_seq <= pa::kPartBlocks)
         return pa_decode_attention(out, q, k_pool, v_pool, block_tables, context_lens, num_seqs,
                                    num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                                    max_context_len_hint, num_blocks, scale, dtype, workspace,

@@ -109,10 +109,12 @@ constexpr int ring_smem_bytes() { return NW * NST * 2 * TILE + NW * NST * 8; }
 // Cross-warp merge of one partition (both element types).  Every warp holds,
 // per padded head g < 8: running max m (log2 units), sum l and unnormalised
 // output row o[g][:] already written to shared memory by the caller.
+// A CTA in which a copy wait gave up (`failed`) writes NaN instead: the result is
+// incomplete, and it must not pass for a correct one even when no error flag was given.
 template <int D, int NW, typename OutT>
 __device__ __forceinline__ void merge_and_store(const KParams& p, const float* sm_o,
                                                 const float* sm_m, const float* sm_l, int s,
-                                                int kvh, int j, int nparts) {
+                                                int kvh, int j, int nparts, bool failed) {
     constexpr int OS = D + 4;
     for (int idx = threadIdx.x; idx < p.G * D; idx += NW * 32) {
         const int g = idx / D, d = idx - (idx / D) * D;
@@ -128,9 +130,10 @@ __device__ __forceinline__ void merge_and_store(const KParams& p, const float* s
                 lsum += wt * sm_l[w * 8 + g];
             }
         }
+        if (failed) M = acc = lsum = __int_as_float(0x7fc00000);
         const size_t row = (size_t)s * p.Hq + (size_t)kvh * p.G + g;
         if (nparts == 1 && p.first_part == 0) {
-            const float v = lsum > 0.f ? acc / lsum : 0.f;
+            const float v = failed ? acc : (lsum > 0.f ? acc / lsum : 0.f);
             if constexpr (sizeof(OutT) == 2)
                 reinterpret_cast<__nv_bfloat16*>(p.out)[row * D + d] = __float2bfloat16_rn(v);
             else
@@ -319,7 +322,7 @@ decode_bf16_kernel(const KParams p) {
         l1 += __shfl_xor_sync(0xffffffffu, l1, x);
     }
 
-    __syncthreads();   // every warp is done with its stages
+    const bool cta_failed = __syncthreads_or(failed);   // every warp is done with its stages
     constexpr int OS = D + 4;
     float* sm_o = reinterpret_cast<float*>(smem);       // [NW][8][OS]
     float* sm_m = sm_o + NW * 8 * OS;                    // [NW][8]
@@ -342,7 +345,7 @@ decode_bf16_kernel(const KParams p) {
         }
     }
     __syncthreads();
-    merge_and_store<D, NW, __nv_bfloat16>(p, sm_o, sm_m, sm_l, s, kvh, j, nparts);
+    merge_and_store<D, NW, __nv_bfloat16>(p, sm_o, sm_m, sm_l, s, kvh, j, nparts, cta_failed);
 }
 
 // ---------------------------------------------------------------------------
@@ -561,7 +564,7 @@ decode_fp8_kernel(const KParams p) {
     l0 *= kPScale;   // the P.V products carry the same factor
     l1 *= kPScale;
 
-    __syncthreads();
+    const bool cta_failed = __syncthreads_or(failed);
     constexpr int OS = D + 4;
     float* sm_o = reinterpret_cast<float*>(smem);
     float* sm_m = sm_o + NW * 8 * OS;
@@ -584,7 +587,7 @@ decode_fp8_kernel(const KParams p) {
         }
     }
     __syncthreads();
-    merge_and_store<D, NW, __nv_bfloat16>(p, sm_o, sm_m, sm_l, s, kvh, j, nparts);
+    merge_and_store<D, NW, __nv_bfloat16>(p, sm_o, sm_m, sm_l, s, kvh, j, nparts, cta_failed);
 }
 
 // ---------------------------------------------------------------------------
@@ -740,7 +743,7 @@ decode_f32_kernel(const KParams p) {
             if ((issued >> st) & 1u) mbar_wait_bounded(ring.bar(st), (phase >> st) & 1u, kWaitLimitNs);
     }
 
-    __syncthreads();
+    const bool cta_failed = __syncthreads_or(failed);
     constexpr int OS = D + 4;
     float* sm_o = reinterpret_cast<float*>(smem);
     float* sm_m = sm_o + NW * 8 * OS;
@@ -762,7 +765,7 @@ decode_f32_kernel(const KParams p) {
         }
     }
     __syncthreads();
-    merge_and_store<D, NW, float>(p, sm_o, sm_m, sm_l, s, kvh, j, nparts);
+    merge_and_store<D, NW, float>(p, sm_o, sm_m, sm_l, s, kvh, j, nparts, cta_failed);
 }
 
 // ---------------------------------------------------------------------------
@@ -795,8 +798,21 @@ decode_reduce_kernel(const KParams p, int num_rows) {
     // one partition and no shared prefix: written directly by the main kernel
     const int min_n = p.first_part > 0 ? 1 : 2;
     if (WPR == 1 && (!live || n < min_n)) return;
+    if (p.first_part > 0 && live && wr == 0 && row % p.Hq == 0) {
+        // shared prefix: check the caller's promise once per sequence -- its table holds
+        // sequence 0's blocks for the shared partitions and its context covers them.  Tables
+        // and lengths are inputs, so this runs while the kernels before are finishing.
+        const int s = row / p.Hq;
+        const int nb = p.first_part * p.part_blocks;
+        bool bad = __ldg(p.lens + s) < nb * kBlockTokens;
+        for (int b = lane; b < nb; b += 32)
+            bad |= __ldg(p.tables + (size_t)s * p.max_blocks + b) != __ldg(p.tables + b);
+        if (__any_sync(0xffffffffu, bad) && lane == 0) raise_flag(p.err, PA_DEV_ERR_BAD_PREFIX);
+    }
     grid_dependency_wait();     // the partials of the kernels before are complete and visible
-    const bool work = live && n >= min_n;
+    // after a copy wait gave up (this call or an earlier one) the partials are not all
+    // written: leave `out` untouched, as the main kernel does
+    const bool work = live && n >= min_n && !aborted(p.err);
     const size_t prow = (size_t)(work ? row : 0) * p.part_stride;
     const float2* ml = p.part_ml + prow;
     const float* po = p.part_o + prow * D + lane * DPL;
@@ -839,6 +855,7 @@ decode_reduce_kernel(const KParams p, int num_rows) {
             for (int k = 0; k < DPL; ++k) acc[k] += sm_acc[w][lane * DPL + k];
         }
     }
+    if (!work) return;
     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
 #pragma unroll
     for (int k = 0; k < DPL; ++k) {

@@ -226,6 +226,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
     }
     const int ntiles = (nblk + kKeyBlocks - 1) / kKeyBlocks;
 
+    // the TIMEOUT bit of the flag: set when a copy wait gave up in this or an earlier call;
+    // read now, acted on (by the whole CTA) after the first barrier
+    const uint32_t aborted_in = (threadIdx.x == 0 && p.err)
+        ? (uint32_t)(*reinterpret_cast<const volatile int32_t*>(p.err) & PA_DEV_ERR_TIMEOUT) : 0u;
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sQ = sbase + L::Q, sK = sbase + L::K, sV = sbase + L::V, sCM = sbase + L::CM;
     const uint32_t bar0 = sbase + L::BAR;
@@ -287,10 +291,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         }
         fence_proxy_async_smem();
     }
+    if (threadIdx.x == 0) *reinterpret_cast<volatile uint32_t*>(smem + L::SLOT + 4) = aborted_in;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::SLOT);
+    if (*reinterpret_cast<volatile uint32_t*>(smem + L::SLOT + 4) != 0u) {
+        // an earlier copy wait gave up: write nothing (the whole CTA returns together)
+        if (warp == kMmaWarp) tmem_dealloc<kTmemCols>(tmem);
+        if (PREFIX) grid_dependency_wait();
+        return;
+    }
     // Registers move from the copy / MMA warpgroup (warps 8-11) to the two softmax
     // warpgroups: 2 x 128 x 200 + 128 x 104 = 384 x 168, the launch's allocation.  Each
     // warpgroup adjusts at the top of its own branch, so that each branch is compiled for
@@ -682,8 +693,19 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
                     }
                 }
             }
-        } else if (lane == 0) {
-            raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
+        } else {
+            // a wait gave up: the row's result is incomplete, so it is written as NaN (visible
+            // even when no error flag was given)
+            if (lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
+            if (row_valid) {
+                if constexpr (PREFIX) {
+                    p.part_ml[orow * p.part_stride + blockIdx.z] =
+                        make_float2(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
+                } else {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow);
+                    for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
+                }
+            }
         }
     }
     }

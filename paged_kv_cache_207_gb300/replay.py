@@ -44,6 +44,7 @@ class ReplayStats:
     gpu_ms: float = 0.0
     wall_s: float = 0.0
     launches: int = 0
+    h2d_bytes: int = 0            # host -> device copies of schedule data (tables, positions)
     per_iteration_running: list = field(default_factory=list)
 
     @property
@@ -233,6 +234,8 @@ class Replay:
             pf_seq = torch.cat([torch.full((p[2],), p[0], dtype=torch.long) for p in prefill]).to(self.dev)
             pf_pos = torch.cat([torch.arange(p[2]) for p in prefill]).to(self.dev)
         pairs_t = self._i32(pairs).reshape(-1, 2) if pairs else None
+        self.stats.h2d_bytes += sum(t.numel() * t.element_size()
+                                    for t in (tables, start, lens, cu, seq_idx, pos_idx))
 
         ev0 = ev1 = None
         if self.time_gpu:
@@ -302,6 +305,7 @@ class Replay:
         for d, h in ((self.g_tables, self.h_tables), (self.g_start, self.h_start),
                      (self.g_lens, self.h_lens), (self.g_seq, self.h_seq), (self.g_pos, self.h_pos)):
             d[:S].copy_(h[:S], non_blocking=True)
+            self.stats.h2d_bytes += h[:S].numel() * h.element_size()
         self.h_free = torch.cuda.Event()
         self.h_free.record()
         if S not in self.graphs:

@@ -193,6 +193,56 @@ def test_twelve_layers_append_at_explicit_start_then_decode_sees_every_token():
         assert not torch.equal(short, out)
 
 
+def test_bf16_append_pools_bit_exact_llama_heads_chunked_and_ragged():
+    """bf16 pools at the Llama-3-8B head shape (8 kv heads x 128): every sequence's context
+    goes in as two chunks (two calls at explicit starts, chunks crossing block borders),
+    then one step's token; after each call the device pools equal the oracle append's
+    bytes, NaN canaries in every slot nothing wrote included."""
+    ctx = [1, 15, 16, 17, 100, 513, 40]
+    wl = W.make_decode_workload("append_bf16", context_lens=ctx, num_q_heads=32, num_kv_heads=8,
+                                head_dim=128, dtype="bf16", seed=91, device="cuda", pool_blocks=80)
+    shape = pk.pool_shape(wl.num_blocks, 8, 128, torch.bfloat16)
+    kd = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    vd = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    kd.view(torch.int16).fill_(-1)          # 0xFFFF: a NaN no N(0, 1) draw gives
+    vd.view(torch.int16).fill_(-1)
+    tables = torch.from_numpy(wl.block_tables).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ko = np.full(orc.pool_shape(wl.num_blocks, 8, 128, orc.BF16), 0xFFFF, np.uint16)
+    vo = ko.copy()
+    kr, vr = wl.k_rows.cpu(), wl.v_rows.cpu()
+    cut = [c // 2 + (c % 3) for c in ctx]     # first chunk: positions [0, cut)
+    for lo_of, hi_of in ((lambda s: 0, lambda s: min(cut[s], ctx[s])),
+                         (lambda s: min(cut[s], ctx[s]), lambda s: ctx[s])):
+        rows, starts, ns = [], [], []
+        for s in range(wl.num_seqs):
+            logical = wl.logical_rows(s)
+            a, b = lo_of(s), hi_of(s)
+            rows.append(logical[a:b])
+            starts.append(a)
+            ns.append(b - a)
+        idx = torch.from_numpy(np.concatenate(rows))
+        cu = np.concatenate([[0], np.cumsum(ns)]).astype(np.int32)
+        pk.append_kv(kd, vd, wl.k_rows[idx.cuda()].contiguous(), wl.v_rows[idx.cuda()].contiguous(),
+                     tables, torch.tensor(starts, dtype=torch.int32, device="cuda"),
+                     torch.from_numpy(cu).cuda(), err_flag=err)
+        assert orc.append_kv(ko, vo, kr[idx], vr[idx], wl.block_tables, np.array(starts, np.int32),
+                             cu, num_kv_heads=8, head_dim=128, num_blocks=wl.num_blocks,
+                             dtype=orc.BF16) == 0
+        torch.cuda.synchronize()
+        assert np.array_equal(pool_bits(kd), ko) and np.array_equal(pool_bits(vd), vo)
+    k_new, v_new = wl.k_rows[torch.from_numpy(wl.new_rows).cuda()], wl.v_rows[torch.from_numpy(wl.new_rows).cuda()]
+    start = torch.from_numpy(wl.context_lens.astype(np.int32)).cuda()
+    pk.append_kv(kd, vd, k_new.contiguous(), v_new.contiguous(), tables, start,
+                 torch.arange(wl.num_seqs + 1, dtype=torch.int32, device="cuda"), err_flag=err)
+    oracle_step_append(wl, ko, vo)
+    torch.cuda.synchronize()
+    assert np.array_equal(pool_bits(kd), ko) and np.array_equal(pool_bits(vd), vo)
+    assert int(err.item()) == 0
+    # slots nothing wrote still hold the canary
+    assert int((ko == 0xFFFF).sum()) > 0
+
+
 def test_copy_block_bit_exact_against_oracle():
     Hkv, D, nb = 8, 128, 40
     shape = pk.pool_shape(nb, Hkv, D, torch.bfloat16)

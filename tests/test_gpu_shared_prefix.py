@@ -64,6 +64,53 @@ def test_short_prefix_falls_back_to_the_ordinary_path_bitwise():
     assert torch.equal(out, ref)
 
 
+def test_one_partition_table_falls_back_to_the_ordinary_path_bitwise():
+    # a 512-token prefix in a table of 32 blocks: every context is the prefix and fits one
+    # partition, no workspace is needed, and the call takes the ordinary path
+    wl = W.make_decode_workload("one_part", context_lens=[511, 511, 511], num_q_heads=32,
+                                num_kv_heads=8, head_dim=128, dtype="bf16", seed=4,
+                                device="cuda", shared_prefix=512)
+    assert wl.max_blocks == 32
+    assert pk.decode_workspace_size(wl.num_seqs, 32, 8, 128, 32) == 0
+    dp = DevicePools(wl)                  # the 512 prefix rows, written once
+    lens_t = torch.full((3,), 512, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(wl.q)
+    pk.decode_attention_shared_prefix(out, wl.q, dp.k, dp.v, dp.tables, lens_t, wl.scale, 512,
+                                      err_flag=dp.err)
+    ref = dp.decode(lens_t)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    assert int(dp.err.item()) == 0
+
+
+def test_broken_prefix_promise_is_flagged():
+    # sequence 1's table points one prefix block elsewhere (as after a copy-on-write split),
+    # sequence 2's context is shorter than the prefix: both break the caller's promise
+    shared = 1024
+    lens = [shared + 40, shared + 300, shared + 5]
+    wl = W.make_decode_workload("broken", context_lens=lens, num_q_heads=8, num_kv_heads=2,
+                                head_dim=128, dtype="bf16", seed=6, device="cuda",
+                                shared_prefix=shared, pool_blocks=400)
+    dp = DevicePools(wl)
+    out, _ = _prefix_step(wl, dp, shared)
+    assert int(dp.err.item()) == 0                     # the promise holds: no flag
+    tables = dp.tables.clone()
+    tables[1, 10] = 399                                 # an unused block of the pool
+    k_new, v_new, start, cu, lens_t = dp.step_inputs()
+    ws = pk.decode_workspace(wl.num_seqs, 8, 2, 128, wl.max_blocks)
+    pk.decode_attention_shared_prefix(out, wl.q, dp.k, dp.v, tables, lens_t, wl.scale, shared,
+                                      workspace=ws, err_flag=dp.err)
+    torch.cuda.synchronize()
+    assert int(dp.err.item()) == pk.DEV_ERR_BAD_PREFIX
+    dp.err.zero_()
+    short = lens_t.clone()
+    short[2] = shared - 3
+    pk.decode_attention_shared_prefix(out, wl.q, dp.k, dp.v, dp.tables, short, wl.scale, shared,
+                                      workspace=ws, err_flag=dp.err)
+    torch.cuda.synchronize()
+    assert int(dp.err.item()) == pk.DEV_ERR_BAD_PREFIX
+
+
 def test_shared_prefix_workload_full_size_sampled():
     wl = W.llama8b_shared_prefix(device="cuda")
     dp = DevicePools(wl, canary=False)
