@@ -87,7 +87,8 @@ typedef enum {
                                     not hold sequence 0's prefix blocks, or its context is
                                     shorter than the shared prefix (its output is wrong) */
 
-/* Tokens per split-KV partition of pa_decode_attention (a multiple of 16). */
+/* Tokens per split-KV partition of pa_decode_attention at head_dim 128 (a multiple
+ * of 16); head_dim 64 uses 2 * PA_PARTITION_TOKENS, the same bytes per partition. */
 #define PA_PARTITION_TOKENS 512
 
 const char* pa_status_string(pa_status s);
@@ -149,14 +150,15 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t n
  * For each sequence s and query head h, with kv head g = h / (Hq / Hkv):
  *   out[s][h] = sum_t softmax_t(scale * <q[s][h], K[s][t][g]>) V[s][t][g]
  * computed in fp32 (bf16 inputs are exact in fp32) and rounded once to the
- * output type.  Contexts are cut into fixed PA_PARTITION_TOKENS-token
- * partitions whose partial results are merged with their log-sum-exp
+ * output type.  Contexts are cut into fixed partitions (PA_PARTITION_TOKENS
+ * tokens at head_dim 128, twice that at head_dim 64) whose partial results are merged with their log-sum-exp
  * weights; the partition of a token depends only on its position, so a
  * sequence's result does not depend on the rest of the batch.  A zero-length
  * context gives zeros.
  *   max_context_len_hint  host bound on every context_lens[s] used to size
- *                    the grid; <= 0 means max_blocks_per_seq * 16.  A longer
- *                    context sets PA_DEV_ERR_HINT and its output is incomplete.
+ *                    the grid; <= 0 means max_blocks_per_seq * 16.  A context
+ *                    that needs more partitions than the hint's sets
+ *                    PA_DEV_ERR_HINT and its output is incomplete.
  *   workspace        device scratch of at least pa_decode_workspace_size()
  *                    bytes (may be NULL when that size is 0); its contents on
  *                    entry do not matter.  Calls sharing a workspace must not

@@ -58,6 +58,15 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.oracle_e4m3_to_double.restype = ctypes.c_double
     L.oracle_append_kv_fp8.argtypes = [p, p, p, p, p, i, p, p, i, i, i, i]
     L.oracle_decode_fp8_pairs.argtypes = [p, p, i, p, p, p, p, p, i, i, i, i, i, ctypes.c_double]
+    L.oracle_e2m1_to_double.argtypes = [ctypes.c_uint8]
+    L.oracle_e2m1_to_double.restype = ctypes.c_double
+    L.oracle_f32_to_e2m1.argtypes = [ctypes.c_float]
+    L.oracle_f32_to_e2m1.restype = ctypes.c_uint8
+    L.oracle_mx_scale_code.argtypes = [ctypes.c_float]
+    L.oracle_mx_scale_code.restype = ctypes.c_uint8
+    L.oracle_append_kv_fp4.argtypes = [p, p, p, p, p, i, p, p, i, i, i, i]
+    L.oracle_decode_fp4_pairs.argtypes = [p, p, i, p, p, p, p, p, i, i, i, i, i, ctypes.c_double]
+    L.oracle_fp4_record_values.argtypes = [p, p, p, p, i]
     return L
 
 
@@ -263,3 +272,71 @@ def pool_shape(num_blocks: int, num_kv_heads: int, head_dim: int, dtype: int):
     """Shape of one pool as a numpy array in the documented layout."""
     x = 8 if dtype == BF16 else 4
     return (num_blocks, num_kv_heads, head_dim // x, BLOCK, x)
+
+
+# ---- block-scaled FP4 (MXFP4) cache ---------------------------------------------
+
+def e2m1_to_double(code: int) -> float:
+    return float(lib().oracle_e2m1_to_double(int(code)))
+
+
+def f32_to_e2m1(x: float) -> int:
+    return int(lib().oracle_f32_to_e2m1(float(x)))
+
+
+def mx_scale_code(amax: float) -> int:
+    """E8M0 code of the shared scale of a 32-value block whose largest magnitude is amax."""
+    return int(lib().oracle_mx_scale_code(float(amax)))
+
+
+def fp4_record_bytes(head_dim: int) -> int:
+    return 8 * head_dim + head_dim // 2
+
+
+def fp4_pool_shape(num_blocks: int, num_kv_heads: int, head_dim: int):
+    """One MXFP4 pool: per (block, kv head) 8*D code bytes + D/2 scale bytes."""
+    return (num_blocks, num_kv_heads, fp4_record_bytes(head_dim))
+
+
+def append_kv_fp4(k_pool, v_pool, k_new, v_new, block_tables, start_pos, cu_new_tokens, *,
+                  num_kv_heads, head_dim, num_blocks) -> int:
+    """Quantise bf16 rows (uint16 bits or torch bf16) into numpy uint8 MXFP4 pools in place."""
+    for p in (k_pool, v_pool):
+        if not (isinstance(p, np.ndarray) and p.dtype == np.uint8 and p.flags.c_contiguous):
+            raise TypeError("FP4 pools must be C-contiguous numpy uint8 arrays")
+    k_new, v_new = _np(k_new, np.uint16), _np(v_new, np.uint16)
+    tables = _np(block_tables, np.int32)
+    start = _np(start_pos, np.int32)
+    cu = _np(cu_new_tokens, np.int32)
+    return lib().oracle_append_kv_fp4(_ptr(k_pool), _ptr(v_pool), _ptr(k_new), _ptr(v_new),
+                                      _ptr(tables), tables.shape[1], _ptr(start), _ptr(cu),
+                                      start.shape[0], num_blocks, num_kv_heads, head_dim)
+
+
+def decode_fp4_pairs(pairs, q, k_pool, v_pool, block_tables, context_lens, *, num_q_heads,
+                     num_kv_heads, head_dim, num_blocks, scale) -> np.ndarray:
+    """Decode attention over MXFP4 pools for chosen (sequence, query head) pairs: float64 [n][D]."""
+    q = _np(q, np.uint16)
+    k_pool, v_pool = _np(k_pool, np.uint8), _np(v_pool, np.uint8)
+    tables = _np(block_tables, np.int32)
+    lens = _np(context_lens, np.int32)
+    pairs = np.ascontiguousarray(np.asarray(pairs, np.int32).reshape(-1, 2))
+    out = np.zeros((pairs.shape[0], head_dim), np.float64)
+    rc = lib().oracle_decode_fp4_pairs(_ptr(out), _ptr(pairs), pairs.shape[0], _ptr(q),
+                                       _ptr(k_pool), _ptr(v_pool), _ptr(tables), _ptr(lens),
+                                       num_q_heads, num_kv_heads, head_dim, tables.shape[1],
+                                       num_blocks, float(scale))
+    if rc != 0:
+        raise ValueError(f"oracle_decode_fp4_pairs failed with code {rc}")
+    return out
+
+
+def fp4_record_values(k_rec, v_rec, head_dim: int):
+    """Dequantised K and V rows ([16][D] float64 each) of one (block, kv head) record."""
+    k_rec, v_rec = _np(k_rec, np.uint8), _np(v_rec, np.uint8)
+    ko = np.zeros((BLOCK, head_dim), np.float64)
+    vo = np.zeros((BLOCK, head_dim), np.float64)
+    rc = lib().oracle_fp4_record_values(_ptr(ko), _ptr(vo), _ptr(k_rec), _ptr(v_rec), head_dim)
+    if rc != 0:
+        raise ValueError(f"oracle_fp4_record_values failed with code {rc}")
+    return ko, vo

@@ -465,3 +465,216 @@ int oracle_decode_fp8_pairs(double* out, const int32_t* pairs, int n, const void
     }
     return rc;
 }
+
+/* ---- block-scaled FP4 (MXFP4) KV cache ------------------------------------ *
+ * Slipstream, "Companion work", names a block-scaled FP4 kernel (qgemm-mx) as
+ * the next step of the same bandwidth-bound decode.  The reading taken here is
+ * the microscaling (MX) format that name refers to: blocks of 32 values along
+ * head_dim share one power-of-two scale stored as an E8M0 byte (value
+ * 2^(code - 127)); each value is an E2M1 code (1 sign bit, 2 exponent bits
+ * with bias 1, 1 mantissa bit: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6; no
+ * infinity or NaN).  The shared exponent of a block with largest magnitude
+ * amax is floor(log2(amax)) - 2 (2 = the exponent of E2M1's largest value,
+ * 6 = 1.5 * 2^2), so amax / scale lies in [4, 8) and values above 6 saturate.
+ * Each (token, kv head) row gets head_dim / 32 scales.
+ *
+ * Record of one (block, kv head), 8 * D code bytes then D / 2 scale bytes:
+ *   K codes: slot t's row of D / 2 bytes at t * D / 2; the byte at
+ *            c * (D / 8) + ks * 2 + half (c < 4, ks < D / 16, half < 2) holds
+ *            dims d0 = 16 ks + 8 half + 2 c (low nibble) and d0 + 1 (high).
+ *   V codes: the byte at ((r * 4 + c) * (D / 16) + mi) * 4 + dh * 2 + half
+ *            (r < 8, c < 4, mi < D / 16, dh < 2, half < 2) holds dim
+ *            16 mi + 8 dh + r of slots 2 c + 8 half (low nibble) and that + 1
+ *            (high nibble).
+ *   scales : at 8 * D, [16 slots][D / 32] E8M0 bytes, K and V alike.
+ * (The byte orders are this library's choice: each tensor-core fragment of a
+ * decode thread is then a run of adjacent bytes.) */
+
+/* Value of a 4-bit E2M1 code. */
+double oracle_e2m1_to_double(uint8_t c) {
+    int sign = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+    double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return sign ? -v : v;
+}
+
+/* Nearest E2M1 code, ties to the even code (mantissa bit 0); magnitudes above
+ * 6 saturate to 6; the sign of a zero result is kept.  Spacing: 0.5 below 2,
+ * 1 in [2, 4), 2 in [4, 6]. */
+uint8_t oracle_f32_to_e2m1(float x) {
+    uint8_t sign = signbit(x) ? 8 : 0;
+    double m = fabs((double)x);
+    if (isnan(x)) return sign;                     /* outside the format; not drawn */
+    double ulp = m < 2.0 ? 0.5 : (m < 4.0 ? 1.0 : 2.0);
+    double r = rint(m / ulp) * ulp;                /* half-way cases to the even multiple */
+    if (r > 6.0) r = 6.0;
+    uint8_t code;
+    if (r < 1.0) code = (uint8_t)(r / 0.5);        /* E = 0: 0 or 0.5 */
+    else {
+        int re;
+        frexp(r, &re);                             /* r in [2^(re-1), 2^re) */
+        int E = re;                                /* bias 1: r = 2^(E-1) (1 + M / 2) */
+        int M = (int)(r / ldexp(1.0, re - 1) * 2.0) - 2;
+        code = (uint8_t)((E << 1) | M);
+    }
+    return sign | code;
+}
+
+/* E8M0 code of the shared scale of a block whose largest magnitude is amax:
+ * 127 + floor(log2(amax)) - 2, kept in [0, 254]; an all-zero block gets 0. */
+uint8_t oracle_mx_scale_code(float amax) {
+    if (!(amax > 0.0f)) return 0;
+    int e;
+    frexp((double)amax, &e);                       /* amax in [2^(e-1), 2^e) */
+    int code = 127 + (e - 1) - 2;
+    if (code < 0) code = 0;
+    if (code > 254) code = 254;
+    return (uint8_t)code;
+}
+
+static size_t fp4_record_bytes(int D) { return (size_t)8 * D + (size_t)D / 2; }
+
+static size_t fp4_k_byte(int t, int d, int D) {
+    int ks = d / 16, half = (d % 16) / 8, c = (d % 8) / 2;
+    return (size_t)t * (D / 2) + (size_t)c * (D / 8) + (size_t)ks * 2 + half;
+}
+
+static size_t fp4_v_byte(int t, int d, int D) {
+    int mi = d / 16, dh = (d % 16) / 8, r = d % 8;
+    int half = t / 8, c = (t % 8) / 2;
+    return ((size_t)(r * 4 + c) * (D / 16) + mi) * 4 + dh * 2 + half;
+}
+
+/* Nibble of a code: the even dim (K) or even slot (V) of a byte is its low nibble. */
+static void put_nibble(uint8_t* rec, size_t byte, int high, uint8_t code) {
+    if (high) rec[byte] = (uint8_t)((rec[byte] & 0x0F) | (code << 4));
+    else rec[byte] = (uint8_t)((rec[byte] & 0xF0) | (code & 0x0F));
+}
+
+static uint8_t get_nibble(const uint8_t* rec, size_t byte, int high) {
+    return high ? (uint8_t)(rec[byte] >> 4) : (uint8_t)(rec[byte] & 0x0F);
+}
+
+/* Quantise one row of D bf16 values: D / 32 scale codes, D E2M1 codes; the
+ * division by the power-of-two scale is exact (done in double). */
+static void quantise_row_fp4(const uint16_t* row, int D, uint8_t* codes, uint8_t* sc) {
+    for (int b = 0; b < D / 32; ++b) {
+        float amax = 0.0f;
+        for (int d = 32 * b; d < 32 * b + 32; ++d) {
+            double v = fabs(bf16_bits_to_double(row[d]));
+            if ((float)v > amax) amax = (float)v;
+        }
+        sc[b] = oracle_mx_scale_code(amax);
+        double X = ldexp(1.0, (int)sc[b] - 127);
+        for (int d = 32 * b; d < 32 * b + 32; ++d)
+            codes[d] = amax > 0.0f ? oracle_f32_to_e2m1((float)(bf16_bits_to_double(row[d]) / X)) : 0;
+    }
+}
+
+/* Append with MXFP4 quantisation: bf16 rows ([sum n][Hkv][D]) to explicit
+ * positions like oracle_append_kv; codes and scales in the record layout above. */
+int oracle_append_kv_fp4(void* k_pool, void* v_pool, const void* k_new, const void* v_new,
+                         const int32_t* tables, int max_blocks, const int32_t* start_pos,
+                         const int32_t* cu_new, int num_seqs, int num_blocks, int Hkv, int D) {
+    if (Hkv <= 0 || D <= 0 || D % 32 != 0 || num_seqs < 0) return OR_BAD_ARG;
+    size_t rec = fp4_record_bytes(D);
+    uint8_t* codes = (uint8_t*)malloc((size_t)D);
+    uint8_t* sc = (uint8_t*)malloc((size_t)D / 32);
+    if (!codes || !sc) { free(codes); free(sc); return OR_BAD_ARG; }
+    int rc = OR_OK;
+    for (int s = 0; s < num_seqs; ++s) {
+        int n = cu_new[s + 1] - cu_new[s];
+        for (int i = 0; i < n; ++i) {
+            int p = start_pos[s] + i;
+            int64_t blk;
+            int r = lookup_block(tables, max_blocks, s, p, num_blocks, &blk);
+            if (r != OR_OK) { rc = r; continue; }
+            int t = p % ORACLE_BLOCK;
+            size_t row = (size_t)(cu_new[s] + i);
+            for (int h = 0; h < Hkv; ++h) {
+                uint8_t* krec = (uint8_t*)k_pool + ((size_t)blk * Hkv + h) * rec;
+                uint8_t* vrec = (uint8_t*)v_pool + ((size_t)blk * Hkv + h) * rec;
+                quantise_row_fp4((const uint16_t*)k_new + (row * Hkv + h) * (size_t)D, D, codes, sc);
+                for (int d = 0; d < D; ++d) put_nibble(krec, fp4_k_byte(t, d, D), d & 1, codes[d]);
+                memcpy(krec + (size_t)8 * D + (size_t)t * (D / 32), sc, (size_t)D / 32);
+                quantise_row_fp4((const uint16_t*)v_new + (row * Hkv + h) * (size_t)D, D, codes, sc);
+                for (int d = 0; d < D; ++d) put_nibble(vrec, fp4_v_byte(t, d, D), t & 1, codes[d]);
+                memcpy(vrec + (size_t)8 * D + (size_t)t * (D / 32), sc, (size_t)D / 32);
+            }
+        }
+    }
+    free(codes);
+    free(sc);
+    return rc;
+}
+
+/* Dequantised value of (slot t, dim d) of a record: code * 2^(scale - 127), exact. */
+static double fp4_value(const uint8_t* recp, int t, int d, int D, int is_v) {
+    uint8_t code = is_v ? get_nibble(recp, fp4_v_byte(t, d, D), t & 1)
+                        : get_nibble(recp, fp4_k_byte(t, d, D), d & 1);
+    uint8_t sc = recp[(size_t)8 * D + (size_t)t * (D / 32) + d / 32];
+    return ldexp(oracle_e2m1_to_double(code), (int)sc - 127);
+}
+
+/* Decode over MXFP4 pools: gather each position through the table, dequantise
+ * and attend in double; q is bf16. */
+int oracle_decode_fp4_one(double* out_row, const void* q, const void* k_pool, const void* v_pool,
+                          const int32_t* tables, const int32_t* context_lens, int s, int h,
+                          int Hq, int Hkv, int D, int max_blocks, int num_blocks, double scale) {
+    if (Hkv <= 0 || D <= 0 || D % 32 != 0 || Hq <= 0 || Hq % Hkv != 0) return OR_BAD_ARG;
+    int g = h / (Hq / Hkv);
+    int L = context_lens[s];
+    for (int d = 0; d < D; ++d) out_row[d] = 0.0;
+    if (L <= 0) return L < 0 ? OR_BAD_POS : OR_OK;
+    if (L > max_blocks * ORACLE_BLOCK) return OR_BAD_POS;
+    size_t rec = fp4_record_bytes(D);
+    double* Kc = (double*)malloc(sizeof(double) * (size_t)L * (size_t)D);
+    double* Vc = (double*)malloc(sizeof(double) * (size_t)L * (size_t)D);
+    double* x = (double*)malloc(sizeof(double) * (size_t)L);
+    double* qv = (double*)malloc(sizeof(double) * (size_t)D);
+    int rc = OR_OK;
+    if (!Kc || !Vc || !x || !qv) { rc = OR_BAD_ARG; goto done; }
+    for (int t = 0; t < L; ++t) {
+        int64_t blk;
+        rc = lookup_block(tables, max_blocks, s, t, num_blocks, &blk);
+        if (rc != OR_OK) goto done;
+        int slot = t % ORACLE_BLOCK;
+        const uint8_t* krec = (const uint8_t*)k_pool + ((size_t)blk * Hkv + g) * rec;
+        const uint8_t* vrec = (const uint8_t*)v_pool + ((size_t)blk * Hkv + g) * rec;
+        for (int d = 0; d < D; ++d) {
+            Kc[(size_t)t * D + d] = fp4_value(krec, slot, d, D, 0);
+            Vc[(size_t)t * D + d] = fp4_value(vrec, slot, d, D, 1);
+        }
+    }
+    for (int d = 0; d < D; ++d) qv[d] = load_elem(q, ((size_t)s * Hq + h) * (size_t)D + d, 1);
+    attend(out_row, qv, Kc, Vc, x, L, D, scale);
+done:
+    free(Kc); free(Vc); free(x); free(qv);
+    return rc;
+}
+
+int oracle_decode_fp4_pairs(double* out, const int32_t* pairs, int n, const void* q,
+                            const void* k_pool, const void* v_pool, const int32_t* tables,
+                            const int32_t* context_lens, int Hq, int Hkv, int D, int max_blocks,
+                            int num_blocks, double scale) {
+    int rc = OR_OK;
+    for (int i = 0; i < n; ++i) {
+        int r = oracle_decode_fp4_one(out + (size_t)i * D, q, k_pool, v_pool, tables, context_lens,
+                                      pairs[2 * i], pairs[2 * i + 1], Hq, Hkv, D, max_blocks,
+                                      num_blocks, scale);
+        if (r != OR_OK) rc = r;
+    }
+    return rc;
+}
+
+/* Dequantised rows of one (block, kv head) record: k_out, v_out [16][D] doubles
+ * (a test view of the stored values). */
+int oracle_fp4_record_values(double* k_out, double* v_out, const void* k_rec, const void* v_rec,
+                             int D) {
+    if (D <= 0 || D % 32 != 0) return OR_BAD_ARG;
+    for (int t = 0; t < ORACLE_BLOCK; ++t)
+        for (int d = 0; d < D; ++d) {
+            k_out[(size_t)t * D + d] = fp4_value((const uint8_t*)k_rec, t, d, D, 0);
+            v_out[(size_t)t * D + d] = fp4_value((const uint8_t*)v_rec, t, d, D, 1);
+        }
+    return OR_OK;
+}

@@ -5,7 +5,7 @@ this package is the thin Python binding (``_native``) plus the seeded workload
 generators (``workloads``).
 """
 from ._native import (  # noqa: F401
-    BLOCK_SIZE, PARTITION_TOKENS, BlockManager, PagedKVError, append_kv, copy_block,
+    BLOCK_SIZE, PARTITION_TOKENS, partition_tokens, BlockManager, PagedKVError, append_kv, copy_block,
     decode_attention, decode_attention_shared_prefix, decode_workspace, decode_workspace_size, lib,
     pool_shape, fp8_pool_shape, append_kv_fp8, decode_attention_fp8, copy_block_fp8,
     prefill_attention,

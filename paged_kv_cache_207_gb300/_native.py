@@ -17,7 +17,12 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpaged_k
 PA_OK = 0
 PA_F32, PA_BF16 = 0, 1
 BLOCK_SIZE = 16
-PARTITION_TOKENS = 512
+PARTITION_TOKENS = 512          # split-KV partition of pa_decode_attention at head_dim 128
+
+
+def partition_tokens(head_dim: int) -> int:
+    """Tokens per split-KV partition of pa_decode_attention (head_dim 64: twice as many)."""
+    return 2 * PARTITION_TOKENS if head_dim == 64 else PARTITION_TOKENS
 
 DEV_ERR_BAD_BLOCK = 1
 DEV_ERR_BAD_POS = 2

@@ -145,9 +145,9 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, cons
     a.head_dim = head_dim;
     a.max_blocks = max_blocks_per_seq;
     a.num_blocks = num_blocks;
-    a.grid_parts = (bound + pa::kPartTokens - 1) / pa::kPartTokens;
+    a.part_blocks = pa::decode_part_blocks(head_dim);
+    a.grid_parts = (bound + a.part_blocks * pa::kBlockTokens - 1) / (a.part_blocks * pa::kBlockTokens);
     a.part_stride = pa::decode_part_stride(max_blocks_per_seq);
-    a.part_blocks = pa::kPartBlocks;
     a.first_part = 0;
     a.scale = scale;
     a.dtype = dtype;

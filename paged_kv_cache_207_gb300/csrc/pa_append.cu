@@ -33,25 +33,11 @@ struct AParams {
     long long items;                                      // total * Hkv * chunks
 };
 
-__global__ void __launch_bounds__(256) append_kernel(const AParams p) {
-    // a decode launched after this kernel may start its set-up now; it waits for this
-    // grid to finish before reading the pools
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (item == 0) {
-        if (__ldg(p.cu) != 0 || __ldg(p.cu + p.S) != p.total) raise_flag(p.err, PA_DEV_ERR_BAD_CU);
-    }
-    if (item >= p.items) return;
-    const int ch = (int)(item % p.chunks);
-    const long long rh = item / p.chunks;
-    const int h = (int)(rh % p.Hkv);
-    const int row = (int)(rh / p.Hkv);
-
-    // the new data depends only on the row: load it first, the address chain follows
-    const size_t src = (((size_t)row * p.Hkv + h) * p.chunks + ch) * 16;
-    const uint4 kv = __ldg(reinterpret_cast<const uint4*>(p.k_new + src));
-    const uint4 vv = __ldg(reinterpret_cast<const uint4*>(p.v_new + src));
-
+// Sequence, position and physical block of new row `row` (reads only cu, start_pos
+// and the tables, which no kernel of this library writes).  Flags and returns false
+// when the row has no valid destination; `report` selects the thread that flags.
+__device__ __forceinline__ bool locate_row(const AParams& p, int row, bool report, int& s_out,
+                                           int& slot_out, int32_t& blk_out) {
     // sequence owning this row: cu[s] <= row < cu[s+1].  Guess by proportion (exact
     // when every sequence appends the same number of rows, e.g. one per decode step),
     // then fall back to a binary search.
@@ -70,21 +56,50 @@ __global__ void __launch_bounds__(256) append_kernel(const AParams p) {
         first = __ldg(p.cu + s);
         next = __ldg(p.cu + s + 1);
         if (row < first || row >= next) {
-            raise_flag(p.err, PA_DEV_ERR_BAD_CU);
-            return;
+            if (report) raise_flag(p.err, PA_DEV_ERR_BAD_CU);
+            return false;
         }
     }
     const long long pos = (long long)__ldg(p.start_pos + s) + (row - first);
     if (pos < 0 || pos >= (long long)p.max_blocks * kBlockTokens) {
-        raise_flag(p.err, PA_DEV_ERR_BAD_POS);
-        return;
+        if (report) raise_flag(p.err, PA_DEV_ERR_BAD_POS);
+        return false;
     }
     const int32_t blk = __ldg(p.tables + (size_t)s * p.max_blocks + (int)(pos / kBlockTokens));
     if (blk < 0 || blk >= p.num_blocks) {
-        raise_flag(p.err, PA_DEV_ERR_BAD_BLOCK);
-        return;
+        if (report) raise_flag(p.err, PA_DEV_ERR_BAD_BLOCK);
+        return false;
     }
-    const int slot = (int)(pos % kBlockTokens);
+    s_out = s;
+    slot_out = (int)(pos % kBlockTokens);
+    blk_out = blk;
+    return true;
+}
+
+__global__ void __launch_bounds__(256) append_kernel(const AParams p) {
+    // a decode launched after this kernel may start its set-up now; it waits for this
+    // grid to finish before reading the pools
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (item == 0) {
+        if (__ldg(p.cu) != 0 || __ldg(p.cu + p.S) != p.total) raise_flag(p.err, PA_DEV_ERR_BAD_CU);
+    }
+    const int ch = (int)(item % p.chunks);
+    const long long rh = item / p.chunks;
+    const int h = (int)(rh % p.Hkv);
+    const int row = (int)(rh / p.Hkv);
+    int s, slot;
+    int32_t blk;
+    const bool ok = item < p.items && locate_row(p, row, true, s, slot, blk);
+
+    // The address chain above read only inputs.  The pools (and, in principle, the new
+    // rows) may still be in use by the previous kernel of the stream: wait for it.  Every
+    // thread waits before it exits, so this grid never completes before that kernel.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (!ok) return;
+    const size_t src = (((size_t)row * p.Hkv + h) * p.chunks + ch) * 16;
+    const uint4 kv = __ldg(reinterpret_cast<const uint4*>(p.k_new + src));
+    const uint4 vv = __ldg(reinterpret_cast<const uint4*>(p.v_new + src));
     // pool byte offset: tile (blk, h), chunk ch, slot  -> 16 bytes
     const size_t dst = ((((size_t)blk * p.Hkv + h) * p.chunks + ch) * kBlockTokens + slot) * 16;
     *reinterpret_cast<uint4*>(p.k_pool + dst) = kv;
@@ -105,9 +120,13 @@ __global__ void __launch_bounds__(256) append_fp8_kernel(const AParams p) {
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         if (__ldg(p.cu) != 0 || __ldg(p.cu + p.S) != p.total) raise_flag(p.err, PA_DEV_ERR_BAD_CU);
     }
-    if (wid >= (long long)p.total * p.Hkv) return;
     const int h = (int)(wid % p.Hkv);
     const int row = (int)(wid / p.Hkv);
+    int s, slot;
+    int32_t blk;
+    const bool ok = wid < (long long)p.total * p.Hkv && locate_row(p, row, lane == 0, s, slot, blk);
+    asm volatile("griddepcontrol.wait;" ::: "memory");           // as in append_kernel
+    if (!ok) return;                                              // warp-uniform
     const size_t src = ((size_t)row * p.Hkv + h) * D + (size_t)lane * VPL;
     float kx[VPL], vx[VPL];
     if constexpr (VPL == 4) {
@@ -135,37 +154,6 @@ __global__ void __launch_bounds__(256) append_fp8_kernel(const AParams p) {
         va = fmaxf(va, __shfl_xor_sync(0xffffffffu, va, x));
     }
     const float ks = __fdiv_rn(ka, 448.f), vs = __fdiv_rn(va, 448.f);
-
-    int s = (int)(((long long)row * p.S) / (p.total > 0 ? p.total : 1));
-    if (s >= p.S) s = p.S - 1;
-    int first = __ldg(p.cu + s);
-    int next = __ldg(p.cu + s + 1);
-    if (!(first <= row && row < next)) {
-        int lo = 0, hi = p.S - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (__ldg(p.cu + mid) <= row) lo = mid;
-            else hi = mid - 1;
-        }
-        s = lo;
-        first = __ldg(p.cu + s);
-        next = __ldg(p.cu + s + 1);
-        if (row < first || row >= next) {
-            if (lane == 0) raise_flag(p.err, PA_DEV_ERR_BAD_CU);
-            return;
-        }
-    }
-    const long long pos = (long long)__ldg(p.start_pos + s) + (row - first);
-    if (pos < 0 || pos >= (long long)p.max_blocks * kBlockTokens) {
-        if (lane == 0) raise_flag(p.err, PA_DEV_ERR_BAD_POS);
-        return;
-    }
-    const int32_t blk = __ldg(p.tables + (size_t)s * p.max_blocks + (int)(pos / kBlockTokens));
-    if (blk < 0 || blk >= p.num_blocks) {
-        if (lane == 0) raise_flag(p.err, PA_DEV_ERR_BAD_BLOCK);
-        return;
-    }
-    const int slot = (int)(pos % kBlockTokens);
     const size_t rec = fp8_record_bytes(D);
     char* krec = p.k_pool + ((size_t)blk * p.Hkv + h) * rec;
     char* vrec = p.v_pool + ((size_t)blk * p.Hkv + h) * rec;
@@ -220,6 +208,24 @@ __global__ void __launch_bounds__(256) copy_kernel(const CParams p) {
         to[i] = from[i];
 }
 
+// Launch as a programmatic dependent of the previous kernel of the stream: the append
+// may start while that kernel finishes, computes its destinations, and waits for it
+// (griddepcontrol.wait) before it reads the new rows or writes the pools.
+template <typename K>
+cudaError_t launch_dependent(K kernel, dim3 grid, cudaStream_t stream, const AParams& p) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 }  // namespace
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
@@ -241,8 +247,7 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
     p.items = (long long)a.total_new * a.num_kv_heads * p.chunks;
     if (p.items == 0) return cudaSuccess;
     const long long blocks = (p.items + 255) / 256;
-    append_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(append_kernel, dim3((unsigned)blocks), stream, p);
 }
 
 cudaError_t launch_append_fp8(const AppendArgs& a, cudaStream_t stream) {
@@ -264,11 +269,8 @@ cudaError_t launch_append_fp8(const AppendArgs& a, cudaStream_t stream) {
     p.items = (long long)a.total_new * a.num_kv_heads;   // warps
     if (p.items == 0) return cudaSuccess;
     const long long blocks = (p.items * 32 + 255) / 256;
-    if (a.head_dim == 64)
-        append_fp8_kernel<64><<<(unsigned)blocks, 256, 0, stream>>>(p);
-    else
-        append_fp8_kernel<128><<<(unsigned)blocks, 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    return a.head_dim == 64 ? launch_dependent(append_fp8_kernel<64>, dim3((unsigned)blocks), stream, p)
+                            : launch_dependent(append_fp8_kernel<128>, dim3((unsigned)blocks), stream, p);
 }
 
 cudaError_t launch_copy(const CopyArgs& a, cudaStream_t stream) {

@@ -172,7 +172,10 @@ decode_bf16_kernel(const KParams p) {
     const int nparts = num_parts(L, p.part_blocks);
     if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0 && nparts > p.grid_parts)
         raise_flag(p.err, PA_DEV_ERR_HINT);
-    if (j >= nparts || aborted(p.err)) return;
+    if (j >= nparts || aborted(p.err)) {
+        grid_dependency_wait();   // a dependent grid never completes before the one it follows
+        return;
+    }
 
     const int blk0 = j * p.part_blocks;                            // first logical block
     const int tok_end = min(L, (j + 1) * p.part_blocks * kBlockTokens);           // one past the last token
@@ -189,21 +192,9 @@ decode_bf16_kernel(const KParams p) {
     }
     __syncwarp();
 
-    // Query fragments (B operand, k = dim, n = query head of the group).
-    uint32_t qb[KS][2];
-    {
-        const bool live = r < p.G;
-        const uint16_t* qrow = reinterpret_cast<const uint16_t*>(p.q) +
-                               ((size_t)s * p.Hq + (size_t)kvh * p.G + (live ? r : 0)) * D;
-#pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-            qb[kk][0] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * c)) : 0u;
-            qb[kk][1] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 8 + 2 * c)) : 0u;
-        }
-    }
-
-    // Everything above reads only the query, the tables and the lengths.  The pools
-    // may still be being written by the previous kernel (an append): wait for it.
+    // Everything above reads only the tables and the lengths, which no kernel of this
+    // library writes.  The pools (an append) and the query (any earlier call's output)
+    // may still be being written by the previous kernel: wait for it.
     grid_dependency_wait();
     grid_launch_dependents();
 
@@ -235,6 +226,20 @@ decode_bf16_kernel(const KParams p) {
 #pragma unroll
     for (int i = 0; i < NST; ++i)
         if (i < nb_w && issue_blk(first_blk[i], i)) issued |= 1u << i;
+
+    // Query fragments (B operand, k = dim, n = query head of the group), loaded while
+    // the first tiles are in flight.
+    uint32_t qb[KS][2];
+    {
+        const bool live = r < p.G;
+        const uint16_t* qrow = reinterpret_cast<const uint16_t*>(p.q) +
+                               ((size_t)s * p.Hq + (size_t)kvh * p.G + (live ? r : 0)) * D;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            qb[kk][0] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * c)) : 0u;
+            qb[kk][1] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 8 + 2 * c)) : 0u;
+        }
+    }
 
     // ldmatrix row addresses: K tile k-step kk reads 512 contiguous bytes.
     const uint32_t k_lane = lane * 16;
@@ -387,7 +392,10 @@ decode_fp8_kernel(const KParams p) {
     const int nparts = num_parts(L, p.part_blocks);
     if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0 && nparts > p.grid_parts)
         raise_flag(p.err, PA_DEV_ERR_HINT);
-    if (j >= nparts || aborted(p.err)) return;
+    if (j >= nparts || aborted(p.err)) {
+        grid_dependency_wait();   // a dependent grid never completes before the one it follows
+        return;
+    }
 
     const int blk0 = j * p.part_blocks;
     const int tok_end = min(L, (j + 1) * p.part_blocks * kBlockTokens);
@@ -403,23 +411,7 @@ decode_fp8_kernel(const KParams p) {
     }
     __syncwarp();
 
-    // query fragments in f16 with the permuted dims: b0 <- dims 16kk+4c, +1; b1 <- +2, +3
-    uint32_t qb[KS][2];
-    {
-        const bool live = r < p.G;
-        const uint16_t* qrow = reinterpret_cast<const uint16_t*>(p.q) +
-                               ((size_t)s * p.Hq + (size_t)kvh * p.G + (live ? r : 0)) * D;
-#pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-            if (live) {
-                const uint2 u = __ldg(reinterpret_cast<const uint2*>(qrow + 16 * kk + 4 * c));
-                qb[kk][0] = pack_f16x2(bf16_lo_to_f32(u.x), bf16_hi_to_f32(u.x));
-                qb[kk][1] = pack_f16x2(bf16_lo_to_f32(u.y), bf16_hi_to_f32(u.y));
-            } else {
-                qb[kk][0] = qb[kk][1] = 0u;
-            }
-        }
-    }
+    // the pools and the query may be written by the previous kernel: wait for it
     grid_dependency_wait();
     grid_launch_dependents();
 
@@ -450,6 +442,25 @@ decode_fp8_kernel(const KParams p) {
 #pragma unroll
     for (int i = 0; i < NST; ++i)
         if (i < nb_w && issue_blk(first_blk[i], i)) issued |= 1u << i;
+
+    // query fragments in f16 with the permuted dims: b0 <- dims 16kk+4c, +1; b1 <- +2, +3
+    // (loaded while the first records are in flight)
+    uint32_t qb[KS][2];
+    {
+        const bool live = r < p.G;
+        const uint16_t* qrow = reinterpret_cast<const uint16_t*>(p.q) +
+                               ((size_t)s * p.Hq + (size_t)kvh * p.G + (live ? r : 0)) * D;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            if (live) {
+                const uint2 u = __ldg(reinterpret_cast<const uint2*>(qrow + 16 * kk + 4 * c));
+                qb[kk][0] = pack_f16x2(bf16_lo_to_f32(u.x), bf16_hi_to_f32(u.x));
+                qb[kk][1] = pack_f16x2(bf16_lo_to_f32(u.y), bf16_hi_to_f32(u.y));
+            } else {
+                qb[kk][0] = qb[kk][1] = 0u;
+            }
+        }
+    }
 
     // K rows gathered in the pi order; lane l addresses row l%8 of matrix l/8:
     // matrices 0 / 1 = rows 0-7 / 8-15 of piece kk, 2 / 3 = the same of piece kk+1
@@ -782,6 +793,9 @@ decode_reduce_kernel(const KParams p, int num_rows) {
     constexpr int WPR = 8 / RPC;                    // warps per row
     __shared__ float sm_acc[8][D];
     __shared__ float sm_l[8];
+    // the next kernel of the stream may start its set-up; every kernel of this library
+    // waits for this grid before reading what it writes (`out`)
+    grid_launch_dependents();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int row = blockIdx.x * RPC + warp / WPR;  // s * Hq + h
     const int wr = warp % WPR;                      // this warp's share of the row
@@ -797,7 +811,10 @@ decode_reduce_kernel(const KParams p, int num_rows) {
     }
     // one partition and no shared prefix: written directly by the main kernel
     const int min_n = p.first_part > 0 ? 1 : 2;
-    if (WPR == 1 && (!live || n < min_n)) return;
+    if (WPR == 1 && (!live || n < min_n)) {
+        grid_dependency_wait();   // a dependent grid never completes before the one it follows
+        return;
+    }
     if (p.first_part > 0 && live && wr == 0 && row % p.Hq == 0) {
         // shared prefix: check the caller's promise once per sequence -- its table holds
         // sequence 0's blocks for the shared partitions and its context covers them.  Tables
@@ -876,12 +893,17 @@ decode_reduce_kernel(const KParams p, int num_rows) {
 #ifndef PA_DECODE_STAGES
 #define PA_DECODE_STAGES 2
 #endif
+#ifndef PA_DECODE_STAGES_D64
+#define PA_DECODE_STAGES_D64 PA_DECODE_STAGES
+#endif
 constexpr int kWarps = PA_DECODE_WARPS;        // warps per CTA
-constexpr int kStagesBf16 = PA_DECODE_STAGES;  // ring stages per warp (bf16)
+// ring stages per warp (bf16), per head_dim
+template <int D>
+constexpr int stages_bf16() { return D == 64 ? PA_DECODE_STAGES_D64 : PA_DECODE_STAGES; }
 constexpr int kStagesF32 = 2;
 
 template <int D>
-constexpr int bf16_smem() { return ring_smem_bytes<kBlockTokens * D * 2, kWarps, kStagesBf16>(); }
+constexpr int bf16_smem() { return ring_smem_bytes<kBlockTokens * D * 2, kWarps, stages_bf16<D>()>(); }
 template <int D>
 constexpr int f32_smem() {
     return ring_smem_bytes<kBlockTokens * D * 4, kWarps, kStagesF32>() +
@@ -958,7 +980,7 @@ cudaError_t launch_for_dim(const KParams& kp, const DecodeArgs& a, cudaStream_t 
     if (launched > 0) {
         const dim3 grid(launched, a.num_kv_heads, a.num_seqs);
         if (a.dtype == PA_BF16) {
-            auto k = decode_bf16_kernel<D, kWarps, kStagesBf16>;
+            auto k = decode_bf16_kernel<D, kWarps, stages_bf16<D>()>;
             if ((e = set_smem(k, bf16_smem<D>())) != cudaSuccess) return e;
             e = launch_dependent(k, grid, dim3(kWarps * 32), bf16_smem<D>(), stream, kp);
         } else {
@@ -969,7 +991,7 @@ cudaError_t launch_for_dim(const KParams& kp, const DecodeArgs& a, cudaStream_t 
         if (e != cudaSuccess) return e;
     }
     if (kp.first_part > 0) {
-        e = launch_prefix_tc(a, stream);
+        e = launch_prefix_tc(a, launched > 0, stream);
         if (e != cudaSuccess) return e;
     }
     if (a.grid_parts > 1 || kp.first_part > 0) {

@@ -42,6 +42,16 @@ inline int decode_part_stride(int max_blocks) {
     return (max_blocks + kPartBlocks - 1) / kPartBlocks;
 }
 
+// Blocks per split-KV partition of pa_decode_attention for a head_dim (a multiple of
+// kPartBlocks, so decode_part_stride bounds the partitions of every path).
+#ifndef PA_D64_PARTITION_BLOCKS
+#define PA_D64_PARTITION_BLOCKS 64
+#endif
+static_assert(PA_D64_PARTITION_BLOCKS % 32 == 0, "partitions are whole 512-token units");
+inline int decode_part_blocks(int head_dim) {
+    return head_dim == 64 ? PA_D64_PARTITION_BLOCKS : kPartBlocks;
+}
+
 // Blocks per split-KV partition of the FP8 path: its tiles are half the bytes of
 // bf16 ones, so a partition covers twice the tokens for the same bytes per CTA.
 #ifndef PA_FP8_PARTITION_BLOCKS
@@ -103,7 +113,8 @@ struct PrefillArgs {
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 // The prefix partitions [0, first_part) of a decode with a shared prefix, on tcgen05:
 // writes their (o, max, sum) partials into the decode workspace for the merge.
-cudaError_t launch_prefix_tc(const DecodeArgs& a, cudaStream_t stream);
+// after_suffix: the suffix decode kernel was launched just before (see PParams).
+cudaError_t launch_prefix_tc(const DecodeArgs& a, bool after_suffix, cudaStream_t stream);
 cudaError_t launch_decode_fp8(const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace pa

@@ -47,6 +47,10 @@ struct PParams {
     float* part_o;
     float2* part_ml;
     int part_stride, part_blocks, num_seqs, rows_per_cta;
+    // prefix mode normally runs beside the suffix kernel launched just before it, which
+    // starts it only after the kernels before have finished; without a suffix kernel it
+    // follows those kernels directly and must wait for them first
+    int wait_first;
 };
 
 __device__ __forceinline__ void raise_flag(int32_t* err, int bits) {
@@ -194,6 +198,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kvh = blockIdx.y;
+    if (PREFIX && p.wait_first) grid_dependency_wait();
     int q0 = 0, n = 0, i0 = 0, start = 0, p_last, nblk, row_base = 0, rows_total = 0;
     const int32_t* trow;
     bool has_b;
@@ -210,12 +215,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         q0 = __ldg(p.cu_q + s);
         n = __ldg(p.cu_q + s + 1) - q0;
         i0 = qt * p.TQ;
-        if (i0 >= n) return;
+        // (a CTA that exits early still waits for the previous grid: a dependent grid never
+        // completes before the one it follows)
+        if (i0 >= n) {
+            grid_dependency_wait();
+            return;
+        }
         start = __ldg(p.start_pos + s);
         const int i_end = min(n, i0 + p.TQ);
         p_last = start + i_end - 1;                       // last position this CTA attends to
         if (start < 0 || p_last >= p.max_blocks * kBlockTokens) {
             if (threadIdx.x == 0 && kvh == 0) raise_flag(p.err, PA_DEV_ERR_BAD_POS);
+            grid_dependency_wait();
             return;
         }
         nblk = p_last / kBlockTokens + 1;
@@ -299,7 +310,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
     if (*reinterpret_cast<volatile uint32_t*>(smem + L::SLOT + 4) != 0u) {
         // an earlier copy wait gave up: write nothing (the whole CTA returns together)
         if (warp == kMmaWarp) tmem_dealloc<kTmemCols>(tmem);
-        if (PREFIX) grid_dependency_wait();
+        grid_dependency_wait();
         return;
     }
     // Registers move from the copy / MMA warpgroup (warps 8-11) to the two softmax
@@ -785,7 +796,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     return launch_tc<128, false>(pp, grid, stream);
 }
 
-cudaError_t launch_prefix_tc(const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_prefix_tc(const DecodeArgs& a, bool after_suffix, cudaStream_t stream) {
     PParams pp = common_params(a.q, a.k_pool, a.v_pool, a.block_tables, a.err, a.num_q_heads,
                                a.num_kv_heads, a.max_blocks, a.num_blocks, a.scale);
     const size_t prow = (size_t)a.num_seqs * a.num_q_heads * a.part_stride;
@@ -794,6 +805,7 @@ cudaError_t launch_prefix_tc(const DecodeArgs& a, cudaStream_t stream) {
     pp.part_stride = a.part_stride;
     pp.part_blocks = a.part_blocks;
     pp.num_seqs = a.num_seqs;
+    pp.wait_first = after_suffix ? 0 : 1;
     // 256 rows (two Q tiles) per CTA when that still gives every SM a CTA, else 128
     const int rows = a.num_seqs * pp.G;
     const long long ctas256 = (long long)((rows + tc::kRowsTC - 1) / tc::kRowsTC) * a.num_kv_heads * a.first_part;

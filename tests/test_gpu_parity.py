@@ -278,13 +278,15 @@ def test_device_errors_are_flagged_and_skipped_without_faulting():
     torch.cuda.synchronize()
     assert int(err.item()) == pk.DEV_ERR_BAD_BLOCK | pk.DEV_ERR_BAD_POS
     assert torch.isfinite(out.float()).all()
-    # a context longer than the host hint is flagged
+    # a context that needs more split-KV partitions than the host hint allows is flagged
+    # (hint 300: one partition of 1024 tokens at head_dim 64; the context needs two)
     err.zero_()
-    tables = torch.tensor([[0, 1, 2, 3, 4, 5, 6, 7] * 9], dtype=torch.int32, device="cuda")
+    tables = torch.tensor([[0, 1, 2, 3, 4, 5, 6, 7] * 12], dtype=torch.int32, device="cuda")
     q1 = torch.zeros(1, 4, D, dtype=torch.bfloat16, device="cuda")
     out1 = torch.empty_like(q1)
-    ws = pk.decode_workspace(1, 4, Hkv, D, 72)
-    pk.decode_attention(out1, q1, kp, vp, tables, torch.tensor([1000], dtype=torch.int32, device="cuda"),
+    ws = pk.decode_workspace(1, 4, Hkv, D, 96)
+    assert pk.partition_tokens(D) == 1024
+    pk.decode_attention(out1, q1, kp, vp, tables, torch.tensor([1500], dtype=torch.int32, device="cuda"),
                         0.125, workspace=ws, max_context_len_hint=300, err_flag=err)
     torch.cuda.synchronize()
     assert int(err.item()) & pk.DEV_ERR_HINT
