@@ -637,12 +637,12 @@ int oracle_decode_fp4_one(double* out_row, const void* q, const void* k_pool, co
         int64_t blk;
         rc = lookup_block(tables, max_blocks, s, t, num_blocks, &blk);
         if (rc != OR_OK) goto done;
-        int slot = t % ORACLE_BLOCK;
+        int t16 = t % ORACLE_BLOCK;
         const uint8_t* krec = (const uint8_t*)k_pool + ((size_t)blk * Hkv + g) * rec;
         const uint8_t* vrec = (const uint8_t*)v_pool + ((size_t)blk * Hkv + g) * rec;
         for (int d = 0; d < D; ++d) {
-            Kc[(size_t)t * D + d] = fp4_value(krec, slot, d, D, 0);
-            Vc[(size_t)t * D + d] = fp4_value(vrec, slot, d, D, 1);
+            Kc[(size_t)t * D + d] = fp4_value(krec, t16, d, D, 0);
+            Vc[(size_t)t * D + d] = fp4_value(vrec, t16, d, D, 1);
         }
     }
     for (int d = 0; d < D; ++d) qv[d] = load_elem(q, ((size_t)s * Hq + h) * (size_t)D + d, 1);

@@ -5,12 +5,14 @@ term, a flipped sign, a wrong block / slot / head index, a missing
 normalisation, a wrong rounding -- builds the copy, and runs the pins of
 test_oracle_pins.py against it.  At least one pin must fail for every mutant;
 otherwise the pins would not be able to tell that mistake from the right answer.
-The mistakes are planted on the CPU only, in a temporary copy.
+The mistakes are planted on the CPU only, in a temporary copy.  The pins are those of
+test_oracle_pins.py, test_oracle_fp8_pins.py and test_oracle_fp4_pins.py.
 """
 import os
 
 import pytest
 
+import test_oracle_fp4_pins as fp4
 import test_oracle_fp8_pins as fp8
 import test_oracle_pins as pins
 
@@ -32,8 +34,8 @@ MUTANTS = {
                     "int32_t b = tables[(size_t)s * (size_t)max_blocks];"),
     "gqa_modulo_map": ("int X = 16 / elem_bytes_of(dtype);\n    int g = h / (Hq / Hkv);",
                        "int X = 16 / elem_bytes_of(dtype);\n    int g = h % Hkv;"),
-    "fp8_gqa_modulo_map": ("return OR_BAD_ARG;\n    int g = h / (Hq / Hkv);",
-                           "return OR_BAD_ARG;\n    int g = h % Hkv;"),
+    "fp8_gqa_modulo_map": ("D % 16 != 0 || Hq <= 0 || Hq % Hkv != 0) return OR_BAD_ARG;\n    int g = h / (Hq / Hkv);",
+                           "D % 16 != 0 || Hq <= 0 || Hq % Hkv != 0) return OR_BAD_ARG;\n    int g = h % Hkv;"),
     "query_of_wrong_head": ("qv[d] = load_elem(q, ((size_t)s * Hq + h) * (size_t)D + d, dtype);",
                             "qv[d] = load_elem(q, ((size_t)s * Hq + g) * (size_t)D + d, dtype);"),
     "round_down": ("double r = rint(m / ulp) * ulp;\n    if (r >= ldexp(1.0, 128))",
@@ -53,6 +55,23 @@ MUTANTS = {
     "fp8_v_layout_untransposed": ("for (int d = 0; d < D; ++d) vrec[(size_t)d * 16 + t] = codes[d];",
                                   "for (int d = 0; d < D; ++d) vrec[((size_t)(d / 16) * 16 + t) * 16 + d % 16] = codes[d];"),
     "fp8_scale_from_first_value": ("        if (f > amax) amax = f;\n", "        if (d == 0) amax = f;\n"),
+    "e2m1_round_down": ("double r = rint(m / ulp) * ulp;                /* half-way cases to the even multiple */",
+                        "double r = floor(m / ulp) * ulp;               /* half-way cases to the even multiple */"),
+    "e2m1_no_saturation": ("    if (r > 6.0) r = 6.0;\n", ""),
+    "e2m1_exponent_bias": ("int E = re;                                /* bias 1", "int E = re - 1;                            /* bias 1"),
+    "mx_scale_emax_3": ("int code = 127 + (e - 1) - 2;", "int code = 127 + (e - 1) - 3;"),
+    "mx_scale_from_first_block": ("for (int d = 32 * b; d < 32 * b + 32; ++d) {\n            double v = fabs",
+                                  "for (int d = 0; d < 32; ++d) {\n            double v = fabs"),
+    "fp4_k_nibbles_swapped": ("put_nibble(krec, fp4_k_byte(t, d, D), d & 1, codes[d]);",
+                              "put_nibble(krec, fp4_k_byte(t, d, D), !(d & 1), codes[d]);"),
+    "fp4_v_untransposed": ("put_nibble(vrec, fp4_v_byte(t, d, D), t & 1, codes[d]);",
+                           "put_nibble(vrec, fp4_k_byte(t, d, D), d & 1, codes[d]);"),
+    "fp4_scale_not_applied": ("return ldexp(oracle_e2m1_to_double(code), (int)sc - 127);",
+                              "return oracle_e2m1_to_double(code);"),
+    "fp4_context_short_by_one": ("    for (int t = 0; t < L; ++t) {\n        int64_t blk;\n        rc = lookup_block(tables, max_blocks, s, t, num_blocks, &blk);\n        if (rc != OR_OK) goto done;\n        int t16",
+                                 "    for (int t = 0; t < L - 1; ++t) {\n        int64_t blk;\n        rc = lookup_block(tables, max_blocks, s, t, num_blocks, &blk);\n        if (rc != OR_OK) goto done;\n        int t16"),
+    "fp4_gqa_modulo_map": ("D % 32 != 0 || Hq <= 0 || Hq % Hkv != 0) return OR_BAD_ARG;\n    int g = h / (Hq / Hkv);",
+                           "D % 32 != 0 || Hq <= 0 || Hq % Hkv != 0) return OR_BAD_ARG;\n    int g = h % Hkv;"),
     "copy_keys_only": ("        memmove((char*)v_pool + (size_t)dst * block_bytes, (char*)v_pool + (size_t)src * block_bytes, block_bytes);\n", ""),
 }
 
@@ -81,6 +100,14 @@ def _pins():
     yield "e4m3_bijection", lambda o: fp8.test_e4m3_codes_and_values_are_a_bijection(o)
     yield "fp8_append", lambda o: fp8.test_quantised_append_scales_and_codes(o)
     yield "fp8_decode", lambda o: fp8.test_fp8_decode_closed_forms_and_library_routine(o)
+    yield "e2m1_table", lambda o: fp4.test_e2m1_value_table(o)
+    yield "e2m1_cases", lambda o: fp4.test_e2m1_hand_worked_cases(o)
+    yield "e2m1_brute", lambda o: fp4.test_e2m1_matches_brute_force_nearest(o)
+    yield "e2m1_bijection", lambda o: fp4.test_e2m1_codes_and_values_are_a_bijection(o)
+    yield "mx_scale", lambda o: fp4.test_mx_scale_hand_worked_and_library(o)
+    yield "fp4_append", lambda o: fp4.test_quantised_append_scales_values_and_error_bound(o)
+    yield "fp4_layout", lambda o: fp4.test_record_layout_positions(o)
+    yield "fp4_decode", lambda o: fp4.test_fp4_decode_closed_forms_and_library_routine(o)
 
 
 def test_every_pin_passes_on_the_unmutated_source(oracle_mod, tmp_path):
