@@ -99,6 +99,8 @@ def kv_bytes_per_token(wl, kv_dtype="bf16") -> int:
     per (slot, kv head) for the FP8 cache."""
     if kv_dtype == "fp8":
         return 2 * wl.num_kv_heads * (wl.head_dim + 4)
+    if kv_dtype == "fp4":            # E2M1 codes + one E8M0 byte per 32 values, K and V
+        return 2 * wl.num_kv_heads * (wl.head_dim // 2 + wl.head_dim // 32)
     e = 2 if wl.dtype == "bf16" else 4
     return 2 * wl.num_kv_heads * wl.head_dim * e
 
@@ -112,7 +114,7 @@ def decode_bytes(wl, kv_dtype="bf16") -> int:
     kv = int((L * kv_bytes_per_token(wl, kv_dtype)).sum())
     qo = 2 * wl.num_seqs * wl.num_q_heads * wl.head_dim * e
     table = int((4 * ((L + 15) // 16)).sum()) + 4 * wl.num_seqs
-    pt = 1024 if (wl.head_dim == 64 and kv_dtype == "bf16") else (1024 if kv_dtype == "fp8" else 512)
+    pt = {"fp8": 1024, "fp4": 2048}.get(kv_dtype, 1024 if wl.head_dim == 64 else 512)
     parts = (L + pt - 1) // pt                   # split-KV partitions of each context
     multi = parts[parts > 1]
     partial = int((multi * wl.num_q_heads * (wl.head_dim + 2) * 4 * 2).sum())
@@ -327,18 +329,18 @@ def run_ours(args, rank, world, local):
     wl = W.WORKLOADS[args.workload](device="cuda", **kw)
     tdt = wl.torch_dtype()
     S, Hq, Hkv, D = wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
-    fp8 = args.kv_dtype == "fp8"
-    if fp8 and wl.dtype != "bf16":
-        raise SystemExit("the FP8 cache takes bf16 rows")
-    if fp8:
-        shape = pk.fp8_pool_shape(wl.num_blocks, Hkv, D)
+    quant = args.kv_dtype if args.kv_dtype in ("fp8", "fp4") else None
+    if quant and wl.dtype != "bf16":
+        raise SystemExit("the quantised caches take bf16 rows")
+    if quant:
+        shape = (pk.fp8_pool_shape if quant == "fp8" else pk.fp4_pool_shape)(wl.num_blocks, Hkv, D)
         kp = torch.zeros(shape, dtype=torch.uint8, device="cuda")
         vp = torch.zeros(shape, dtype=torch.uint8, device="cuda")
     else:
         shape = pk.pool_shape(wl.num_blocks, Hkv, D, tdt)
         kp = torch.zeros(shape, dtype=tdt, device="cuda")
         vp = torch.zeros(shape, dtype=tdt, device="cuda")
-    append = pk.append_kv_fp8 if fp8 else pk.append_kv
+    append = {"fp8": pk.append_kv_fp8, "fp4": pk.append_kv_fp4}.get(quant, pk.append_kv)
     tables = torch.from_numpy(wl.block_tables).cuda()
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     # fill the context (untimed set-up), one append call
@@ -373,9 +375,10 @@ def run_ours(args, rank, world, local):
 
     def decode(q_, tab_, lens_, pool, out=out):
         kp, vp = pools[pool]
-        if fp8:
-            pk.decode_attention_fp8(out, q_, kp, vp, tab_, lens_, wl.scale, workspace=ws,
-                                    max_context_len_hint=hint, err_flag=err, stream=stream)
+        if quant:
+            dec = pk.decode_attention_fp8 if quant == "fp8" else pk.decode_attention_fp4
+            dec(out, q_, kp, vp, tab_, lens_, wl.scale, workspace=ws, max_context_len_hint=hint,
+                err_flag=err, stream=stream)
         elif shared:
             pk.decode_attention_shared_prefix(out, q_, kp, vp, tab_, lens_, wl.scale, shared,
                                               workspace=ws, max_context_len_hint=hint,
@@ -468,17 +471,20 @@ def run_ours(args, rank, world, local):
     else:
         peak, peak_src = 6800.0, "fallback"
     achieved = dbytes / (dec_ms / 1e3) / 1e9
-    launches_per_step = (1 + 1 + (1 if int(math.ceil(hint / 512)) > 1 or shared >= 512 else 0) +
+    pt = {"fp8": 1024, "fp4": 2048}.get(args.kv_dtype, 1024 if D == 64 and not shared else 512)
+    launches_per_step = (1 + 1 + (1 if int(math.ceil(hint / pt)) > 1 or shared >= 512 else 0) +
                          (1 if shared >= 512 else 0)) * rot
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp8_e4m3 K/V, bf16 q/out, fp32 softmax" if fp8 else wl.dtype,
+        "dtype": {"fp8": "fp8_e4m3 K/V, bf16 q/out, fp32 softmax",
+                  "fp4": "mxfp4 (e2m1, e8m0 per 32) K/V, bf16 q/out, fp32 softmax"}.get(quant, wl.dtype),
         "data": "synthetic",
         "config": {"workload": args.workload, "num_seqs_per_gpu": S, "num_q_heads": Hq,
-                   "kv_cache": "fp8_e4m3 (per-slot fp32 scales)" if fp8 else wl.dtype,
+                   "kv_cache": {"fp8": "fp8_e4m3 (per-slot fp32 scales)",
+                                "fp4": "mxfp4 (e2m1 codes, one e8m0 scale per 32 values)"}.get(quant, wl.dtype),
                    "num_kv_heads": Hkv, "head_dim": D, "block_size": 16,
                    "context_tokens_after_append": int((wl.context_lens + 1).sum()),
                    "max_context": int(hint),
@@ -504,11 +510,11 @@ def run_ours(args, rank, world, local):
             "logical_gbs": round(value * (step_bytes - unique_kv_bytes(wl, wl_shared) +
                                           logical_kv_bytes(wl)) / step_bytes, 1)} if wl_shared else {}),
         "tokens_per_s": round(tokens_per_s, 1),
-        "roofline": {"kernel": ("pa_decode_attention_fp8" if fp8 else "pa_decode_attention") +
-                               " (main kernel + partition merge)",
+        "roofline": {"kernel": {"fp8": "pa_decode_attention_fp8", "fp4": "pa_decode_attention_fp4"}.get(
+                                 quant, "pa_decode_attention") + " (main kernel + partition merge)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None if wl_shared else profiled_traffic(args.workload, fp8),
+                     "frac": round(achieved / peak, 4), "traffic": None if wl_shared or quant == "fp4" else profiled_traffic(args.workload, quant == "fp8"),
                      "algorithmic_bytes_per_launch": dbytes, "avg_launch_ms": round(dec_ms, 5)},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms / K, 5),
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
@@ -865,6 +871,8 @@ EXTRA_CONFIGS = [
                                           "shared_prefix": 4096}),
     ("llama3-8b_batch256+fp8", {"workload": "llama3-8b_batch256", "kv_dtype": "fp8"}),
     ("llama3-8b_long_context+fp8", {"workload": "llama3-8b_long_context", "kv_dtype": "fp8"}),
+    ("llama3-8b_batch256+fp4", {"workload": "llama3-8b_batch256", "kv_dtype": "fp4"}),
+    ("llama3-8b_long_context+fp4", {"workload": "llama3-8b_long_context", "kv_dtype": "fp4"}),
     ("spindle_replay", {"workload": "spindle_replay"}),
     ("llama3-8b_prefill", {"workload": "llama3-8b_prefill"}),
 ]
@@ -911,8 +919,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graphs", action="store_true",
                     help="replay: launch every kernel directly instead of one CUDA graph per step")
-    ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
-                    help="K/V cache element type; fp8 = E4M3 codes with per-slot scales")
+    ap.add_argument("--kv-dtype", choices=["bf16", "fp8", "fp4"], default="bf16",
+                    help="K/V cache element type; fp8 = E4M3 codes with per-slot scales, "
+                         "fp4 = MXFP4 (E2M1 codes, one E8M0 scale per 32 values)")
     ap.add_argument("--shared-prefix", type=int, default=0,
                     help="decode through pa_decode_attention_shared_prefix with this many shared "
                          "tokens (the llama3-8b_shared_prefix workload shares 4096)")

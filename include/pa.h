@@ -67,7 +67,8 @@ typedef enum {
 typedef enum {
     PA_F32 = 0,
     PA_BF16 = 1,
-    PA_FP8_E4M3 = 2   /* pools only: E4M3 codes with per-slot fp32 scales (see pa_append_kv_fp8) */
+    PA_FP8_E4M3 = 2,  /* pools only: E4M3 codes with per-slot fp32 scales (see pa_append_kv_fp8) */
+    PA_FP4_E2M1 = 3   /* pools only: MXFP4 records (see pa_append_kv_fp4) */
 } pa_dtype;
 
 /* Bits OR-ed into *dev_err_flag by the kernels. */
@@ -226,6 +227,55 @@ pa_status pa_append_kv_fp8(void* k_pool, void* v_pool, const void* k_new, const 
  * bf16, scores and the softmax in fp32, the products on the tensor cores in f16
  * (every E4M3 code is exact in f16).  Same workspace, partitions, errors. */
 pa_status pa_decode_attention_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                  const int32_t* block_tables, const int32_t* context_lens,
+                                  int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t max_blocks_per_seq,
+                                  int32_t max_context_len_hint, int32_t num_blocks, float scale,
+                                  void* workspace, size_t workspace_bytes, int32_t* dev_err_flag,
+                                  void* stream);
+
+/*
+ * Block-scaled FP4 (MXFP4) KV cache -- a quarter of the bf16 bytes per token
+ * (Slipstream, "Companion work": qgemm-mx, a block-scaled FP4 kernel for the same
+ * bandwidth-bound decode path).  The format is the microscaling one: E2M1 codes
+ * (1 sign, 2 exponent bits with bias 1, 1 mantissa bit: magnitudes 0, 0.5, 1,
+ * 1.5, 2, 3, 4, 6), and one E8M0 scale byte (value 2^(code - 127)) per 32 values
+ * along head_dim of each (token, kv head); value = code * scale.
+ *
+ * Pools: uint8 [num_blocks][num_kv_heads][PA_FP4_RECORD_BYTES(head_dim)].  A record
+ * holds the 16 slots of one (block, kv head): 8 * head_dim code bytes, then
+ * 16 * head_dim / 32 scale bytes ([16 slots][head_dim / 32]).  Code bytes (D =
+ * head_dim; the low nibble holds the first of the two codes):
+ *   K: slot t's row of D / 2 bytes at t * D / 2; the byte at c * (D / 8) +
+ *      2 ks + half (c < 4, ks < D / 16, half < 2) holds dims 16 ks + 8 half + 2 c
+ *      and + 1.
+ *   V: the byte at ((4 r + c) * (D / 16) + mi) * 4 + 2 dh + half (r < 8, c < 4,
+ *      mi < D / 16, dh < 2, half < 2) holds dim 16 mi + 8 dh + r of slots
+ *      2 c + 8 half and + 1.
+ * (These byte orders put each tensor-core fragment of a decode thread in adjacent
+ * bytes.)  pa_copy_block takes dtype PA_FP4_E2M1 for these pools.
+ */
+#define PA_FP4_RECORD_BYTES(head_dim) (8 * (head_dim) + (head_dim) / 2)
+
+/* pa_append_kv_fp4 -- like pa_append_kv, with bf16 rows k_new / v_new quantised on
+ * the way in: each block of 32 values of a (row, kv head) gets the scale code
+ * 127 + floor(log2 amax) - 2 (at least 0; an all-zero block gets 0) and codes
+ * E2M1(x / scale) (exact power-of-two scaling, round to nearest even, saturating
+ * at 6).  Rows of one call may share slots' V bytes; the kernel updates them
+ * atomically.  head_dim 64 or 128. */
+pa_status pa_append_kv_fp4(void* k_pool, void* v_pool, const void* k_new, const void* v_new,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* start_pos, const int32_t* cu_new_tokens,
+                           int32_t num_seqs, int32_t total_new_tokens, int32_t num_blocks,
+                           int32_t num_kv_heads, int32_t head_dim, int32_t* dev_err_flag,
+                           void* stream);
+
+/* pa_decode_attention_fp4 -- pa_decode_attention over MXFP4 pools; q and out are
+ * bf16, scores and the softmax in fp32, the products on the tensor cores in f16
+ * (every E2M1 code is exact in f16; the scales are applied in fp32, and to the
+ * probabilities as powers of two).  Same workspace and errors; 2048-token
+ * partitions. */
+pa_status pa_decode_attention_fp4(void* out, const void* q, const void* k_pool, const void* v_pool,
                                   const int32_t* block_tables, const int32_t* context_lens,
                                   int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                   int32_t head_dim, int32_t max_blocks_per_seq,

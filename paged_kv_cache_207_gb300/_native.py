@@ -36,6 +36,7 @@ EXPORTED = [
     "pa_status_string", "pa_abi_version", "pa_append_kv", "pa_copy_block",
     "pa_decode_workspace_size", "pa_decode_attention", "pa_decode_attention_shared_prefix",
     "pa_decode_attention_noalloc", "pa_append_kv_fp8", "pa_decode_attention_fp8",
+    "pa_append_kv_fp4", "pa_decode_attention_fp4",
     "pa_prefill_attention", "pa_bm_create", "pa_bm_destroy",
     "pa_bm_add_seq", "pa_bm_fork", "pa_bm_free_seq", "pa_bm_blocks_needed",
     "pa_bm_prepare_append", "pa_bm_block_table", "pa_bm_seq_len", "pa_bm_refcount", "pa_bm_stats",
@@ -87,6 +88,11 @@ def lib() -> ctypes.CDLL:
     L.pa_decode_attention_fp8.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32,
                                           ctypes.c_float, p, sz, p, p]
     L.pa_decode_attention_fp8.restype = ctypes.c_int
+    L.pa_append_kv_fp4.argtypes = [p, p, p, p, p, i32, p, p, i32, i32, i32, i32, i32, p, p]
+    L.pa_append_kv_fp4.restype = ctypes.c_int
+    L.pa_decode_attention_fp4.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32,
+                                          ctypes.c_float, p, sz, p, p]
+    L.pa_decode_attention_fp4.restype = ctypes.c_int
     L.pa_prefill_attention.argtypes = [p, p, p, p, p, i32, p, p, i32, i32, i32, i32, i32, i32, i32,
                                        ctypes.c_float, ctypes.c_int, p, p]
     L.pa_prefill_attention.restype = ctypes.c_int
@@ -200,6 +206,53 @@ def copy_block_fp8(k_pool, v_pool, pairs, err_flag=None, stream=None) -> None:
     nb, hkv, d = _fp8_dims(k_pool)
     check("pa_copy_block", lib().pa_copy_block(
         _ptr(k_pool), _ptr(v_pool), _i32(pairs, "pairs"), pairs.shape[0], nb, hkv, d, 2,
+        None if err_flag is None else _i32(err_flag, "err_flag"), _stream(stream)))
+
+
+def fp4_pool_shape(num_blocks: int, num_kv_heads: int, head_dim: int):
+    """Shape of one MXFP4 pool: per (block, kv head) 8*D code bytes + D/2 scale bytes."""
+    return (num_blocks, num_kv_heads, 8 * head_dim + head_dim // 2)
+
+
+def _fp4_dims(k_pool: torch.Tensor):
+    if k_pool.dim() != 3 or k_pool.dtype != torch.uint8 or k_pool.shape[2] % 17:
+        raise ValueError("FP4 pools must be uint8 [num_blocks][Hkv][8*D + D/2]")
+    return k_pool.shape[0], k_pool.shape[1], k_pool.shape[2] * 2 // 17
+
+
+def append_kv_fp4(k_pool, v_pool, k_new, v_new, block_tables, start_pos, cu_new_tokens,
+                  err_flag=None, stream=None) -> None:
+    """Quantise bf16 rows ([tokens][Hkv][D]) into MXFP4 pools at explicit positions."""
+    nb, hkv, d = _fp4_dims(k_pool)
+    if k_new.dtype != torch.bfloat16 or v_new.dtype != torch.bfloat16:
+        raise TypeError("new rows must be bf16")
+    check("pa_append_kv_fp4", lib().pa_append_kv_fp4(
+        _ptr(k_pool), _ptr(v_pool), _ptr(k_new), _ptr(v_new), _i32(block_tables, "block_tables"),
+        block_tables.shape[1], _i32(start_pos, "start_pos"), _i32(cu_new_tokens, "cu_new_tokens"),
+        start_pos.shape[0], k_new.shape[0], nb, hkv, d,
+        None if err_flag is None else _i32(err_flag, "err_flag"), _stream(stream)))
+
+
+def decode_attention_fp4(out, q, k_pool, v_pool, block_tables, context_lens, scale, workspace=None,
+                         max_context_len_hint: int = 0, err_flag=None, stream=None) -> None:
+    """decode_attention over MXFP4 pools (bf16 q and out)."""
+    nb, hkv, d = _fp4_dims(k_pool)
+    if q.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
+        raise TypeError("q and out must be bf16")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    check("pa_decode_attention_fp4", lib().pa_decode_attention_fp4(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _i32(block_tables, "block_tables"),
+        _i32(context_lens, "context_lens"), q.shape[0], q.shape[1], hkv, d, block_tables.shape[1],
+        int(max_context_len_hint), nb, float(scale),
+        None if workspace is None else _ptr(workspace), ws_bytes,
+        None if err_flag is None else _i32(err_flag, "err_flag"), _stream(stream)))
+
+
+def copy_block_fp4(k_pool, v_pool, pairs, err_flag=None, stream=None) -> None:
+    """copy_block for MXFP4 pools."""
+    nb, hkv, d = _fp4_dims(k_pool)
+    check("pa_copy_block", lib().pa_copy_block(
+        _ptr(k_pool), _ptr(v_pool), _i32(pairs, "pairs"), pairs.shape[0], nb, hkv, d, 3,
         None if err_flag is None else _i32(err_flag, "err_flag"), _stream(stream)))
 
 

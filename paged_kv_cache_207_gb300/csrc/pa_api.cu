@@ -74,10 +74,11 @@ pa_status pa_append_kv(void* k_pool, void* v_pool, const void* k_new, const void
 pa_status pa_copy_block(void* k_pool, void* v_pool, const int32_t* src_dst_pairs,
                         int32_t num_pairs, int32_t num_blocks, int32_t num_kv_heads,
                         int32_t head_dim, pa_dtype dtype, int32_t* dev_err_flag, void* stream) {
-    if (!dtype_ok(dtype) && dtype != PA_FP8_E4M3) return PA_ERR_INVALID_ARG;
+    if (!dtype_ok(dtype) && dtype != PA_FP8_E4M3 && dtype != PA_FP4_E2M1) return PA_ERR_INVALID_ARG;
     if (num_pairs < 0 || num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0)
         return PA_ERR_INVALID_ARG;
-    if ((head_dim * pa::elem_bytes(dtype)) % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (dtype == PA_FP4_E2M1 ? (head_dim % 32 != 0) : ((head_dim * pa::elem_bytes(dtype)) % 16 != 0))
+        return PA_ERR_UNSUPPORTED;
     if (num_pairs == 0) return PA_OK;
     if (!k_pool || !v_pool || !src_dst_pairs) return PA_ERR_INVALID_ARG;
     if (!aligned16(k_pool) || !aligned16(v_pool)) return PA_ERR_INVALID_ARG;
@@ -300,6 +301,93 @@ pa_status pa_decode_attention_fp8(void* out, const void* q, const void* k_pool, 
     a.scale = scale;
     a.dtype = PA_FP8_E4M3;
     return cuda_status(pa::launch_decode_fp8(a, static_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_append_kv_fp4(void* k_pool, void* v_pool, const void* k_new, const void* v_new,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* start_pos, const int32_t* cu_new_tokens,
+                           int32_t num_seqs, int32_t total_new_tokens, int32_t num_blocks,
+                           int32_t num_kv_heads, int32_t head_dim, int32_t* dev_err_flag,
+                           void* stream) {
+    if (num_seqs < 0 || total_new_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0 ||
+        max_blocks_per_seq <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0 && total_new_tokens != 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!k_pool || !v_pool || !block_tables || !start_pos || !cu_new_tokens) return PA_ERR_INVALID_ARG;
+    if (total_new_tokens > 0 && (!k_new || !v_new)) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_pool) || !aligned16(v_pool) || (k_new && !aligned16(k_new)) ||
+        (v_new && !aligned16(v_new)))
+        return PA_ERR_INVALID_ARG;
+    if ((long long)max_blocks_per_seq * pa::kBlockTokens > INT32_MAX) return PA_ERR_INVALID_ARG;
+    pa::AppendArgs a;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.block_tables = block_tables;
+    a.start_pos = start_pos;
+    a.cu_new = cu_new_tokens;
+    a.err = dev_err_flag;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_seqs = num_seqs;
+    a.total_new = total_new_tokens;
+    a.num_blocks = num_blocks;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.dtype = PA_FP4_E2M1;
+    return cuda_status(pa::launch_append_fp4(a, static_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_decode_attention_fp4(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                  const int32_t* block_tables, const int32_t* context_lens,
+                                  int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t max_blocks_per_seq,
+                                  int32_t max_context_len_hint, int32_t num_blocks, float scale,
+                                  void* workspace, size_t workspace_bytes, int32_t* dev_err_flag,
+                                  void* stream) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
+        max_blocks_per_seq <= 0 || !std::isfinite(scale))
+        return PA_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (num_q_heads / num_kv_heads > 8) return PA_ERR_UNSUPPORTED;
+    if ((long long)max_blocks_per_seq * pa::kBlockTokens > INT32_MAX) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+    if (!out || !q || !k_pool || !v_pool || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
+        return PA_ERR_INVALID_ARG;
+    const size_t need =
+        pa::decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+        return PA_ERR_INVALID_ARG;
+    const int cap = max_blocks_per_seq * pa::kBlockTokens;
+    const int bound = (max_context_len_hint > 0 && max_context_len_hint < cap) ? max_context_len_hint : cap;
+    pa::DecodeArgs a;
+    a.out = out;
+    a.q = q;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.err = dev_err_flag;
+    a.workspace = need > 0 ? workspace : nullptr;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    const int part_tokens = pa::kFp4PartBlocks * pa::kBlockTokens;
+    a.grid_parts = (bound + part_tokens - 1) / part_tokens;
+    a.part_stride = pa::decode_part_stride(max_blocks_per_seq);   // >= the FP4 partitions used
+    a.part_blocks = pa::kFp4PartBlocks;
+    a.first_part = 0;
+    a.scale = scale;
+    a.dtype = PA_FP4_E2M1;
+    return cuda_status(pa::launch_decode_fp4(a, static_cast<cudaStream_t>(stream)));
 }
 
 pa_status pa_prefill_attention(void* out, const void* q, const void* k_pool, const void* v_pool,

@@ -181,6 +181,103 @@ __global__ void __launch_bounds__(256) append_fp8_kernel(const AParams p) {
     }
 }
 
+// MXFP4 append: one warp per (row, kv head), D / 32 values per lane.  Each block of
+// 32 values (8 or 16 lanes) gets the E8M0 scale 2^(floor(log2 amax) - 2) -- the
+// biased exponent of amax minus 2, at least 0; an all-zero block gets code 0 --
+// and E2M1 codes of x / scale (exact power-of-two scaling in fp32, then round to
+// nearest even, saturating at 6).  K: the slot's row holds the codes in pairs of
+// dims, the byte of dims (16 ks + 8 half + 2c, +1) at c (D / 8) + 2 ks + half.
+// V: a byte holds two slots of one dim; the byte of (dim 16 mi + 8 dh + r, slots
+// 2c + 8 half, +1) is at ((4 r + c) (D / 16) + mi) 4 + 2 dh + half, low nibble the
+// even slot.  Rows appended by the same call may share these V bytes, so each
+// nibble is cleared and set with atomics on its 32-bit word.  Scales: byte
+// 8 D + slot (D / 32) + b of the record.
+template <int D>
+__global__ void __launch_bounds__(256) append_fp4_kernel(const AParams p) {
+    constexpr int VPL = D / 32;          // values per lane: 4 (D = 128) or 2 (D = 64)
+    constexpr int LPB = 32 / VPL;        // lanes per 32-value block
+    constexpr int NB = D / 32;
+    constexpr int REC = 8 * D + D / 2;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        if (__ldg(p.cu) != 0 || __ldg(p.cu + p.S) != p.total) raise_flag(p.err, PA_DEV_ERR_BAD_CU);
+    }
+    const int h = (int)(wid % p.Hkv);
+    const int row = (int)(wid / p.Hkv);
+    int s, slot;
+    int32_t blk;
+    const bool ok = wid < (long long)p.total * p.Hkv && locate_row(p, row, lane == 0, s, slot, blk);
+    asm volatile("griddepcontrol.wait;" ::: "memory");           // as in append_kernel
+    if (!ok) return;                                              // warp-uniform
+
+    const size_t src = ((size_t)row * p.Hkv + h) * D + (size_t)lane * VPL;
+    float kx[VPL], vx[VPL];
+    if constexpr (VPL == 4) {
+        const uint2 kr = __ldg(reinterpret_cast<const uint2*>(p.k_new) + src / 4);
+        const uint2 vr = __ldg(reinterpret_cast<const uint2*>(p.v_new) + src / 4);
+        kx[0] = __uint_as_float(kr.x << 16); kx[1] = __uint_as_float(kr.x & 0xffff0000u);
+        kx[2] = __uint_as_float(kr.y << 16); kx[3] = __uint_as_float(kr.y & 0xffff0000u);
+        vx[0] = __uint_as_float(vr.x << 16); vx[1] = __uint_as_float(vr.x & 0xffff0000u);
+        vx[2] = __uint_as_float(vr.y << 16); vx[3] = __uint_as_float(vr.y & 0xffff0000u);
+    } else {
+        const uint32_t kr = __ldg(reinterpret_cast<const uint32_t*>(p.k_new) + src / 2);
+        const uint32_t vr = __ldg(reinterpret_cast<const uint32_t*>(p.v_new) + src / 2);
+        kx[0] = __uint_as_float(kr << 16); kx[1] = __uint_as_float(kr & 0xffff0000u);
+        vx[0] = __uint_as_float(vr << 16); vx[1] = __uint_as_float(vr & 0xffff0000u);
+    }
+    float ka = 0.f, va = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) {
+        ka = fmaxf(ka, fabsf(kx[k]));
+        va = fmaxf(va, fabsf(vx[k]));
+    }
+#pragma unroll
+    for (int x = 1; x < LPB; x <<= 1) {            // within the lane's 32-value block
+        ka = fmaxf(ka, __shfl_xor_sync(0xffffffffu, ka, x));
+        va = fmaxf(va, __shfl_xor_sync(0xffffffffu, va, x));
+    }
+    const int kcode = ka > 0.f ? max((int)(__float_as_uint(ka) >> 23) - 2, 0) : 0;
+    const int vcode = va > 0.f ? max((int)(__float_as_uint(va) >> 23) - 2, 0) : 0;
+    const float kinv = exp2i(127 - kcode), vinv = exp2i(127 - vcode);   // 1 / scale, exact
+
+    char* krec = p.k_pool + ((size_t)blk * p.Hkv + h) * REC;
+    char* vrec = p.v_pool + ((size_t)blk * p.Hkv + h) * REC;
+    const int d0 = lane * VPL;
+    // K: pairs of dims, one byte each
+#pragma unroll
+    for (int k = 0; k < VPL; k += 2) {
+        const int d = d0 + k;
+        const uint32_t byte = ka > 0.f ? pack_e2m1x2(kx[k] * kinv, kx[k + 1] * kinv) : 0u;
+        const int ks = d / 16, half = (d % 16) / 8, c = (d % 8) / 2;
+        krec[(size_t)slot * (D / 2) + c * (D / 8) + ks * 2 + half] = (char)byte;
+    }
+    // V: one nibble per dim, in words shared with other slots
+    const int half = slot / 8, c = (slot % 8) / 2, nib = slot & 1;
+#pragma unroll
+    for (int k = 0; k < VPL; k += 2) {
+        const uint32_t pair = va > 0.f ? pack_e2m1x2(vx[k] * vinv, vx[k + 1] * vinv) : 0u;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int d = d0 + k + e;
+            const uint32_t code = (pair >> (4 * e)) & 0xfu;
+            const int mi = d / 16, dh = (d % 16) / 8, rr = d % 8;
+            const int idx = ((rr * 4 + c) * (D / 16) + mi) * 4 + dh * 2 + half;
+            unsigned int* word = reinterpret_cast<unsigned int*>(vrec + (idx & ~3));
+            const int shift = (idx & 3) * 8 + nib * 4;
+            atomicAnd(word, ~(0xfu << shift));
+            atomicOr(word, code << shift);
+        }
+    }
+    // scales: the first lane of each 32-value block
+    if (lane % LPB == 0) {
+        const int b = lane / LPB;
+        krec[8 * D + slot * NB + b] = (char)kcode;
+        vrec[8 * D + slot * NB + b] = (char)vcode;
+    }
+}
+
 struct CParams {
     char* k_pool;
     char* v_pool;
@@ -281,14 +378,37 @@ cudaError_t launch_copy(const CopyArgs& a, cudaStream_t stream) {
     p.pairs = a.pairs;
     p.err = a.err;
     p.num_blocks = a.num_blocks;
-    p.block_bytes = a.dtype == PA_FP8_E4M3
-                        ? (size_t)a.num_kv_heads * fp8_record_bytes(a.head_dim)
-                        : (size_t)a.num_kv_heads * kBlockTokens * a.head_dim * elem_bytes(a.dtype);
+    p.block_bytes = a.dtype == PA_FP8_E4M3 ? (size_t)a.num_kv_heads * fp8_record_bytes(a.head_dim)
+                  : a.dtype == PA_FP4_E2M1 ? (size_t)a.num_kv_heads * fp4_record_bytes(a.head_dim)
+                  : (size_t)a.num_kv_heads * kBlockTokens * a.head_dim * elem_bytes(a.dtype);
     const size_t n16 = p.block_bytes / 16;
     const unsigned slices = (unsigned)((n16 + 256 * 4 - 1) / (256 * 4));   // ~4 vectors per thread
     const dim3 grid(a.num_pairs, 2, slices > 0 ? (slices < 64 ? slices : 64) : 1);
     copy_kernel<<<grid, 256, 0, stream>>>(p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_append_fp4(const AppendArgs& a, cudaStream_t stream) {
+    AParams p;
+    p.k_pool = static_cast<char*>(a.k_pool);
+    p.v_pool = static_cast<char*>(a.v_pool);
+    p.k_new = static_cast<const char*>(a.k_new);
+    p.v_new = static_cast<const char*>(a.v_new);
+    p.tables = a.block_tables;
+    p.start_pos = a.start_pos;
+    p.cu = a.cu_new;
+    p.err = a.err;
+    p.max_blocks = a.max_blocks;
+    p.S = a.num_seqs;
+    p.total = a.total_new;
+    p.num_blocks = a.num_blocks;
+    p.Hkv = a.num_kv_heads;
+    p.chunks = 0;
+    p.items = (long long)a.total_new * a.num_kv_heads;   // warps
+    if (p.items == 0) return cudaSuccess;
+    const long long blocks = (p.items * 32 + 255) / 256;
+    return a.head_dim == 64 ? launch_dependent(append_fp4_kernel<64>, dim3((unsigned)blocks), stream, p)
+                            : launch_dependent(append_fp4_kernel<128>, dim3((unsigned)blocks), stream, p);
 }
 
 }  // namespace pa

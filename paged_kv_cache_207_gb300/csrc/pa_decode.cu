@@ -602,6 +602,332 @@ decode_fp8_kernel(const KParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// FP4 kernel: MXFP4 records (E2M1 codes; one E8M0 scale per token and 32 dims),
+// bf16 q and out.  The bf16 pipeline again, with the codes converted to f16 in
+// registers (exact) and the tensor cores running f16 x f16 -> fp32.
+//   K: a record row is one token; thread (r, c) reads D / 8 adjacent bytes of
+//      tokens r and r + 8, whose byte 2 ks + half holds dims 16 ks + 8 half + 2c,
+//      +1 -- the A fragment of k-step ks.  The scale varies along the dot product,
+//      so each 32-dim block gets its own 2-MMA product, multiplied by the token's
+//      scale and summed in fp32.
+//   V: a record byte holds two tokens of one dim; thread (r, c) reads D / 4
+//      adjacent bytes, byte 4 mi + 2 dh + half holding dim 16 mi + 8 dh + r of
+//      tokens 2c + 8 half, +1 -- the A fragments of P.V for m-tile mi.  The scale
+//      varies along the contraction (tokens), so it multiplies the probabilities:
+//      block b's output dims take P_b = p 2^(e_b(t) - 127) c_b, with c_b =
+//      2^(135 - R_b) and R_b the largest scale code of block b seen so far (raised,
+//      and block b's accumulators rescaled, when a tile brings a larger one), so P_b
+//      stays at most 2^8, within f16's range.  A scale code of 0 (a block below
+//      2^-123) counts as 0.
+//   Codes reach f16 through E4M3: the E2M1 code (s, e1 e0, m) is bit for bit the
+//   E4M3 code (s, 0 0 e1 e0, m 0 0) of the value times 2^-6, and E4M3 -> f16 is the
+//   exact conversion the FP8 kernel uses; the 2^-6 is undone with the scales.
+// ---------------------------------------------------------------------------
+// The NB (2 or 4) E8M0 scale bytes of one token, byte b in bits 8b .. 8b+7.
+template <int NB>
+__device__ __forceinline__ uint32_t scale_bytes(const uint8_t* sm) {
+    if constexpr (NB == 4) return *reinterpret_cast<const uint32_t*>(sm);
+    else return *reinterpret_cast<const uint16_t*>(sm);
+}
+
+// Scale byte b of w as the fp32 2^(code - 127) (its bits are code << 23; code 0 gives 0).
+template <int B>
+__device__ __forceinline__ float scale_value(uint32_t w) {
+    constexpr int sh = 23 - 8 * B;
+    return __uint_as_float((sh >= 0 ? (w << sh) : (w >> -sh)) & 0x7F800000u);
+}
+
+// E2M1 codes of a word as four f16x2 (byte i -> o[i]), times 2^kFp4CodeExp.
+#ifndef PA_FP4_UNPACK_E4M3
+#define PA_FP4_UNPACK_E4M3 0
+#endif
+constexpr int kFp4CodeExp = PA_FP4_UNPACK_E4M3 ? -6 : 0;
+__device__ __forceinline__ void fp4_unpack(uint32_t w, uint32_t (&o)[4]) {
+    if constexpr (PA_FP4_UNPACK_E4M3) e2m1x8_to_f16x2x4_scaled(w, o);
+    else e2m1x8_to_f16x2x4(w, o);
+}
+
+#ifndef PA_FP4_MIN_CTAS
+#define PA_FP4_MIN_CTAS 1
+#endif
+template <int D, int NW, int NST>
+__global__ void __launch_bounds__(NW * 32, PA_FP4_MIN_CTAS)
+decode_fp4_kernel(const KParams p) {
+    constexpr int REC = 8 * D + D / 2;          // bytes of one (block, kv head) record
+    constexpr int KS = D / 16;                  // k-steps of the scores = m-tiles of P.V
+    constexpr int NB = D / 32;                  // scale blocks per token
+    constexpr int KW = D / 32;                  // 32-bit words of a thread's K bytes per token
+    constexpr int VW = D / 16;                  // 32-bit words of a thread's V bytes
+    // the stage rings, reused by the cross-warp merge at the end; the barriers after both
+    constexpr int RING = NW * NST * 2 * REC;
+    constexpr int MERGE = NW * 8 * (D + 4) * 4 + 2 * NW * 8 * 4;
+    constexpr int BAR_OFF = RING > MERGE ? RING : MERGE;
+    extern __shared__ __align__(128) uint8_t smem[];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = lane >> 2, c = lane & 3;
+    const int j = blockIdx.x + p.first_part, kvh = blockIdx.y, s = blockIdx.z;
+    const int32_t* trow = p.tables + (size_t)s * p.max_blocks;
+    int32_t first_blk[NST];
+#pragma unroll
+    for (int i = 0; i < NST; ++i) {
+        const int b = j * p.part_blocks + warp + i * NW;
+        first_blk[i] = b < p.max_blocks ? __ldg(trow + b) : -1;
+    }
+    const int L = clamped_len(p, s);
+    const int nparts = num_parts(L, p.part_blocks);
+    if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0 && nparts > p.grid_parts)
+        raise_flag(p.err, PA_DEV_ERR_HINT);
+    if (j >= nparts || aborted(p.err)) {
+        grid_dependency_wait();   // a dependent grid never completes before the one it follows
+        return;
+    }
+
+    const int blk0 = j * p.part_blocks;
+    const int tok_end = min(L, (j + 1) * p.part_blocks * kBlockTokens);
+    const int nblk = (tok_end - blk0 * kBlockTokens + kBlockTokens - 1) / kBlockTokens;
+    const int nb_w = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;
+
+    const uint32_t stage0 = smem_u32(smem) + warp * NST * 2 * REC;
+    const uint32_t bar0 = smem_u32(smem) + BAR_OFF + warp * NST * 8;
+    if (lane == 0) {
+#pragma unroll
+        for (int st = 0; st < NST; ++st) mbar_init(bar0 + st * 8, 1);
+        fence_proxy_async_smem();
+    }
+    __syncwarp();
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    const uint64_t pol = l2_policy_evict_first();
+    auto issue_blk = [&](int32_t blk, int st) -> bool {
+        const bool ok = blk >= 0 && blk < p.num_blocks;
+        if (lane == 0) {
+            if (ok) {
+                const size_t off = ((size_t)blk * p.Hkv + kvh) * (size_t)REC;
+                const uint32_t bar = bar0 + st * 8;
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(bar, 2 * REC);
+                bulk_g2s(stage0 + st * 2 * REC, p.k_pool + off, REC, bar, pol);
+                bulk_g2s(stage0 + st * 2 * REC + REC, p.v_pool + off, REC, bar, pol);
+            } else {
+                raise_flag(p.err, PA_DEV_ERR_BAD_BLOCK);
+            }
+        }
+        return ok;
+    };
+
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float o[KS][4];
+#pragma unroll
+    for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    int ref[NB];                                // R_b, warp-uniform
+    uint32_t ref_packed = 0;                    // the R_b as bytes
+    float cb[NB];                               // c_b = 2^(135 - R_b), at most 2^127
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        ref[b] = 0;
+        cb[b] = exp2i(127);
+    }
+    // score factor: log2(e) scale, and the 2^-kFp4CodeExp the unpacked codes lack
+    const float ksl = p.scale_log2 * exp2i(-kFp4CodeExp);
+    uint32_t issued = 0, phase = 0;
+    bool failed = false;
+#pragma unroll
+    for (int i = 0; i < NST; ++i)
+        if (i < nb_w && issue_blk(first_blk[i], i)) issued |= 1u << i;
+
+    // query fragments in f16: b0 <- dims 16kk + 2c, +1; b1 <- dims 16kk + 8 + 2c, +1
+    uint32_t qb[KS][2];
+    {
+        const bool live = r < p.G;
+        const uint16_t* qrow = reinterpret_cast<const uint16_t*>(p.q) +
+                               ((size_t)s * p.Hq + (size_t)kvh * p.G + (live ? r : 0)) * D;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            const uint32_t u0 = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * c)) : 0u;
+            const uint32_t u1 = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 8 + 2 * c)) : 0u;
+            qb[kk][0] = pack_f16x2(bf16_lo_to_f32(u0), bf16_hi_to_f32(u0));
+            qb[kk][1] = pack_f16x2(bf16_lo_to_f32(u1), bf16_hi_to_f32(u1));
+        }
+    }
+
+    for (int i = 0; i < nb_w; ++i) {
+        const int st = i % NST;
+        if ((issued >> st) & 1u) {
+            if (!mbar_wait_bounded(bar0 + st * 8, (phase >> st) & 1u, kWaitLimitNs)) {
+                failed = true;
+                break;
+            }
+            phase ^= 1u << st;
+            issued &= ~(1u << st);
+            const int tok0 = (blk0 + warp + i * NW) * kBlockTokens;
+            const uint8_t* kt = smem + (size_t)(warp * NST + st) * 2 * REC;
+            const uint8_t* vt = kt + REC;
+            const bool ok0 = tok0 + r < tok_end, ok1 = tok0 + r + 8 < tok_end;
+
+            // ---- scores: per 32-dim block, codes . q, times the token's block scale
+            uint32_t kr[KW], kr8[KW];
+#pragma unroll
+            for (int w = 0; w < KW; ++w) {
+                kr[w] = *reinterpret_cast<const uint32_t*>(kt + r * (D / 2) + c * (D / 8) + 4 * w);
+                kr8[w] = *reinterpret_cast<const uint32_t*>(kt + (r + 8) * (D / 2) + c * (D / 8) + 4 * w);
+            }
+            const uint32_t ksr = scale_bytes<NB>(kt + 8 * D + r * NB);     // tokens r, r + 8
+            const uint32_t ksr8 = scale_bytes<NB>(kt + 8 * D + (r + 8) * NB);
+            float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                uint32_t a[4], a8[4];
+                fp4_unpack(kr[b], a);                   // bytes 4b .. 4b+3: k-steps 2b, 2b+1
+                fp4_unpack(kr8[b], a8);
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_f16_16816(acc, a[0], a8[0], a[1], a8[1], qb[2 * b][0], qb[2 * b][1]);
+                mma_f16_16816(acc, a[2], a8[2], a[3], a8[3], qb[2 * b + 1][0], qb[2 * b + 1][1]);
+                float f0, f1;
+                if (b == 0) { f0 = scale_value<0>(ksr); f1 = scale_value<0>(ksr8); }
+                else if (b == 1) { f0 = scale_value<1>(ksr); f1 = scale_value<1>(ksr8); }
+                else if (b == 2) { f0 = scale_value<2>(ksr); f1 = scale_value<2>(ksr8); }
+                else { f0 = scale_value<3>(ksr); f1 = scale_value<3>(ksr8); }
+                f0 *= ksl;
+                f1 *= ksl;
+                sc[0] = fmaf(acc[0], f0, sc[0]);
+                sc[1] = fmaf(acc[1], f0, sc[1]);
+                sc[2] = fmaf(acc[2], f1, sc[2]);
+                sc[3] = fmaf(acc[3], f1, sc[3]);
+            }
+            // slots past the context may hold anything: select, never multiply
+            const float s0 = ok0 ? sc[0] : -INFINITY;
+            const float s1 = ok0 ? sc[1] : -INFINITY;
+            const float s2 = ok1 ? sc[2] : -INFINITY;
+            const float s3 = ok1 ? sc[3] : -INFINITY;
+            float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
+#pragma unroll
+            for (int x = 4; x < 32; x <<= 1) {
+                bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, x));
+                bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, x));
+            }
+            const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+            const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+            m0 = mn0;
+            m1 = mn1;
+            const float p0 = fast_exp2(s0 - mn0), p1 = fast_exp2(s1 - mn1);
+            const float p2 = fast_exp2(s2 - mn0), p3 = fast_exp2(s3 - mn1);
+            l0 = l0 * al0 + (p0 + p2);
+            l1 = l1 * al1 + (p1 + p3);
+            const bool rescale = !kLazyRescale || __any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f);
+
+            // ---- value scales: the tile's largest per block (live tokens only) raises R_b
+            const uint32_t vsr = ok0 ? scale_bytes<NB>(vt + 8 * D + r * NB) : 0u;
+            const uint32_t vsr8 = ok1 ? scale_bytes<NB>(vt + 8 * D + (r + 8) * NB) : 0u;
+            uint32_t tmax = __vmaxu4(vsr, vsr8);
+#pragma unroll
+            for (int x = 4; x < 32; x <<= 1) tmax = __vmaxu4(tmax, __shfl_xor_sync(0xffffffffu, tmax, x));
+            // one warp-uniform test per tile (the packed references are compared bytewise);
+            // after the first tile of a partition a raise is rare
+            if (__vmaxu4(tmax, ref_packed) != ref_packed) {
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    const int eb = (int)((tmax >> (8 * b)) & 0xffu);
+                    if (eb > ref[b]) {
+                        const float cn = exp2i(min(135 - eb, 127));
+                        const float f = cn / cb[b];      // a power of two: exact
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) {
+                            o[2 * b][x] *= f;
+                            o[2 * b + 1][x] *= f;
+                        }
+                        ref[b] = eb;
+                        cb[b] = cn;
+                    }
+                }
+                ref_packed = __vmaxu4(tmax, ref_packed);
+            }
+            if (rescale) {
+#pragma unroll
+                for (int mi = 0; mi < KS; ++mi) {
+                    o[mi][0] *= al0; o[mi][1] *= al1; o[mi][2] *= al0; o[mi][3] *= al1;
+                }
+            }
+
+            // ---- P_b . V for each block of output dims
+            uint32_t vw[VW];
+#pragma unroll
+            for (int w = 0; w < VW; ++w)
+                vw[w] = *reinterpret_cast<const uint32_t*>(vt + (r * 4 + c) * (KS * 4) + 4 * w);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                // slots past the context have p = 0 and scale code 0 here (g = 0): no select
+                float g0, g1;
+                if (b == 0) { g0 = scale_value<0>(vsr); g1 = scale_value<0>(vsr8); }
+                else if (b == 1) { g0 = scale_value<1>(vsr); g1 = scale_value<1>(vsr8); }
+                else if (b == 2) { g0 = scale_value<2>(vsr); g1 = scale_value<2>(vsr8); }
+                else { g0 = scale_value<3>(vsr); g1 = scale_value<3>(vsr8); }
+                g0 *= cb[b];
+                g1 *= cb[b];
+                const uint32_t pb0 = movmatrix_trans(pack_f16x2(p0 * g0, p1 * g0));
+                const uint32_t pb1 = movmatrix_trans(pack_f16x2(p2 * g1, p3 * g1));
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int mi = 2 * b + h2;
+                    uint32_t a[4];                       // (dh 0, half 0), (0, 1), (1, 0), (1, 1)
+                    fp4_unpack(vw[mi], a);
+                    mma_f16_16816(o[mi], a[0], a[2], a[1], a[3], pb0, pb1);
+                }
+            }
+        }
+        __syncwarp();
+        if (i + NST < nb_w && issue_blk(__ldg(trow + blk0 + warp + (i + NST) * NW), st))
+            issued |= 1u << st;
+    }
+    if (failed) {
+        if (lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
+        for (int st = 0; st < NST; ++st)
+            if ((issued >> st) & 1u) mbar_wait_bounded(bar0 + st * 8, (phase >> st) & 1u, kWaitLimitNs);
+    }
+#pragma unroll
+    for (int x = 4; x < 32; x <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, x);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, x);
+    }
+    // back to true units: block b's outputs carry c_b and the codes' 2^kFp4CodeExp
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        const float f = exp2i(-kFp4CodeExp) / cb[b];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            o[2 * b][x] *= f;
+            o[2 * b + 1][x] *= f;
+        }
+    }
+
+    const bool cta_failed = __syncthreads_or(failed);
+    constexpr int OS = D + 4;
+    float* sm_o = reinterpret_cast<float*>(smem);
+    float* sm_m = sm_o + NW * 8 * OS;
+    float* sm_l = sm_m + NW * 8;
+    {
+        float* ow = sm_o + warp * 8 * OS;
+#pragma unroll
+        for (int mi = 0; mi < KS; ++mi) {
+            const int d0 = 16 * mi + r, d1 = d0 + 8;
+            ow[(2 * c) * OS + d0] = o[mi][0];
+            ow[(2 * c + 1) * OS + d0] = o[mi][1];
+            ow[(2 * c) * OS + d1] = o[mi][2];
+            ow[(2 * c + 1) * OS + d1] = o[mi][3];
+        }
+        if (r == 0) {
+            sm_m[warp * 8 + 2 * c] = m0;
+            sm_m[warp * 8 + 2 * c + 1] = m1;
+            sm_l[warp * 8 + 2 * c] = l0;
+            sm_l[warp * 8 + 2 * c + 1] = l1;
+        }
+    }
+    __syncthreads();
+    merge_and_store<D, NW, __nv_bfloat16>(p, sm_o, sm_m, sm_l, s, kvh, j, nparts, cta_failed);
+}
+
+// ---------------------------------------------------------------------------
 // fp32 kernel: CUDA-core FMAs on the same pipeline
 // ---------------------------------------------------------------------------
 template <int D, int NW, int NST>
@@ -1010,6 +1336,44 @@ cudaError_t launch_for_dim(const KParams& kp, const DecodeArgs& a, cudaStream_t 
     return e;
 }
 
+// FP4 launch shape (MXFP4 records of 8.5 D bytes).
+#ifndef PA_FP4_STAGES
+#define PA_FP4_STAGES 4
+#endif
+#ifndef PA_FP4_WARPS
+#define PA_FP4_WARPS 4
+#endif
+constexpr int kStagesFp4 = PA_FP4_STAGES;
+constexpr int kWarpsFp4 = PA_FP4_WARPS;
+
+template <int D>
+constexpr int fp4_smem() {
+    // the stage rings (or the cross-warp merge that reuses them, if larger), then the barriers
+    constexpr int ring = kWarpsFp4 * kStagesFp4 * 2 * (8 * D + D / 2);
+    constexpr int merge = kWarpsFp4 * 8 * (D + 4) * 4 + 2 * kWarpsFp4 * 8 * 4;
+    return (ring > merge ? ring : merge) + kWarpsFp4 * kStagesFp4 * 8;
+}
+
+template <int D>
+cudaError_t launch_fp4_for_dim(const KParams& kp, const DecodeArgs& a, cudaStream_t stream) {
+    cudaError_t e;
+    const dim3 grid(a.grid_parts, a.num_kv_heads, a.num_seqs);
+    auto k = decode_fp4_kernel<D, kWarpsFp4, kStagesFp4>;
+    if ((e = set_smem(k, fp4_smem<D>())) != cudaSuccess) return e;
+    if ((e = launch_dependent(k, grid, dim3(kWarpsFp4 * 32), fp4_smem<D>(), stream, kp)) != cudaSuccess)
+        return e;
+    if (a.grid_parts > 1) {
+        const int rows = a.num_seqs * a.num_q_heads;
+        if (a.grid_parts <= 32)
+            e = launch_dependent_rows(decode_reduce_kernel<D, 8, __nv_bfloat16>, dim3((rows + 7) / 8),
+                                      dim3(256), stream, kp, rows);
+        else
+            e = launch_dependent_rows(decode_reduce_kernel<D, 1, __nv_bfloat16>, dim3(rows), dim3(256),
+                                      stream, kp, rows);
+    }
+    return e;
+}
+
 template <int D>
 cudaError_t launch_fp8_for_dim(const KParams& kp, const DecodeArgs& a, cudaStream_t stream) {
     cudaError_t e;
@@ -1048,6 +1412,12 @@ cudaError_t launch_decode_fp8(const DecodeArgs& a, cudaStream_t stream) {
     const KParams kp = make_params(a);
     if (a.head_dim == 64) return launch_fp8_for_dim<64>(kp, a, stream);
     return launch_fp8_for_dim<128>(kp, a, stream);
+}
+
+cudaError_t launch_decode_fp4(const DecodeArgs& a, cudaStream_t stream) {
+    const KParams kp = make_params(a);
+    if (a.head_dim == 64) return launch_fp4_for_dim<64>(kp, a, stream);
+    return launch_fp4_for_dim<128>(kp, a, stream);
 }
 
 namespace {

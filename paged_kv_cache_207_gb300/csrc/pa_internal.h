@@ -17,6 +17,13 @@ static_assert(kPartTokens % kBlockTokens == 0, "partition must be whole blocks")
 
 inline int elem_bytes(pa_dtype t) { return t == PA_BF16 ? 2 : (t == PA_FP8_E4M3 ? 1 : 4); }
 
+// Blocks per split-KV partition of the FP4 path (a multiple of kPartBlocks).
+#ifndef PA_FP4_PARTITION_BLOCKS
+#define PA_FP4_PARTITION_BLOCKS 128
+#endif
+constexpr int kFp4PartBlocks = PA_FP4_PARTITION_BLOCKS;
+static_assert(PA_FP4_PARTITION_BLOCKS % 32 == 0, "FP4 partitions are whole 512-token units");
+
 struct DecodeArgs {
     void* out;
     const void* q;
@@ -116,5 +123,13 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 // after_suffix: the suffix decode kernel was launched just before (see PParams).
 cudaError_t launch_prefix_tc(const DecodeArgs& a, bool after_suffix, cudaStream_t stream);
 cudaError_t launch_decode_fp8(const DecodeArgs& a, cudaStream_t stream);
+
+// MXFP4 cache: per (block, kv head) a record of 8 * D code bytes then D / 2 E8M0 scale
+// bytes (layout in pa.h).
+__host__ __device__ inline size_t fp4_record_bytes(int head_dim) {
+    return (size_t)8 * head_dim + (size_t)head_dim / 2;
+}
+cudaError_t launch_append_fp4(const AppendArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_fp4(const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace pa

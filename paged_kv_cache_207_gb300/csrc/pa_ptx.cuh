@@ -181,6 +181,45 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// The four bytes of a word, each a pair of E2M1 codes (low nibble first), as four
+// f16x2 (exact: every E2M1 value is an f16 value); o[i] comes from byte i.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&o)[4]) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+        : "r"(w));
+}
+
+// The same through E4M3: an E2M1 code (s, e1 e0, m) is, bit for bit, the E4M3 code
+// (s, 0 0 e1 e0, m 0 0) of the value times 2^-6 (E2M1's subnormal 0.5 lands on an E4M3
+// subnormal), and E4M3 -> f16 is exact.  o[i] from byte i as above, times 2^-6.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4_scaled(uint32_t w, uint32_t (&o)[4]) {
+    const uint32_t lo = ((w << 2) & 0x1C1C1C1Cu) | ((w << 4) & 0x80808080u);   // low nibbles
+    const uint32_t hi = ((w >> 2) & 0x1C1C1C1Cu) | (w & 0x80808080u);          // high nibbles
+    const uint32_t p01 = __byte_perm(lo, hi, 0x5140), p23 = __byte_perm(lo, hi, 0x7362);
+    o[0] = e4m3x2_to_f16x2((uint16_t)(p01 & 0xffffu));
+    o[1] = e4m3x2_to_f16x2((uint16_t)(p01 >> 16));
+    o[2] = e4m3x2_to_f16x2((uint16_t)(p23 & 0xffffu));
+    o[3] = e4m3x2_to_f16x2((uint16_t)(p23 >> 16));
+}
+
+// Two fp32 -> two E2M1 codes in one byte (round to nearest even, saturating at 6):
+// `lo` in bits 0..3, `hi` in bits 4..7.
+__device__ __forceinline__ uint32_t pack_e2m1x2(float lo, float hi) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 b;\n\tcvt.rn.satfinite.e2m1x2.f32 b, %1, %2;\n\tcvt.u32.u8 %0, b;\n\t}"
+        : "=r"(r)
+        : "f"(hi), "f"(lo));
+    return r;
+}
+
+// 2^e as an fp32, exactly, for e <= 127 (subnormal results down to 2^-149, 0 below).
+__device__ __forceinline__ float exp2i(int e) {
+    if (e >= -126) return __uint_as_float((uint32_t)(e + 127) << 23);
+    return e >= -149 ? __uint_as_float(1u << (e + 149)) : 0.f;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
