@@ -54,7 +54,16 @@ struct KParams {
     int first_part;     // partitions below this are a shared prefix done by the prefix kernel
     int part_blocks;    // blocks per split-KV partition (a fixed constant of each path)
     float scale_log2;   // scale * log2(e): scores live in log2 units
+    // shared-prefix suffix kernel launched after the prefix kernel, which starts it only
+    // once every kernel before the prefix (the append) has finished: it needs no wait of
+    // its own, and CTA 0 waits for the prefix grid before exiting so that this grid never
+    // completes before it
+    int after_prefix;
 };
+
+__device__ __forceinline__ bool first_cta() {
+    return blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+}
 
 // Rescale the output accumulators only in blocks where a running maximum moved
 // (any lane of the warp); after the first blocks of a partition it rarely does.
@@ -173,7 +182,8 @@ decode_bf16_kernel(const KParams p) {
     if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0 && nparts > p.grid_parts)
         raise_flag(p.err, PA_DEV_ERR_HINT);
     if (j >= nparts || aborted(p.err)) {
-        grid_dependency_wait();   // a dependent grid never completes before the one it follows
+        // a dependent grid never completes before the one it follows
+        if (!p.after_prefix || first_cta()) grid_dependency_wait();
         return;
     }
 
@@ -194,8 +204,9 @@ decode_bf16_kernel(const KParams p) {
 
     // Everything above reads only the tables and the lengths, which no kernel of this
     // library writes.  The pools (an append) and the query (any earlier call's output)
-    // may still be being written by the previous kernel: wait for it.
-    grid_dependency_wait();
+    // may still be being written by the previous kernel: wait for it (after the prefix
+    // kernel, that kernel's start already did).
+    if (!p.after_prefix) grid_dependency_wait();
     grid_launch_dependents();
 
     const uint64_t pol = l2_policy_evict_first();
@@ -327,6 +338,7 @@ decode_bf16_kernel(const KParams p) {
         l1 += __shfl_xor_sync(0xffffffffu, l1, x);
     }
 
+    if (p.after_prefix && first_cta()) grid_dependency_wait();
     const bool cta_failed = __syncthreads_or(failed);   // every warp is done with its stages
     constexpr int OS = D + 4;
     float* sm_o = reinterpret_cast<float*>(smem);       // [NW][8][OS]
@@ -1159,15 +1171,61 @@ decode_reduce_kernel(const KParams p, int num_rows) {
     const size_t prow = (size_t)(work ? row : 0) * p.part_stride;
     const float2* ml = p.part_ml + prow;
     const float* po = p.part_o + prow * D + lane * DPL;
+    float acc[DPL];
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) acc[k] = 0.f;
+    float lsum = 0.f;
+    if constexpr (WPR == 1) {
+        // a warp per row, at most 32 partitions: the maxima (one per lane) and the first
+        // kChunk partial rows are loaded together, so the merge takes one round trip
+        constexpr int kChunk = 8;
+        float2 mlv = make_float2(-INFINITY, 0.f);
+        if (work && lane < n) mlv = ml[lane];
+        float ov[kChunk][DPL];
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            const bool has = work && i < n;
+            if constexpr (DPL == 4) {
+                const float4 o = has ? *reinterpret_cast<const float4*>(po + (size_t)i * D)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                ov[i][0] = o.x; ov[i][1] = o.y; ov[i][2] = o.z; ov[i][3] = o.w;
+            } else {
+                const float2 o = has ? *reinterpret_cast<const float2*>(po + (size_t)i * D)
+                                     : make_float2(0.f, 0.f);
+                ov[i][0] = o.x; ov[i][1] = o.y;
+            }
+        }
+        float M = mlv.x;
+#pragma unroll
+        for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
+        if (work && M != -INFINITY) {
+            // partitions in order 0, 1, ...: the sum's order is fixed
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) {
+                const float mi = __shfl_sync(0xffffffffu, mlv.x, i);
+                const float li = __shfl_sync(0xffffffffu, mlv.y, i);
+                if (i < n) {
+                    const float wt = fast_exp2(mi - M);
+                    lsum += wt * li;
+#pragma unroll
+                    for (int k = 0; k < DPL; ++k) acc[k] += wt * ov[i][k];
+                }
+            }
+            for (int i = kChunk; i < n; ++i) {
+                const float mi = __shfl_sync(0xffffffffu, mlv.x, i);
+                const float li = __shfl_sync(0xffffffffu, mlv.y, i);
+                const float wt = fast_exp2(mi - M);
+                lsum += wt * li;
+#pragma unroll
+                for (int k = 0; k < DPL; ++k) acc[k] += wt * po[(size_t)i * D + k];
+            }
+        }
+    } else {
     float M = -INFINITY;
     if (work)
         for (int i = lane; i < n; i += 32) M = fmaxf(M, ml[i].x);
 #pragma unroll
     for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
-    float acc[DPL];
-#pragma unroll
-    for (int k = 0; k < DPL; ++k) acc[k] = 0.f;
-    float lsum = 0.f;
     if (work && M != -INFINITY) {
 #pragma unroll 8
         for (int i = wr; i < n; i += WPR) {
@@ -1182,6 +1240,7 @@ decode_reduce_kernel(const KParams p, int num_rows) {
                 acc[0] += wt * o.x; acc[1] += wt * o.y;
             }
         }
+    }
     }
     if constexpr (WPR > 1) {
 #pragma unroll
@@ -1238,6 +1297,11 @@ constexpr int f32_smem() {
 
 template <typename K>
 cudaError_t set_smem(K kernel, int bytes) {
+    // all of the SM's unified memory as shared memory, so that CTAs of the decode and
+    // prefix kernels can share an SM whatever the carve-out the other asked for
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
@@ -1300,9 +1364,17 @@ template <int D>
 cudaError_t launch_fp8_for_dim(const KParams& kp, const DecodeArgs& a, cudaStream_t stream);
 
 template <int D>
-cudaError_t launch_for_dim(const KParams& kp, const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_for_dim(const KParams& kp_in, const DecodeArgs& a, cudaStream_t stream) {
     cudaError_t e = cudaSuccess;
+    KParams kp = kp_in;
     const int launched = a.grid_parts - kp.first_part;   // partitions of the main kernel
+    if (kp.first_part > 0) {
+        // the shared prefix first: its CTAs take one SM each for a chain of tensor-core
+        // steps; the suffix kernel after it fills the rest of the GPU and runs beside it
+        e = launch_prefix_tc(a, false, stream);
+        if (e != cudaSuccess) return e;
+        kp.after_prefix = 1;
+    }
     if (launched > 0) {
         const dim3 grid(launched, a.num_kv_heads, a.num_seqs);
         if (a.dtype == PA_BF16) {
@@ -1316,10 +1388,7 @@ cudaError_t launch_for_dim(const KParams& kp, const DecodeArgs& a, cudaStream_t 
         }
         if (e != cudaSuccess) return e;
     }
-    if (kp.first_part > 0) {
-        e = launch_prefix_tc(a, launched > 0, stream);
-        if (e != cudaSuccess) return e;
-    }
+
     if (a.grid_parts > 1 || kp.first_part > 0) {
         const int rows = a.num_seqs * a.num_q_heads;
         if (a.grid_parts <= 32) {          // few partitions: a warp per row
@@ -1445,6 +1514,7 @@ KParams make_params(const DecodeArgs& a) {
     kp.first_part = a.first_part;
     kp.part_blocks = a.part_blocks;
     kp.scale_log2 = a.scale * kLog2e;
+    kp.after_prefix = 0;
     return kp;
 }
 }  // namespace

@@ -47,9 +47,9 @@ struct PParams {
     float* part_o;
     float2* part_ml;
     int part_stride, part_blocks, num_seqs, rows_per_cta;
-    // prefix mode normally runs beside the suffix kernel launched just before it, which
-    // starts it only after the kernels before have finished; without a suffix kernel it
-    // follows those kernels directly and must wait for them first
+    // prefix mode: wait for the previous kernel of the stream (the append) before reading
+    // the query or the pools (set by every launch of the decode path, which starts this
+    // kernel first and the suffix kernel after it)
     int wait_first;
 };
 
@@ -84,10 +84,17 @@ constexpr int kHalfRows = 128;
 constexpr int kRowsTC = 2 * kHalfRows;
 constexpr int kKeyBlocks = 8;
 constexpr int kKeyTok = kKeyBlocks * kBlockTokens;
-constexpr int kSoftWarps = 8;                   // warps 0-3: tile a, 4-7: tile b
-constexpr int kProducerWarp = kSoftWarps;       // V tiles
-constexpr int kMmaWarp = kSoftWarps + 1;        // TMEM owner, MMA issue
-constexpr int kRepackWarp = kSoftWarps + 2;     // K tiles: copy in, repack chunk-major
+// Warp roles for SW softmax warpgroups (2: Q tiles a and b; 1: tile a only, the
+// 128-row prefix mode): warps 0 .. 4 SW - 1 softmax, then the V producer, the MMA
+// warp and two K repack warps.
+template <int SW>
+struct Roles {
+    static constexpr int kSoftWarps = 4 * SW;
+    static constexpr int kProducerWarp = kSoftWarps;       // V tiles
+    static constexpr int kMmaWarp = kSoftWarps + 1;        // TMEM owner, MMA issue
+    static constexpr int kRepackWarp = kSoftWarps + 2;     // K tiles: copy in, repack chunk-major
+    static constexpr int kThreads = (kSoftWarps + 4) * 32;
+};
 constexpr int kRepackWarps = 2;
 // 16-byte loads in flight per lane of a repack warp (8 fits in the 104 registers the
 // copy warpgroup keeps; 16 would spill there)
@@ -95,7 +102,7 @@ constexpr int kRepackWarps = 2;
 #define PA_REPACK_BATCH 8
 #endif
 constexpr int kRepackBatch = PA_REPACK_BATCH;
-constexpr int kThreadsTC = (kSoftWarps + 2 + kRepackWarps) * 32;
+constexpr int kThreadsTC = Roles<2>::kThreads;  // the register budget is set for this size
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;
 
@@ -190,9 +197,15 @@ __device__ __forceinline__ uint32_t check_blocks(const PParams& p, int32_t& blk,
 // kv head, partition j of a prefix shared by every sequence, read through table row 0);
 // every key is visible and the CTA writes unnormalised partials (o, max, sum) of
 // partition j for the split-KV merge instead of outputs.
-template <int D, bool PREFIX>
+// SW = 1 launches 256 threads under the same per-thread register budget (168), so a
+// CTA takes 256 x 168 registers and leaves room for a decode CTA on its SM.
+template <int D, bool PREFIX, int SW>
 __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams p) {
     using L = Smem<D>;
+    constexpr int kSoftWarps = Roles<SW>::kSoftWarps;
+    constexpr int kProducerWarp = Roles<SW>::kProducerWarp;
+    constexpr int kMmaWarp = Roles<SW>::kMmaWarp;
+    constexpr int kRepackWarp = Roles<SW>::kRepackWarp;
     constexpr int TILE = L::TILE, KTILE = L::KTILE;
     constexpr int KSTEPS = D / 16;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -208,7 +221,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         nblk = p.part_blocks;
         p_last = nblk * kBlockTokens - 1;                 // positions relative to the partition
         trow = p.tables + (size_t)blockIdx.z * p.part_blocks;
-        has_b = p.rows_per_cta > kHalfRows && row_base + kHalfRows < rows_total;
+        has_b = SW == 2 && p.rows_per_cta > kHalfRows && row_base + kHalfRows < rows_total;
     } else {
         const int qt = gridDim.x - 1 - blockIdx.x;        // later (longer) tiles first
         const int s = blockIdx.z;
@@ -233,7 +246,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         trow = p.tables + (size_t)s * p.max_blocks;
         // tile b holds rows 128 .. 255; it is skipped when none of them is a chunk row
         const int tl_b = kHalfRows / p.G;
-        has_b = tl_b < p.TQ && i0 + tl_b < n;
+        has_b = SW == 2 && tl_b < p.TQ && i0 + tl_b < n;
     }
     const int ntiles = (nblk + kKeyBlocks - 1) / kKeyBlocks;
 
@@ -291,14 +304,25 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         // a negative scale is applied as |scale| to -q (exact), so that the softmax can
         // take the row maximum of the unscaled scores
         const uint32_t flip = p.scale_log2 < 0.f ? 0x80008000u : 0u;
-#pragma unroll 4
-        for (int kg = 0; kg < D / 8; ++kg) {
-            uint4 v = row_valid ? __ldg(qsrc + kg) : make_uint4(0u, 0u, 0u, 0u);
-            v.x ^= flip;
-            v.y ^= flip;
-            v.z ^= flip;
-            v.w ^= flip;
-            st_shared_v4(qdst + kg * 2048, v);
+        // loads in flight together, then the stores: the whole row in the short prefix
+        // CTAs (one round trip on their critical path), half of it in the prefill, whose
+        // register budget here is tighter
+        constexpr int QB = PREFIX ? D / 8 : D / 16;
+#pragma unroll
+        for (int k0 = 0; k0 < D / 8; k0 += QB) {
+            uint4 qv[QB];
+#pragma unroll
+            for (int u = 0; u < QB; ++u)
+                qv[u] = row_valid ? __ldg(qsrc + k0 + u) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int u = 0; u < QB; ++u) {
+                uint4 v = qv[u];
+                v.x ^= flip;
+                v.y ^= flip;
+                v.z ^= flip;
+                v.w ^= flip;
+                st_shared_v4(qdst + (k0 + u) * 2048, v);
+            }
         }
         fence_proxy_async_smem();
     }
@@ -726,8 +750,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         tc_fence_after();
         tmem_dealloc<kTmemCols>(tmem);
     }
-    // prefix mode: this grid overlaps the suffix kernel launched before it, and the merge
-    // after it waits on this grid only, so it must not finish before that kernel has
+    // (prefix mode: every thread has waited for the previous grid; this is a no-op then)
     if (PREFIX) grid_dependency_wait();
 }
 
@@ -735,18 +758,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
 
 template <typename K>
 cudaError_t set_smem(K kernel, int bytes) {
+    // all of the SM's unified memory as shared memory, so that CTAs of the decode and
+    // prefix kernels can share an SM whatever the carve-out the other asked for
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-template <int D, bool PREFIX>
+template <int D, bool PREFIX, int SW>
 cudaError_t launch_tc(const PParams& pp, dim3 grid, cudaStream_t stream) {
-    auto k = tc::prefill_tc_kernel<D, PREFIX>;
+    auto k = tc::prefill_tc_kernel<D, PREFIX, SW>;
     constexpr int smem = tc::Smem<D>::BYTES;
     cudaError_t e = set_smem(k, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(tc::kThreadsTC);
+    cfg.blockDim = dim3(tc::Roles<SW>::kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -792,11 +820,12 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     pp.cu_q = a.cu_q;
     pp.TQ = tc::kRowsTC / pp.G;
     const dim3 grid((a.max_chunk + pp.TQ - 1) / pp.TQ, pp.Hkv, a.num_seqs);
-    if (a.head_dim == 64) return launch_tc<64, false>(pp, grid, stream);
-    return launch_tc<128, false>(pp, grid, stream);
+    if (a.head_dim == 64) return launch_tc<64, false, 2>(pp, grid, stream);
+    return launch_tc<128, false, 2>(pp, grid, stream);
 }
 
 cudaError_t launch_prefix_tc(const DecodeArgs& a, bool after_suffix, cudaStream_t stream) {
+    // (after_suffix: an older launch order; the decode path now starts this kernel first)
     PParams pp = common_params(a.q, a.k_pool, a.v_pool, a.block_tables, a.err, a.num_q_heads,
                                a.num_kv_heads, a.max_blocks, a.num_blocks, a.scale);
     const size_t prow = (size_t)a.num_seqs * a.num_q_heads * a.part_stride;
@@ -814,8 +843,10 @@ cudaError_t launch_prefix_tc(const DecodeArgs& a, bool after_suffix, cudaStream_
     pp.rows_per_cta = PA_PREFIX_TC_ROWS;              // tuning builds: 128 or 256
 #endif
     const dim3 grid((rows + pp.rows_per_cta - 1) / pp.rows_per_cta, a.num_kv_heads, a.first_part);
-    if (a.head_dim == 64) return launch_tc<64, true>(pp, grid, stream);
-    return launch_tc<128, true>(pp, grid, stream);
+    const bool one = pp.rows_per_cta <= tc::kHalfRows;    // one Q tile: one softmax warpgroup
+    if (a.head_dim == 64)
+        return one ? launch_tc<64, true, 1>(pp, grid, stream) : launch_tc<64, true, 2>(pp, grid, stream);
+    return one ? launch_tc<128, true, 1>(pp, grid, stream) : launch_tc<128, true, 2>(pp, grid, stream);
 }
 
 }  // namespace pa
