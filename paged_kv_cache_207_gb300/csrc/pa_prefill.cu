@@ -111,13 +111,15 @@ constexpr float kRescaleLog2 = 8.f;
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 2 * kKeyTok;
 
-template <int D>
+// NQ Q tiles (the softmax warpgroups of the launch): with one, a 128-row prefix CTA
+// takes 192 KB at D = 128 and leaves room on its SM for a one-stage decode CTA.
+template <int D, int NQ = 2>
 struct Smem {
     static constexpr int TILE = kBlockTokens * D * 2;          // one (block, kv head) tile
     static constexpr int KTILE = kKeyBlocks * TILE;            // one ring stage
     static constexpr int QTILE = kHalfRows * D * 2;            // [D/8][16][8 rows][16 B]
-    static constexpr int Q = 0;                                // tiles a, b
-    static constexpr int K = Q + 2 * QTILE;                    // K tiles as copied, 2 stages
+    static constexpr int Q = 0;                                // tiles a (, b)
+    static constexpr int K = Q + NQ * QTILE;                   // K tiles as copied, 2 stages
     static constexpr int V = K + 2 * KTILE;                    // V tiles, 2 stages
     static constexpr int CM = V + 2 * KTILE;                   // K tile chunk-major
     static constexpr int BAR = CM + KTILE;
@@ -201,7 +203,7 @@ __device__ __forceinline__ uint32_t check_blocks(const PParams& p, int32_t& blk,
 // CTA takes 256 x 168 registers and leaves room for a decode CTA on its SM.
 template <int D, bool PREFIX, int SW>
 __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams p) {
-    using L = Smem<D>;
+    using L = Smem<D, SW>;
     constexpr int kSoftWarps = Roles<SW>::kSoftWarps;
     constexpr int kProducerWarp = Roles<SW>::kProducerWarp;
     constexpr int kMmaWarp = Roles<SW>::kMmaWarp;
@@ -769,7 +771,7 @@ cudaError_t set_smem(K kernel, int bytes) {
 template <int D, bool PREFIX, int SW>
 cudaError_t launch_tc(const PParams& pp, dim3 grid, cudaStream_t stream) {
     auto k = tc::prefill_tc_kernel<D, PREFIX, SW>;
-    constexpr int smem = tc::Smem<D>::BYTES;
+    constexpr int smem = tc::Smem<D, SW>::BYTES;
     cudaError_t e = set_smem(k, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
