@@ -220,10 +220,11 @@ def decode_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str, fp8: bool = False):
+def profiled_traffic(workload: str, kv_dtype: str = "bf16"):
     """dram bytes per decode launch from a committed ncu summary, if it was taken on
     the current decode source; else None."""
-    path = os.path.join(ROOT, "profiles", f"decode_{'fp8_' if fp8 else ''}{workload}_dram.txt")
+    tag = "" if kv_dtype == "bf16" else kv_dtype + "_"
+    path = os.path.join(ROOT, "profiles", f"decode_{tag}{workload}_dram.txt")
     if not os.path.exists(path):
         return None
     kv = {}
@@ -514,7 +515,7 @@ def run_ours(args, rank, world, local):
                                  quant, "pa_decode_attention") + " (main kernel + partition merge)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None if wl_shared or quant == "fp4" else profiled_traffic(args.workload, quant == "fp8"),
+                     "frac": round(achieved / peak, 4), "traffic": None if wl_shared else profiled_traffic(args.workload, args.kv_dtype),
                      "algorithmic_bytes_per_launch": dbytes, "avg_launch_ms": round(dec_ms, 5)},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms / K, 5),
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
