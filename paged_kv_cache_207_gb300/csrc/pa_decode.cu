@@ -1200,11 +1200,13 @@ decode_reduce_kernel(const KParams p, int num_rows) {
         for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
         if (work && M != -INFINITY) {
             // partitions in order 0, 1, ...: the sum's order is fixed
+            // an empty partition (maximum -inf: a slot a longer prefix partition left unused)
+            // is skipped, whatever its partial holds
 #pragma unroll
             for (int i = 0; i < kChunk; ++i) {
                 const float mi = __shfl_sync(0xffffffffu, mlv.x, i);
                 const float li = __shfl_sync(0xffffffffu, mlv.y, i);
-                if (i < n) {
+                if (i < n && mi != -INFINITY) {
                     const float wt = fast_exp2(mi - M);
                     lsum += wt * li;
 #pragma unroll
@@ -1214,6 +1216,7 @@ decode_reduce_kernel(const KParams p, int num_rows) {
             for (int i = kChunk; i < n; ++i) {
                 const float mi = __shfl_sync(0xffffffffu, mlv.x, i);
                 const float li = __shfl_sync(0xffffffffu, mlv.y, i);
+                if (mi == -INFINITY) continue;
                 const float wt = fast_exp2(mi - M);
                 lsum += wt * li;
 #pragma unroll
@@ -1230,6 +1233,7 @@ decode_reduce_kernel(const KParams p, int num_rows) {
 #pragma unroll 8
         for (int i = wr; i < n; i += WPR) {
             const float2 v = ml[i];
+            if (v.x == -INFINITY) continue;               // an empty partition
             const float wt = fast_exp2(v.x - M);
             lsum += wt * v.y;
             if constexpr (DPL == 4) {

@@ -51,6 +51,10 @@ struct PParams {
     // the query or the pools (set by every launch of the decode path, which starts this
     // kernel first and the suffix kernel after it)
     int wait_first;
+    // prefix mode: a CTA covers slot_mult split-KV partitions of the decode (part_blocks is
+    // slot_mult times the decode's); it writes its partial into the first of those workspace
+    // slots and an empty one -- maximum -inf, sum 0 -- into the others
+    int slot_mult;
 };
 
 __device__ __forceinline__ void raise_flag(int32_t* err, int bits) {
@@ -695,7 +699,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         if (ok) ok = warp_wait(bar(kODone + h), 0);
         if (ok && PREFIX) {
             tc_fence_after();
-            float4* po = reinterpret_cast<float4*>(p.part_o + (orow * p.part_stride + blockIdx.z) * D);
+            const size_t slot = orow * p.part_stride + (size_t)blockIdx.z * p.slot_mult;
+            float4* po = reinterpret_cast<float4*>(p.part_o + slot * D);
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
@@ -708,7 +713,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
                                                     __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
                 }
             }
-            if (row_valid) p.part_ml[orow * p.part_stride + blockIdx.z] = make_float2(m_used, l);
+            if (row_valid) {
+                p.part_ml[slot] = make_float2(m_used, l);
+                for (int e = 1; e < p.slot_mult; ++e) p.part_ml[slot + e] = make_float2(-INFINITY, 0.f);
+            }
         } else if (ok) {
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -736,7 +744,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
             if (lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
             if (row_valid) {
                 if constexpr (PREFIX) {
-                    p.part_ml[orow * p.part_stride + blockIdx.z] =
+                    p.part_ml[orow * p.part_stride + (size_t)blockIdx.z * p.slot_mult] =
                         make_float2(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
                 } else {
                     uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow);
@@ -834,17 +842,25 @@ cudaError_t launch_prefix_tc(const DecodeArgs& a, bool after_suffix, cudaStream_
     pp.part_o = static_cast<float*>(a.workspace);
     pp.part_ml = reinterpret_cast<float2*>(static_cast<char*>(a.workspace) + prow * a.head_dim * sizeof(float));
     pp.part_stride = a.part_stride;
-    pp.part_blocks = a.part_blocks;
     pp.num_seqs = a.num_seqs;
     pp.wait_first = after_suffix ? 0 : 1;
+    // Prefix CTAs take an SM each; when the prefix is a whole number of such pairs, one CTA
+    // covers PA_PREFIX_PART_MULT decode partitions: fewer CTAs, each longer, which leaves SMs
+    // to the suffix decode running beside them and cuts the partials the merge reads.
+#ifndef PA_PREFIX_PART_MULT
+#define PA_PREFIX_PART_MULT 2
+#endif
+    pp.slot_mult = a.first_part % PA_PREFIX_PART_MULT == 0 ? PA_PREFIX_PART_MULT : 1;
+    pp.part_blocks = a.part_blocks * pp.slot_mult;
+    const int pre_parts = a.first_part / pp.slot_mult;
     // 256 rows (two Q tiles) per CTA when that still gives every SM a CTA, else 128
     const int rows = a.num_seqs * pp.G;
-    const long long ctas256 = (long long)((rows + tc::kRowsTC - 1) / tc::kRowsTC) * a.num_kv_heads * a.first_part;
+    const long long ctas256 = (long long)((rows + tc::kRowsTC - 1) / tc::kRowsTC) * a.num_kv_heads * pre_parts;
     pp.rows_per_cta = ctas256 >= sm_count() ? tc::kRowsTC : tc::kHalfRows;
 #ifdef PA_PREFIX_TC_ROWS
     pp.rows_per_cta = PA_PREFIX_TC_ROWS;              // tuning builds: 128 or 256
 #endif
-    const dim3 grid((rows + pp.rows_per_cta - 1) / pp.rows_per_cta, a.num_kv_heads, a.first_part);
+    const dim3 grid((rows + pp.rows_per_cta - 1) / pp.rows_per_cta, a.num_kv_heads, pre_parts);
     const bool one = pp.rows_per_cta <= tc::kHalfRows;    // one Q tile: one softmax warpgroup
     if (a.head_dim == 64)
         return one ? launch_tc<64, true, 1>(pp, grid, stream) : launch_tc<64, true, 2>(pp, grid, stream);
