@@ -64,11 +64,21 @@ __device__ __forceinline__ void raise_flag(int32_t* err, int bits) {
 // ============================================================================
 // The tcgen05 kernel.
 //
-// Warp roles: 0-7 softmax (0-3 for Q tile a, 4-7 for tile b; a warp reaches the
-// TMEM lanes 32 (warp % 4) ..), 8 streams V tiles with bulk copies, 9 owns the
-// TMEM and issues the MMAs, 10-11 copy K tiles in and repack them chunk-major.
-// setmaxnreg moves registers from warps 8-11 (104 each) to the softmax warps (200
-// each), which hold a 128-column row of S.
+// Warp roles (two Q tiles): 0-7 softmax (0-3 for Q tile a, 4-7 for tile b; a warp
+// reaches the TMEM lanes 32 (warp % 4) ..), 8 streams V tiles with bulk copies, 9 owns
+// the TMEM and issues the MMAs, 10-11 copy K tiles in with 16-byte copies.  setmaxnreg
+// moves registers from the copy / MMA warps (104 each) to the softmax warps (200 each),
+// which hold a 128-column row of S.  setmaxnreg is collective over a warpgroup: every
+// warp of a warpgroup runs the same one, so the copy / MMA warps fill whole warpgroups
+// (idle warps pad them) and lower their budget together at the start.
+// A K tile lands chunk-major, [D/8][8 blocks][16 slots][16 B]: every 8-token group
+// of the tile is 128 B after the previous one, so Q K^T over the tile's 128 tokens is
+// one MMA per 16 dims.  The pool holds a block as [D/8][16 slots][16 B], so each
+// 16-byte piece has its own place in the stage.  K comes through the load/store path
+// and V through the bulk-copy engine: an SM takes in more from DRAM through both than
+// through either (measured on GB300 with 64 busy SMs: 4 KB bulk copies alone about
+// 77 GB/s per SM, both about 97 GB/s), and bulk copies of the 256-byte pieces would
+// be far slower (about 64 cycles per copy).
 // Each softmax thread reads its row of S_h from TMEM, applies the causal mask,
 // keeps a running maximum that is raised only when a tile exceeds it by more than
 // 2^8 (O_h is then rescaled in TMEM), writes its bf16 probabilities over the
@@ -90,23 +100,21 @@ constexpr int kKeyBlocks = 8;
 constexpr int kKeyTok = kKeyBlocks * kBlockTokens;
 // Warp roles for SW softmax warpgroups (2: Q tiles a and b; 1: tile a only, the
 // 128-row prefix mode): warps 0 .. 4 SW - 1 softmax, then the V producer, the MMA
-// warp and two K repack warps.
+// warp and the K copy warps: two with two Q tiles (the register budget holds no more),
+// four with one, whose CTAs stream their keys from DRAM (copies in flight are limited
+// per scheduler, so the K copies are spread over all four).
 template <int SW>
 struct Roles {
     static constexpr int kSoftWarps = 4 * SW;
     static constexpr int kProducerWarp = kSoftWarps;       // V tiles
     static constexpr int kMmaWarp = kSoftWarps + 1;        // TMEM owner, MMA issue
-    static constexpr int kRepackWarp = kSoftWarps + 2;     // K tiles: copy in, repack chunk-major
-    static constexpr int kThreads = (kSoftWarps + 4) * 32;
+    static constexpr int kKWarp = kSoftWarps + 2;          // K tiles
+    static constexpr int kKWarps = SW == 1 ? 4 : 2;
+    static constexpr int kOtherWarps = (2 + kKWarps + 3) / 4 * 4;   // whole warpgroups
+    static constexpr int kThreads = (kSoftWarps + kOtherWarps) * 32;
 };
-constexpr int kRepackWarps = 2;
-// 16-byte loads in flight per lane of a repack warp (8 fits in the 104 registers the
-// copy warpgroup keeps; 16 would spill there)
-#ifndef PA_REPACK_BATCH
-#define PA_REPACK_BATCH 8
-#endif
-constexpr int kRepackBatch = PA_REPACK_BATCH;
 constexpr int kThreadsTC = Roles<2>::kThreads;  // the register budget is set for this size
+static_assert(Roles<1>::kThreads <= kThreadsTC, "launch bounds");
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;
 
@@ -115,27 +123,30 @@ constexpr float kRescaleLog2 = 8.f;
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 2 * kKeyTok;
 
-// NQ Q tiles (the softmax warpgroups of the launch): with one, a 128-row prefix CTA
-// takes 192 KB at D = 128 and leaves room on its SM for a one-stage decode CTA.
+// NQ Q tiles (the softmax warpgroups of the launch) and rings of KST K and VST V tiles,
+// as deep as 227 KB allow: three K stages keep the next copies in flight while a tile
+// is used (a copy takes a few microseconds to land when the GPU is busy).
 template <int D, int NQ = 2>
 struct Smem {
     static constexpr int TILE = kBlockTokens * D * 2;          // one (block, kv head) tile
     static constexpr int KTILE = kKeyBlocks * TILE;            // one ring stage
     static constexpr int QTILE = kHalfRows * D * 2;            // [D/8][16][8 rows][16 B]
+    static constexpr int KST = 3;
+    static constexpr int VST = (NQ == 1 || D == 64) ? 3 : 2;
     static constexpr int Q = 0;                                // tiles a (, b)
-    static constexpr int K = Q + NQ * QTILE;                   // K tiles as copied, 2 stages
-    static constexpr int V = K + 2 * KTILE;                    // V tiles, 2 stages
-    static constexpr int CM = V + 2 * KTILE;                   // K tile chunk-major
-    static constexpr int BAR = CM + KTILE;
-    static constexpr int NBAR = 16;
+    static constexpr int K = Q + NQ * QTILE;                   // K tiles, chunk-major
+    static constexpr int V = K + KST * KTILE;                  // V tiles as copied
+    static constexpr int BAR = V + VST * KTILE;
+    static constexpr int NBAR = 24;
     static constexpr int SLOT = BAR + NBAR * 8;
     // at least 120 KB so that one CTA (and its 512 TMEM columns) owns an SM
     static constexpr int BYTES = SLOT + 16 < 122880 ? 122880 : SLOT + 16;
+    static_assert(SLOT + 16 <= 232448, "shared memory of one CTA");
 };
 
-// barrier indices
-constexpr int kKFull = 0, kVFull = 2, kVEmpty = 4, kCmFull = 6, kCmFree = 7, kSFull = 8,
-              kPFull = 10, kODone = 12, kDone = 14, kPVDone = 15;
+// barrier indices (rings of up to 4 stages)
+constexpr int kKFull = 0, kKEmpty = 4, kVFull = 8, kVEmpty = 12, kSFull = 16, kPFull = 18,
+              kODone = 20, kDone = 22, kPVDone = 23;
 
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     uint64_t pol;
@@ -143,6 +154,12 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     return pol;
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr) : "memory");
+    return v;
+}
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)
@@ -178,12 +195,19 @@ __device__ __forceinline__ uint64_t fadd_f32x2(uint64_t a, uint64_t b) {
     return r;
 }
 
-// Table entry of block b of key tile j for lane b of a warp (-1 for lanes past the
-// tile's or the sequence's last block).
-__device__ __forceinline__ int32_t fetch_block(const int32_t* trow, int j, int nblk, int ntiles,
-                                               int lane) {
-    const int b = j * kKeyBlocks + lane;
-    return (j < ntiles && lane < kKeyBlocks && b < nblk) ? __ldg(trow + b) : -1;
+// The copy warps read the table in windows of 32 entries, four key tiles, one entry per
+// lane (-1 past the CTA's last block), a window ahead of its use: read one tile ahead,
+// every tile would wait for a dependent load (over a microsecond when HBM is busy).
+constexpr int kWinTiles = 32 / kKeyBlocks;
+__device__ __forceinline__ int32_t fetch_window(const int32_t* trow, int w, int nblk, int lane) {
+    const int b = 32 * w + lane;
+    return b < nblk ? __ldg(trow + b) : -1;
+}
+// Table entry of block `lane` of key tile j from the window holding it (-1 for lanes past
+// the tile's blocks).
+__device__ __forceinline__ int32_t window_block(int32_t win, int j, int lane) {
+    const int32_t b = __shfl_sync(0xffffffffu, win, (j % kWinTiles) * kKeyBlocks + (lane & (kKeyBlocks - 1)));
+    return lane < kKeyBlocks ? b : -1;
 }
 
 // Flags a needed block whose entry is not a block of the pool (its tile is skipped) and
@@ -211,8 +235,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
     constexpr int kSoftWarps = Roles<SW>::kSoftWarps;
     constexpr int kProducerWarp = Roles<SW>::kProducerWarp;
     constexpr int kMmaWarp = Roles<SW>::kMmaWarp;
-    constexpr int kRepackWarp = Roles<SW>::kRepackWarp;
-    constexpr int TILE = L::TILE, KTILE = L::KTILE;
+    constexpr int kKWarp = Roles<SW>::kKWarp, kKWarps = Roles<SW>::kKWarps;
+    constexpr int TILE = L::TILE, KTILE = L::KTILE, KST = L::KST, VST = L::VST;
     constexpr int KSTEPS = D / 16;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -256,33 +280,298 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
     }
     const int ntiles = (nblk + kKeyBlocks - 1) / kKeyBlocks;
 
-    // the TIMEOUT bit of the flag: set when a copy wait gave up in this or an earlier call;
-    // read now, acted on (by the whole CTA) after the first barrier
+    // the TIMEOUT bit of the flag: set when a copy wait gave up in this or an earlier call
+    // (then nothing is written).  Thread 0 reads it for the softmax and MMA warps, which
+    // act on it after their setup barrier; the copy warps read it themselves.
     const uint32_t aborted_in = (threadIdx.x == 0 && p.err)
         ? (uint32_t)(*reinterpret_cast<const volatile int32_t*>(p.err) & PA_DEV_ERR_TIMEOUT) : 0u;
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sQ = sbase + L::Q, sK = sbase + L::K, sV = sbase + L::V, sCM = sbase + L::CM;
+    const uint32_t sQ = sbase + L::Q, sK = sbase + L::K, sV = sbase + L::V;
     const uint32_t bar0 = sbase + L::BAR;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
 
     if (threadIdx.x == 0) {
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(kKFull + i), 1);
+        for (int i = 0; i < KST; ++i) {
+            mbar_init(bar(kKFull + i), kKWarps);
+            mbar_init(bar(kKEmpty + i), 1);
+        }
+#pragma unroll
+        for (int i = 0; i < VST; ++i) {
             mbar_init(bar(kVFull + i), 1);
             mbar_init(bar(kVEmpty + i), 1);
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
             mbar_init(bar(kSFull + i), 1);
             mbar_init(bar(kPFull + i), 4);
             mbar_init(bar(kODone + i), 1);
         }
-        mbar_init(bar(kCmFull), kRepackWarps);
-        mbar_init(bar(kCmFree), 1);
         mbar_init(bar(kDone), 1);
         mbar_init(bar(kPVDone), 1);
         fence_proxy_async_smem();
     }
-    if (warp == kMmaWarp) tmem_alloc<kTmemCols>(sbase + L::SLOT);
+    // The copy warps start at once, without the setup barrier of the others: warp 0
+    // tells them that the mbarriers exist (and whether an earlier call gave up).
+    constexpr int kCopyThreads = 32 * (2 + kKWarps);       // warp 0 and the copy warps
+    if (warp == 0) {
+        __syncwarp();
+        named_bar_arrive(1, kCopyThreads);
+        // for the softmax and MMA warps, after their setup barrier
+        if (lane == 0) *reinterpret_cast<volatile uint32_t*>(smem + L::SLOT + 4) = aborted_in;
+    }
+    // ---- copy warps.  V: one bulk copy per (block, kv head) tile, lane b handles block b.
+    // K: the threads of the K warps copy each block tile's 16-byte pieces (piece c * 16 +
+    // slot), consecutive threads on consecutive pieces, each to its chunk-major place, one
+    // commit group per tile; a tile is published (its barrier completes) once every
+    // thread has seen its own copies land and made them visible to the tensor cores (a
+    // proxy fence in the writing thread).  Blocks past the tile's last one and entries
+    // that are not blocks of the pool (flagged) are not copied: their columns of S are
+    // masked, or the call has failed.  The copy warps start while the others set up.
+    const bool vwarp = warp == kProducerWarp, kwarp = warp >= kKWarp && warp < kKWarp + kKWarps;
+    int32_t win = -1, win_next = -1;
+    int wcur = 0, issued = 0;
+    auto block_of = [&](int j) {
+        while (j / kWinTiles > wcur) {
+            win = win_next;
+            ++wcur;
+            win_next = fetch_window(trow, wcur + 1, nblk, lane);
+        }
+        return window_block(win, j, lane);
+    };
+    auto issue_v = [&](int j, uint64_t pol) {
+        const int st = j % VST;
+        int32_t blk = block_of(j);
+        const uint32_t bytes = check_blocks(p, blk, j, nblk, lane, TILE);
+        if (lane == 0) {
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar(kVFull + st), bytes);
+        }
+        __syncwarp();
+        if (lane < kKeyBlocks && blk >= 0)
+            bulk_g2s(sV + st * KTILE + lane * TILE, p.v_pool + ((size_t)blk * p.Hkv + kvh) * (size_t)TILE,
+                     TILE, bar(kVFull + st), pol);
+        issued = j + 1;
+    };
+    auto issue_k = [&](int j, uint64_t pol) {
+        constexpr int kPer = kBlockTokens * (D / 8) / (32 * kKWarps);   // pieces per thread and block
+        const int kt = (warp - kKWarp) * 32 + lane;
+        const int st = j % KST;
+        int32_t blk = block_of(j);
+        check_blocks(p, blk, j, nblk, lane, TILE);
+        const uint32_t dst = sK + st * KTILE;
+#pragma unroll
+        for (int b = 0; b < kKeyBlocks; ++b) {
+            const int32_t bb = __shfl_sync(0xffffffffu, blk, b);
+            if (bb >= 0) {
+                const char* src = p.k_pool + ((size_t)bb * p.Hkv + kvh) * (size_t)TILE;
+#pragma unroll
+                for (int u = 0; u < kPer; ++u) {
+                    const int piece = u * 32 * kKWarps + kt;
+                    cp_async_16(dst + (piece >> 4) * (kKeyBlocks * 256) + b * 256 + (piece & 15) * 16,
+                                src + piece * 16, pol);
+                }
+            }
+        }
+        cp_async_commit();
+        issued = j + 1;
+    };
+    // before exit: every copy of the warp has landed (and every arrival it triggers)
+    auto drain = [&]() {
+        if (kwarp) {
+            cp_async_wait<0>();
+        } else if (vwarp && lane == 0) {
+            for (int jj = max(0, issued - VST); jj < issued; ++jj)
+                mbar_wait_bounded(bar(kVFull + jj % VST), (jj / VST) & 1, kWaitLimitNs);
+        }
+    };
+    // Roles.  setmaxnreg is collective over a warpgroup, so each runs at the head of its
+    // branch: the copy / MMA warpgroups hand registers to the softmax warpgroups, which
+    // take them after their setup (8 x 32 x 200 + 4 x 32 x 104 <= 384 x 168, the launch's
+    // allocation, with two Q tiles; 4 x 32 x 200 + 8 x 32 x 104 with one).
+    if (warp >= kSoftWarps) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 104;" ::: "memory");
+    if (vwarp || kwarp) {
+        // the first table windows and the flag load while warp 0 sets up the barriers (no
+        // kernel of this library writes the tables)
+        win = fetch_window(trow, 0, nblk, lane);
+        win_next = fetch_window(trow, 1, nblk, lane);
+        const bool gave_up = __shfl_sync(0xffffffffu, lane == 0 && p.err &&
+            (*reinterpret_cast<const volatile int32_t*>(p.err) & PA_DEV_ERR_TIMEOUT), 0);
+        named_bar_sync(1, kCopyThreads);
+        if (!gave_up) {
+            if (!PREFIX) grid_dependency_wait();  // the chunk's own K/V come from the append before
+            __syncwarp();
+            if (vwarp) {
+                // ---------------------------------------------------------------- V tiles
+                if (lane == 0) grid_launch_dependents();
+                const uint64_t pol = l2_policy_evict_last();   // tiles are re-read by other query tiles
+                bool ok = true;
+                for (int j = 0; j < ntiles; ++j) {
+                    if (j >= VST) {                          // PV of tile j - VST is done
+                        ok = warp_wait(bar(kVEmpty + j % VST), (j / VST - 1) & 1);
+                        if (!ok) break;
+                    }
+                    issue_v(j, pol);
+                }
+                if (!ok && lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
+                } else {
+                // ---------------------------------------------------------------- K tiles
+                // Tiles are published in order, each as soon as its copies have landed; a new
+                // tile is issued whenever its stage is free (the S MMAs of the tile KST earlier
+                // are done), tested without waiting while copies are in flight.
+                static_assert(KST <= 3, "the landing waits below cover up to two newer tiles");
+                const uint64_t pol = l2_policy_evict_last();   // tiles are re-read by other query tiles
+                auto stage_free = [&](int j) {
+                    return j < KST || __all_sync(0xffffffffu, mbar_test(bar(kKEmpty + j % KST), (j / KST - 1) & 1));
+                };
+                bool ok = true;
+                for (int pub = 0; pub < ntiles; ++pub) {
+                    // (two tiles ahead at most, so that the first is published early)
+                    while (issued < ntiles && issued - pub < 2 && stage_free(issued)) issue_k(issued, pol);
+                    if (issued == pub) {               // nothing in flight: wait for the stage
+                        ok = warp_wait(bar(kKEmpty + issued % KST), (issued / KST - 1) & 1);
+                        if (!ok) break;
+                        issue_k(issued, pol);
+                    }
+                    const int newer = issued - pub - 1;   // this thread's tiles after `pub` in flight
+                    if (newer >= 2) cp_async_wait<2>();
+                    else if (newer == 1) cp_async_wait<1>();
+                    else cp_async_wait<0>();
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(kKFull + pub % KST));
+                }
+                if (!ok && lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
+                }
+        }
+        drain();
+    } else if (warp == kMmaWarp) {
+    tmem_alloc<kTmemCols>(sbase + L::SLOT);
+    tc_fence_before();
+    named_bar_sync(2, 32 * (kSoftWarps + 1));          // Q is in place, the TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::SLOT);
+    if (*reinterpret_cast<volatile uint32_t*>(smem + L::SLOT + 4) == 0u) {   // (else write nothing)
 
+        // ---------------------------------------------------------------- MMA issue
+        // S_h(j) = Q_h K_j^T: A = Q_h (shared), B = the chunk-major K tile, N = 128 tokens.
+        // O_h += P_h(j) V_j: A = P_h(j) in TMEM (over S_h's first columns), B = one V block
+        // tile (MN-major), K = 16 tokens.  MMAs of this thread execute in issue order, so
+        // S_h(j + 1) overwrites P_h(j) only after PV_h(j) has read it, and a commit after
+        // S_h(j + 1) also covers PV_h(j).  Without a tile b its S columns are a second S
+        // buffer for tile a: S(j) goes to buffer j % 2 and S(j + 2) is issued right after
+        // PV(j), so the scores of the next tile are ready when the softmax finishes.
+        constexpr uint32_t idS = umma_idesc_bf16(128, kKeyTok, 0);
+        constexpr uint32_t idO = umma_idesc_bf16(128, D, 1);
+        bool ok = true;
+        auto issue_s = [&](int hh, int buf, int j) {
+            tc_fence_after();
+            if (lane == 0) {
+                // columns of blocks past the tile's last one hold stale products (masked)
+                const uint64_t qdesc = umma_desc(sQ + hh * L::QTILE, 2048, 128);
+                const uint64_t kdesc = umma_desc(sK + (j % KST) * KTILE, kKeyBlocks * 256, 128);
+                const uint32_t dcol = tmem + kColS + (uint32_t)(buf * kKeyTok);
+#pragma unroll
+                for (int ks = 0; ks < KSTEPS; ++ks)
+                    umma_ss(dcol, qdesc + (uint64_t)(ks * 256),
+                            kdesc + (uint64_t)((ks * 2 * kKeyBlocks * 256) >> 4), idS, ks > 0);
+                umma_commit(bar(kSFull + buf));
+            }
+            __syncwarp();
+        };
+        auto issue_pv = [&](int hh, int j, int buf) {
+            const int st = j % VST;
+            // (one Q tile: P(j) comes on barrier j % 2, as S is double-buffered -- the softmax
+            // may write P(j + 1) before this wait for P(j) begins, and a parity wait on one
+            // barrier could not tell its phase j + 2 from phase j)
+            ok = has_b ? warp_wait(bar(kPFull + hh), j & 1) : warp_wait(bar(kPFull + (j & 1)), (j >> 1) & 1);
+            if (!ok) return;
+            const int nb = min(kKeyBlocks, nblk - j * kKeyBlocks);
+            if (hh == 0) {
+                ok = warp_wait(bar(kVFull + st), (j / VST) & 1);
+                if (!ok) return;
+                if (j == ntiles - 1) {
+                    // V rows past the last attended position may hold anything (even NaN)
+                    const int first_stale = p_last - (nblk - 1) * kBlockTokens + 1;
+                    if (first_stale < kBlockTokens) {
+                        const int nst = kBlockTokens - first_stale;
+                        uint8_t* vt = smem + L::V + st * KTILE + (nb - 1) * TILE;
+                        for (int idx = lane; idx < (D / 8) * nst; idx += 32) {
+                            const int c = idx / nst, sl = first_stale + (idx - c * nst);
+                            *reinterpret_cast<uint4*>(vt + c * 256 + sl * 16) = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        fence_proxy_async_smem();
+                    }
+                    __syncwarp();
+                }
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint64_t vdesc = umma_desc(sV + st * KTILE, 128, 256);
+                const uint32_t pcol = tmem + kColS + (uint32_t)(buf * kKeyTok);
+                const uint32_t ocol = tmem + kColO + (uint32_t)(hh * kKeyTok);
+                for (int b = 0; b < nb; ++b)
+                    umma_ts(ocol, pcol + 8 * b, vdesc + (uint64_t)((b * TILE) >> 4), idO,
+                            (j > 0 || b > 0) ? 1u : 0u);
+                if (j == ntiles - 1) umma_commit(bar(kODone + hh));
+                if (hh == 1 || !has_b) umma_commit(bar(kVEmpty + st));
+                if (!has_b) umma_commit(bar(kPVDone));
+            }
+            __syncwarp();
+        };
+        auto k_ready = [&](int j) { return warp_wait(bar(kKFull + j % KST), (j / KST) & 1); };
+        auto k_free = [&](int j) {                // after the tile's last S MMA
+            if (lane == 0) umma_commit(bar(kKEmpty + j % KST));
+            __syncwarp();
+        };
+        auto next_s = [&](int j, int buf) {       // S of tile j for tile a, then free the K tile
+            ok = k_ready(j);
+            if (!ok) return;
+            issue_s(0, buf, j);
+            k_free(j);
+        };
+        if (!has_b) {
+            // one Q tile, S double-buffered: S(0) S(1) | PV(0) S(2) | PV(1) S(3) ...
+            next_s(0, 0);
+            if (ok && ntiles > 1) next_s(1, 1);
+            for (int j = 0; ok && j < ntiles; ++j) {
+                issue_pv(0, j, j & 1);
+                if (ok && j + 2 < ntiles) next_s(j + 2, j & 1);
+            }
+        } else {
+            // two Q tiles: S_a(0) S_b(0) | PV_a(0) S_a(1) PV_b(0) S_b(1) | ...
+            ok = k_ready(0);
+            if (ok) {
+                issue_s(0, 0, 0);
+                issue_s(1, 1, 0);
+                k_free(0);
+            }
+            for (int j = 0; ok && j < ntiles; ++j) {
+                const bool more = j + 1 < ntiles;
+                issue_pv(0, j, 0);
+                if (!ok) break;
+                if (more) {
+                    ok = k_ready(j + 1);
+                    if (!ok) break;
+                    issue_s(0, 0, j + 1);
+                }
+                issue_pv(1, j, 1);
+                if (!ok) break;
+                if (more) {
+                    issue_s(1, 1, j + 1);
+                    k_free(j + 1);
+                }
+            }
+        }
+        if (!ok && lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
+        // nothing may still be running on the tensor cores when TMEM is freed
+        if (lane == 0) umma_commit(bar(kDone));
+        __syncwarp();
+        mbar_wait_bounded(bar(kDone), 0, kWaitLimitNs);
+            }
+    }
+    } else {
     // rows: (chunk token, query head of this kv head), token-major; one per softmax thread
     const int row = threadIdx.x;                          // 0 .. 255 for the softmax warps
     const int h = warp >> 2;                              // Q tile of a softmax warp
@@ -332,249 +621,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         }
         fence_proxy_async_smem();
     }
-    if (threadIdx.x == 0) *reinterpret_cast<volatile uint32_t*>(smem + L::SLOT + 4) = aborted_in;
     tc_fence_before();
-    __syncthreads();
+    named_bar_sync(2, 32 * (kSoftWarps + 1));
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::SLOT);
-    if (*reinterpret_cast<volatile uint32_t*>(smem + L::SLOT + 4) != 0u) {
-        // an earlier copy wait gave up: write nothing (the whole CTA returns together)
-        if (warp == kMmaWarp) tmem_dealloc<kTmemCols>(tmem);
-        grid_dependency_wait();
-        return;
-    }
-    // Registers move from the copy / MMA warpgroup (warps 8-11) to the two softmax
-    // warpgroups: 2 x 128 x 200 + 128 x 104 = 384 x 168, the launch's allocation.  Each
-    // warpgroup adjusts at the top of its own branch, so that each branch is compiled for
-    // its own budget.
-    if (warp >= kSoftWarps) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 104;" ::: "memory");
-    if (warp == kProducerWarp) {
-        // ---------------------------------------------------------------- V tiles
-        // one bulk copy per (block, kv head) tile, lane b handles block b
-        if (!PREFIX) grid_dependency_wait();  // the chunk's own K/V come from the append before
-        __syncwarp();
-        if (lane == 0) grid_launch_dependents();
-        const uint64_t pol = l2_policy_evict_last();   // tiles are re-read by other query tiles
-        int issued = 0;
-        bool ok = true;
-        int32_t next_blk = fetch_block(trow, 0, nblk, ntiles, lane);
-        for (int j = 0; j < ntiles; ++j) {
-            const int st = j & 1;
-            int32_t blk = next_blk;
-            next_blk = fetch_block(trow, j + 1, nblk, ntiles, lane);   // in flight during the wait
-            const uint32_t bytes = check_blocks(p, blk, j, nblk, lane, TILE);
-            if (j >= 2) {
-                ok = warp_wait(bar(kVEmpty + st), ((j >> 1) - 1) & 1);
-                if (!ok) break;
-            }
-            if (lane == 0) {
-                fence_proxy_async_smem();
-                mbar_arrive_expect_tx(bar(kVFull + st), bytes);
-            }
-            __syncwarp();
-            if (lane < kKeyBlocks && blk >= 0)
-                bulk_g2s(sV + st * KTILE + lane * TILE, p.v_pool + ((size_t)blk * p.Hkv + kvh) * (size_t)TILE,
-                         TILE, bar(kVFull + st), pol);
-            issued = j + 1;
-        }
-        if (!ok && lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
-        // no copy may still be landing when the CTA exits (a stage's earlier tile
-        // completed before the stage was refilled)
-        if (lane == 0)
-            for (int jj = max(0, issued - 2); jj < issued; ++jj)
-                mbar_wait_bounded(bar(kVFull + (jj & 1)), (jj >> 1) & 1, kWaitLimitNs);
-    } else if (warp >= kRepackWarp) {
-        // ---------------------------------------------------------------- K tiles
-        // Copied in per (block, kv head) tile, [8 blocks][D/8][16 slots][16 B], then moved
-        // chunk-major, [D/8][8 blocks][16 slots][16 B]: every 8-token group of the tile is
-        // then 128 B after the previous one, so Q K^T over the tile's 128 tokens is one
-        // MMA per 16 dims.  Each (block, 8-dim chunk) run of 256 B moves whole; the two
-        // repack warps take half of the runs each, and the first also issues the copies.
-        const int rw = warp - kRepackWarp;
-        if (!PREFIX) grid_dependency_wait();
-        __syncwarp();
-        const uint64_t pol = l2_policy_evict_last();
-        int issued = 0, consumed = 0;
-        bool ok = true;
-        auto load_k = [&](int j, int32_t blk) {
-            const int st = j & 1;
-            const uint32_t bytes = check_blocks(p, blk, j, nblk, lane, TILE);
-            if (lane == 0) {
-                fence_proxy_async_smem();
-                mbar_arrive_expect_tx(bar(kKFull + st), bytes);
-            }
-            __syncwarp();
-            if (lane < kKeyBlocks && blk >= 0)
-                bulk_g2s(sK + st * KTILE + lane * TILE, p.k_pool + ((size_t)blk * p.Hkv + kvh) * (size_t)TILE,
-                         TILE, bar(kKFull + st), pol);
-            issued = j + 1;
-        };
-        if (rw == 0)
-            for (int j = 0; j < min(2, ntiles); ++j) load_k(j, fetch_block(trow, j, nblk, ntiles, lane));
-        for (int j = 0; j < ntiles; ++j) {
-            const int st = j & 1;
-            const int32_t next_blk = rw == 0 ? fetch_block(trow, j + 2, nblk, ntiles, lane) : -1;
-            ok = warp_wait(bar(kKFull + st), (j >> 1) & 1);
-            if (!ok) break;
-            consumed = j + 1;
-            if (j >= 1) {                     // the S MMAs of tile j - 1 have read the buffer
-                ok = warp_wait(bar(kCmFree), (j - 1) & 1);
-                if (!ok) break;
-            }
-            const int nb = min(kKeyBlocks, nblk - j * kKeyBlocks);
-            const uint8_t* src = smem + L::K + st * KTILE;
-            uint8_t* dst = smem + L::CM;
-            const int piece = (lane & 15) * 16;
-            // a batch of loads in flight before their stores (a store could alias a later
-            // load, so the compiler would otherwise keep each load behind the previous store)
-            constexpr int kRuns = kKeyBlocks * (D / 8);
-            constexpr int kPerLane = kRuns / (2 * kRepackWarps);
-            static_assert(kPerLane % kRepackBatch == 0, "repack batch must divide a lane's runs");
-            const int r0 = rw * (kRuns / kRepackWarps) + (lane >> 4);
-#pragma unroll 1
-            for (int u0 = 0; u0 < kPerLane; u0 += kRepackBatch) {
-                uint4 v[kRepackBatch];
-#pragma unroll
-                for (int u = 0; u < kRepackBatch; ++u) {
-                    const int r = r0 + 2 * (u0 + u);
-                    const int b = r / (D / 8), c = r % (D / 8);
-                    if (b < nb) v[u] = *reinterpret_cast<const uint4*>(src + b * TILE + c * 256 + piece);
-                }
-#pragma unroll
-                for (int u = 0; u < kRepackBatch; ++u) {
-                    const int r = r0 + 2 * (u0 + u);
-                    const int b = r / (D / 8), c = r % (D / 8);
-                    if (b < nb) *reinterpret_cast<uint4*>(dst + c * (kKeyBlocks * 256) + b * 256 + piece) = v[u];
-                }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kCmFull));
-            if (rw == 0 && j + 2 < ntiles) {
-                // both warps are done with the copy stage: fetch tile j + 2 into it
-                ok = warp_wait(bar(kCmFull), j & 1);
-                if (!ok) break;
-                load_k(j + 2, next_blk);
-            }
-        }
-        if (!ok && lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
-        if (lane == 0)
-            for (int jj = consumed; jj < issued; ++jj)
-                mbar_wait_bounded(bar(kKFull + (jj & 1)), (jj >> 1) & 1, kWaitLimitNs);
-    } else if (warp == kMmaWarp) {
-        // ---------------------------------------------------------------- MMA issue
-        // S_h(j) = Q_h K_j^T: A = Q_h (shared), B = the chunk-major K tile, N = 128 tokens.
-        // O_h += P_h(j) V_j: A = P_h(j) in TMEM (over S_h's first columns), B = one V block
-        // tile (MN-major), K = 16 tokens.  MMAs of this thread execute in issue order, so
-        // S_h(j + 1) overwrites P_h(j) only after PV_h(j) has read it, and a commit after
-        // S_h(j + 1) also covers PV_h(j).  Without a tile b its S columns are a second S
-        // buffer for tile a: S(j) goes to buffer j % 2 and S(j + 2) is issued right after
-        // PV(j), so the scores of the next tile are ready when the softmax finishes.
-        constexpr uint32_t idS = umma_idesc_bf16(128, kKeyTok, 0);
-        constexpr uint32_t idO = umma_idesc_bf16(128, D, 1);
-        const uint64_t kdesc = umma_desc(sCM, kKeyBlocks * 256, 128);
-        bool ok = true;
-        auto issue_s = [&](int hh, int buf) {
-            tc_fence_after();
-            if (lane == 0) {
-                // columns of blocks past the tile's last one hold stale products (masked)
-                const uint64_t qdesc = umma_desc(sQ + hh * L::QTILE, 2048, 128);
-                const uint32_t dcol = tmem + kColS + (uint32_t)(buf * kKeyTok);
-#pragma unroll
-                for (int ks = 0; ks < KSTEPS; ++ks)
-                    umma_ss(dcol, qdesc + (uint64_t)(ks * 256),
-                            kdesc + (uint64_t)((ks * 2 * kKeyBlocks * 256) >> 4), idS, ks > 0);
-                umma_commit(bar(kSFull + buf));
-            }
-            __syncwarp();
-        };
-        auto issue_pv = [&](int hh, int j, int buf) {
-            const int st = j & 1;
-            ok = warp_wait(bar(kPFull + hh), j & 1);
-            if (!ok) return;
-            const int nb = min(kKeyBlocks, nblk - j * kKeyBlocks);
-            if (hh == 0) {
-                ok = warp_wait(bar(kVFull + st), (j >> 1) & 1);
-                if (!ok) return;
-                if (j == ntiles - 1) {
-                    // V rows past the last attended position may hold anything (even NaN)
-                    const int first_stale = p_last - (nblk - 1) * kBlockTokens + 1;
-                    if (first_stale < kBlockTokens) {
-                        const int nst = kBlockTokens - first_stale;
-                        uint8_t* vt = smem + L::V + st * KTILE + (nb - 1) * TILE;
-                        for (int idx = lane; idx < (D / 8) * nst; idx += 32) {
-                            const int c = idx / nst, sl = first_stale + (idx - c * nst);
-                            *reinterpret_cast<uint4*>(vt + c * 256 + sl * 16) = make_uint4(0u, 0u, 0u, 0u);
-                        }
-                        fence_proxy_async_smem();
-                    }
-                    __syncwarp();
-                }
-            }
-            tc_fence_after();
-            if (lane == 0) {
-                const uint64_t vdesc = umma_desc(sV + st * KTILE, 128, 256);
-                const uint32_t pcol = tmem + kColS + (uint32_t)(buf * kKeyTok);
-                const uint32_t ocol = tmem + kColO + (uint32_t)(hh * kKeyTok);
-                for (int b = 0; b < nb; ++b)
-                    umma_ts(ocol, pcol + 8 * b, vdesc + (uint64_t)((b * TILE) >> 4), idO,
-                            (j > 0 || b > 0) ? 1u : 0u);
-                if (j == ntiles - 1) umma_commit(bar(kODone + hh));
-                if (hh == 1 || !has_b) umma_commit(bar(kVEmpty + st));
-                if (!has_b) umma_commit(bar(kPVDone));
-            }
-            __syncwarp();
-        };
-        auto next_s = [&](int j, int buf) {       // S of tile j for tile a, then free the K tile
-            ok = warp_wait(bar(kCmFull), j & 1);
-            if (!ok) return;
-            issue_s(0, buf);
-            if (lane == 0) umma_commit(bar(kCmFree));
-            __syncwarp();
-        };
-        if (!has_b) {
-            // one Q tile, S double-buffered: S(0) S(1) | PV(0) S(2) | PV(1) S(3) ...
-            next_s(0, 0);
-            if (ok && ntiles > 1) next_s(1, 1);
-            for (int j = 0; ok && j < ntiles; ++j) {
-                issue_pv(0, j, j & 1);
-                if (ok && j + 2 < ntiles) next_s(j + 2, j & 1);
-            }
-        } else {
-            // two Q tiles: S_a(0) S_b(0) | PV_a(0) S_a(1) PV_b(0) S_b(1) | ...
-            ok = warp_wait(bar(kCmFull), 0);
-            if (ok) {
-                issue_s(0, 0);
-                issue_s(1, 1);
-                if (lane == 0) umma_commit(bar(kCmFree));
-                __syncwarp();
-            }
-            for (int j = 0; ok && j < ntiles; ++j) {
-                const bool more = j + 1 < ntiles;
-                issue_pv(0, j, 0);
-                if (!ok) break;
-                if (more) {
-                    ok = warp_wait(bar(kCmFull), (j + 1) & 1);
-                    if (!ok) break;
-                    issue_s(0, 0);
-                }
-                issue_pv(1, j, 1);
-                if (!ok) break;
-                if (more) {
-                    issue_s(1, 1);
-                    if (lane == 0) umma_commit(bar(kCmFree));
-                    __syncwarp();
-                }
-            }
-        }
-        if (!ok && lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
-        // nothing may still be running on the tensor cores when TMEM is freed
-        if (lane == 0) umma_commit(bar(kDone));
-        __syncwarp();
-        mbar_wait_bounded(bar(kDone), 0, kWaitLimitNs);
-    }
-    } else {
+    if (*reinterpret_cast<volatile uint32_t*>(smem + L::SLOT + 4) == 0u) {   // (else write nothing)
+    // (every warp of both softmax warpgroups, at this one instruction)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 200;" ::: "memory");
     if (h == 0 || has_b) {
         // ---------------------------------------------------------------- softmax rows
@@ -694,24 +746,44 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kPFull + h));
+            if (lane == 0) mbar_arrive(bar(kPFull + (has_b ? h : (j & 1))));
         }
         if (ok) ok = warp_wait(bar(kODone + h), 0);
         if (ok && PREFIX) {
             tc_fence_after();
+            // Each 32-column piece of the warp's 32 rows passes through shared memory (the K
+            // stages: every MMA has completed), 16-byte units of row r at unit u ^ (r % 8),
+            // so that both the writes and the reads are free of bank conflicts and each
+            // global store covers 128 contiguous bytes of four rows (a thread storing its
+            // own row scatters 16-byte pieces over 32 rows per instruction).
             const size_t slot = orow * p.part_stride + (size_t)blockIdx.z * p.slot_mult;
-            float4* po = reinterpret_cast<float4*>(p.part_o + slot * D);
+            const uint32_t stg = sK + (uint32_t)warp * (32 * 128);
+            const uint32_t valid = __ballot_sync(0xffffffffu, row_valid);
+            const int sub = lane >> 3, unit = lane & 7;       // row 4 i + sub, unit `unit`
+            float* dst[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const unsigned long long a = __shfl_sync(0xffffffffu, (unsigned long long)(p.part_o + slot * D), 4 * i + sub);
+                dst[i] = reinterpret_cast<float*>(a) + unit * 4;
+            }
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
                 tmem_ld32(tl_addr + ocol + 32 * c, o);
                 tmem_wait_ld();
-                if (row_valid) {
 #pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        po[8 * c + v] = make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
-                                                    __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
+                for (int u = 0; u < 8; ++u)
+                    st_shared_v4(stg + lane * 128 + ((u ^ (lane & 7)) * 16),
+                                 make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]));
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int r = 4 * i + sub;
+                    const uint4 v = ld_shared_v4(stg + r * 128 + ((unit ^ (r & 7)) * 16));
+                    if ((valid >> r) & 1u)
+                        *reinterpret_cast<uint4*>(dst[i] + 32 * c) = v;
                 }
+                __syncwarp();
             }
             if (row_valid) {
                 p.part_ml[slot] = make_float2(m_used, l);
@@ -753,12 +825,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
             }
         }
     }
+            }
     }
+
     tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc<kTmemCols>(tmem);
+        tmem_dealloc<kTmemCols>(*reinterpret_cast<volatile uint32_t*>(smem + L::SLOT));
     }
     // (prefix mode: every thread has waited for the previous grid; this is a no-op then)
     if (PREFIX) grid_dependency_wait();
