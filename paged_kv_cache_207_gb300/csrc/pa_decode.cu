@@ -52,6 +52,7 @@ struct KParams {
     int grid_parts;     // partitions covered per (sequence, kv head): first_part + launched
     int part_stride;
     int first_part;     // partitions below this are a shared prefix done by the prefix kernel
+    int prefix_stride;  // ... which wrote a partial into every prefix_stride-th of their slots
     int part_blocks;    // blocks per split-KV partition (a fixed constant of each path)
     float scale_log2;   // scale * log2(e): scores live in log2 units
     // shared-prefix suffix kernel launched after the prefix kernel, which starts it only
@@ -1168,6 +1169,11 @@ decode_reduce_kernel(const KParams p, int num_rows) {
     // after a copy wait gave up (this call or an earlier one) the partials are not all
     // written: leave `out` untouched, as the main kernel does
     const bool work = live && n >= min_n && !aborted(p.err);
+    // the row's partials: with a shared prefix, one per prefix_stride prefix slots, then
+    // one per suffix partition (slots first_part ..); without, slots 0 .. n - 1
+    const int np = p.first_part / p.prefix_stride;
+    const int nm = min(np, n) + max(n - p.first_part, 0);    // partials to merge
+    auto slot = [&](int i) { return i < np ? i * p.prefix_stride : p.first_part + (i - np); };
     const size_t prow = (size_t)(work ? row : 0) * p.part_stride;
     const float2* ml = p.part_ml + prow;
     const float* po = p.part_o + prow * D + lane * DPL;
@@ -1180,17 +1186,18 @@ decode_reduce_kernel(const KParams p, int num_rows) {
         // kChunk partial rows are loaded together, so the merge takes one round trip
         constexpr int kChunk = 8;
         float2 mlv = make_float2(-INFINITY, 0.f);
-        if (work && lane < n) mlv = ml[lane];
+        if (work && lane < nm) mlv = ml[slot(lane)];
         float ov[kChunk][DPL];
 #pragma unroll
         for (int i = 0; i < kChunk; ++i) {
-            const bool has = work && i < n;
+            const bool has = work && i < nm;
+            const size_t off = (size_t)slot(i) * D;
             if constexpr (DPL == 4) {
-                const float4 o = has ? *reinterpret_cast<const float4*>(po + (size_t)i * D)
+                const float4 o = has ? *reinterpret_cast<const float4*>(po + off)
                                      : make_float4(0.f, 0.f, 0.f, 0.f);
                 ov[i][0] = o.x; ov[i][1] = o.y; ov[i][2] = o.z; ov[i][3] = o.w;
             } else {
-                const float2 o = has ? *reinterpret_cast<const float2*>(po + (size_t)i * D)
+                const float2 o = has ? *reinterpret_cast<const float2*>(po + off)
                                      : make_float2(0.f, 0.f);
                 ov[i][0] = o.x; ov[i][1] = o.y;
             }
@@ -1199,48 +1206,47 @@ decode_reduce_kernel(const KParams p, int num_rows) {
 #pragma unroll
         for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
         if (work && M != -INFINITY) {
-            // partitions in order 0, 1, ...: the sum's order is fixed
-            // an empty partition (maximum -inf: a slot a longer prefix partition left unused)
-            // is skipped, whatever its partial holds
+            // partials in order 0, 1, ...: the sum's order is fixed; one whose maximum is
+            // -inf (no key) is skipped, whatever its row holds
 #pragma unroll
             for (int i = 0; i < kChunk; ++i) {
                 const float mi = __shfl_sync(0xffffffffu, mlv.x, i);
                 const float li = __shfl_sync(0xffffffffu, mlv.y, i);
-                if (i < n && mi != -INFINITY) {
+                if (i < nm && mi != -INFINITY) {
                     const float wt = fast_exp2(mi - M);
                     lsum += wt * li;
 #pragma unroll
                     for (int k = 0; k < DPL; ++k) acc[k] += wt * ov[i][k];
                 }
             }
-            for (int i = kChunk; i < n; ++i) {
+            for (int i = kChunk; i < nm; ++i) {
                 const float mi = __shfl_sync(0xffffffffu, mlv.x, i);
                 const float li = __shfl_sync(0xffffffffu, mlv.y, i);
                 if (mi == -INFINITY) continue;
                 const float wt = fast_exp2(mi - M);
                 lsum += wt * li;
 #pragma unroll
-                for (int k = 0; k < DPL; ++k) acc[k] += wt * po[(size_t)i * D + k];
+                for (int k = 0; k < DPL; ++k) acc[k] += wt * po[(size_t)slot(i) * D + k];
             }
         }
     } else {
     float M = -INFINITY;
     if (work)
-        for (int i = lane; i < n; i += 32) M = fmaxf(M, ml[i].x);
+        for (int i = lane; i < nm; i += 32) M = fmaxf(M, ml[slot(i)].x);
 #pragma unroll
     for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
     if (work && M != -INFINITY) {
 #pragma unroll 8
-        for (int i = wr; i < n; i += WPR) {
-            const float2 v = ml[i];
-            if (v.x == -INFINITY) continue;               // an empty partition
+        for (int i = wr; i < nm; i += WPR) {
+            const float2 v = ml[slot(i)];
+            if (v.x == -INFINITY) continue;               // no key
             const float wt = fast_exp2(v.x - M);
             lsum += wt * v.y;
             if constexpr (DPL == 4) {
-                const float4 o = *reinterpret_cast<const float4*>(po + (size_t)i * D);
+                const float4 o = *reinterpret_cast<const float4*>(po + (size_t)slot(i) * D);
                 acc[0] += wt * o.x; acc[1] += wt * o.y; acc[2] += wt * o.z; acc[3] += wt * o.w;
             } else {
-                const float2 o = *reinterpret_cast<const float2*>(po + (size_t)i * D);
+                const float2 o = *reinterpret_cast<const float2*>(po + (size_t)slot(i) * D);
                 acc[0] += wt * o.x; acc[1] += wt * o.y;
             }
         }
@@ -1516,6 +1522,7 @@ KParams make_params(const DecodeArgs& a) {
     kp.grid_parts = a.grid_parts;
     kp.part_stride = a.part_stride;
     kp.first_part = a.first_part;
+    kp.prefix_stride = a.first_part > 0 ? prefix_slot_mult(a.first_part) : 1;
     kp.part_blocks = a.part_blocks;
     kp.scale_log2 = a.scale * kLog2e;
     kp.after_prefix = 0;

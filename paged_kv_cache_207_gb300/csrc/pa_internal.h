@@ -59,6 +59,17 @@ inline int decode_part_blocks(int head_dim) {
     return head_dim == 64 ? PA_D64_PARTITION_BLOCKS : kPartBlocks;
 }
 
+// Shared-prefix decode: one prefix CTA covers this many decode partitions (its keys are
+// that many times a partition's) when the prefix is a whole number of such groups, else
+// one.  Its partial goes to the first workspace slot of the group; the merge reads only
+// those slots of the prefix.
+#ifndef PA_PREFIX_PART_MULT
+#define PA_PREFIX_PART_MULT 2
+#endif
+inline int prefix_slot_mult(int first_part) {
+    return first_part % PA_PREFIX_PART_MULT == 0 ? PA_PREFIX_PART_MULT : 1;
+}
+
 // Blocks per split-KV partition of the FP8 path: its tiles are half the bytes of
 // bf16 ones, so a partition covers twice the tokens for the same bytes per CTA.
 #ifndef PA_FP8_PARTITION_BLOCKS

@@ -52,8 +52,8 @@ struct PParams {
     // kernel first and the suffix kernel after it)
     int wait_first;
     // prefix mode: a CTA covers slot_mult split-KV partitions of the decode (part_blocks is
-    // slot_mult times the decode's); it writes its partial into the first of those workspace
-    // slots and an empty one -- maximum -inf, sum 0 -- into the others
+    // slot_mult times the decode's) and writes its partial into the first of their
+    // workspace slots
     int slot_mult;
 };
 
@@ -785,10 +785,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
                 }
                 __syncwarp();
             }
-            if (row_valid) {
-                p.part_ml[slot] = make_float2(m_used, l);
-                for (int e = 1; e < p.slot_mult; ++e) p.part_ml[slot + e] = make_float2(-INFINITY, 0.f);
-            }
+            if (row_valid) p.part_ml[slot] = make_float2(m_used, l);
         } else if (ok) {
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -918,13 +915,10 @@ cudaError_t launch_prefix_tc(const DecodeArgs& a, bool after_suffix, cudaStream_
     pp.part_stride = a.part_stride;
     pp.num_seqs = a.num_seqs;
     pp.wait_first = after_suffix ? 0 : 1;
-    // Prefix CTAs take an SM each; when the prefix is a whole number of such pairs, one CTA
-    // covers PA_PREFIX_PART_MULT decode partitions: fewer CTAs, each longer, which leaves SMs
-    // to the suffix decode running beside them and cuts the partials the merge reads.
-#ifndef PA_PREFIX_PART_MULT
-#define PA_PREFIX_PART_MULT 2
-#endif
-    pp.slot_mult = a.first_part % PA_PREFIX_PART_MULT == 0 ? PA_PREFIX_PART_MULT : 1;
+    // Prefix CTAs take an SM each; one covers several decode partitions: fewer CTAs, each
+    // longer, which leaves SMs to the suffix decode running beside them and cuts the
+    // partials the merge reads.
+    pp.slot_mult = prefix_slot_mult(a.first_part);
     pp.part_blocks = a.part_blocks * pp.slot_mult;
     const int pre_parts = a.first_part / pp.slot_mult;
     // 256 rows (two Q tiles) per CTA when that still gives every SM a CTA, else 128
