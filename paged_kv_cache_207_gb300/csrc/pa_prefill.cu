@@ -199,15 +199,15 @@ __device__ __forceinline__ uint64_t fadd_f32x2(uint64_t a, uint64_t b) {
 // lane (-1 past the CTA's last block), a window ahead of its use: read one tile ahead,
 // every tile would wait for a dependent load (over a microsecond when HBM is busy).
 constexpr int kWinTiles = 32 / kKeyBlocks;
-__device__ __forceinline__ int32_t fetch_window(const int32_t* trow, int w, int nblk, int lane) {
+__device__ __forceinline__ int32_t fetch_window(const int32_t* trow, int w, int lim, int lane) {
     const int b = 32 * w + lane;
-    return b < nblk ? __ldg(trow + b) : -1;
+    return b < lim ? __ldg(trow + b) : -1;
 }
 // Table entry of block `lane` of key tile j from the window holding it (-1 for lanes past
-// the tile's blocks).
-__device__ __forceinline__ int32_t window_block(int32_t win, int j, int lane) {
+// the tile's blocks or the CTA's last block).
+__device__ __forceinline__ int32_t window_block(int32_t win, int j, int lane, int nblk) {
     const int32_t b = __shfl_sync(0xffffffffu, win, (j % kWinTiles) * kKeyBlocks + (lane & (kKeyBlocks - 1)));
-    return lane < kKeyBlocks ? b : -1;
+    return (lane < kKeyBlocks && j * kKeyBlocks + lane < nblk) ? b : -1;
 }
 
 // Flags a needed block whose entry is not a block of the pool (its tile is skipped) and
@@ -243,20 +243,37 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
     const int kvh = blockIdx.y;
     if (PREFIX && p.wait_first) grid_dependency_wait();
     int q0 = 0, n = 0, i0 = 0, start = 0, p_last, nblk, row_base = 0, rows_total = 0;
-    const int32_t* trow;
     bool has_b;
+    const int32_t* trow = PREFIX ? p.tables + (size_t)blockIdx.z * p.part_blocks
+                                 : p.tables + (size_t)blockIdx.z * p.max_blocks;
+    // The copy warps' first table windows load at once, bounded by the table row (the
+    // CTA's own last block is known one round trip later; no kernel of this library writes
+    // the tables).
+    // The TIMEOUT bit of the flag: set when a copy wait gave up in this or an earlier call
+    // (then nothing is written).  Thread 0 reads it for the softmax and MMA warps, which
+    // act on it after their setup barrier; the copy warps read it themselves.
+    int32_t win = -1, win_next = -1, flag_in = 0;
+    if (warp == kProducerWarp || (warp >= kKWarp && warp < kKWarp + kKWarps)) {
+        const int lim = PREFIX ? p.part_blocks : p.max_blocks;
+        win = fetch_window(trow, 0, lim, lane);
+        win_next = fetch_window(trow, 1, lim, lane);
+        if (lane == 0 && p.err) flag_in = *reinterpret_cast<const volatile int32_t*>(p.err);
+    }
+    if (threadIdx.x == 0 && p.err) flag_in = *reinterpret_cast<const volatile int32_t*>(p.err);
     if constexpr (PREFIX) {
         rows_total = p.num_seqs * p.G;
         row_base = blockIdx.x * p.rows_per_cta;
         nblk = p.part_blocks;
         p_last = nblk * kBlockTokens - 1;                 // positions relative to the partition
-        trow = p.tables + (size_t)blockIdx.z * p.part_blocks;
         has_b = SW == 2 && p.rows_per_cta > kHalfRows && row_base + kHalfRows < rows_total;
     } else {
         const int qt = gridDim.x - 1 - blockIdx.x;        // later (longer) tiles first
         const int s = blockIdx.z;
+        // the chunk's place: three loads in flight together
         q0 = __ldg(p.cu_q + s);
-        n = __ldg(p.cu_q + s + 1) - q0;
+        n = __ldg(p.cu_q + s + 1);
+        start = __ldg(p.start_pos + s);
+        n -= q0;
         i0 = qt * p.TQ;
         // (a CTA that exits early still waits for the previous grid: a dependent grid never
         // completes before the one it follows)
@@ -264,7 +281,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
             grid_dependency_wait();
             return;
         }
-        start = __ldg(p.start_pos + s);
         const int i_end = min(n, i0 + p.TQ);
         p_last = start + i_end - 1;                       // last position this CTA attends to
         if (start < 0 || p_last >= p.max_blocks * kBlockTokens) {
@@ -273,18 +289,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
             return;
         }
         nblk = p_last / kBlockTokens + 1;
-        trow = p.tables + (size_t)s * p.max_blocks;
         // tile b holds rows 128 .. 255; it is skipped when none of them is a chunk row
         const int tl_b = kHalfRows / p.G;
         has_b = SW == 2 && tl_b < p.TQ && i0 + tl_b < n;
     }
     const int ntiles = (nblk + kKeyBlocks - 1) / kKeyBlocks;
 
-    // the TIMEOUT bit of the flag: set when a copy wait gave up in this or an earlier call
-    // (then nothing is written).  Thread 0 reads it for the softmax and MMA warps, which
-    // act on it after their setup barrier; the copy warps read it themselves.
-    const uint32_t aborted_in = (threadIdx.x == 0 && p.err)
-        ? (uint32_t)(*reinterpret_cast<const volatile int32_t*>(p.err) & PA_DEV_ERR_TIMEOUT) : 0u;
+    const uint32_t aborted_in = (uint32_t)(flag_in & PA_DEV_ERR_TIMEOUT);   // (thread 0)
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sQ = sbase + L::Q, sK = sbase + L::K, sV = sbase + L::V;
     const uint32_t bar0 = sbase + L::BAR;
@@ -329,7 +340,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
     // that are not blocks of the pool (flagged) are not copied: their columns of S are
     // masked, or the call has failed.  The copy warps start while the others set up.
     const bool vwarp = warp == kProducerWarp, kwarp = warp >= kKWarp && warp < kKWarp + kKWarps;
-    int32_t win = -1, win_next = -1;
     int wcur = 0, issued = 0;
     auto block_of = [&](int j) {
         while (j / kWinTiles > wcur) {
@@ -337,7 +347,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
             ++wcur;
             win_next = fetch_window(trow, wcur + 1, nblk, lane);
         }
-        return window_block(win, j, lane);
+        return window_block(win, j, lane, nblk);
     };
     auto issue_v = [&](int j, uint64_t pol) {
         const int st = j % VST;
@@ -392,12 +402,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
     if (warp >= kSoftWarps) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 104;" ::: "memory");
     if (vwarp || kwarp) {
-        // the first table windows and the flag load while warp 0 sets up the barriers (no
-        // kernel of this library writes the tables)
-        win = fetch_window(trow, 0, nblk, lane);
-        win_next = fetch_window(trow, 1, nblk, lane);
-        const bool gave_up = __shfl_sync(0xffffffffu, lane == 0 && p.err &&
-            (*reinterpret_cast<const volatile int32_t*>(p.err) & PA_DEV_ERR_TIMEOUT), 0);
+        const bool gave_up = __shfl_sync(0xffffffffu, flag_in & PA_DEV_ERR_TIMEOUT, 0) != 0;
         named_bar_sync(1, kCopyThreads);
         if (!gave_up) {
             if (!PREFIX) grid_dependency_wait();  // the chunk's own K/V come from the append before
@@ -427,8 +432,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
                 };
                 bool ok = true;
                 for (int pub = 0; pub < ntiles; ++pub) {
-                    // (two tiles ahead at most, so that the first is published early)
-                    while (issued < ntiles && issued - pub < 2 && stage_free(issued)) issue_k(issued, pol);
+                    // (two tiles ahead at most; the first alone, as the first scores wait for it)
+                    while (issued < ntiles && issued - pub < (pub == 0 ? 1 : 2) && stage_free(issued))
+                        issue_k(issued, pol);
                     if (issued == pub) {               // nothing in flight: wait for the stage
                         ok = warp_wait(bar(kKEmpty + issued % KST), (issued / KST - 1) & 1);
                         if (!ok) break;
@@ -599,10 +605,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         // a negative scale is applied as |scale| to -q (exact), so that the softmax can
         // take the row maximum of the unscaled scores
         const uint32_t flip = p.scale_log2 < 0.f ? 0x80008000u : 0u;
-        // loads in flight together, then the stores: the whole row in the short prefix
-        // CTAs (one round trip on their critical path), half of it in the prefill, whose
-        // register budget here is tighter
-        constexpr int QB = PREFIX ? D / 8 : D / 16;
+        // the whole row's loads in flight together, then the stores: one round trip on the
+        // critical path of the CTA's first scores
+        constexpr int QB = D / 8;
 #pragma unroll
         for (int k0 = 0; k0 < D / 8; k0 += QB) {
             uint4 qv[QB];
