@@ -165,3 +165,59 @@ def test_repeated_prefill_calls_give_the_same_bits():
         torch.cuda.synchronize()
         assert torch.equal(again, out)
     assert int(dp.err.item()) == 0
+
+
+def test_prefill_step_loop_full_size_stays_exact():
+    # The prefill workload of the benchmark (16 sequences, 512-token chunks at starts up to
+    # 3584), run as a step loop: append the chunk, then prefill, back to back with no
+    # synchronisation, alternating two copies of the pools.  A wait that gives up (TIMEOUT)
+    # or an ordering slip between the kernel's warp roles would show as a flag or as bits
+    # that differ from the first step's.
+    rng = np.random.default_rng(213)
+    S, n = 16, 512
+    starts = rng.integers(0, 3585, size=S)
+    wl = W.make_decode_workload("prefill_loop", context_lens=starts + n - 1, num_q_heads=32,
+                                num_kv_heads=8, head_dim=128, dtype="bf16", seed=213,
+                                device="cuda")
+    shape = pk.pool_shape(wl.num_blocks, 8, 128, torch.bfloat16)
+    kp = torch.zeros(shape, dtype=torch.bfloat16, device="cuda")
+    vp = torch.zeros_like(kp)
+    tables = torch.from_numpy(wl.block_tables).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rows = [torch.from_numpy(wl.logical_rows(s)) for s in range(S)]
+    ctx = torch.cat([r[:int(st)] for r, st in zip(rows, starts)]).cuda()
+    chunk = torch.cat([r[int(st):int(st) + n] for r, st in zip(rows, starts)]).cuda()
+    cu_ctx = torch.tensor(np.concatenate([[0], np.cumsum(starts)]), dtype=torch.int32, device="cuda")
+    pk.append_kv(kp, vp, wl.k_rows[ctx].contiguous(), wl.v_rows[ctx].contiguous(), tables,
+                 torch.zeros(S, dtype=torch.int32, device="cuda"), cu_ctx, err_flag=err)
+    k_chunk, v_chunk = wl.k_rows[chunk].contiguous(), wl.v_rows[chunk].contiguous()
+    pools = [(kp, vp), (kp.clone(), vp.clone())]
+    g = torch.Generator(device="cuda").manual_seed(7)
+    q = torch.randn(S * n, 32, 128, generator=g, device="cuda").to(torch.bfloat16)
+    start_t = torch.from_numpy(starts.astype(np.int32)).cuda()
+    cu_q = torch.arange(0, S * n + 1, n, dtype=torch.int32, device="cuda")
+    outs = [torch.empty_like(q) for _ in range(2)]
+    first = None
+    for rep in range(4):
+        for i in range(10):
+            kpp, vpp = pools[i % 2]
+            pk.append_kv(kpp, vpp, k_chunk, v_chunk, tables, start_t, cu_q, err_flag=err)
+            pk.prefill_attention(outs[i % 2], q, kpp, vpp, tables, start_t, cu_q, wl.scale,
+                                 max_chunk=n, err_flag=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0, (rep, int(err.item()))
+        if first is None:
+            first = outs[0].clone()
+        assert torch.equal(outs[0], first) and torch.equal(outs[1], first), rep
+    # one sampled row per sequence against the oracle (the full-size parity lives elsewhere)
+    s = int(np.argmax(starts))
+    base = s * n
+    p = int(starts[s]) + n - 1
+    K = wl.k_rows[rows[s][:p + 1].cuda()].cpu().contiguous()
+    V = wl.v_rows[rows[s][:p + 1].cuda()].cpu().contiguous()
+    qc = q.cpu()
+    for h in (0, 13, 31):
+        want = orc.decode_contig(qc[base + n - 1, h], K, V, h // 4, num_kv_heads=8, head_dim=128,
+                                 scale=wl.scale, dtype=orc.BF16)
+        got = first[base + n - 1, h].float().cpu().double().numpy()
+        assert np.abs(got - want).max() <= BF16_ATOL
