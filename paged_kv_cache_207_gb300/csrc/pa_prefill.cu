@@ -70,15 +70,15 @@ __device__ __forceinline__ void raise_flag(int32_t* err, int bits) {
 // moves registers from the copy / MMA warps (104 each) to the softmax warps (200 each),
 // which hold a 128-column row of S.  setmaxnreg is collective over a warpgroup: every
 // warp of a warpgroup runs the same one, so the copy / MMA warps fill whole warpgroups
-// (idle warps pad them) and lower their budget together at the start.
+// (idle warps pad them) and lower their budget together, at the head of their branch.
 // A K tile lands chunk-major, [D/8][8 blocks][16 slots][16 B]: every 8-token group
 // of the tile is 128 B after the previous one, so Q K^T over the tile's 128 tokens is
 // one MMA per 16 dims.  The pool holds a block as [D/8][16 slots][16 B], so each
 // 16-byte piece has its own place in the stage.  K comes through the load/store path
 // and V through the bulk-copy engine: an SM takes in more from DRAM through both than
 // through either (measured on GB300 with 64 busy SMs: 4 KB bulk copies alone about
-// 77 GB/s per SM, both about 97 GB/s), and bulk copies of the 256-byte pieces would
-// be far slower (about 64 cycles per copy).
+// 77 GB/s per SM, both about 97 GB/s), and small bulk copies are slow (1 KB ones: about
+// 33 GB/s per SM), so the 256-byte pieces are not placed that way.
 // Each softmax thread reads its row of S_h from TMEM, applies the causal mask,
 // keeps a running maximum that is raised only when a tile exceeds it by more than
 // 2^8 (O_h is then rescaled in TMEM), writes its bf16 probabilities over the
