@@ -8,18 +8,23 @@
 // must see the explicit positions, not an inferred length of zero; chunked
 // prefill is one of the engine parts Slipstream lists in "Horizon").
 //
-// Work split: CTA = (query tile, kv head, sequence).  Rows are (chunk token,
-// query head of the kv head) pairs, token-major, 256 / G tokens per CTA, in two
-// Q tiles of 128 rows that share every K/V tile.  The 5th-generation tensor cores
-// (tcgen05) compute, per key tile of 128 tokens (8 blocks) and Q tile h,
+// Work split: an item = (query tile, kv head, sequence).  Rows are (chunk token,
+// query head of the kv head) pairs, token-major, 256 / G tokens per item, in two
+// Q tiles of 128 rows that share every K/V tile.  The grid is persistent, one CTA
+// per SM; each CTA sorts the items by their key tiles (the same way in every CTA)
+// and takes its share of them, dealt out largest first, and while one item ends
+// it already loads the next one's query rows and K/V tiles.  The 5th-generation
+// tensor cores (tcgen05) compute, per key tile of 128 tokens (8 blocks) and Q tile h,
 //   S_h = Q_h K^T   into TMEM (one M128 N128 K16 MMA per 16 dims),
 //   O_h += P_h V    into TMEM (one M128 N=D K16 MMA per block, P_h from TMEM),
 // one thread issuing every MMA; the softmax runs one row per thread of eight
 // warps (a warpgroup per Q tile), with the causal mask applied per row.
-// Later query tiles (which read more blocks) are scheduled first.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+#include <climits>
 #include <cmath>
+#include <cstdint>
 
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
@@ -55,6 +60,8 @@ struct PParams {
     // slot_mult times the decode's) and writes its partial into the first of their
     // workspace slots
     int slot_mult;
+    // prefill: query tiles per chunk (of TQ tokens) and work items (nqt x Hkv x num_seqs)
+    int nqt, num_items;
 };
 
 __device__ __forceinline__ void raise_flag(int32_t* err, int bits) {
@@ -85,7 +92,10 @@ __device__ __forceinline__ void raise_flag(int32_t* err, int bits) {
 // first half of S_h's columns, and at the end reads its row of O_h, divides by
 // the row sum and stores it (the prefix mode stores the unnormalised partial and
 // its maximum and sum instead).  A CTA with a single Q tile uses tile b's S
-// columns as a second S buffer for tile a.
+// columns as a second S buffer for tile a.  (Scores in 64-key halves, double-buffered
+// per Q tile in the same TMEM columns, were measured slower: an M128 N64 MMA takes
+// about as long as an M128 N128 one, 33-36 ns on GB300, so the halves double the cost
+// of Q K^T.)
 // ============================================================================
 
 namespace tc {
@@ -137,16 +147,22 @@ struct Smem {
     static constexpr int K = Q + NQ * QTILE;                   // K tiles, chunk-major
     static constexpr int V = K + KST * KTILE;                  // V tiles as copied
     static constexpr int BAR = V + VST * KTILE;
-    static constexpr int NBAR = 24;
+    static constexpr int NBAR = 28;
+    // SLOT: TMEM address, aborted flag, length of the CTA's item list (-1: none)
     static constexpr int SLOT = BAR + NBAR * 8;
+    static constexpr int LIST = SLOT + 16;                     // the CTA's items, in order
+    static constexpr int LISTCAP = (232448 - LIST) / 16 < 1024 ? (232448 - LIST) / 16 : 1024;
     // at least 120 KB so that one CTA (and its 512 TMEM columns) owns an SM
-    static constexpr int BYTES = SLOT + 16 < 122880 ? 122880 : SLOT + 16;
-    static_assert(SLOT + 16 <= 232448, "shared memory of one CTA");
+    static constexpr int END = LIST + 16 * LISTCAP;
+    static constexpr int BYTES = END < 122880 ? 122880 : END;
+    static_assert(END <= 232448, "shared memory of one CTA");
+    // the schedule's counters and group costs use the Q tiles before the queries are stored
+    static constexpr int SCRATCH = NQ * QTILE / 4;
 };
 
 // barrier indices (rings of up to 4 stages)
 constexpr int kKFull = 0, kKEmpty = 4, kVFull = 8, kVEmpty = 12, kSFull = 16, kPFull = 18,
-              kODone = 20, kDone = 22, kPVDone = 23;
+              kODone = 20, kDone = 22, kPVDone = 23, kQFull = 24, kOFree = 26;
 
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     uint64_t pol;
@@ -163,6 +179,14 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// One 32-byte store (the address a multiple of 32).
+__device__ __forceinline__ void st_global_v8(void* addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                             uint32_t e, uint32_t f, uint32_t g, uint32_t h) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(addr), "r"(a), "r"(b),
+                 "r"(c), "r"(d), "r"(e), "r"(f), "r"(g), "r"(h)
                  : "memory");
 }
 
@@ -222,11 +246,170 @@ __device__ __forceinline__ uint32_t check_blocks(const PParams& p, int32_t& blk,
     return (uint32_t)__popc(__ballot_sync(0xffffffffu, blk >= 0)) * tile;
 }
 
-// PREFIX = false: causal prefill of chunk rows (CTA = query tile, kv head, sequence).
-// PREFIX = true: rows are (sequence, query head) pairs of the kv head (CTA = row group,
-// kv head, partition j of a prefix shared by every sequence, read through table row 0);
-// every key is visible and the CTA writes unnormalised partials (o, max, sum) of
-// partition j for the split-KV merge instead of outputs.
+// One work item: the prefill's (query tile, kv head, sequence) triple, natural index
+// (s Hkv + kvh) nqt + x with query tile nqt - 1 - x, or the prefix mode's one (row group,
+// kv head, partition range) per CTA.
+struct Item {
+    int kvh, row_base;          // row_base: prefix mode
+    int qrow0, p0, rows;        // prefill: the tile's first chunk row (a row of q), its position, its rows
+    int p_last, nblk;           // last position attended to, blocks read
+    const int32_t* trow;
+    bool live;                  // rows and keys to process
+    bool bad_pos;               // a position outside the table (flagged, skipped)
+};
+// The prefill's items as the CTA's list keeps them: the natural index and the geometry that
+// would otherwise take three dependent loads per item.
+struct ListEntry { int it, qrow0, p0, rows; };
+
+__device__ __forceinline__ Item finish_item(const PParams& p, int it, int qrow0, int p0, int rows) {
+    Item g{};
+    const int s = it / (p.nqt * p.Hkv);
+    g.kvh = it / p.nqt - s * p.Hkv;
+    g.qrow0 = qrow0;
+    g.p0 = p0;
+    g.rows = rows;
+    g.trow = p.tables + (size_t)s * p.max_blocks;
+    if (rows <= 0) return g;
+    g.p_last = p0 + rows - 1;
+    if (p0 < 0 || g.p_last >= p.max_blocks * kBlockTokens) {
+        g.bad_pos = true;
+        return g;
+    }
+    g.nblk = g.p_last / kBlockTokens + 1;
+    g.live = true;
+    return g;
+}
+template <bool PREFIX>
+__device__ __forceinline__ Item item_at(const PParams& p, int it) {
+    if constexpr (PREFIX) {
+        Item g{};
+        g.kvh = blockIdx.y;
+        g.row_base = blockIdx.x * p.rows_per_cta;
+        g.nblk = p.part_blocks;
+        g.p_last = g.nblk * kBlockTokens - 1;             // positions relative to the partition
+        g.trow = p.tables + (size_t)blockIdx.z * p.part_blocks;
+        g.live = true;
+        return g;
+    } else {
+        const int x = it % p.nqt, s = it / (p.nqt * p.Hkv);
+        const int i0 = (p.nqt - 1 - x) * p.TQ;
+        // the chunk's place: three loads in flight together
+        const int q0 = __ldg(p.cu_q + s), q1 = __ldg(p.cu_q + s + 1), start = __ldg(p.start_pos + s);
+        // (a chunk's start is checked with its first tile's positions)
+        return finish_item(p, it, q0 + i0, start < 0 ? -1 : start + i0, min(q1 - q0 - i0, p.TQ));
+    }
+}
+// Cost of the items of query tile nqt - 1 - x of sequence s (every kv head alike): their
+// key tiles, 0 without work, -1 for positions outside the table.
+__device__ __forceinline__ int group_cost(const PParams& p, int grp) {
+    const Item g = item_at<false>(p, grp / p.nqt * p.Hkv * p.nqt + grp % p.nqt);
+    if (g.bad_pos) return -1;
+    return g.live ? (g.nblk + kKeyBlocks - 1) / kKeyBlocks : 0;
+}
+
+// The prefill's schedule.  The grid is persistent (at most one CTA per SM); the items,
+// sorted by decreasing cost (key tiles; ties by natural index), are dealt out in rounds of
+// gridDim.x, in CTA order in even rounds and reverse order in odd ones, so that every CTA
+// ends up with about the same work (a static stride over the natural order leaves the CTAs
+// that drew long chunks well behind).  Every CTA sorts the (sequence, query tile) groups
+// itself, the same way: the groups' costs and their histogram, a scan over the costs from
+// the largest, and a placement of the groups in natural order by one warp (equal costs keep
+// that order); it keeps the list of its own items with their geometry.  Where the costs or
+// the list would not fit, the CTA takes items blockIdx.x, + gridDim.x, ... instead (list
+// length -1).
+template <int D>
+__device__ void build_schedule(const PParams& p, uint8_t* smem) {
+    using L = Smem<D, 2>;
+    int* cnt = reinterpret_cast<int*>(smem + L::Q);      // [ncost] counts, then offsets
+    ListEntry* list = reinterpret_cast<ListEntry*>(smem + L::LIST);
+    volatile int* nlist = reinterpret_cast<volatile int*>(smem + L::SLOT + 8);
+    const int grid = gridDim.x, cta = blockIdx.x;
+    const int ncost = (p.max_blocks + kKeyBlocks - 1) / kKeyBlocks + 1;     // costs 0 .. ncost - 1
+    const int ngroups = p.num_seqs * p.nqt;
+    // per group: cost, first row, its position, rows
+    int* gcost = cnt + ncost;
+    int* gq = gcost + ngroups;
+    int* gp = gq + ngroups;
+    int* gr = gp + ngroups;
+    const bool sorted = (long long)ncost + 4ll * ngroups <= L::SCRATCH && (p.num_items + grid - 1) / grid <= L::LISTCAP;
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    if (!sorted) {
+        if (cta == 0)                                  // positions outside the table, flagged once
+            for (int g = tid; g < ngroups; g += nthr)
+                if (group_cost(p, g) < 0) raise_flag(p.err, PA_DEV_ERR_BAD_POS);
+        if (tid == 0) *nlist = -1;
+        __syncthreads();
+        return;
+    }
+    for (int c = tid; c < ncost; c += nthr) cnt[c] = 0;
+    __syncthreads();
+    for (int g = tid; g < ngroups; g += nthr) {
+        const Item it = item_at<false>(p, g / p.nqt * p.Hkv * p.nqt + g % p.nqt);
+        const int c = it.bad_pos ? -1 : it.live ? (it.nblk + kKeyBlocks - 1) / kKeyBlocks : 0;
+        gcost[g] = c;
+        gq[g] = it.qrow0;
+        gp[g] = it.p0;
+        gr[g] = it.rows;
+        if (c > 0) atomicAdd(&cnt[c], 1);
+        else if (c < 0 && cta == 0) raise_flag(p.err, PA_DEV_ERR_BAD_POS);
+    }
+    __syncthreads();
+    if (tid < 32) {
+        const int lane = tid;
+        // cnt[c] := groups of cost > c (an exclusive scan from the top)
+        int run = 0;
+        for (int c0 = ncost - 1; c0 >= 0; c0 -= 32) {
+            const int c = c0 - lane;
+            const int v = c >= 0 ? cnt[c] : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += u;
+            }
+            if (c >= 0) cnt[c] = run + incl - v;
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        __syncwarp();
+        const int total = run * p.Hkv;                 // live items
+        // rank R of the sorted items goes to CTA owner(R) as its item R / grid
+        const uint32_t lt = (1u << lane) - 1u;
+        for (int g0 = 0; g0 < ngroups; g0 += 32) {
+            const int g = g0 + lane;
+            const int c = g < ngroups ? gcost[g] : 0;
+            const uint32_t same = __match_any_sync(0xffffffffu, c > 0 ? c : -1);
+            int pos = 0;
+            if (c > 0) pos = cnt[c] + __popc(same & lt);
+            __syncwarp();
+            if (c > 0 && (same & lt) == 0u) cnt[c] += __popc(same);
+            __syncwarp();
+            if (c > 0) {
+                const int r0 = pos * p.Hkv, r1 = r0 + p.Hkv;        // the group's ranks
+                const int s = g / p.nqt, x = g - s * p.nqt;
+                for (int rd = r0 / grid; rd * grid < r1; ++rd) {
+                    const int R = rd * grid + ((rd & 1) ? grid - 1 - cta : cta);
+                    if (R >= r0 && R < r1) list[rd] = ListEntry{(s * p.Hkv + (R - r0)) * p.nqt + x, gq[g], gp[g], gr[g]};
+                }
+            }
+        }
+        if (lane == 0) {
+            int m = 0;
+            while (m * grid + ((m & 1) ? grid - 1 - cta : cta) < total) ++m;
+            *nlist = m;
+        }
+    }
+    __syncthreads();
+}
+
+// PREFIX = false: causal prefill of chunk rows.  Persistent: each CTA walks its list of
+// (query tile, kv head, sequence) items, the next item's query rows, table windows and first
+// K/V tiles loading while the current one finishes.  A CTA always runs both Q tiles (an item
+// whose second tile has no chunk rows computes it on zero rows and stores nothing), so that
+// every item takes the same barrier phases.
+// PREFIX = true: one item per CTA; rows are (sequence, query head) pairs of the kv head
+// (CTA = row group, kv head, partition range of a prefix shared by every sequence, read
+// through table row 0); every key is visible and the CTA writes each row's unnormalised
+// partial (o, max, sum) into the decode workspace for the split-KV merge.
 // SW = 1 launches 256 threads under the same per-thread register budget (168), so a
 // CTA takes 256 x 168 registers and leaves room for a decode CTA on its SM.
 template <int D, bool PREFIX, int SW>
@@ -238,63 +421,21 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
     constexpr int kKWarp = Roles<SW>::kKWarp, kKWarps = Roles<SW>::kKWarps;
     constexpr int TILE = L::TILE, KTILE = L::KTILE, KST = L::KST, VST = L::VST;
     constexpr int KSTEPS = D / 16;
+    static_assert(PREFIX || SW == 2, "the prefill runs two Q tiles per CTA");
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kvh = blockIdx.y;
     if (PREFIX && p.wait_first) grid_dependency_wait();
-    int q0 = 0, n = 0, i0 = 0, start = 0, p_last, nblk, row_base = 0, rows_total = 0;
-    bool has_b;
-    const int32_t* trow = PREFIX ? p.tables + (size_t)blockIdx.z * p.part_blocks
-                                 : p.tables + (size_t)blockIdx.z * p.max_blocks;
-    // The copy warps' first table windows load at once, bounded by the table row (the
-    // CTA's own last block is known one round trip later; no kernel of this library writes
-    // the tables).
+    // two Q tiles: the prefill always, the prefix mode when its rows fill both
+    const bool has_b = SW == 2 && (!PREFIX || (p.rows_per_cta > kHalfRows &&
+                                               (int)blockIdx.x * p.rows_per_cta + kHalfRows < p.num_seqs * p.G));
+
     // The TIMEOUT bit of the flag: set when a copy wait gave up in this or an earlier call
     // (then nothing is written).  Thread 0 reads it for the softmax and MMA warps, which
     // act on it after their setup barrier; the copy warps read it themselves.
-    int32_t win = -1, win_next = -1, flag_in = 0;
-    if (warp == kProducerWarp || (warp >= kKWarp && warp < kKWarp + kKWarps)) {
-        const int lim = PREFIX ? p.part_blocks : p.max_blocks;
-        win = fetch_window(trow, 0, lim, lane);
-        win_next = fetch_window(trow, 1, lim, lane);
-        if (lane == 0 && p.err) flag_in = *reinterpret_cast<const volatile int32_t*>(p.err);
-    }
-    if (threadIdx.x == 0 && p.err) flag_in = *reinterpret_cast<const volatile int32_t*>(p.err);
-    if constexpr (PREFIX) {
-        rows_total = p.num_seqs * p.G;
-        row_base = blockIdx.x * p.rows_per_cta;
-        nblk = p.part_blocks;
-        p_last = nblk * kBlockTokens - 1;                 // positions relative to the partition
-        has_b = SW == 2 && p.rows_per_cta > kHalfRows && row_base + kHalfRows < rows_total;
-    } else {
-        const int qt = gridDim.x - 1 - blockIdx.x;        // later (longer) tiles first
-        const int s = blockIdx.z;
-        // the chunk's place: three loads in flight together
-        q0 = __ldg(p.cu_q + s);
-        n = __ldg(p.cu_q + s + 1);
-        start = __ldg(p.start_pos + s);
-        n -= q0;
-        i0 = qt * p.TQ;
-        // (a CTA that exits early still waits for the previous grid: a dependent grid never
-        // completes before the one it follows)
-        if (i0 >= n) {
-            grid_dependency_wait();
-            return;
-        }
-        const int i_end = min(n, i0 + p.TQ);
-        p_last = start + i_end - 1;                       // last position this CTA attends to
-        if (start < 0 || p_last >= p.max_blocks * kBlockTokens) {
-            if (threadIdx.x == 0 && kvh == 0) raise_flag(p.err, PA_DEV_ERR_BAD_POS);
-            grid_dependency_wait();
-            return;
-        }
-        nblk = p_last / kBlockTokens + 1;
-        // tile b holds rows 128 .. 255; it is skipped when none of them is a chunk row
-        const int tl_b = kHalfRows / p.G;
-        has_b = SW == 2 && tl_b < p.TQ && i0 + tl_b < n;
-    }
-    const int ntiles = (nblk + kKeyBlocks - 1) / kKeyBlocks;
-
+    int32_t flag_in = 0;
+    const bool vwarp = warp == kProducerWarp, kwarp = warp >= kKWarp && warp < kKWarp + kKWarps;
+    if ((vwarp || kwarp) ? lane == 0 : threadIdx.x == 0)
+        if (p.err) flag_in = *reinterpret_cast<const volatile int32_t*>(p.err);
     const uint32_t aborted_in = (uint32_t)(flag_in & PA_DEV_ERR_TIMEOUT);   // (thread 0)
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sQ = sbase + L::Q, sK = sbase + L::K, sV = sbase + L::V;
@@ -320,8 +461,34 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         }
         mbar_init(bar(kDone), 1);
         mbar_init(bar(kPVDone), 1);
+        mbar_init(bar(kQFull), 4);
+        mbar_init(bar(kQFull + 1), 4);
+        mbar_init(bar(kOFree), kSoftWarps);
         fence_proxy_async_smem();
     }
+    // The CTA's items: the i-th is item_of(i, the (i-1)-th), -1 past the last.
+    if constexpr (!PREFIX) build_schedule<D>(p, smem);
+    const int nlist = PREFIX ? 1 : *reinterpret_cast<volatile int*>(smem + L::SLOT + 8);
+    const ListEntry* list = reinterpret_cast<const ListEntry*>(smem + L::LIST);
+    auto item_of = [&](int i, int prev) -> int {       // a list position, or a natural index
+        if constexpr (PREFIX) {
+            return i == 0 ? 0 : -1;
+        } else {
+            if (nlist >= 0) return i < nlist ? i : -1;
+            for (int it = i == 0 ? (int)blockIdx.x : prev + (int)gridDim.x; it < p.num_items; it += gridDim.x)
+                if (item_at<false>(p, it).live) return it;
+            return -1;
+        }
+    };
+    auto item_get = [&](int idx) -> Item {             // the item item_of gave
+        if constexpr (PREFIX) {
+            return item_at<true>(p, 0);
+        } else {
+            if (nlist < 0) return item_at<false>(p, idx);
+            const ListEntry e = list[idx];
+            return finish_item(p, e.it, e.qrow0, e.p0, e.rows);
+        }
+    };
     // The copy warps start at once, without the setup barrier of the others: warp 0
     // tells them that the mbarriers exist (and whether an earlier call gave up).
     constexpr int kCopyThreads = 32 * (2 + kKWarps);       // warp 0 and the copy warps
@@ -331,135 +498,136 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         // for the softmax and MMA warps, after their setup barrier
         if (lane == 0) *reinterpret_cast<volatile uint32_t*>(smem + L::SLOT + 4) = aborted_in;
     }
-    // ---- copy warps.  V: one bulk copy per (block, kv head) tile, lane b handles block b.
-    // K: the threads of the K warps copy each block tile's 16-byte pieces (piece c * 16 +
-    // slot), consecutive threads on consecutive pieces, each to its chunk-major place, one
-    // commit group per tile; a tile is published (its barrier completes) once every
-    // thread has seen its own copies land and made them visible to the tensor cores (a
-    // proxy fence in the writing thread).  Blocks past the tile's last one and entries
-    // that are not blocks of the pool (flagged) are not copied: their columns of S are
-    // masked, or the call has failed.  The copy warps start while the others set up.
-    const bool vwarp = warp == kProducerWarp, kwarp = warp >= kKWarp && warp < kKWarp + kKWarps;
-    int wcur = 0, issued = 0;
-    auto block_of = [&](int j) {
-        while (j / kWinTiles > wcur) {
-            win = win_next;
-            ++wcur;
-            win_next = fetch_window(trow, wcur + 1, nblk, lane);
-        }
-        return window_block(win, j, lane, nblk);
-    };
-    auto issue_v = [&](int j, uint64_t pol) {
-        const int st = j % VST;
-        int32_t blk = block_of(j);
-        const uint32_t bytes = check_blocks(p, blk, j, nblk, lane, TILE);
-        if (lane == 0) {
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar(kVFull + st), bytes);
-        }
-        __syncwarp();
-        if (lane < kKeyBlocks && blk >= 0)
-            bulk_g2s(sV + st * KTILE + lane * TILE, p.v_pool + ((size_t)blk * p.Hkv + kvh) * (size_t)TILE,
-                     TILE, bar(kVFull + st), pol);
-        issued = j + 1;
-    };
-    auto issue_k = [&](int j, uint64_t pol) {
-        constexpr int kPer = kBlockTokens * (D / 8) / (32 * kKWarps);   // pieces per thread and block
-        const int kt = (warp - kKWarp) * 32 + lane;
-        const int st = j % KST;
-        int32_t blk = block_of(j);
-        check_blocks(p, blk, j, nblk, lane, TILE);
-        const uint32_t dst = sK + st * KTILE;
-#pragma unroll
-        for (int b = 0; b < kKeyBlocks; ++b) {
-            const int32_t bb = __shfl_sync(0xffffffffu, blk, b);
-            if (bb >= 0) {
-                const char* src = p.k_pool + ((size_t)bb * p.Hkv + kvh) * (size_t)TILE;
-#pragma unroll
-                for (int u = 0; u < kPer; ++u) {
-                    const int piece = u * 32 * kKWarps + kt;
-                    cp_async_16(dst + (piece >> 4) * (kKeyBlocks * 256) + b * 256 + (piece & 15) * 16,
-                                src + piece * 16, pol);
-                }
-            }
-        }
-        cp_async_commit();
-        issued = j + 1;
-    };
-    // before exit: every copy of the warp has landed (and every arrival it triggers)
-    auto drain = [&]() {
-        if (kwarp) {
-            cp_async_wait<0>();
-        } else if (vwarp && lane == 0) {
-            for (int jj = max(0, issued - VST); jj < issued; ++jj)
-                mbar_wait_bounded(bar(kVFull + jj % VST), (jj / VST) & 1, kWaitLimitNs);
-        }
-    };
+
     // Roles.  setmaxnreg is collective over a warpgroup, so each runs at the head of its
     // branch: the copy / MMA warpgroups hand registers to the softmax warpgroups, which
     // take them after their setup (8 x 32 x 200 + 4 x 32 x 104 <= 384 x 168, the launch's
-    // allocation, with two Q tiles; 4 x 32 x 200 + 8 x 32 x 104 with one).
+    // allocation, with two Q tiles; 4 x 32 x 200 + 8 x 32 x 104 with one).  Tile and item
+    // counts run on across the CTA's items, so barrier phases and ring stages do too.
     if (warp >= kSoftWarps) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 104;" ::: "memory");
     if (vwarp || kwarp) {
+        // ---------------------------------------------------------------- copy warps
+        // V: one bulk copy per (block, kv head) tile, lane b handles block b.  K: the threads
+        // of the K warps copy each block tile's 16-byte pieces (piece c * 16 + slot),
+        // consecutive threads on consecutive pieces, each to its chunk-major place, one commit
+        // group per tile; a tile is published (its barrier completes) once every thread has
+        // seen its own copies land and made them visible to the tensor cores (a proxy fence
+        // in the writing thread).  Blocks past the tile's last one and entries that are not
+        // blocks of the pool (flagged) are not copied: their columns of S are masked, or the
+        // call has failed.  The table is read in windows of four tiles, one window ahead.
         const bool gave_up = __shfl_sync(0xffffffffu, flag_in & PA_DEV_ERR_TIMEOUT, 0) != 0;
+        int issued = 0;                               // tiles of all items issued so far
         named_bar_sync(1, kCopyThreads);
         if (!gave_up) {
-            if (!PREFIX) grid_dependency_wait();  // the chunk's own K/V come from the append before
+            if (!PREFIX) grid_dependency_wait();  // the chunks' K/V come from the append before
             __syncwarp();
-            if (vwarp) {
-                // ---------------------------------------------------------------- V tiles
-                if (lane == 0) grid_launch_dependents();
-                const uint64_t pol = l2_policy_evict_last();   // tiles are re-read by other query tiles
-                bool ok = true;
-                for (int j = 0; j < ntiles; ++j) {
-                    if (j >= VST) {                          // PV of tile j - VST is done
-                        ok = warp_wait(bar(kVEmpty + j % VST), (j / VST - 1) & 1);
-                        if (!ok) break;
+            if (vwarp && lane == 0) grid_launch_dependents();
+            const uint64_t pol = l2_policy_evict_last();   // tiles are re-read by other query tiles
+            bool ok = true;
+            int t0 = 0;                               // tiles of the earlier items
+            for (int i = 0, it = item_of(0, -1); ok && it >= 0; it = item_of(++i, it)) {
+                const Item g = item_get(it);
+                const int ntiles = (g.nblk + kKeyBlocks - 1) / kKeyBlocks;
+                int32_t win = fetch_window(g.trow, 0, g.nblk, lane), win_next = fetch_window(g.trow, 1, g.nblk, lane);
+                int wcur = 0;
+                auto block_of = [&](int j) {
+                    while (j / kWinTiles > wcur) {
+                        win = win_next;
+                        ++wcur;
+                        win_next = fetch_window(g.trow, wcur + 1, g.nblk, lane);
                     }
-                    issue_v(j, pol);
-                }
-                if (!ok && lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
-                } else {
-                // ---------------------------------------------------------------- K tiles
-                // Tiles are published in order, each as soon as its copies have landed; a new
-                // tile is issued whenever its stage is free (the S MMAs of the tile KST earlier
-                // are done), tested without waiting while copies are in flight.
-                static_assert(KST <= 3, "the landing waits below cover up to two newer tiles");
-                const uint64_t pol = l2_policy_evict_last();   // tiles are re-read by other query tiles
-                auto stage_free = [&](int j) {
-                    return j < KST || __all_sync(0xffffffffu, mbar_test(bar(kKEmpty + j % KST), (j / KST - 1) & 1));
+                    return window_block(win, j, lane, g.nblk);
                 };
-                bool ok = true;
-                for (int pub = 0; pub < ntiles; ++pub) {
-                    // (two tiles ahead at most; the first alone, as the first scores wait for it)
-                    while (issued < ntiles && issued - pub < (pub == 0 ? 1 : 2) && stage_free(issued))
-                        issue_k(issued, pol);
-                    if (issued == pub) {               // nothing in flight: wait for the stage
-                        ok = warp_wait(bar(kKEmpty + issued % KST), (issued / KST - 1) & 1);
-                        if (!ok) break;
-                        issue_k(issued, pol);
+                if (vwarp) {
+                    for (int j = 0; j < ntiles; ++j) {
+                        const int t = t0 + j, st = t % VST;
+                        if (t >= VST) {                      // PV of tile t - VST is done
+                            ok = warp_wait(bar(kVEmpty + st), (t / VST - 1) & 1);
+                            if (!ok) break;
+                        }
+                        int32_t blk = block_of(j);
+                        const uint32_t bytes = check_blocks(p, blk, j, g.nblk, lane, TILE);
+                        if (lane == 0) {
+                            fence_proxy_async_smem();
+                            mbar_arrive_expect_tx(bar(kVFull + st), bytes);
+                        }
+                        __syncwarp();
+                        if (lane < kKeyBlocks && blk >= 0)
+                            bulk_g2s(sV + st * KTILE + lane * TILE,
+                                     p.v_pool + ((size_t)blk * p.Hkv + g.kvh) * (size_t)TILE, TILE,
+                                     bar(kVFull + st), pol);
+                        issued = t + 1;
                     }
-                    const int newer = issued - pub - 1;   // this thread's tiles after `pub` in flight
-                    if (newer >= 2) cp_async_wait<2>();
-                    else if (newer == 1) cp_async_wait<1>();
-                    else cp_async_wait<0>();
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(kKFull + pub % KST));
+                } else {
+                    // Tiles are published in order, each as soon as its copies have landed; a
+                    // new tile is issued whenever its stage is free (the S MMAs of the tile
+                    // KST earlier are done), tested without waiting while copies are in flight.
+                    static_assert(KST <= 3, "the landing waits below cover up to two newer tiles");
+                    constexpr int kPer = kBlockTokens * (D / 8) / (32 * kKWarps);   // pieces per thread and block
+                    const int kt = (warp - kKWarp) * 32 + lane;
+                    int jn = 0;                              // this item's next tile to issue
+                    auto issue_k = [&]() {
+                        const int t = t0 + jn, st = t % KST;
+                        int32_t blk = block_of(jn);
+                        check_blocks(p, blk, jn, g.nblk, lane, TILE);
+                        const uint32_t dst = sK + st * KTILE;
+#pragma unroll
+                        for (int b = 0; b < kKeyBlocks; ++b) {
+                            const int32_t bb = __shfl_sync(0xffffffffu, blk, b);
+                            if (bb >= 0) {
+                                const char* src = p.k_pool + ((size_t)bb * p.Hkv + g.kvh) * (size_t)TILE;
+#pragma unroll
+                                for (int u = 0; u < kPer; ++u) {
+                                    const int piece = u * 32 * kKWarps + kt;
+                                    cp_async_16(dst + (piece >> 4) * (kKeyBlocks * 256) + b * 256 + (piece & 15) * 16,
+                                                src + piece * 16, pol);
+                                }
+                            }
+                        }
+                        cp_async_commit();
+                        ++jn;
+                        issued = t + 1;
+                    };
+                    auto stage_free = [&](int t) {
+                        return t < KST || __all_sync(0xffffffffu, mbar_test(bar(kKEmpty + t % KST), (t / KST - 1) & 1));
+                    };
+                    for (int pub = 0; pub < ntiles; ++pub) {
+                        // (two tiles ahead at most; the CTA's first tile alone, as the first
+                        // scores wait for it)
+                        while (jn < ntiles && jn - pub < (t0 + pub == 0 ? 1 : 2) && stage_free(t0 + jn)) issue_k();
+                        if (jn == pub) {                     // nothing in flight: wait for the stage
+                            ok = warp_wait(bar(kKEmpty + (t0 + jn) % KST), ((t0 + jn) / KST - 1) & 1);
+                            if (!ok) break;
+                            issue_k();
+                        }
+                        const int newer = jn - pub - 1;      // this thread's tiles after `pub` in flight
+                        if (newer >= 2) cp_async_wait<2>();
+                        else if (newer == 1) cp_async_wait<1>();
+                        else cp_async_wait<0>();
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(kKFull + (t0 + pub) % KST));
+                    }
                 }
-                if (!ok && lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
-                }
+                t0 += ntiles;
+            }
+            if (!ok && lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
         }
-        drain();
+        // before exit: every copy of the warp has landed
+        if (kwarp) {
+            cp_async_wait<0>();
+        } else if (lane == 0) {
+            for (int t = max(0, issued - VST); t < issued; ++t)
+                mbar_wait_bounded(bar(kVFull + t % VST), (t / VST) & 1, kWaitLimitNs);
+        }
     } else if (warp == kMmaWarp) {
     tmem_alloc<kTmemCols>(sbase + L::SLOT);
     tc_fence_before();
-    named_bar_sync(2, 32 * (kSoftWarps + 1));          // Q is in place, the TMEM allocated
+    named_bar_sync(2, 32 * (kSoftWarps + 1));          // the TMEM is allocated
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::SLOT);
     if (*reinterpret_cast<volatile uint32_t*>(smem + L::SLOT + 4) == 0u) {   // (else write nothing)
-
         // ---------------------------------------------------------------- MMA issue
         // S_h(j) = Q_h K_j^T: A = Q_h (shared), B = the chunk-major K tile, N = 128 tokens.
         // O_h += P_h(j) V_j: A = P_h(j) in TMEM (over S_h's first columns), B = one V block
@@ -467,164 +635,203 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         // S_h(j + 1) overwrites P_h(j) only after PV_h(j) has read it, and a commit after
         // S_h(j + 1) also covers PV_h(j).  Without a tile b its S columns are a second S
         // buffer for tile a: S(j) goes to buffer j % 2 and S(j + 2) is issued right after
-        // PV(j), so the scores of the next tile are ready when the softmax finishes.
+        // PV(j), so the scores of the next tile are ready when the softmax finishes.  An
+        // item's scores start once its query rows are in place; its first P V (which starts
+        // O afresh) once the previous item's O has been read.
         constexpr uint32_t idS = umma_idesc_bf16(128, kKeyTok, 0);
         constexpr uint32_t idO = umma_idesc_bf16(128, D, 1);
         bool ok = true;
-        auto issue_s = [&](int hh, int buf, int j) {
-            tc_fence_after();
-            if (lane == 0) {
-                // columns of blocks past the tile's last one hold stale products (masked)
-                const uint64_t qdesc = umma_desc(sQ + hh * L::QTILE, 2048, 128);
-                const uint64_t kdesc = umma_desc(sK + (j % KST) * KTILE, kKeyBlocks * 256, 128);
-                const uint32_t dcol = tmem + kColS + (uint32_t)(buf * kKeyTok);
+        int t0 = 0;                                   // tiles of the earlier items
+        for (int ic = 0, it = item_of(0, -1); ok && it >= 0; it = item_of(++ic, it)) {
+            const Item g = item_get(it);
+            const int nblk = g.nblk, ntiles = (nblk + kKeyBlocks - 1) / kKeyBlocks;
+            auto issue_s = [&](int hh, int buf, int j) {
+                tc_fence_after();
+                if (lane == 0) {
+                    // columns of blocks past the tile's last one hold stale products (masked)
+                    const uint64_t qdesc = umma_desc(sQ + hh * L::QTILE, 2048, 128);
+                    const uint64_t kdesc = umma_desc(sK + ((t0 + j) % KST) * KTILE, kKeyBlocks * 256, 128);
+                    const uint32_t dcol = tmem + kColS + (uint32_t)(buf * kKeyTok);
 #pragma unroll
-                for (int ks = 0; ks < KSTEPS; ++ks)
-                    umma_ss(dcol, qdesc + (uint64_t)(ks * 256),
-                            kdesc + (uint64_t)((ks * 2 * kKeyBlocks * 256) >> 4), idS, ks > 0);
-                umma_commit(bar(kSFull + buf));
-            }
-            __syncwarp();
-        };
-        auto issue_pv = [&](int hh, int j, int buf) {
-            const int st = j % VST;
-            // (one Q tile: P(j) comes on barrier j % 2, as S is double-buffered -- the softmax
-            // may write P(j + 1) before this wait for P(j) begins, and a parity wait on one
-            // barrier could not tell its phase j + 2 from phase j)
-            ok = has_b ? warp_wait(bar(kPFull + hh), j & 1) : warp_wait(bar(kPFull + (j & 1)), (j >> 1) & 1);
-            if (!ok) return;
-            const int nb = min(kKeyBlocks, nblk - j * kKeyBlocks);
-            if (hh == 0) {
-                ok = warp_wait(bar(kVFull + st), (j / VST) & 1);
+                    for (int ks = 0; ks < KSTEPS; ++ks)
+                        umma_ss(dcol, qdesc + (uint64_t)(ks * 256),
+                                kdesc + (uint64_t)((ks * 2 * kKeyBlocks * 256) >> 4), idS, ks > 0);
+                    umma_commit(bar(kSFull + buf));
+                }
+                __syncwarp();
+            };
+            auto issue_pv = [&](int hh, int j, int buf) {
+                const int t = t0 + j, st = t % VST;
+                // (one Q tile: P(j) comes on barrier j % 2, as S is double-buffered -- the softmax
+                // may write P(j + 1) before this wait for P(j) begins, and a parity wait on one
+                // barrier could not tell its phase j + 2 from phase j)
+                ok = has_b ? warp_wait(bar(kPFull + hh), t & 1) : warp_wait(bar(kPFull + (j & 1)), (j >> 1) & 1);
                 if (!ok) return;
-                if (j == ntiles - 1) {
-                    // V rows past the last attended position may hold anything (even NaN)
-                    const int first_stale = p_last - (nblk - 1) * kBlockTokens + 1;
-                    if (first_stale < kBlockTokens) {
-                        const int nst = kBlockTokens - first_stale;
-                        uint8_t* vt = smem + L::V + st * KTILE + (nb - 1) * TILE;
-                        for (int idx = lane; idx < (D / 8) * nst; idx += 32) {
-                            const int c = idx / nst, sl = first_stale + (idx - c * nst);
-                            *reinterpret_cast<uint4*>(vt + c * 256 + sl * 16) = make_uint4(0u, 0u, 0u, 0u);
+                if (j == 0 && hh == 0 && ic > 0) {
+                    ok = warp_wait(bar(kOFree), (ic - 1) & 1);     // the last item's O is read
+                    if (!ok) return;
+                }
+                const int nb = min(kKeyBlocks, nblk - j * kKeyBlocks);
+                if (hh == 0) {
+                    ok = warp_wait(bar(kVFull + st), (t / VST) & 1);
+                    if (!ok) return;
+                    if (j == ntiles - 1) {
+                        // V rows past the last attended position may hold anything (even NaN)
+                        const int first_stale = g.p_last - (nblk - 1) * kBlockTokens + 1;
+                        if (first_stale < kBlockTokens) {
+                            const int nst = kBlockTokens - first_stale;
+                            uint8_t* vt = smem + L::V + st * KTILE + (nb - 1) * TILE;
+                            for (int idx = lane; idx < (D / 8) * nst; idx += 32) {
+                                const int c = idx / nst, sl = first_stale + (idx - c * nst);
+                                *reinterpret_cast<uint4*>(vt + c * 256 + sl * 16) = make_uint4(0u, 0u, 0u, 0u);
+                            }
+                            fence_proxy_async_smem();
                         }
-                        fence_proxy_async_smem();
+                        __syncwarp();
                     }
-                    __syncwarp();
                 }
-            }
-            tc_fence_after();
-            if (lane == 0) {
-                const uint64_t vdesc = umma_desc(sV + st * KTILE, 128, 256);
-                const uint32_t pcol = tmem + kColS + (uint32_t)(buf * kKeyTok);
-                const uint32_t ocol = tmem + kColO + (uint32_t)(hh * kKeyTok);
-                for (int b = 0; b < nb; ++b)
-                    umma_ts(ocol, pcol + 8 * b, vdesc + (uint64_t)((b * TILE) >> 4), idO,
-                            (j > 0 || b > 0) ? 1u : 0u);
-                if (j == ntiles - 1) umma_commit(bar(kODone + hh));
-                if (hh == 1 || !has_b) umma_commit(bar(kVEmpty + st));
-                if (!has_b) umma_commit(bar(kPVDone));
-            }
-            __syncwarp();
-        };
-        auto k_ready = [&](int j) { return warp_wait(bar(kKFull + j % KST), (j / KST) & 1); };
-        auto k_free = [&](int j) {                // after the tile's last S MMA
-            if (lane == 0) umma_commit(bar(kKEmpty + j % KST));
-            __syncwarp();
-        };
-        auto next_s = [&](int j, int buf) {       // S of tile j for tile a, then free the K tile
-            ok = k_ready(j);
-            if (!ok) return;
-            issue_s(0, buf, j);
-            k_free(j);
-        };
-        if (!has_b) {
-            // one Q tile, S double-buffered: S(0) S(1) | PV(0) S(2) | PV(1) S(3) ...
-            next_s(0, 0);
-            if (ok && ntiles > 1) next_s(1, 1);
-            for (int j = 0; ok && j < ntiles; ++j) {
-                issue_pv(0, j, j & 1);
-                if (ok && j + 2 < ntiles) next_s(j + 2, j & 1);
-            }
-        } else {
-            // two Q tiles: S_a(0) S_b(0) | PV_a(0) S_a(1) PV_b(0) S_b(1) | ...
-            ok = k_ready(0);
-            if (ok) {
-                issue_s(0, 0, 0);
-                issue_s(1, 1, 0);
-                k_free(0);
-            }
-            for (int j = 0; ok && j < ntiles; ++j) {
-                const bool more = j + 1 < ntiles;
-                issue_pv(0, j, 0);
-                if (!ok) break;
-                if (more) {
-                    ok = k_ready(j + 1);
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint64_t vdesc = umma_desc(sV + st * KTILE, 128, 256);
+                    const uint32_t pcol = tmem + kColS + (uint32_t)(buf * kKeyTok);
+                    const uint32_t ocol = tmem + kColO + (uint32_t)(hh * kKeyTok);
+                    for (int b = 0; b < nb; ++b)
+                        umma_ts(ocol, pcol + 8 * b, vdesc + (uint64_t)((b * TILE) >> 4), idO,
+                                (j > 0 || b > 0) ? 1u : 0u);
+                    if (j == ntiles - 1) umma_commit(bar(kODone + hh));
+                    if (hh == 1 || !has_b) umma_commit(bar(kVEmpty + st));
+                    if (!has_b) umma_commit(bar(kPVDone));
+                }
+                __syncwarp();
+            };
+            auto k_ready = [&](int j) { return warp_wait(bar(kKFull + (t0 + j) % KST), ((t0 + j) / KST) & 1); };
+            auto k_free = [&](int j) {                // after the tile's last S MMA
+                if (lane == 0) umma_commit(bar(kKEmpty + (t0 + j) % KST));
+                __syncwarp();
+            };
+            auto next_s = [&](int j, int buf) {       // S of tile j for tile a, then free the K tile
+                ok = k_ready(j);
+                if (!ok) return;
+                issue_s(0, buf, j);
+                k_free(j);
+            };
+            // (each Q tile's scores start once its query rows are in place)
+            ok = warp_wait(bar(kQFull), ic & 1);
+            if (!ok) break;
+            if (!has_b) {
+                // one Q tile, S double-buffered: S(0) S(1) | PV(0) S(2) | PV(1) S(3) ...
+                next_s(0, 0);
+                if (ok && ntiles > 1) next_s(1, 1);
+                for (int j = 0; ok && j < ntiles; ++j) {
+                    issue_pv(0, j, j & 1);
+                    if (ok && j + 2 < ntiles) next_s(j + 2, j & 1);
+                }
+            } else {
+                // two Q tiles: S_a(0) S_b(0) | PV_a(0) S_a(1) PV_b(0) S_b(1) | ...
+                ok = k_ready(0);
+                if (ok) issue_s(0, 0, 0);
+                if (ok) ok = warp_wait(bar(kQFull + 1), ic & 1);
+                if (ok) {
+                    issue_s(1, 1, 0);
+                    k_free(0);
+                }
+                for (int j = 0; ok && j < ntiles; ++j) {
+                    const bool more = j + 1 < ntiles;
+                    issue_pv(0, j, 0);
                     if (!ok) break;
-                    issue_s(0, 0, j + 1);
-                }
-                issue_pv(1, j, 1);
-                if (!ok) break;
-                if (more) {
-                    issue_s(1, 1, j + 1);
-                    k_free(j + 1);
+                    if (more) {
+                        ok = k_ready(j + 1);
+                        if (!ok) break;
+                        issue_s(0, 0, j + 1);
+                    }
+                    issue_pv(1, j, 1);
+                    if (!ok) break;
+                    if (more) {
+                        issue_s(1, 1, j + 1);
+                        k_free(j + 1);
+                    }
                 }
             }
+            t0 += ntiles;
         }
         if (!ok && lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
         // nothing may still be running on the tensor cores when TMEM is freed
         if (lane == 0) umma_commit(bar(kDone));
         __syncwarp();
         mbar_wait_bounded(bar(kDone), 0, kWaitLimitNs);
-            }
+    }
     }
     } else {
+    // ---------------------------------------------------------------- softmax warps
     // rows: (chunk token, query head of this kv head), token-major; one per softmax thread
     const int row = threadIdx.x;                          // 0 .. 255 for the softmax warps
     const int h = warp >> 2;                              // Q tile of a softmax warp
-    int pos = p_last;                                     // rows outside the chunk see all (finite)
-    bool row_valid = false;
-    size_t orow = 0;
-    if (warp < kSoftWarps) {
+    const int lr = row & (kHalfRows - 1);
+    const uint32_t qdst = sQ + h * L::QTILE + (uint32_t)((lr >> 3) * 128 + (lr & 7) * 16);
+    // a negative scale is applied as |scale| to -q (exact), so that the softmax can take the
+    // row maximum of the unscaled scores
+    const uint32_t flip = p.scale_log2 < 0.f ? 0x80008000u : 0u;
+    constexpr int QB = D / 8;                            // 16-byte pieces of a query row
+    struct RowOf { int pos; bool valid; size_t orow; };
+    auto row_of = [&](const Item& g) {
+        RowOf r{g.p_last, false, 0};                      // rows outside the chunk see all (finite)
         if constexpr (PREFIX) {
-            const int r = row_base + row, sq = r / p.G, g = r - sq * p.G;
-            row_valid = row < p.rows_per_cta && r < rows_total;
-            if (row_valid) orow = (size_t)sq * p.Hq + (size_t)kvh * p.G + g;   // partial row
+            const int rr = g.row_base + row, sq = rr / p.G, gq = rr - sq * p.G;
+            r.valid = row < p.rows_per_cta && rr < p.num_seqs * p.G;
+            if (r.valid) r.orow = (size_t)sq * p.Hq + (size_t)g.kvh * p.G + gq;   // partial row
         } else {
-            const int tl = row / p.G, g = row - tl * p.G;
-            row_valid = tl < p.TQ && i0 + tl < n;
-            if (row_valid) {
-                pos = start + i0 + tl;
-                orow = ((size_t)(q0 + i0 + tl) * p.Hq + (size_t)kvh * p.G + g) * D;
+            const int tl = row / p.G, gq = row - tl * p.G;
+            r.valid = tl < g.rows;                        // (rows <= TQ)
+            if (r.valid) {
+                r.pos = g.p0 + tl;
+                r.orow = ((size_t)(g.qrow0 + tl) * p.Hq + (size_t)g.kvh * p.G + gq) * D;
             }
-            grid_dependency_wait();
         }
-        const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
-                                                           (PREFIX ? orow * D : orow));
-        const int lr = row & (kHalfRows - 1);
-        const uint32_t qdst = sQ + h * L::QTILE + (uint32_t)((lr >> 3) * 128 + (lr & 7) * 16);
-        // a negative scale is applied as |scale| to -q (exact), so that the softmax can
-        // take the row maximum of the unscaled scores
-        const uint32_t flip = p.scale_log2 < 0.f ? 0x80008000u : 0u;
-        // the whole row's loads in flight together, then the stores: one round trip on the
-        // critical path of the CTA's first scores
-        constexpr int QB = D / 8;
+        return r;
+    };
+    // The row's query goes straight into its place in the Q tile by 16-byte async copies
+    // (zeros for rows outside the chunk); publish_q waits for them, applies a negative
+    // scale's sign and makes the tile visible to the tensor cores.
+    auto load_q = [&](const RowOf& r) {
+        if (r.valid) {
+            const uint16_t* qsrc = static_cast<const uint16_t*>(p.q) + (PREFIX ? r.orow * D : r.orow);
 #pragma unroll
-        for (int k0 = 0; k0 < D / 8; k0 += QB) {
-            uint4 qv[QB];
+            for (int u = 0; u < QB; ++u) cp_async_16(qdst + u * 2048, qsrc + 8 * u);
+        } else {
 #pragma unroll
-            for (int u = 0; u < QB; ++u)
-                qv[u] = row_valid ? __ldg(qsrc + k0 + u) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
+            for (int u = 0; u < QB; ++u) st_shared_v4(qdst + u * 2048, make_uint4(0u, 0u, 0u, 0u));
+        }
+        cp_async_commit();
+    };
+    auto publish_q = [&]() {
+        cp_async_wait<0>();
+        __syncwarp();                                     // (the row came from the warp's lanes)
+        if (flip) {
+#pragma unroll 1
             for (int u = 0; u < QB; ++u) {
-                uint4 v = qv[u];
+                uint4 v = ld_shared_v4(qdst + u * 2048);
                 v.x ^= flip;
                 v.y ^= flip;
                 v.z ^= flip;
                 v.w ^= flip;
-                st_shared_v4(qdst + (k0 + u) * 2048, v);
+                st_shared_v4(qdst + u * 2048, v);
             }
         }
         fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kQFull + h));
+    };
+    // Through an item's tiles a thread keeps only its row's position (its output row is
+    // derived again for the epilogue: the registers go to the row of S).
+    int it = item_of(0, -1);
+    int ntiles = 0, pos = 0;
+    if (!PREFIX) grid_dependency_wait();                 // the queries may come from a kernel before
+    if (it >= 0) {
+        const Item g = item_get(it);
+        ntiles = (g.nblk + kKeyBlocks - 1) / kKeyBlocks;
+        const RowOf r = row_of(g);
+        pos = r.pos;
+        load_q(r);
     }
     tc_fence_before();
     named_bar_sync(2, 32 * (kSoftWarps + 1));
@@ -633,23 +840,31 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
     if (*reinterpret_cast<volatile uint32_t*>(smem + L::SLOT + 4) == 0u) {   // (else write nothing)
     // (every warp of both softmax warpgroups, at this one instruction)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 200;" ::: "memory");
-    if (h == 0 || has_b) {
-        // ---------------------------------------------------------------- softmax rows
-        // Warp w reaches TMEM lanes 32 (w % 4) ..; this thread's row of tile h is lane
-        // row % 128.  With two tiles a commit after S_h(j) covers every earlier MMA, so when
-        // S_h(j) is seen complete, PV_h(j - 1) is too: O_h may be rescaled and P_h(j)
-        // written at once.
-        const uint32_t tl_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        // without a tile b, tile a's S alternates between both S buffers (see the MMA warp)
-        const uint32_t ocol = kColO + (uint32_t)(h * kKeyTok);
-        const float cs = fabsf(p.scale_log2);          // a negative scale was moved into Q
+    // Warp w reaches TMEM lanes 32 (w % 4) ..; this thread's row of tile h is lane row % 128.
+    // With two tiles a commit after S_h(j) covers every earlier MMA, so when S_h(j) is seen
+    // complete, PV_h(j - 1) is too: O_h may be rescaled and P_h(j) written at once.
+    const uint32_t tl_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    // without a tile b, tile a's S alternates between both S buffers (see the MMA warp)
+    const uint32_t ocol = kColO + (uint32_t)(h * kKeyTok);
+    const float cs = fabsf(p.scale_log2);              // a negative scale was moved into Q
+    const bool active = h == 0 || has_b;
+    bool ok = true;
+    int t0 = 0, ic = 0;                                // tiles and items of the earlier items
+    if (it >= 0) publish_q();
+    while (ok && it >= 0) {
         float m_used = -INFINITY, l = 0.f;
-        bool ok = true;
-        for (int j = 0; j < ntiles; ++j) {
+        for (int j = 0; active && j < ntiles; ++j) {
+            const int t = t0 + j;
             const int sb = has_b ? h : (j & 1);
             const uint32_t scol = kColS + (uint32_t)(sb * kKeyTok);
-            ok = warp_wait(bar(kSFull + sb), has_b ? (j & 1) : ((j >> 1) & 1));
+            ok = warp_wait(bar(kSFull + sb), has_b ? (t & 1) : ((j >> 1) & 1));
             if (!ok) break;
+            if (!PREFIX && j == ntiles - 1 && nlist >= 0) {
+                // S_h of the item's last tile is complete, so Q_h is free: the next item's query
+                // rows start loading now, under this tile's softmax and the output's epilogue
+                const int nx = item_of(ic + 1, it);
+                if (nx >= 0) load_q(row_of(item_get(nx)));
+            }
             tc_fence_after();
             uint32_t sr[4][32];
 #pragma unroll
@@ -706,45 +921,40 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
                     tmem_st32(tl_addr + ocol + 32 * c, o);
                 }
             }
-            // probabilities, bf16 pairs, over the first 64 columns of S_h (already read);
-            // a full tile takes s c - m for two keys in one packed FFMA and sums in pairs
+            // probabilities, bf16 pairs, over the first 64 columns of S_h (already read), 16
+            // columns per store (32 scores: the fewest registers held beside the row); a full
+            // tile takes s c - m for two keys in one packed FFMA and sums in pairs
             float sum;
             if (full) {
                 const uint64_t c2 = pack_f32x2(cs, cs), nm2 = pack_f32x2(-m_used, -m_used);
                 uint64_t sum2[2] = {pack_f32x2(0.f, 0.f), pack_f32x2(0.f, 0.f)};
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t pk[32];
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc)
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            const int c = 2 * half + cc;
-                            const uint64_t x2 = ffma_f32x2(pack_f32x2(__uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1])), c2, nm2);
-                            const float e0 = fast_exp2(lo_f32(x2)), e1 = fast_exp2(hi_f32(x2));
-                            sum2[(i >> 1) & 1] = fadd_f32x2(sum2[(i >> 1) & 1], pack_f32x2(e0, e1));
-                            pk[16 * cc + (i >> 1)] = pack_bf16x2(e0, e1);
-                        }
-                    tmem_st32(tl_addr + scol + 32 * half, pk);
+                    for (int i = 0; i < 32; i += 2) {
+                        const uint64_t x2 = ffma_f32x2(pack_f32x2(__uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1])), c2, nm2);
+                        const float e0 = fast_exp2(lo_f32(x2)), e1 = fast_exp2(hi_f32(x2));
+                        sum2[(i >> 1) & 1] = fadd_f32x2(sum2[(i >> 1) & 1], pack_f32x2(e0, e1));
+                        pk[i >> 1] = pack_bf16x2(e0, e1);
+                    }
+                    tmem_st16(tl_addr + scol + 16 * c, pk);
                 }
-                const uint64_t t = fadd_f32x2(sum2[0], sum2[1]);
-                sum = lo_f32(t) + hi_f32(t);
+                const uint64_t tsum = fadd_f32x2(sum2[0], sum2[1]);
+                sum = lo_f32(tsum) + hi_f32(tsum);
             } else {
                 sum = 0.f;
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t pk[32];
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc)
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            const int c = 2 * half + cc;
-                            const float e0 = fast_exp2(__uint_as_float(sr[c][i]) - m_used);
-                            const float e1 = fast_exp2(__uint_as_float(sr[c][i + 1]) - m_used);
-                            sum += e0 + e1;
-                            pk[16 * cc + (i >> 1)] = pack_bf16x2(e0, e1);
-                        }
-                    tmem_st32(tl_addr + scol + 32 * half, pk);
+                    for (int i = 0; i < 32; i += 2) {
+                        const float e0 = fast_exp2(__uint_as_float(sr[c][i]) - m_used);
+                        const float e1 = fast_exp2(__uint_as_float(sr[c][i + 1]) - m_used);
+                        sum += e0 + e1;
+                        pk[i >> 1] = pack_bf16x2(e0, e1);
+                    }
+                    tmem_st16(tl_addr + scol + 16 * c, pk);
                 }
             }
             l = l * alpha + sum;
@@ -753,81 +963,123 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kPFull + (has_b ? h : (j & 1))));
         }
-        if (ok) ok = warp_wait(bar(kODone + h), 0);
-        if (ok && PREFIX) {
-            tc_fence_after();
-            // Each 32-column piece of the warp's 32 rows passes through shared memory (the K
-            // stages: every MMA has completed), 16-byte units of row r at unit u ^ (r % 8),
-            // so that both the writes and the reads are free of bank conflicts and each
-            // global store covers 128 contiguous bytes of four rows (a thread storing its
-            // own row scatters 16-byte pieces over 32 rows per instruction).
-            const size_t slot = orow * p.part_stride + (size_t)blockIdx.z * p.slot_mult;
-            const uint32_t stg = sK + (uint32_t)warp * (32 * 128);
-            const uint32_t valid = __ballot_sync(0xffffffffu, row_valid);
-            const int sub = lane >> 3, unit = lane & 7;       // row 4 i + sub, unit `unit`
-            float* dst[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const unsigned long long a = __shfl_sync(0xffffffffu, (unsigned long long)(p.part_o + slot * D), 4 * i + sub);
-                dst[i] = reinterpret_cast<float*>(a) + unit * 4;
-            }
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(tl_addr + ocol + 32 * c, o);
-                tmem_wait_ld();
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    st_shared_v4(stg + lane * 128 + ((u ^ (lane & 7)) * 16),
-                                 make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]));
-                __syncwarp();
+        if (!ok) break;
+        // the next item's query rows (published once this item's output is read)
+        const int it_next = item_of(ic + 1, it);
+        int ntiles_next = 0, pos_next = 0;
+        if (it_next >= 0) {
+            const Item gn = item_get(it_next);
+            ntiles_next = (gn.nblk + kKeyBlocks - 1) / kKeyBlocks;
+            const RowOf rn = row_of(gn);
+            pos_next = rn.pos;
+            if (PREFIX || nlist < 0) load_q(rn);          // (else under way since the last tile)
+        }
+        const RowOf rw = row_of(item_get(it));
+        if (active) {
+            ok = warp_wait(bar(kODone + h), ic & 1);
+            if (ok && PREFIX) {
+                tc_fence_after();
+                // Each 32-column piece of the warp's 32 rows passes through shared memory (the K
+                // stages: every MMA has completed), 16-byte units of row r at unit u ^ (r % 8),
+                // so that both the writes and the reads are free of bank conflicts and each
+                // global store covers 128 contiguous bytes of four rows (a thread storing its
+                // own row scatters 16-byte pieces over 32 rows per instruction).
+                const size_t slot = rw.orow * p.part_stride + (size_t)blockIdx.z * p.slot_mult;
+                const uint32_t stg = sK + (uint32_t)warp * (32 * 128);
+                const uint32_t valid = __ballot_sync(0xffffffffu, rw.valid);
+                const int sub = lane >> 3, unit = lane & 7;       // row 4 i + sub, unit `unit`
+                float* dst[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const int r = 4 * i + sub;
-                    const uint4 v = ld_shared_v4(stg + r * 128 + ((unit ^ (r & 7)) * 16));
-                    if ((valid >> r) & 1u)
-                        *reinterpret_cast<uint4*>(dst[i] + 32 * c) = v;
+                    const unsigned long long a = __shfl_sync(0xffffffffu, (unsigned long long)(p.part_o + slot * D), 4 * i + sub);
+                    dst[i] = reinterpret_cast<float*>(a) + unit * 4;
                 }
-                __syncwarp();
-            }
-            if (row_valid) p.part_ml[slot] = make_float2(m_used, l);
-        } else if (ok) {
-            tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow);
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(tl_addr + ocol + 32 * c, o);
-                tmem_wait_ld();
-                if (row_valid) {
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tl_addr + ocol + 32 * c, o);
+                    tmem_wait_ld();
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-                        dst[4 * c + v] = w;
+                    for (int u = 0; u < 8; ++u)
+                        st_shared_v4(stg + lane * 128 + ((u ^ (lane & 7)) * 16),
+                                     make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]));
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int r = 4 * i + sub;
+                        const uint4 v = ld_shared_v4(stg + r * 128 + ((unit ^ (r & 7)) * 16));
+                        if ((valid >> r) & 1u)
+                            *reinterpret_cast<uint4*>(dst[i] + 32 * c) = v;
+                    }
+                    __syncwarp();
+                }
+                if (rw.valid) p.part_ml[slot] = make_float2(m_used, l);
+            } else if (ok) {
+                tc_fence_after();
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                uint16_t* dst = static_cast<uint16_t*>(p.out) + rw.orow;
+                // 32-byte stores where the output allows them: the warp's 32 rows lie apart, so
+                // a store instruction touches a sector per lane, and wider stores need half as many
+                const bool wide = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0u;
+                // 32 columns at a time (the next item's first scores may be in flight)
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tl_addr + ocol + 32 * c, o);
+                    tmem_wait_ld();
+                    if (rw.valid) {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+                        uint16_t* d = dst + 32 * c;
+                        if (wide) {
+                            st_global_v8(d, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+                            st_global_v8(d + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+                        } else {
+#pragma unroll
+                            for (int v = 0; v < 4; ++v)
+                                reinterpret_cast<uint4*>(d)[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+                        }
                     }
                 }
+                // O is read: the next item's P V may start afresh
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kOFree));
             }
-        } else {
-            // a wait gave up: the row's result is incomplete, so it is written as NaN (visible
-            // even when no error flag was given)
-            if (lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
-            if (row_valid) {
+        } else if (lane == 0) {
+            mbar_arrive(bar(kOFree));                     // (a tile b without rows)
+        }
+        if (ok && it_next >= 0) publish_q();
+        if (!ok) break;
+        if (PREFIX) break;                                // one item per CTA
+        t0 += ntiles;
+        ++ic;
+        it = it_next;
+        ntiles = ntiles_next;
+        pos = pos_next;
+    }
+    if (!ok) {
+        // a wait gave up: the rows of this item and of the CTA's later items are incomplete,
+        // so they are written as NaN (visible even when no error flag was given)
+        if (lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
+        for (; it >= 0; it = item_of(++ic, it)) {
+            const RowOf rw = row_of(item_get(it));
+            if (rw.valid && active) {
                 if constexpr (PREFIX) {
-                    p.part_ml[orow * p.part_stride + (size_t)blockIdx.z * p.slot_mult] =
+                    p.part_ml[rw.orow * p.part_stride + (size_t)blockIdx.z * p.slot_mult] =
                         make_float2(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
                 } else {
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow);
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + rw.orow);
                     for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
                 }
             }
         }
     }
-            }
+    }
+    // (no query copy may still be landing when the CTA ends)
+    cp_async_wait<0>();
     }
 
     tc_fence_before();
@@ -836,8 +1088,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) prefill_tc_kernel(const PParams
         tc_fence_after();
         tmem_dealloc<kTmemCols>(*reinterpret_cast<volatile uint32_t*>(smem + L::SLOT));
     }
-    // (prefix mode: every thread has waited for the previous grid; this is a no-op then)
-    if (PREFIX) grid_dependency_wait();
+    // every thread waits for the previous grid before exiting: a dependent grid never
+    // completes before the one it follows (a no-op where it already waited)
+    grid_dependency_wait();
 }
 
 }  // namespace tc
@@ -905,7 +1158,14 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     pp.start_pos = a.start_pos;
     pp.cu_q = a.cu_q;
     pp.TQ = tc::kRowsTC / pp.G;
-    const dim3 grid((a.max_chunk + pp.TQ - 1) / pp.TQ, pp.Hkv, a.num_seqs);
+    pp.num_seqs = a.num_seqs;
+    pp.nqt = (a.max_chunk + pp.TQ - 1) / pp.TQ;
+    const long long items = (long long)pp.nqt * pp.Hkv * a.num_seqs;
+    if (items <= 0) return cudaSuccess;
+    if (items > INT32_MAX) return cudaErrorInvalidValue;
+    pp.num_items = (int)items;
+    // persistent: one CTA per SM at most (a CTA fills an SM's shared memory and TMEM)
+    const dim3 grid((unsigned)std::min<long long>(items, sm_count()));
     if (a.head_dim == 64) return launch_tc<64, false, 2>(pp, grid, stream);
     return launch_tc<128, false, 2>(pp, grid, stream);
 }
