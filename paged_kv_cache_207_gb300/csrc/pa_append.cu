@@ -4,8 +4,11 @@
 // Append (spindle, "Two bugs worth recording": append takes an explicit start
 // position): row i of sequence s goes to position start_pos[s] + i, i.e. slot
 // (pos % 16) of block block_tables[s][pos / 16].  One thread moves one 16-byte
-// piece of one (row, kv head) of K or V; reads are coalesced along the row,
-// writes land on the slot's 16-byte piece inside each chunk of the tile.
+// piece of one (row, kv head) of K and of V.  A warp takes 16 consecutive rows and
+// two adjacent pieces of one kv head (lane % 16 the row, lane / 16 the piece): it
+// reads whole 32-byte sectors of the rows, and where the rows fill consecutive slots
+// of a block (a chunk of a prefill) each store instruction writes two 256-byte runs
+// of the tile (a piece's 16 slots are contiguous in the pool).
 //
 // Copy (spindle, "Paging": refcounted copy-on-write forking): every byte of
 // block src goes to block dst in both pools; 16-byte vector loads and stores.
@@ -30,7 +33,8 @@ struct AParams {
     const int32_t* cu;
     int32_t* err;
     int max_blocks, S, total, num_blocks, Hkv, chunks;   // chunks = 16-byte pieces per row and head
-    long long items;                                      // total * Hkv * chunks
+    long long items;                                      // (FP8 / FP4) total * Hkv warps; (plain)
+                                                          // groups of 16 rows x Hkv x piece pairs x 32
 };
 
 // Sequence, position and physical block of new row `row` (reads only cu, start_pos
@@ -84,13 +88,18 @@ __global__ void __launch_bounds__(256) append_kernel(const AParams p) {
     if (item == 0) {
         if (__ldg(p.cu) != 0 || __ldg(p.cu + p.S) != p.total) raise_flag(p.err, PA_DEV_ERR_BAD_CU);
     }
-    const int ch = (int)(item % p.chunks);
-    const long long rh = item / p.chunks;
-    const int h = (int)(rh % p.Hkv);
-    const int row = (int)(rh / p.Hkv);
+    const int pairs = (p.chunks + 1) >> 1;
+    const long long wi = item >> 5;                       // the warp's (row group, head, pair)
+    const int pr = (int)(wi % pairs);
+    const long long gh = wi / pairs;
+    const int h = (int)(gh % p.Hkv);
+    const int row = (int)(gh / p.Hkv) * 16 + (int)(item & 15);
+    const int ch = 2 * pr + (int)((item >> 4) & 1);
     int s, slot;
     int32_t blk;
-    const bool ok = item < p.items && locate_row(p, row, true, s, slot, blk);
+    // (the two lanes of a row both look it up; the piece-0 lane reports a failure)
+    const bool ok = item < p.items && row < p.total && ch < p.chunks &&
+                    locate_row(p, row, ch == 0, s, slot, blk);
 
     // The address chain above read only inputs.  The pools (and, in principle, the new
     // rows) may still be in use by the previous kernel of the stream: wait for it.  Every
@@ -341,8 +350,8 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
     p.num_blocks = a.num_blocks;
     p.Hkv = a.num_kv_heads;
     p.chunks = a.head_dim * elem_bytes(a.dtype) / 16;
-    p.items = (long long)a.total_new * a.num_kv_heads * p.chunks;
-    if (p.items == 0) return cudaSuccess;
+    p.items = (long long)((a.total_new + 15) / 16) * a.num_kv_heads * ((p.chunks + 1) / 2) * 32;
+    if (a.total_new == 0 || p.chunks == 0) return cudaSuccess;
     const long long blocks = (p.items + 255) / 256;
     return launch_dependent(append_kernel, dim3((unsigned)blocks), stream, p);
 }
