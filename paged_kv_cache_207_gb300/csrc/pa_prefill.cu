@@ -334,9 +334,9 @@ __device__ void build_schedule(const PParams& p, uint8_t* smem) {
     const bool sorted = (long long)ncost + 4ll * ngroups <= L::SCRATCH && (p.num_items + grid - 1) / grid <= L::LISTCAP;
     const int tid = threadIdx.x, nthr = blockDim.x;
     if (!sorted) {
-        if (cta == 0)                                  // positions outside the table, flagged once
-            for (int g = tid; g < ngroups; g += nthr)
-                if (group_cost(p, g) < 0) raise_flag(p.err, PA_DEV_ERR_BAD_POS);
+        // positions outside the table, flagged once: each CTA checks its share of the groups
+        for (int g = cta * nthr + tid; g < ngroups; g += grid * nthr)
+            if (group_cost(p, g) < 0) raise_flag(p.err, PA_DEV_ERR_BAD_POS);
         if (tid == 0) *nlist = -1;
         __syncthreads();
         return;

@@ -18,7 +18,7 @@ from oracle import oracle as orc
 pytestmark = pytest.mark.gpu
 
 
-def _prefill_case(chunks, hq, hkv, d, seed):
+def _prefill_case(chunks, hq, hkv, d, seed, max_chunk=None):
     """chunks: list of (start, n).  Returns (workload, pools, q, out, starts, ns)."""
     totals = [s + n for s, n in chunks]
     wl = W.make_decode_workload("prefill", context_lens=np.array(totals) - 1, num_q_heads=hq,
@@ -35,7 +35,7 @@ def _prefill_case(chunks, hq, hkv, d, seed):
     cu_q = torch.tensor(np.concatenate([[0], np.cumsum(ns)]), dtype=torch.int32, device="cuda")
     pk.prefill_attention(out, q, dp.k, dp.v, dp.tables,
                          torch.tensor(starts, dtype=torch.int32, device="cuda"), cu_q, wl.scale,
-                         max_chunk=max(ns), err_flag=dp.err)
+                         max_chunk=max(ns) if max_chunk is None else max_chunk, err_flag=dp.err)
     torch.cuda.synchronize()
     return wl, dp, q, out, starts, ns
 
@@ -72,6 +72,21 @@ def test_prefill_chunks_against_oracle(hq, hkv, d):
     assert int(dp.err.item()) == 0
     assert torch.isfinite(out.float()).all()
     _check(wl, q, out, starts, ns)
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (14, 2, 64)])
+def test_prefill_items_beyond_the_schedule_lists(hq, hkv, d):
+    # A host bound on the chunk length far above the chunks (4096 against 1-9 tokens) gives
+    # 256 sequences x 57-114 query tiles x the kv heads as work items, and as many (sequence,
+    # query tile) groups: more than a CTA's shared-memory schedule holds, so every CTA walks
+    # the items by a stride over their natural order instead of a sorted list.  Most items are
+    # empty; every row must still match the oracle and nothing may be flagged.
+    rng = np.random.default_rng(31)
+    chunks = [(int(a), int(b)) for a, b in zip(rng.integers(0, 300, 256), rng.integers(1, 10, 256))]
+    wl, dp, q, out, starts, ns = _prefill_case(chunks, hq, hkv, d, seed=31, max_chunk=4096)
+    assert int(dp.err.item()) == 0
+    assert torch.isfinite(out.float()).all()
+    _check(wl, q, out, starts, ns, only=set(range(0, 256, 4)) | {255})
 
 
 def test_prefill_last_row_equals_decode_at_that_position():
