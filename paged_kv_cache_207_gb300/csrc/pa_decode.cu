@@ -767,6 +767,8 @@ decode_fp4_kernel(const KParams p) {
 
     for (int i = 0; i < nb_w; ++i) {
         const int st = i % NST;
+        // the table entry of the block this stage takes next, in flight during the tile
+        const int32_t nxt = i + NST < nb_w ? __ldg(trow + blk0 + warp + (i + NST) * NW) : -1;
         if ((issued >> st) & 1u) {
             if (!mbar_wait_bounded(bar0 + st * 8, (phase >> st) & 1u, kWaitLimitNs)) {
                 failed = true;
@@ -890,8 +892,7 @@ decode_fp4_kernel(const KParams p) {
             }
         }
         __syncwarp();
-        if (i + NST < nb_w && issue_blk(__ldg(trow + blk0 + warp + (i + NST) * NW), st))
-            issued |= 1u << st;
+        if (i + NST < nb_w && issue_blk(nxt, st)) issued |= 1u << st;
     }
     if (failed) {
         if (lane == 0) raise_flag(p.err, PA_DEV_ERR_TIMEOUT);
