@@ -374,37 +374,68 @@ def run_ours(args, rank, world, local):
 
     shared = args.shared_prefix
 
-    def decode(q_, tab_, lens_, pool, out=out):
+    def decode(q_, tab_, lens_, pool, out=out, strm=stream):
         kp, vp = pools[pool]
         if quant:
             dec = pk.decode_attention_fp8 if quant == "fp8" else pk.decode_attention_fp4
             dec(out, q_, kp, vp, tab_, lens_, wl.scale, workspace=ws, max_context_len_hint=hint,
-                err_flag=err, stream=stream)
+                err_flag=err, stream=strm)
         elif shared:
             pk.decode_attention_shared_prefix(out, q_, kp, vp, tab_, lens_, wl.scale, shared,
                                               workspace=ws, max_context_len_hint=hint,
-                                              err_flag=err, stream=stream)
+                                              err_flag=err, stream=strm)
         else:
             pk.decode_attention(out, q_, kp, vp, tab_, lens_, wl.scale, workspace=ws,
-                                max_context_len_hint=hint, err_flag=err, stream=stream)
+                                max_context_len_hint=hint, err_flag=err, stream=strm)
 
-    def step(ev_d0=None, ev_d1=None):
+    def step(ev_d0=None, ev_d1=None, strm=stream):
         base = counter[0] * rot
         counter[0] += 1
         for layer in range(rot):
             pool = (base + layer) % npools
-            append(*pools[pool], k_new, v_new, tables, start, cu, err_flag=err, stream=stream)
+            append(*pools[pool], k_new, v_new, tables, start, cu, err_flag=err, stream=strm)
             if ev_d0 is not None:
-                ev_d0[layer].record(stream)
-            decode(q, tables, lens, pool)
+                ev_d0[layer].record(strm)
+            decode(q, tables, lens, pool, strm=strm)
             if ev_d1 is not None:
-                ev_d1[layer].record(stream)
+                ev_d1[layer].record(strm)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     if int(err.item()) != 0:
         raise RuntimeError(f"device error flag {int(err.item())} during warm-up")
+
+    # The timed steps replay CUDA graphs of the same calls (one per phase of the pool
+    # rotation), as a serving loop would, so that host launch time does not pace short steps;
+    # without graph support (or with --no-graphs) they are launched directly.  The
+    # shared-prefix call is always launched directly: its prefix and suffix kernels run side
+    # by side through programmatic dependent launch, and replayed from a graph its step took
+    # 28.4 us against 24.3 us (GB300).
+    period = npools // math.gcd(rot, npools)
+    graphs = []
+    if not args.no_graphs and not shared:
+        try:
+            for j in range(period):
+                counter[0] = j
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, capture_error_mode="relaxed"):
+                    step(strm=None)                   # (the capture stream)
+                graphs.append(g)
+            for g in graphs:
+                g.replay()
+            torch.cuda.synchronize()
+        except Exception:                             # noqa: BLE001 -- plain launches instead
+            graphs = []
+            torch.cuda.synchronize()
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error flag {int(err.item())} in the captured steps")
+
+    def timed_step(i):
+        if graphs:
+            graphs[i % period].replay()
+        else:
+            step()
 
     K = args.steps
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -414,7 +445,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     t0.record(stream)
     for i in range(K):
-        step()
+        timed_step(i)
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -496,6 +527,7 @@ def run_ours(args, rank, world, local):
                    "layers_for_tokens_per_s": layers,
                    "layer_pools": rot,
                    "pool_sets": npools,
+                   "cuda_graphs": bool(graphs),
                    "l2": ("inputs larger than L2 (K/V pools %.2f GB per GPU vs 129 MB L2%s), no flush"
                           if pool_bytes > L2_BYTES else
                           "K/V pools %.2f GB fit in the 129 MB L2%s")
@@ -878,6 +910,12 @@ EXTRA_CONFIGS = [
     ("llama3-8b_prefill", {"workload": "llama3-8b_prefill"}),
 ]
 DROP_KEYS = ("metric", "n_gpus", "higher_is_better", "scaling", "vs_baseline", "data")
+# Workloads whose step is short (tens of microseconds; 0.1-0.2 ms) run at least this many
+# timed steps (and warm-up steps) in the default run: about 10 ms of timed work each.
+MIN_CONFIG_STEPS = {"llama3-8b_shared_prefix": 100, "llama3-8b_shared_prefix+sharing": 400,
+                    "llama3-8b_batch256+fp8": 60, "llama3-8b_batch256+fp4": 60,
+                    "llama3-8b_long_context+fp8": 50, "llama3-8b_long_context+fp4": 50}
+MIN_CONFIG_WARMUP = {"llama3-8b_shared_prefix+sharing": 20}
 
 
 def run_one(args, rank, world, local):
@@ -899,6 +937,9 @@ def run_extra_configs(args, rank, world, local) -> dict:
             setattr(sub, k, v)
         sub.steps = max(1, min(args.steps, 50))
         sub.warmup = max(3, min(args.warmup, 5))
+        # short steps get enough of them for a timed region of several milliseconds
+        sub.steps = max(sub.steps, MIN_CONFIG_STEPS.get(name, 0))
+        sub.warmup = max(sub.warmup, MIN_CONFIG_WARMUP.get(name, 0))
         try:
             res = run_one(sub, rank, world, local)
             out[name] = {k: v for k, v in res.items() if k not in DROP_KEYS}
@@ -919,7 +960,9 @@ def main():
     ap.add_argument("--workload", default="llama3-8b_batch256")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graphs", action="store_true",
-                    help="replay: launch every kernel directly instead of one CUDA graph per step")
+                    help="launch every kernel of the timed steps directly instead of replaying "
+                         "CUDA graphs of them (decode workloads: one per pool-rotation phase; "
+                         "replay: one per batch size)")
     ap.add_argument("--kv-dtype", choices=["bf16", "fp8", "fp4"], default="bf16",
                     help="K/V cache element type; fp8 = E4M3 codes with per-slot scales, "
                          "fp4 = MXFP4 (E2M1 codes, one E8M0 scale per 32 values)")
