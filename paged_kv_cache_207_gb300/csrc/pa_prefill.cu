@@ -100,7 +100,7 @@ __device__ __forceinline__ void raise_flag(int32_t* err, int bits) {
 
 namespace tc {
 
-// Two Q tiles of 128 rows (a, b) per CTA share every K/V tile; each has its own softmax
+// Two Q tiles of 128 rows (a, b) per item share every K/V tile; each has its own softmax
 // warpgroup, S and O in TMEM.  The MMA thread interleaves them so that one tile's
 // softmax runs while the tensor cores work for the other:
 //   S_a(0) S_b(0) | PV_a(0) S_a(1) PV_b(0) S_b(1) | PV_a(1) S_a(2) ...
@@ -309,14 +309,17 @@ __device__ __forceinline__ int group_cost(const PParams& p, int grp) {
 
 // The prefill's schedule.  The grid is persistent (at most one CTA per SM); the items,
 // sorted by decreasing cost (key tiles; ties by natural index), are dealt out in rounds of
-// gridDim.x, in CTA order in even rounds and reverse order in odd ones, so that every CTA
-// ends up with about the same work (a static stride over the natural order leaves the CTAs
-// that drew long chunks well behind).  Every CTA sorts the (sequence, query tile) groups
-// itself, the same way: the groups' costs and their histogram, a scan over the costs from
-// the largest, and a placement of the groups in natural order by one warp (equal costs keep
-// that order); it keeps the list of its own items with their geometry.  Where the costs or
-// the list would not fit, the CTA takes items blockIdx.x, + gridDim.x, ... instead (list
-// length -1).
+// gridDim.x: in CTA order in even rounds and reverse order in odd ones, and the last round
+// to the CTAs in order of their load so far (least loaded first, each item's estimated time
+// being 1.79 us per key tile plus 3.7 us), so that every CTA ends up with about the same
+// work (a static stride over the natural order leaves the CTAs that drew long chunks well
+// behind, and the plain alternation leaves the CTAs that take a last item behind those that
+// do not).  Every CTA sorts the (sequence, query tile) groups itself, the same way: the
+// groups' costs and their histogram, a scan over the costs from the largest, and a
+// placement of the groups in natural order by one warp (equal costs keep that order); it
+// keeps the list of its own items with their geometry.  Where the costs or the list would
+// not fit, the CTA takes items blockIdx.x, + gridDim.x, ... instead (list length -1).
+constexpr int kTileCost = 179, kItemCost = 370;      // (units of 10 ns)
 template <int D>
 __device__ void build_schedule(const PParams& p, uint8_t* smem) {
     using L = Smem<D, 2>;
@@ -326,12 +329,15 @@ __device__ void build_schedule(const PParams& p, uint8_t* smem) {
     const int grid = gridDim.x, cta = blockIdx.x;
     const int ncost = (p.max_blocks + kKeyBlocks - 1) / kKeyBlocks + 1;     // costs 0 .. ncost - 1
     const int ngroups = p.num_seqs * p.nqt;
-    // per group: cost, first row, its position, rows
+    // per group: cost, first row, its position, rows; the groups in sorted order; the CTAs' loads
     int* gcost = cnt + ncost;
     int* gq = gcost + ngroups;
     int* gp = gq + ngroups;
     int* gr = gp + ngroups;
-    const bool sorted = (long long)ncost + 4ll * ngroups <= L::SCRATCH && (p.num_items + grid - 1) / grid <= L::LISTCAP;
+    int* order = gr + ngroups;
+    int* load = order + ngroups;
+    const bool sorted = (long long)ncost + 5ll * ngroups + grid + 1 <= L::SCRATCH &&
+                        (p.num_items + grid - 1) / grid <= L::LISTCAP;
     const int tid = threadIdx.x, nthr = blockDim.x;
     if (!sorted) {
         // positions outside the table, flagged once: each CTA checks its share of the groups
@@ -371,8 +377,7 @@ __device__ void build_schedule(const PParams& p, uint8_t* smem) {
             run += __shfl_sync(0xffffffffu, incl, 31);
         }
         __syncwarp();
-        const int total = run * p.Hkv;                 // live items
-        // rank R of the sorted items goes to CTA owner(R) as its item R / grid
+        // order[position] = group
         const uint32_t lt = (1u << lane) - 1u;
         for (int g0 = 0; g0 < ngroups; g0 += 32) {
             const int g = g0 + lane;
@@ -383,20 +388,40 @@ __device__ void build_schedule(const PParams& p, uint8_t* smem) {
             __syncwarp();
             if (c > 0 && (same & lt) == 0u) cnt[c] += __popc(same);
             __syncwarp();
-            if (c > 0) {
-                const int r0 = pos * p.Hkv, r1 = r0 + p.Hkv;        // the group's ranks
-                const int s = g / p.nqt, x = g - s * p.nqt;
-                for (int rd = r0 / grid; rd * grid < r1; ++rd) {
-                    const int R = rd * grid + ((rd & 1) ? grid - 1 - cta : cta);
-                    if (R >= r0 && R < r1) list[rd] = ListEntry{(s * p.Hkv + (R - r0)) * p.nqt + x, gq[g], gp[g], gr[g]};
-                }
-            }
+            if (c > 0) order[pos] = g;
         }
-        if (lane == 0) {
-            int m = 0;
-            while (m * grid + ((m & 1) ? grid - 1 - cta : cta) < total) ++m;
-            *nlist = m;
+        if (lane == 0) load[grid] = run;              // live groups
+    }
+    __syncthreads();
+    const int total = load[grid] * p.Hkv;              // live items
+    const int rounds = (total + grid - 1) / grid;
+    // item of rank R (position R / Hkv of the sorted groups, kv head R % Hkv)
+    auto entry = [&](int R) {
+        const int g = order[R / p.Hkv], s = g / p.nqt, x = g - s * p.nqt;
+        return ListEntry{(s * p.Hkv + R % p.Hkv) * p.nqt + x, gq[g], gp[g], gr[g]};
+    };
+    auto snake = [&](int rd, int c) { return rd * grid + ((rd & 1) ? grid - 1 - c : c); };
+    // the rounds before the last, alternating: every CTA's load, and this CTA's items
+    for (int c = tid; c < grid; c += nthr) {
+        int l = 0;
+        for (int rd = 0; rd + 1 < rounds; ++rd) l += gcost[order[snake(rd, c) / p.Hkv]] * kTileCost + kItemCost;
+        load[c] = l;
+    }
+    for (int rd = tid; rd + 1 < rounds; rd += nthr) list[rd] = entry(snake(rd, cta));
+    __syncthreads();
+    if (tid == 0 && rounds > 0) {
+        // the last round: its k-th largest item to the CTA with the k-th smallest load
+        const int mine = load[cta];
+        int k = 0;
+        for (int c = 0; c < grid; ++c) {
+            const int l = load[c];
+            k += (l < mine || (l == mine && c < cta)) ? 1 : 0;
         }
+        const int R = (rounds - 1) * grid + k;
+        if (R < total) list[rounds - 1] = entry(R);
+        *nlist = R < total ? rounds : rounds - 1;
+    } else if (tid == 0) {
+        *nlist = 0;
     }
     __syncthreads();
 }
