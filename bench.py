@@ -727,10 +727,16 @@ def run_replay(args, rank, world, local):
     rw = W.spindle_replay(device="cuda", seed=208 + 1000 * rank)
     barrier(world)
     graphs = not args.no_graphs
-    for _ in range(max(1, min(args.warmup, 3))):
-        Replay(rw, device="cuda", use_graphs=graphs).run()
+    # warm-up runs on the instance that is timed, so that its graphs (one per running-batch
+    # size) are captured before the timed run, as an engine captures them once
+    rp = Replay(rw, device="cuda", use_graphs=graphs)
+    for i in range(max(1, min(args.warmup, 3))):
+        if i:
+            rp.reset()
+        rp.run()
     torch.cuda.synchronize()
-    st = Replay(rw, device="cuda", time_gpu=True, use_graphs=graphs).run()
+    rp.reset(time_gpu=True)
+    st = rp.run()
     barrier(world)
     wall = all_max(st.wall_s, world)
     gpu_s = all_max(st.gpu_ms / 1e3, world)

@@ -396,6 +396,12 @@ pa_status pa_bm_prepare_append(pa_block_manager* bm, int32_t seq, int32_t start_
 /* Host array row_out (max_blocks entries) receives the block table, -1 padded. */
 pa_status pa_bm_block_table(const pa_block_manager* bm, int32_t seq, int32_t* row_out,
                             int32_t max_blocks, int32_t* num_blocks_out);
+/* The block tables of num_seqs sequences in one call (an engine's per-iteration batch):
+ * host array rows_out [num_seqs][max_blocks] receives row i = the table of seqs[i], -1
+ * padded, as pa_bm_block_table would write it.  PA_ERR_INVALID_ARG for an unknown sequence
+ * or a table longer than max_blocks (rows before it may have been written). */
+pa_status pa_bm_block_tables(const pa_block_manager* bm, const int32_t* seqs, int32_t num_seqs,
+                             int32_t* rows_out, int32_t max_blocks);
 pa_status pa_bm_seq_len(const pa_block_manager* bm, int32_t seq, int32_t* len_out);
 pa_status pa_bm_refcount(const pa_block_manager* bm, int32_t block, int32_t* refcount_out);
 pa_status pa_bm_stats(const pa_block_manager* bm, pa_bm_stats_t* out);

@@ -10,6 +10,8 @@ from __future__ import annotations
 import ctypes
 import os
 
+import numpy as np
+
 import torch
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpaged_kv.so")
@@ -39,7 +41,8 @@ EXPORTED = [
     "pa_append_kv_fp4", "pa_decode_attention_fp4",
     "pa_prefill_attention", "pa_bm_create", "pa_bm_destroy",
     "pa_bm_add_seq", "pa_bm_fork", "pa_bm_free_seq", "pa_bm_blocks_needed",
-    "pa_bm_prepare_append", "pa_bm_block_table", "pa_bm_seq_len", "pa_bm_refcount", "pa_bm_stats",
+    "pa_bm_prepare_append", "pa_bm_block_table", "pa_bm_block_tables", "pa_bm_seq_len",
+    "pa_bm_refcount", "pa_bm_stats",
 ]
 
 
@@ -108,11 +111,13 @@ def lib() -> ctypes.CDLL:
     L.pa_bm_blocks_needed.argtypes = [p, i32, i32, i32, ip]
     L.pa_bm_prepare_append.argtypes = [p, i32, i32, i32, ip, i32, ip]
     L.pa_bm_block_table.argtypes = [p, i32, ip, i32, ip]
+    L.pa_bm_block_tables.argtypes = [p, ip, i32, ip, i32]
     L.pa_bm_seq_len.argtypes = [p, i32, ip]
     L.pa_bm_refcount.argtypes = [p, i32, ip]
     L.pa_bm_stats.argtypes = [p, ctypes.POINTER(BmStats)]
     for n in ("pa_bm_create", "pa_bm_add_seq", "pa_bm_fork", "pa_bm_free_seq",
               "pa_bm_blocks_needed", "pa_bm_prepare_append", "pa_bm_block_table",
+              "pa_bm_block_tables",
               "pa_bm_seq_len", "pa_bm_refcount", "pa_bm_stats"):
         getattr(L, n).restype = ctypes.c_int
     _lib = L
@@ -397,6 +402,20 @@ class BlockManager:
         buf = (ctypes.c_int32 * max(max_blocks, 1))()
         check("pa_bm_block_table", lib().pa_bm_block_table(self._h, seq, buf, max_blocks, None))
         return list(buf[:max_blocks])
+
+    def block_tables(self, seqs, max_blocks: int, out=None):
+        """The tables of several sequences in one call: int32 array [len(seqs)][max_blocks]
+        (written into `out`, a C-contiguous int32 numpy array of that shape, if given)."""
+        ids = np.ascontiguousarray(np.asarray(seqs, np.int32))
+        n = int(ids.size)
+        if out is None:
+            out = np.empty((n, max_blocks), np.int32)
+        if out.dtype != np.int32 or not out.flags.c_contiguous or out.shape != (n, max_blocks):
+            raise ValueError("out: a C-contiguous int32 array of shape (len(seqs), max_blocks)")
+        ipp = ctypes.POINTER(ctypes.c_int32)
+        check("pa_bm_block_tables", lib().pa_bm_block_tables(
+            self._h, ids.ctypes.data_as(ipp), n, out.ctypes.data_as(ipp), max_blocks))
+        return out
 
     def seq_len(self, seq: int) -> int:
         out = ctypes.c_int32()

@@ -163,6 +163,18 @@ pa_status pa_bm_block_table(const pa_block_manager* bm, int32_t seq, int32_t* ro
     return PA_OK;
 }
 
+pa_status pa_bm_block_tables(const pa_block_manager* bm, const int32_t* seqs, int32_t num_seqs,
+                             int32_t* rows_out, int32_t max_blocks) {
+    if (!bm || num_seqs < 0 || max_blocks < 0 || (num_seqs > 0 && !seqs)) return PA_ERR_INVALID_ARG;
+    if (num_seqs > 0 && max_blocks > 0 && !rows_out) return PA_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < num_seqs; ++i) {
+        const pa_status st = pa_bm_block_table(bm, seqs[i], rows_out + (size_t)i * max_blocks,
+                                               max_blocks, nullptr);
+        if (st != PA_OK) return st;
+    }
+    return PA_OK;
+}
+
 pa_status pa_bm_seq_len(const pa_block_manager* bm, int32_t seq, int32_t* len_out) {
     if (!bm || !len_out) return PA_ERR_INVALID_ARG;
     auto it = bm->seqs.find(seq);

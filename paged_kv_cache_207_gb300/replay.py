@@ -89,6 +89,22 @@ class Replay:
             self.h_pos = torch.empty_like(self.g_pos, device="cpu").pin_memory()
             self.graphs = {}          # running-batch size -> (graph, per-layer outputs)
             self.h_free = None        # event: the last staging copy has been read
+        self._owns_bm = block_manager is None
+        self._reset_host()
+
+    def reset(self, time_gpu: bool | None = None) -> None:
+        """Start the workload over on the same pools, buffers and captured graphs (as an
+        engine keeps its graphs across batches): the schedule, the block manager and the
+        statistics begin afresh.  Every value a decode reads is appended again first."""
+        if not self._owns_bm:
+            raise RuntimeError("reset() needs the replay's own block manager")
+        if time_gpu is not None:
+            self.time_gpu = time_gpu and self.dev is not None
+        self.bm = pk.BlockManager(self.rw.num_blocks)
+        self._reset_host()
+
+    def _reset_host(self) -> None:
+        rw = self.rw
         n = rw.num_seqs
         self.gen_done = [0] * n
         self.bm_id = [-1] * n
@@ -98,6 +114,7 @@ class Replay:
         if rw.num_children:
             self.waiting.append(("group", list(range(first_child, n))))
         self.running: list[int] = []          # admission order
+        self._timed: list = []                 # (start, end) events of the timed iterations
         self.stats = ReplayStats()
 
     # -- host scheduling ------------------------------------------------------
@@ -162,6 +179,14 @@ class Replay:
         return pairs
 
     # -- device work ------------------------------------------------------------
+    def _tables_into(self, ids: list, out: np.ndarray) -> np.ndarray:
+        """The block tables of sequences `ids` into the int32 rows of `out`: one call into
+        the native block manager where it offers the batch, else one per sequence."""
+        if hasattr(self.bm, "block_tables"):
+            return self.bm.block_tables(ids, self.max_blocks, out=out)
+        out[:] = np.asarray([self.bm.block_table(i, self.max_blocks) for i in ids], np.int32)
+        return out
+
     def _i32(self, a) -> torch.Tensor:
         return torch.tensor(np.asarray(a, np.int32), dtype=torch.int32, device=self.dev)
 
@@ -221,7 +246,8 @@ class Replay:
             return self._device_work_graph(run, ctx, prefill, pairs, observer)
         rw = self.rw
         S = len(run)
-        tables = self._i32([self.bm.block_table(self.bm_id[s], self.max_blocks) for s in run])
+        tables = self._i32(self._tables_into([self.bm_id[s] for s in run],
+                                             np.empty((S, self.max_blocks), np.int32)))
         start = self._i32(ctx)
         lens = self._i32(ctx + 1)
         cu = self._i32(np.arange(S + 1))
@@ -266,25 +292,37 @@ class Replay:
         if observer is not None:
             observer(self, run, ctx, outs)
         if ev0 is not None:
-            ev1.synchronize()
-            self.stats.gpu_ms += ev0.elapsed_time(ev1)
+            self._timed.append((ev0, ev1))        # read after the run: no wait per iteration
 
     def _device_work_graph(self, run, ctx, prefill, pairs, observer) -> None:
         rw = self.rw
         S = len(run)
+        # host side first: the iteration's tables and positions into the pinned staging (the
+        # previous iteration's copies out of it must be done), and the admission / copy inputs
+        if self.h_free is not None:
+            self.h_free.synchronize()
+        self._tables_into([self.bm_id[s] for s in run], self.h_tables[:S].numpy())
+        self.h_start[:S].numpy()[:] = ctx
+        self.h_lens[:S].numpy()[:] = ctx + 1
+        self.h_seq[:S].numpy()[:] = np.asarray(run, np.int64)
+        self.h_pos[:S].numpy()[:] = ctx.astype(np.int64)
+        pf_tables = pf_start = pf_cu = pf_seq = pf_pos = None
+        if prefill:
+            pf_tables = self._i32([p[1] for p in prefill])
+            pf_start = self._i32([0] * len(prefill))
+            pf_cu = self._i32(np.concatenate([[0], np.cumsum([p[2] for p in prefill])]))
+            pf_seq = torch.cat([torch.full((p[2],), p[0], dtype=torch.long) for p in prefill]).to(self.dev)
+            pf_pos = torch.cat([torch.arange(p[2]) for p in prefill]).to(self.dev)
+        pairs_t = self._i32(pairs).reshape(-1, 2) if pairs else None
+        if S not in self.graphs:
+            self.graphs[S] = self._capture(S)
+        g, outs = self.graphs[S]
+        # then the device work, back to back
         ev0 = ev1 = None
         if self.time_gpu:
             ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             ev0.record()
         if prefill or pairs:       # admissions and copy-on-write copies: ordinary launches
-            pf_tables = pf_start = pf_cu = pf_seq = pf_pos = None
-            if prefill:
-                pf_tables = self._i32([p[1] for p in prefill])
-                pf_start = self._i32([0] * len(prefill))
-                pf_cu = self._i32(np.concatenate([[0], np.cumsum([p[2] for p in prefill])]))
-                pf_seq = torch.cat([torch.full((p[2],), p[0], dtype=torch.long) for p in prefill]).to(self.dev)
-                pf_pos = torch.cat([torch.arange(p[2]) for p in prefill]).to(self.dev)
-            pairs_t = self._i32(pairs).reshape(-1, 2) if pairs else None
             for l in range(rw.num_layers):
                 if prefill:
                     pk.append_kv(self.k[l], self.v[l], rw.k[pf_seq, l, pf_pos].contiguous(),
@@ -294,32 +332,19 @@ class Replay:
                 if pairs_t is not None:
                     pk.copy_block(self.k[l], self.v[l], pairs_t, err_flag=self.err)
                     self.stats.launches += 1
-        if self.h_free is not None:      # the previous copy out of the staging must be done
-            self.h_free.synchronize()
-        self.h_tables[:S].numpy()[:] = np.asarray([self.bm.block_table(self.bm_id[s], self.max_blocks)
-                                                   for s in run], np.int32)
-        self.h_start[:S].numpy()[:] = ctx
-        self.h_lens[:S].numpy()[:] = ctx + 1
-        self.h_seq[:S].numpy()[:] = np.asarray(run, np.int64)
-        self.h_pos[:S].numpy()[:] = ctx.astype(np.int64)
         for d, h in ((self.g_tables, self.h_tables), (self.g_start, self.h_start),
                      (self.g_lens, self.h_lens), (self.g_seq, self.h_seq), (self.g_pos, self.h_pos)):
             d[:S].copy_(h[:S], non_blocking=True)
             self.stats.h2d_bytes += h[:S].numel() * h.element_size()
         self.h_free = torch.cuda.Event()
         self.h_free.record()
-        if S not in self.graphs:
-            self.graphs[S] = self._capture(S)
-        g, outs = self.graphs[S]
         g.replay()
         self.stats.launches += 2 * rw.num_layers
         if ev1 is not None:
             ev1.record()
+            self._timed.append((ev0, ev1))        # read after the run: no wait per iteration
         if observer is not None:
             observer(self, run, ctx, [o.clone() for o in outs])
-        if ev0 is not None:
-            ev1.synchronize()
-            self.stats.gpu_ms += ev0.elapsed_time(ev1)
 
     def _finish_iteration(self, run, ctx) -> None:
         """Accounting, then advance every running length once for the whole iteration."""
@@ -353,6 +378,8 @@ class Replay:
             return self.stats
         torch.cuda.synchronize()
         self.stats.wall_s = time.perf_counter() - t
+        self.stats.gpu_ms += sum(a.elapsed_time(b) for a, b in self._timed)
+        self._timed.clear()
         if int(self.err.item()) != 0:
             raise RuntimeError(f"device error flag {int(self.err.item())} during the replay")
         return self.stats

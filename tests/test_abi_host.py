@@ -127,6 +127,14 @@ def test_block_manager_matches_oracle_model_op_for_op(native):
         for s, p in ids.items():
             assert bm.block_table(p, 64)[:len(om.tables[s])] == om.tables[s]
             assert bm.seq_len(p) == om.lengths[s]
+        if ids:
+            # the batched tables equal the per-sequence ones, row for row (-1 padded)
+            order = list(ids)
+            rnd.shuffle(order)
+            rows = bm.block_tables([ids[s] for s in order], 64)
+            for r, s in zip(rows, order):
+                want = om.tables[s] + [-1] * (64 - len(om.tables[s]))
+                assert r.tolist() == want
         st = bm.stats()
         assert st["physical_blocks"] == om.physical_blocks()
         assert st["logical_tokens"] == om.logical_tokens()
@@ -152,6 +160,13 @@ def test_block_manager_fork_numbers_from_the_paging_section(native):
 def test_block_manager_rejects_holes_and_unknown_sequences(native):
     bm = native.BlockManager(8)
     s = bm.add_seq()
+    with pytest.raises(native.PagedKVError):
+        bm.block_tables([s, 99], 4)           # an unknown sequence in the batch
+    t = bm.add_seq()
+    bm.prepare_append(t, 0, 40)
+    with pytest.raises(native.PagedKVError):
+        bm.block_tables([t], 2)               # three blocks do not fit in two entries
+    assert bm.block_tables([], 4).shape == (0, 4)
     with pytest.raises(native.PagedKVError):
         bm.prepare_append(s, 17, 1)          # would skip block 0
     with pytest.raises(native.PagedKVError):

@@ -15,7 +15,7 @@ from oracle import oracle as orc
 pytestmark = pytest.mark.gpu
 
 
-def _run_checked(rw, **kw):
+def _run_checked(rw, reruns=0, **kw):
     from paged_kv_cache_207_gb300 import build
     build.build()
     from paged_kv_cache_207_gb300.replay import Replay
@@ -39,6 +39,12 @@ def _run_checked(rw, **kw):
 
     rp = Replay(rw, device="cuda", **kw)
     stats = rp.run(observer=observer)
+    for _ in range(reruns):
+        # the same workload again on the same pools and captured graphs: blocks now hold
+        # the first run's values instead of NaN, and every read must still be this run's
+        rp.reset()
+        checked[0] = 0
+        stats = rp.run(observer=observer)
     assert all(s == "done" for s in rp.state)
     assert worst[0] <= BF16_ATOL, worst[0]
     assert checked[0] > 0
@@ -64,6 +70,14 @@ def test_spindle_replay_with_cuda_graphs():
     rw = W.spindle_replay(device="cuda", num_blocks=150)
     stats = _run_checked(rw, use_graphs=True)
     assert stats.preemptions > 0
+
+
+def test_spindle_replay_reset_reuses_pools_and_graphs():
+    from paged_kv_cache_207_gb300 import workloads as W
+    rw = W.spindle_replay(device="cuda", num_blocks=150)
+    stats = _run_checked(rw, reruns=1, use_graphs=True)
+    assert stats.preemptions > 0
+    assert stats.generated_tokens == int(rw.gen_lens.sum())
 
 
 def test_spindle_replay_partial_parent_copies_on_write():
