@@ -18,7 +18,7 @@ from oracle import oracle as orc
 pytestmark = pytest.mark.gpu
 
 
-def _prefill_case(chunks, hq, hkv, d, seed, max_chunk=None):
+def _prefill_case(chunks, hq, hkv, d, seed, max_chunk=None, scale=None):
     """chunks: list of (start, n).  Returns (workload, pools, q, out, starts, ns)."""
     totals = [s + n for s, n in chunks]
     wl = W.make_decode_workload("prefill", context_lens=np.array(totals) - 1, num_q_heads=hq,
@@ -34,13 +34,14 @@ def _prefill_case(chunks, hq, hkv, d, seed, max_chunk=None):
     out = torch.full_like(q, float("nan"))
     cu_q = torch.tensor(np.concatenate([[0], np.cumsum(ns)]), dtype=torch.int32, device="cuda")
     pk.prefill_attention(out, q, dp.k, dp.v, dp.tables,
-                         torch.tensor(starts, dtype=torch.int32, device="cuda"), cu_q, wl.scale,
+                         torch.tensor(starts, dtype=torch.int32, device="cuda"), cu_q,
+                         wl.scale if scale is None else scale,
                          max_chunk=max(ns) if max_chunk is None else max_chunk, err_flag=dp.err)
     torch.cuda.synchronize()
     return wl, dp, q, out, starts, ns
 
 
-def _check(wl, q, out, starts, ns, rows_per_seq=None, only=None):
+def _check(wl, q, out, starts, ns, rows_per_seq=None, only=None, scale=None):
     kr, vr = wl.k_rows.cpu(), wl.v_rows.cpu()
     qc, oc = q.cpu(), out.float().cpu().double().numpy()
     G = wl.num_q_heads // wl.num_kv_heads
@@ -59,7 +60,8 @@ def _check(wl, q, out, starts, ns, rows_per_seq=None, only=None):
             V = vr[logical[:p + 1]].contiguous()
             for h in range(wl.num_q_heads):
                 want = orc.decode_contig(qc[base + i, h], K, V, h // G, num_kv_heads=wl.num_kv_heads,
-                                         head_dim=wl.head_dim, scale=wl.scale, dtype=orc.BF16)
+                                         head_dim=wl.head_dim, scale=wl.scale if scale is None else scale,
+                                         dtype=orc.BF16)
                 worst = max(worst, float(np.abs(oc[base + i, h] - want).max()))
         base += n
     assert worst <= BF16_ATOL, worst
@@ -87,6 +89,18 @@ def test_prefill_items_beyond_the_schedule_lists(hq, hkv, d):
     assert int(dp.err.item()) == 0
     assert torch.isfinite(out.float()).all()
     _check(wl, q, out, starts, ns, only=set(range(0, 256, 4)) | {255})
+
+
+@pytest.mark.parametrize("hq,hkv,d,sign", [(32, 8, 128, -1.0), (14, 2, 64, -1.0), (32, 8, 128, 0.0)])
+def test_prefill_negative_and_zero_scale(hq, hkv, d, sign):
+    # A negative scale goes to the tensor cores as |scale| on -q (the sign flipped in the
+    # query tile); a zero scale weighs every visible key alike (each row: the mean of V).
+    chunks = [(0, 70), (300, 130), (17, 9)]
+    scale = sign / float(np.sqrt(d))
+    wl, dp, q, out, starts, ns = _prefill_case(chunks, hq, hkv, d, seed=5, scale=scale)
+    assert int(dp.err.item()) == 0
+    assert torch.isfinite(out.float()).all()
+    _check(wl, q, out, starts, ns, scale=scale)
 
 
 def test_prefill_last_row_equals_decode_at_that_position():

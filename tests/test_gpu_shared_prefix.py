@@ -53,6 +53,24 @@ def test_shared_prefix_against_oracle(shared, suffixes, hq, hkv, d):
     assert_close(wl, as_f64(out), as_f64(ref), "prefix vs ordinary")
 
 
+@pytest.mark.parametrize("rows_hq", [(8, 32), (64, 32)])
+def test_shared_prefix_negative_scale(rows_hq):
+    # The prefix partitions run on the tensor cores with |scale| on -q (the sign moved into
+    # the query tile): 8 sequences give one 128-row Q tile per prefix CTA, 64 give two.
+    S, hq = rows_hq
+    suffixes = [1 + 37 * i % 400 for i in range(S)]
+    lens = [1024 + n - 1 for n in suffixes]
+    wl = W.make_decode_workload("prefix_neg", context_lens=lens, num_q_heads=hq, num_kv_heads=8,
+                                head_dim=128, dtype="bf16", seed=77 + S, device="cuda",
+                                shared_prefix=1024, scale=-1.0 / np.sqrt(128.0))
+    dp = DevicePools(wl)
+    out, _ = _prefix_step(wl, dp, 1024)
+    pairs = [(s, h) for s in range(wl.num_seqs) for h in range(hq)]
+    want = oracle_contig(wl, pairs)
+    assert_close(wl, as_f64(out).reshape(len(pairs), 128), want, "prefix, negative scale")
+    assert int(dp.err.item()) == 0
+
+
 def test_short_prefix_falls_back_to_the_ordinary_path_bitwise():
     lens = [300 + n for n in (1, 50, 200)]
     wl = W.make_decode_workload("short", context_lens=lens, num_q_heads=32, num_kv_heads=8,
