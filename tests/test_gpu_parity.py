@@ -368,3 +368,27 @@ def test_repeated_calls_on_one_workspace_give_the_same_bits():
         ws.fill_(0x7F)     # garbage for the next call
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
     assert int(dp.err.item()) == 0
+
+
+def test_one_workspace_across_batch_sizes_and_head_dims():
+    # a workspace sized for the largest call serves smaller calls of other shapes, in
+    # between and after: no call depends on what another left in it
+    big = W.make_decode_workload("ws_big", context_lens=[5000, 700, 2600, 3100], num_q_heads=32,
+                                 num_kv_heads=8, head_dim=128, dtype="bf16", seed=12, device="cuda")
+    small = W.make_decode_workload("ws_small", context_lens=[1500, 3000], num_q_heads=14,
+                                   num_kv_heads=2, head_dim=64, dtype="bf16", seed=13, device="cuda")
+    ws = pk.decode_workspace(4, 32, 8, 128, big.max_blocks)
+    for wl in (big, small, big):
+        dp = DevicePools(wl, canary=False)
+        k_new, v_new, start, cu, lens = dp.step_inputs()
+        pk.append_kv(dp.k, dp.v, k_new, v_new, dp.tables, start, cu, err_flag=dp.err)
+        out = torch.empty_like(wl.q)
+        assert ws.numel() >= pk.decode_workspace_size(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads,
+                                                      wl.head_dim, wl.max_blocks)
+        pk.decode_attention(out, wl.q, dp.k, dp.v, dp.tables, lens, wl.scale, workspace=ws,
+                            err_flag=dp.err)
+        torch.cuda.synchronize()
+        pairs = _all_pairs(wl)
+        assert_close(wl, as_f64(out).reshape(len(pairs), wl.head_dim), oracle_contig(wl, pairs),
+                     f"shared workspace {wl.name}")
+        assert int(dp.err.item()) == 0
