@@ -373,6 +373,14 @@ def run_ours(args, rank, world, local):
     counter = [0]          # steps issued so far: step i, layer l uses pool (i rot + l) % npools
 
     shared = args.shared_prefix
+    # the bf16 / f32 caches take the step as one call (the decode kernel writes the new
+    # token itself); the shared-prefix and quantised paths append, then decode
+    fused = not quant and not shared
+
+    def append_decode(q_, kn, vn, tab_, lens_, pool, out=out, strm=stream):
+        kp, vp = pools[pool]
+        pk.append_decode_attention(out, q_, kp, vp, kn, vn, tab_, lens_, wl.scale, workspace=ws,
+                                   max_context_len_hint=hint, err_flag=err, stream=strm)
 
     def decode(q_, tab_, lens_, pool, out=out, strm=stream):
         kp, vp = pools[pool]
@@ -393,10 +401,14 @@ def run_ours(args, rank, world, local):
         counter[0] += 1
         for layer in range(rot):
             pool = (base + layer) % npools
-            append(*pools[pool], k_new, v_new, tables, start, cu, err_flag=err, stream=strm)
+            if not fused:
+                append(*pools[pool], k_new, v_new, tables, start, cu, err_flag=err, stream=strm)
             if ev_d0 is not None:
                 ev_d0[layer].record(strm)
-            decode(q, tables, lens, pool, strm=strm)
+            if fused:
+                append_decode(q, k_new, v_new, tables, lens, pool, strm=strm)
+            else:
+                decode(q, tables, lens, pool, strm=strm)
             if ev_d1 is not None:
                 ev_d1[layer].record(strm)
 
@@ -489,8 +501,11 @@ def run_ours(args, rank, world, local):
         counter[0] += 1
         for layer in range(rot):
             pool = (base + layer) % npools
-            append(*pools[pool], d_k, d_v, d_tab, d_start, d_cu, err_flag=err, stream=stream)
-            decode(d_q, d_tab, d_lens, pool, o)
+            if fused:
+                append_decode(d_q, d_k, d_v, d_tab, d_lens, pool, o)
+            else:
+                append(*pools[pool], d_k, d_v, d_tab, d_start, d_cu, err_flag=err, stream=stream)
+                decode(d_q, d_tab, d_lens, pool, o)
     e2e_step_ms, host_ms, h_last = e2e.run(e2e_compute, max(3, args.warmup), K, world)
     e2e_ms = e2e_step_ms * K
     e2e_value = total_bytes / (e2e_ms / 1e3) / 1e9
@@ -502,9 +517,13 @@ def run_ours(args, rank, world, local):
         peak, peak_src = float(peaks["hbm_gbs"]), "measured"
     else:
         peak, peak_src = 6800.0, "fallback"
-    achieved = dbytes / (dec_ms / 1e3) / 1e9
+    # the timed call's algorithmic bytes: the decode's, and the append's when the decode
+    # kernel writes the new token itself
+    kbytes = dbytes + (append_bytes(wl, args.kv_dtype) if fused else 0)
+    achieved = kbytes / (dec_ms / 1e3) / 1e9
     pt = {"fp8": 1024, "fp4": 2048}.get(args.kv_dtype, 1024 if D == 64 and not shared else 512)
-    launches_per_step = (1 + 1 + (1 if int(math.ceil(hint / pt)) > 1 or shared >= 512 else 0) +
+    launches_per_step = ((0 if fused else 1) + 1 +
+                         (1 if int(math.ceil(hint / pt)) > 1 or shared >= 512 else 0) +
                          (1 if shared >= 512 else 0)) * rot
 
     result = {
@@ -520,8 +539,12 @@ def run_ours(args, rank, world, local):
                    "num_kv_heads": Hkv, "head_dim": D, "block_size": 16,
                    "context_tokens_after_append": int((wl.context_lens + 1).sum()),
                    "max_context": int(hint),
-                   "step": ("%d layers x (" % rot if rot > 1 else "") + "pa_append_kv (1 token/seq) + " +
-                           ("pa_decode_attention_shared_prefix" if shared else "pa_decode_attention") +
+                   "step": ("%d layers x (" % rot if rot > 1 else "") +
+                           ("pa_append_decode_attention (1 token/seq appended by the decode kernel)"
+                            if fused else "pa_append_kv (1 token/seq) + " +
+                            ("pa_decode_attention_shared_prefix" if shared else
+                             {"fp8": "pa_decode_attention_fp8",
+                              "fp4": "pa_decode_attention_fp4"}.get(quant, "pa_decode_attention"))) +
                            (")" if rot > 1 else ""),
                    "shared_prefix_tokens": shared,
                    "layers_for_tokens_per_s": layers,
@@ -543,12 +566,14 @@ def run_ours(args, rank, world, local):
             "logical_gbs": round(value * (step_bytes - unique_kv_bytes(wl, wl_shared) +
                                           logical_kv_bytes(wl)) / step_bytes, 1)} if wl_shared else {}),
         "tokens_per_s": round(tokens_per_s, 1),
-        "roofline": {"kernel": {"fp8": "pa_decode_attention_fp8", "fp4": "pa_decode_attention_fp4"}.get(
-                                 quant, "pa_decode_attention") + " (main kernel + partition merge)",
+        "roofline": {"kernel": ("pa_append_decode_attention (main kernel with the append + partition merge)"
+                                if fused else
+                                {"fp8": "pa_decode_attention_fp8", "fp4": "pa_decode_attention_fp4"}.get(
+                                    quant, "pa_decode_attention") + " (main kernel + partition merge)"),
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None if wl_shared else profiled_traffic(args.workload, args.kv_dtype),
-                     "algorithmic_bytes_per_launch": dbytes, "avg_launch_ms": round(dec_ms, 5)},
+                     "algorithmic_bytes_per_launch": kbytes, "avg_launch_ms": round(dec_ms, 5)},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms / K, 5),
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "host_enqueue_ms_per_step": round(host_ms, 5)},

@@ -175,6 +175,38 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, cons
                               int32_t* dev_err_flag, void* stream);
 
 /*
+ * pa_append_decode_attention -- one decode step in one call: the step's new
+ * token is written into the cache, then attended over with the rest (spindle,
+ * "Paging" for the step, "Two bugs worth recording" for the explicit position).
+ *
+ *   k_new, v_new     [num_seqs][num_kv_heads][head_dim], element type `dtype`,
+ *                    16-byte aligned: sequence s's new K and V rows
+ *   context_lens     int32 [num_seqs]: the length AFTER the append; the new
+ *                    rows go to position context_lens[s] - 1
+ * Every other argument, the workspace and the result are those of
+ * pa_decode_attention.  The pools after the call hold exactly the bytes of
+ * pa_append_kv(k_new, v_new, start_pos = context_lens - 1, one row per
+ * sequence), and `out` equals pa_decode_attention's after that append, bit for
+ * bit: this call is the two in one kernel (the CTA of the partition holding
+ * the last position stores the row into the pools and into its own copy of
+ * that block).  A sequence of
+ * length 0 appends nothing.  A table entry out of range for the new position
+ * sets PA_DEV_ERR_BAD_BLOCK and nothing is written there; a length beyond the
+ * table sets PA_DEV_ERR_BAD_POS, appends nothing (as pa_append_kv) and is
+ * clamped for the attention (as in pa_decode_attention).
+ * While PA_DEV_ERR_TIMEOUT is set the call writes neither `out` nor the pools.
+ * bf16 and f32 caches (the FP8 and FP4 paths keep their own append).
+ */
+pa_status pa_append_decode_attention(void* out, const void* q, void* k_pool, void* v_pool,
+                                     const void* k_new, const void* v_new,
+                                     const int32_t* block_tables, const int32_t* context_lens,
+                                     int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, int32_t max_blocks_per_seq,
+                                     int32_t max_context_len_hint, int32_t num_blocks, float scale,
+                                     pa_dtype dtype, void* workspace, size_t workspace_bytes,
+                                     int32_t* dev_err_flag, void* stream);
+
+/*
  * pa_prefill_attention -- causal attention of chunks of new tokens over the
  * paged cache (chunked prefill; Slipstream, "Horizon", lists chunked prefill
  * among the engine's parts; spindle, "Two bugs worth recording": positions are

@@ -104,13 +104,14 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t n
                                       max_blocks_per_seq);
 }
 
-pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
-                              const int32_t* block_tables, const int32_t* context_lens,
-                              int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-                              int32_t head_dim, int32_t max_blocks_per_seq,
-                              int32_t max_context_len_hint, int32_t num_blocks, float scale,
-                              pa_dtype dtype, void* workspace, size_t workspace_bytes,
-                              int32_t* dev_err_flag, void* stream) {
+// pa_decode_attention, and pa_append_decode_attention when k_new / v_new are given.
+static pa_status decode_call(void* out, const void* q, const void* k_pool, const void* v_pool,
+                             const void* k_new, const void* v_new, const int32_t* block_tables,
+                             const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                             int32_t num_kv_heads, int32_t head_dim, int32_t max_blocks_per_seq,
+                             int32_t max_context_len_hint, int32_t num_blocks, float scale,
+                             pa_dtype dtype, void* workspace, size_t workspace_bytes,
+                             int32_t* dev_err_flag, void* stream) {
     if (!dtype_ok(dtype)) return PA_ERR_INVALID_ARG;
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
         max_blocks_per_seq <= 0 || !std::isfinite(scale))
@@ -124,6 +125,8 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, cons
     if (!out || !q || !k_pool || !v_pool || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
         return PA_ERR_INVALID_ARG;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PA_ERR_INVALID_ARG;
+    if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PA_ERR_INVALID_ARG;
     const size_t need =
         pa::decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
@@ -136,6 +139,8 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, cons
     a.q = q;
     a.k_pool = k_pool;
     a.v_pool = v_pool;
+    a.k_new = k_new;
+    a.v_new = v_new;
     a.block_tables = block_tables;
     a.context_lens = context_lens;
     a.err = dev_err_flag;
@@ -153,6 +158,34 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, cons
     a.scale = scale;
     a.dtype = dtype;
     return cuda_status(pa::launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
+                              const int32_t* block_tables, const int32_t* context_lens,
+                              int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t max_blocks_per_seq,
+                              int32_t max_context_len_hint, int32_t num_blocks, float scale,
+                              pa_dtype dtype, void* workspace, size_t workspace_bytes,
+                              int32_t* dev_err_flag, void* stream) {
+    return decode_call(out, q, k_pool, v_pool, nullptr, nullptr, block_tables, context_lens,
+                       num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                       max_context_len_hint, num_blocks, scale, dtype, workspace, workspace_bytes,
+                       dev_err_flag, stream);
+}
+
+pa_status pa_append_decode_attention(void* out, const void* q, void* k_pool, void* v_pool,
+                                     const void* k_new, const void* v_new,
+                                     const int32_t* block_tables, const int32_t* context_lens,
+                                     int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, int32_t max_blocks_per_seq,
+                                     int32_t max_context_len_hint, int32_t num_blocks, float scale,
+                                     pa_dtype dtype, void* workspace, size_t workspace_bytes,
+                                     int32_t* dev_err_flag, void* stream) {
+    if (num_seqs > 0 && (!k_new || !v_new)) return PA_ERR_INVALID_ARG;
+    return decode_call(out, q, k_pool, v_pool, k_new, v_new, block_tables, context_lens,
+                       num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                       max_context_len_hint, num_blocks, scale, dtype, workspace, workspace_bytes,
+                       dev_err_flag, stream);
 }
 
 pa_status pa_decode_attention_shared_prefix(

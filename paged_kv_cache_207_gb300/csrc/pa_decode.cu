@@ -47,6 +47,10 @@ struct KParams {
     const int32_t* lens;
     float* part_o;      // [S*Hq][part_stride][D]
     float2* part_ml;    // [S*Hq][part_stride] : (max in log2 units, sum)
+    // decode with append: each sequence's new K and V rows ([S][Hkv][D]), written at
+    // position L - 1 (into the pools above) before it is read; null for a plain decode
+    const char* k_new;
+    const char* v_new;
     int32_t* err;
     int Hq, Hkv, G, max_blocks, num_blocks;
     int grid_parts;     // partitions covered per (sequence, kv head): first_part + launched
@@ -115,6 +119,61 @@ struct Ring {
 // Shared-memory bytes of the stage rings plus the barriers.
 template <int TILE, int NW, int NST>
 constexpr int ring_smem_bytes() { return NW * NST * 2 * TILE + NW * NST * 8; }
+
+// Decode with append, f32 kernel: the new token's K and V rows go to position L - 1 of the
+// sequence (the bytes pa_append_kv writes there), written by one warp of the CTA of the
+// partition that holds it, before the CTA issues its copies.  Each lane stores 16-byte
+// pieces and fences them to the async proxy; the caller's CTA barrier then orders the
+// stores before the bulk copies that read the block.  An invalid table entry is left to
+// the copy issue, which flags it; a length past the table (flagged, clamped) writes nothing.
+template <int ROWB>   // bytes of one (token, kv head) row
+__device__ __forceinline__ void write_new_token(const KParams& p, int s, int kvh, int L,
+                                                const int32_t* trow, int lane) {
+    constexpr int PIECES = ROWB / 16;
+    if (__ldg(p.lens + s) != L) return;
+    const int pos = L - 1;
+    const int32_t blk = __ldg(trow + pos / kBlockTokens);
+    if (blk < 0 || blk >= p.num_blocks) return;
+    for (int t = lane; t < 2 * PIECES; t += 32) {
+        const bool is_v = t >= PIECES;
+        const int ch = is_v ? t - PIECES : t;
+        const size_t src = (((size_t)s * p.Hkv + kvh) * PIECES + ch) * 16;
+        const size_t dst =
+            ((((size_t)blk * p.Hkv + kvh) * PIECES + ch) * kBlockTokens + pos % kBlockTokens) * 16;
+        // (the new rows may come from the kernel before: a plain load after the grid wait)
+        const uint4 v = *reinterpret_cast<const uint4*>((is_v ? p.v_new : p.k_new) + src);
+        // the pools are writable when k_new is given (the caller's pointers are not const)
+        *reinterpret_cast<uint4*>(const_cast<char*>(is_v ? p.v_pool : p.k_pool) + dst) = v;
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Decode with append, bf16 kernel: the warp whose copies read the new position's block
+// loads its lane's 16-byte piece of the new K or V row (lanes 0 .. P-1: K, P .. 2P-1: V),
+// stores it into the pool for later steps (no fence: this grid's copies never need it
+// there), and keeps it to patch into its own copy of the block once that lands.  Returns
+// the piece's byte offset within a (block, kv head) tile, or -1 (no piece for this lane,
+// an invalid table entry -- flagged by the copy issue -- or a length past the table).
+template <int D>
+__device__ __forceinline__ int new_token_piece(const KParams& p, int s, int kvh, int L,
+                                               const int32_t* trow, int lane, uint4& piece,
+                                               bool& is_v) {
+    constexpr int PIECES = D / 8;                 // 16-byte pieces of one bf16 row
+    if (lane >= 2 * PIECES || __ldg(p.lens + s) != L) return -1;
+    const int pos = L - 1;
+    const int32_t blk = __ldg(trow + pos / kBlockTokens);
+    if (blk < 0 || blk >= p.num_blocks) return -1;
+    is_v = lane >= PIECES;
+    const int ch = is_v ? lane - PIECES : lane;
+    const size_t src = (((size_t)s * p.Hkv + kvh) * PIECES + ch) * 16;
+    // (the new rows may come from the kernel before: a plain load after the grid wait)
+    piece = *reinterpret_cast<const uint4*>((is_v ? p.v_new : p.k_new) + src);
+    const int off = (ch * kBlockTokens + pos % kBlockTokens) * 16;
+    // the pools are writable when k_new is given (the caller's pointers are not const)
+    *reinterpret_cast<uint4*>(const_cast<char*>(is_v ? p.v_pool : p.k_pool) +
+                              ((size_t)blk * p.Hkv + kvh) * (size_t)(kBlockTokens * D * 2) + off) = piece;
+    return off;
+}
 
 // Cross-warp merge of one partition (both element types).  Every warp holds,
 // per padded head g < 8: running max m (log2 units), sum l and unnormalised
@@ -239,6 +298,18 @@ decode_bf16_kernel(const KParams p) {
     for (int i = 0; i < NST; ++i)
         if (i < nb_w && issue_blk(first_blk[i], i)) issued |= 1u << i;
 
+    // Decode with append: the new position is in this partition's last block (or, past the
+    // grid's hint, in none of this CTA's blocks); the warp that reads that block writes the
+    // new row to the pools while its first tiles are in flight, and patches it into its copy
+    // of the block at iteration patch_it.
+    uint4 piece = make_uint4(0u, 0u, 0u, 0u);
+    bool piece_v = false;
+    int piece_off = -1, patch_it = -1;
+    if (p.k_new && L > 0 && j == min(nparts, p.grid_parts) - 1 && warp == (nblk - 1) % NW) {
+        piece_off = new_token_piece<D>(p, s, kvh, L, trow, lane, piece, piece_v);
+        if (j == nparts - 1) patch_it = (nblk - 1) / NW;
+    }
+
     // Query fragments (B operand, k = dim, n = query head of the group), loaded while
     // the first tiles are in flight.
     uint32_t qb[KS][2];
@@ -267,6 +338,15 @@ decode_bf16_kernel(const KParams p) {
             }
             phase ^= 1u << st;
             issued &= ~(1u << st);
+            if (i == patch_it) {
+                // the new token's block: its row as written, whatever the copy read there; the
+                // proxy fence orders the store before the stage's next bulk copy
+                if (piece_off >= 0) {
+                    st_shared_v4((piece_v ? ring.v(st) : ring.k(st)) + piece_off, piece);
+                    fence_proxy_async_smem();
+                }
+                __syncwarp();
+            }
             const int tok0 = (blk0 + warp + i * NW) * kBlockTokens;
             // scores: 16 tokens x 8 heads
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -979,13 +1059,15 @@ decode_f32_kernel(const KParams p) {
         for (int st = 0; st < NST; ++st) mbar_init(ring.bar(st), 1);
         fence_proxy_async_smem();
     }
+    const int32_t* trow = p.tables + (size_t)s * p.max_blocks;
+    if (p.k_new && L > 0 && j == min(nparts, p.grid_parts) - 1 && warp == 0)
+        write_new_token<D * 4>(p, s, kvh, L, trow, lane);    // ordered by the barrier below
     const float* qbase = reinterpret_cast<const float*>(p.q) + ((size_t)s * p.Hq + (size_t)kvh * p.G) * D;
     for (int idx = threadIdx.x; idx < 8 * D; idx += NW * 32)
         sq[idx] = idx < p.G * D ? __ldg(qbase + idx) : 0.f;
     __syncthreads();
 
     const uint64_t pol = l2_policy_evict_first();
-    const int32_t* trow = p.tables + (size_t)s * p.max_blocks;
     auto issue = [&](int i, int st) -> bool {
         const int b = blk0 + warp + i * NW;
         const int32_t blk = __ldg(trow + b);
@@ -1514,6 +1596,8 @@ KParams make_params(const DecodeArgs& a) {
     kp.part_ml = a.workspace ? reinterpret_cast<float2*>(static_cast<char*>(a.workspace) +
                                                          rows * a.head_dim * sizeof(float))
                              : nullptr;
+    kp.k_new = static_cast<const char*>(a.k_new);
+    kp.v_new = static_cast<const char*>(a.v_new);
     kp.err = a.err;
     kp.Hq = a.num_q_heads;
     kp.Hkv = a.num_kv_heads;

@@ -33,6 +33,10 @@ struct DecodeArgs {
     const int32_t* context_lens;
     int32_t* err;            // device error flag, may be null
     void* workspace;
+    // decode with append (bf16 / f32 caches): the new K and V rows [num_seqs][Hkv][D],
+    // written at position context_len - 1 by the decode kernel itself; null otherwise
+    const void* k_new = nullptr;
+    const void* v_new = nullptr;
     int num_seqs, num_q_heads, num_kv_heads, head_dim;
     int max_blocks, num_blocks;
     int grid_parts;          // partitions launched per (sequence, kv head)

@@ -28,6 +28,12 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 
 // Make mbarrier initialisation (and earlier generic-proxy shared-memory
 // accesses) visible to the async proxy before bulk copies use the memory.
+// 16-byte store to shared memory (a generic-proxy write).
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                 :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -79,6 +79,30 @@ def test_decode_rejects_bad_arguments_without_launching(native):
     assert _decode(L, S=0) == 0                                # nothing to do
 
 
+def _append_decode(L, kn=16, vn=16, **kw):
+    a = dict(out=16, q=16, k=16, v=16, tables=16, lens=16, S=1, Hq=4, Hkv=2, D=64, mb=4, hint=0,
+             nb=8, scale=0.125, dtype=1, ws=None, wsb=0, err=None)
+    a.update(kw)
+    return L.pa_append_decode_attention(a["out"], a["q"], a["k"], a["v"], kn, vn, a["tables"],
+                                        a["lens"], a["S"], a["Hq"], a["Hkv"], a["D"], a["mb"],
+                                        a["hint"], a["nb"], a["scale"], a["dtype"], a["ws"],
+                                        a["wsb"], a["err"], None)
+
+
+def test_append_decode_rejects_bad_arguments_without_launching(native):
+    L = native.lib()
+    INVALID, UNSUPPORTED = 1, 2
+    assert _append_decode(L, kn=None) == INVALID               # the new rows are required
+    assert _append_decode(L, vn=None) == INVALID
+    assert _append_decode(L, kn=8) == INVALID                  # not 16-byte aligned
+    assert _append_decode(L, vn=24) == INVALID
+    assert _append_decode(L, D=96) == UNSUPPORTED
+    assert _append_decode(L, dtype=2) == INVALID               # the FP8 cache has its own append
+    assert _append_decode(L, dtype=3) == INVALID               # and so has the FP4 one
+    assert _append_decode(L, mb=40) == INVALID                 # needs a workspace, none given
+    assert _append_decode(L, S=0, kn=None, vn=None) == 0       # nothing to do
+
+
 def test_append_and_copy_reject_bad_arguments(native):
     L = native.lib()
     assert L.pa_append_kv(16, 16, 16, 16, 16, 4, 16, 16, 1, 1, 8, 2, 64, 5, None, None) == 1
