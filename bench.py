@@ -374,13 +374,20 @@ def run_ours(args, rank, world, local):
 
     shared = args.shared_prefix
     # the bf16 / f32 caches take the step as one call (the decode kernel writes the new
-    # token itself); the shared-prefix and quantised paths append, then decode
-    fused = not quant and not shared
+    # token itself, with or without a shared prefix); the quantised paths append, then decode
+    fused = not quant
 
     def append_decode(q_, kn, vn, tab_, lens_, pool, out=out, strm=stream):
         kp, vp = pools[pool]
-        pk.append_decode_attention(out, q_, kp, vp, kn, vn, tab_, lens_, wl.scale, workspace=ws,
-                                   max_context_len_hint=hint, err_flag=err, stream=strm)
+        if shared:
+            pk.append_decode_attention_shared_prefix(out, q_, kp, vp, kn, vn, tab_, lens_, wl.scale,
+                                                     shared, workspace=ws,
+                                                     max_context_len_hint=hint, err_flag=err,
+                                                     stream=strm)
+        else:
+            pk.append_decode_attention(out, q_, kp, vp, kn, vn, tab_, lens_, wl.scale,
+                                       workspace=ws, max_context_len_hint=hint, err_flag=err,
+                                       stream=strm)
 
     def decode(q_, tab_, lens_, pool, out=out, strm=stream):
         kp, vp = pools[pool]
@@ -540,11 +547,12 @@ def run_ours(args, rank, world, local):
                    "context_tokens_after_append": int((wl.context_lens + 1).sum()),
                    "max_context": int(hint),
                    "step": ("%d layers x (" % rot if rot > 1 else "") +
-                           ("pa_append_decode_attention (1 token/seq appended by the decode kernel)"
+                           (("pa_append_decode_attention_shared_prefix" if shared else
+                             "pa_append_decode_attention") +
+                            " (1 token/seq appended by the decode kernel)"
                             if fused else "pa_append_kv (1 token/seq) + " +
-                            ("pa_decode_attention_shared_prefix" if shared else
-                             {"fp8": "pa_decode_attention_fp8",
-                              "fp4": "pa_decode_attention_fp4"}.get(quant, "pa_decode_attention"))) +
+                            {"fp8": "pa_decode_attention_fp8",
+                             "fp4": "pa_decode_attention_fp4"}.get(quant, "pa_decode_attention")) +
                            (")" if rot > 1 else ""),
                    "shared_prefix_tokens": shared,
                    "layers_for_tokens_per_s": layers,
@@ -566,7 +574,9 @@ def run_ours(args, rank, world, local):
             "logical_gbs": round(value * (step_bytes - unique_kv_bytes(wl, wl_shared) +
                                           logical_kv_bytes(wl)) / step_bytes, 1)} if wl_shared else {}),
         "tokens_per_s": round(tokens_per_s, 1),
-        "roofline": {"kernel": ("pa_append_decode_attention (main kernel with the append + partition merge)"
+        "roofline": {"kernel": ("pa_append_decode_attention_shared_prefix (prefix kernel, suffix kernel "
+                                "with the append, partition merge)" if fused and shared else
+                                "pa_append_decode_attention (main kernel with the append + partition merge)"
                                 if fused else
                                 {"fp8": "pa_decode_attention_fp8", "fp4": "pa_decode_attention_fp4"}.get(
                                     quant, "pa_decode_attention") + " (main kernel + partition merge)"),

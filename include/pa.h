@@ -86,7 +86,10 @@ typedef enum {
 #define PA_DEV_ERR_BAD_PAIR 32   /* a copy pair names a block outside [0, num_blocks) */
 #define PA_DEV_ERR_BAD_PREFIX 64 /* pa_decode_attention_shared_prefix: a sequence's table does
                                     not hold sequence 0's prefix blocks, or its context is
-                                    shorter than the shared prefix (its output is wrong) */
+                                    shorter than the shared prefix (its output is wrong); with
+                                    the step's new rows (pa_append_decode_attention_shared_prefix),
+                                    also a new row that would fall inside the prefix (not
+                                    written) */
 
 /* Tokens per split-KV partition of pa_decode_attention at head_dim 128 (a multiple
  * of 16); head_dim 64 uses 2 * PA_PARTITION_TOKENS, the same bytes per partition. */
@@ -345,6 +348,26 @@ pa_status pa_decode_attention_shared_prefix(void* out, const void* q, const void
                                             int32_t shared_prefix_tokens, void* workspace,
                                             size_t workspace_bytes, int32_t* dev_err_flag,
                                             void* stream);
+
+/*
+ * pa_append_decode_attention_shared_prefix -- pa_decode_attention_shared_prefix
+ * with the step's new rows written by the decode kernel, as
+ * pa_append_decode_attention does for pa_decode_attention: k_new and v_new
+ * ([num_seqs][num_kv_heads][head_dim] bf16, 16-byte aligned) go to position
+ * context_lens[s] - 1, and pools and `out` equal those of pa_append_kv followed
+ * by pa_decode_attention_shared_prefix, bit for bit.  A new row must lie past
+ * the shared prefix (context_lens[s] > shared_prefix_tokens: it goes to the
+ * sequence's own block); one that would not is not written and sets
+ * PA_DEV_ERR_BAD_PREFIX.  The fallbacks of pa_decode_attention_shared_prefix
+ * fall back to pa_append_decode_attention, with the same check.
+ */
+pa_status pa_append_decode_attention_shared_prefix(
+    void* out, const void* q, void* k_pool, void* v_pool, const void* k_new, const void* v_new,
+    const int32_t* block_tables, const int32_t* context_lens, int32_t num_seqs,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t max_blocks_per_seq,
+    int32_t max_context_len_hint, int32_t num_blocks, float scale, pa_dtype dtype,
+    int32_t shared_prefix_tokens, void* workspace, size_t workspace_bytes, int32_t* dev_err_flag,
+    void* stream);
 
 /*
  * pa_decode_attention_noalloc -- pa_decode_attention for callers that cannot

@@ -6,7 +6,8 @@ generators (``workloads``).
 """
 from ._native import (  # noqa: F401
     BLOCK_SIZE, PARTITION_TOKENS, partition_tokens, BlockManager, PagedKVError, append_kv, copy_block,
-    decode_attention, append_decode_attention, decode_attention_shared_prefix, decode_workspace,
+    decode_attention, append_decode_attention, decode_attention_shared_prefix,
+    append_decode_attention_shared_prefix, decode_workspace,
     decode_workspace_size, lib,
     pool_shape, fp8_pool_shape, append_kv_fp8, decode_attention_fp8, copy_block_fp8,
     fp4_pool_shape, append_kv_fp4, decode_attention_fp4, copy_block_fp4,

@@ -37,7 +37,7 @@ DEV_ERR_BAD_PREFIX = 64
 EXPORTED = [
     "pa_status_string", "pa_abi_version", "pa_append_kv", "pa_copy_block",
     "pa_decode_workspace_size", "pa_decode_attention", "pa_append_decode_attention",
-    "pa_decode_attention_shared_prefix",
+    "pa_decode_attention_shared_prefix", "pa_append_decode_attention_shared_prefix",
     "pa_decode_attention_noalloc", "pa_append_kv_fp8", "pa_decode_attention_fp8",
     "pa_append_kv_fp4", "pa_decode_attention_fp4",
     "pa_prefill_attention", "pa_bm_create", "pa_bm_destroy",
@@ -90,6 +90,10 @@ def lib() -> ctypes.CDLL:
                                                     i32, ctypes.c_float, ctypes.c_int, i32, p, sz,
                                                     p, p]
     L.pa_decode_attention_shared_prefix.restype = ctypes.c_int
+    L.pa_append_decode_attention_shared_prefix.argtypes = [p, p, p, p, p, p, p, p, i32, i32, i32,
+                                                           i32, i32, i32, i32, ctypes.c_float,
+                                                           ctypes.c_int, i32, p, sz, p, p]
+    L.pa_append_decode_attention_shared_prefix.restype = ctypes.c_int
     L.pa_append_kv_fp8.argtypes = [p, p, p, p, p, i32, p, p, i32, i32, i32, i32, i32, p, p]
     L.pa_append_kv_fp8.restype = ctypes.c_int
     L.pa_decode_attention_fp8.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32,
@@ -334,6 +338,26 @@ def append_decode_attention(out, q, k_pool, v_pool, k_new, v_new, block_tables, 
         q.shape[1], hkv, d, block_tables.shape[1], int(max_context_len_hint), nb, float(scale),
         _dtype_code(q), None if workspace is None else _ptr(workspace), ws_bytes,
         None if err_flag is None else _i32(err_flag, "err_flag"), _stream(stream)))
+
+
+def append_decode_attention_shared_prefix(out, q, k_pool, v_pool, k_new, v_new, block_tables,
+                                          context_lens, scale, shared_prefix_tokens: int,
+                                          workspace=None, max_context_len_hint: int = 0,
+                                          err_flag=None, stream=None) -> None:
+    """decode_attention_shared_prefix with the step's new rows written by the decode kernel
+    (k_new / v_new [S][Hkv][D] go to position context_lens[s] - 1, past the prefix)."""
+    nb, hkv, d = _pool_dims(k_pool)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    for t, name in ((k_new, "k_new"), (v_new, "v_new")):
+        if tuple(t.shape) != (q.shape[0], hkv, d) or t.dtype != k_pool.dtype or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [num_seqs][num_kv_heads][head_dim] "
+                             f"tensor of the pool's type")
+    check("pa_append_decode_attention_shared_prefix", lib().pa_append_decode_attention_shared_prefix(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_new), _ptr(v_new),
+        _i32(block_tables, "block_tables"), _i32(context_lens, "context_lens"), q.shape[0],
+        q.shape[1], hkv, d, block_tables.shape[1], int(max_context_len_hint), nb, float(scale),
+        _dtype_code(q), int(shared_prefix_tokens), None if workspace is None else _ptr(workspace),
+        ws_bytes, None if err_flag is None else _i32(err_flag, "err_flag"), _stream(stream)))
 
 
 def decode_attention_shared_prefix(out, q, k_pool, v_pool, block_tables, context_lens, scale,

@@ -106,7 +106,8 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t n
 
 // pa_decode_attention, and pa_append_decode_attention when k_new / v_new are given.
 static pa_status decode_call(void* out, const void* q, const void* k_pool, const void* v_pool,
-                             const void* k_new, const void* v_new, const int32_t* block_tables,
+                             const void* k_new, const void* v_new, int32_t new_min_pos,
+                             const int32_t* block_tables,
                              const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
                              int32_t num_kv_heads, int32_t head_dim, int32_t max_blocks_per_seq,
                              int32_t max_context_len_hint, int32_t num_blocks, float scale,
@@ -141,6 +142,7 @@ static pa_status decode_call(void* out, const void* q, const void* k_pool, const
     a.v_pool = v_pool;
     a.k_new = k_new;
     a.v_new = v_new;
+    a.new_min_pos = new_min_pos;
     a.block_tables = block_tables;
     a.context_lens = context_lens;
     a.err = dev_err_flag;
@@ -167,7 +169,7 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, cons
                               int32_t max_context_len_hint, int32_t num_blocks, float scale,
                               pa_dtype dtype, void* workspace, size_t workspace_bytes,
                               int32_t* dev_err_flag, void* stream) {
-    return decode_call(out, q, k_pool, v_pool, nullptr, nullptr, block_tables, context_lens,
+    return decode_call(out, q, k_pool, v_pool, nullptr, nullptr, 0, block_tables, context_lens,
                        num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                        max_context_len_hint, num_blocks, scale, dtype, workspace, workspace_bytes,
                        dev_err_flag, stream);
@@ -182,18 +184,20 @@ pa_status pa_append_decode_attention(void* out, const void* q, void* k_pool, voi
                                      pa_dtype dtype, void* workspace, size_t workspace_bytes,
                                      int32_t* dev_err_flag, void* stream) {
     if (num_seqs > 0 && (!k_new || !v_new)) return PA_ERR_INVALID_ARG;
-    return decode_call(out, q, k_pool, v_pool, k_new, v_new, block_tables, context_lens,
+    return decode_call(out, q, k_pool, v_pool, k_new, v_new, 0, block_tables, context_lens,
                        num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                        max_context_len_hint, num_blocks, scale, dtype, workspace, workspace_bytes,
                        dev_err_flag, stream);
 }
 
-pa_status pa_decode_attention_shared_prefix(
-    void* out, const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
-    const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-    int32_t head_dim, int32_t max_blocks_per_seq, int32_t max_context_len_hint, int32_t num_blocks,
-    float scale, pa_dtype dtype, int32_t shared_prefix_tokens, void* workspace,
-    size_t workspace_bytes, int32_t* dev_err_flag, void* stream) {
+// pa_decode_attention_shared_prefix, and its one-call form when k_new / v_new are given.
+static pa_status shared_call(
+    void* out, const void* q, const void* k_pool, const void* v_pool, const void* k_new,
+    const void* v_new, const int32_t* block_tables, const int32_t* context_lens, int32_t num_seqs,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t max_blocks_per_seq,
+    int32_t max_context_len_hint, int32_t num_blocks, float scale, pa_dtype dtype,
+    int32_t shared_prefix_tokens, void* workspace, size_t workspace_bytes, int32_t* dev_err_flag,
+    void* stream) {
     if (shared_prefix_tokens < 0 || shared_prefix_tokens % pa::kBlockTokens != 0)
         return PA_ERR_INVALID_ARG;
     if ((long long)shared_prefix_tokens > (long long)max_blocks_per_seq * pa::kBlockTokens)
@@ -201,10 +205,10 @@ pa_status pa_decode_attention_shared_prefix(
     const int first_part = shared_prefix_tokens / pa::kPartTokens;
     // nothing whole to share, or every context fits one partition: the ordinary path
     if (first_part == 0 || num_seqs <= 0 || max_blocks_per_seq <= pa::kPartBlocks)
-        return pa_decode_attention(out, q, k_pool, v_pool, block_tables, context_lens, num_seqs,
-                                   num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
-                                   max_context_len_hint, num_blocks, scale, dtype, workspace,
-                                   workspace_bytes, dev_err_flag, stream);
+        return decode_call(out, q, k_pool, v_pool, k_new, v_new, k_new ? shared_prefix_tokens : 0,
+                           block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                           head_dim, max_blocks_per_seq, max_context_len_hint, num_blocks, scale,
+                           dtype, workspace, workspace_bytes, dev_err_flag, stream);
     if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
     if (num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 ||
         !std::isfinite(scale))
@@ -217,6 +221,8 @@ pa_status pa_decode_attention_shared_prefix(
     if (!out || !q || !k_pool || !v_pool || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
         return PA_ERR_INVALID_ARG;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PA_ERR_INVALID_ARG;
+    if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PA_ERR_INVALID_ARG;
     const size_t need =
         pa::decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
     if (need == 0 || !workspace || workspace_bytes < need || !aligned16(workspace))
@@ -229,6 +235,9 @@ pa_status pa_decode_attention_shared_prefix(
     a.q = q;
     a.k_pool = k_pool;
     a.v_pool = v_pool;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.new_min_pos = k_new ? shared_prefix_tokens : 0;
     a.block_tables = block_tables;
     a.context_lens = context_lens;
     a.err = dev_err_flag;
@@ -247,6 +256,32 @@ pa_status pa_decode_attention_shared_prefix(
     a.scale = scale;
     a.dtype = dtype;
     return cuda_status(pa::launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_decode_attention_shared_prefix(
+    void* out, const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
+    const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t max_blocks_per_seq, int32_t max_context_len_hint, int32_t num_blocks,
+    float scale, pa_dtype dtype, int32_t shared_prefix_tokens, void* workspace,
+    size_t workspace_bytes, int32_t* dev_err_flag, void* stream) {
+    return shared_call(out, q, k_pool, v_pool, nullptr, nullptr, block_tables, context_lens,
+                       num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                       max_context_len_hint, num_blocks, scale, dtype, shared_prefix_tokens,
+                       workspace, workspace_bytes, dev_err_flag, stream);
+}
+
+pa_status pa_append_decode_attention_shared_prefix(
+    void* out, const void* q, void* k_pool, void* v_pool, const void* k_new, const void* v_new,
+    const int32_t* block_tables, const int32_t* context_lens, int32_t num_seqs,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t max_blocks_per_seq,
+    int32_t max_context_len_hint, int32_t num_blocks, float scale, pa_dtype dtype,
+    int32_t shared_prefix_tokens, void* workspace, size_t workspace_bytes, int32_t* dev_err_flag,
+    void* stream) {
+    if (num_seqs > 0 && (!k_new || !v_new)) return PA_ERR_INVALID_ARG;
+    return shared_call(out, q, k_pool, v_pool, k_new, v_new, block_tables, context_lens,
+                       num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                       max_context_len_hint, num_blocks, scale, dtype, shared_prefix_tokens,
+                       workspace, workspace_bytes, dev_err_flag, stream);
 }
 
 pa_status pa_append_kv_fp8(void* k_pool, void* v_pool, const void* k_new, const void* v_new,

@@ -51,6 +51,7 @@ struct KParams {
     // position L - 1 (into the pools above) before it is read; null for a plain decode
     const char* k_new;
     const char* v_new;
+    int new_min_pos;    // with a shared prefix: the first position a new row may take
     int32_t* err;
     int Hq, Hkv, G, max_blocks, num_blocks;
     int grid_parts;     // partitions covered per (sequence, kv head): first_part + launched
@@ -132,6 +133,10 @@ __device__ __forceinline__ void write_new_token(const KParams& p, int s, int kvh
     constexpr int PIECES = ROWB / 16;
     if (__ldg(p.lens + s) != L) return;
     const int pos = L - 1;
+    if (pos < p.new_min_pos) {            // inside a shared prefix: every sequence's block
+        if (lane == 0) raise_flag(p.err, PA_DEV_ERR_BAD_PREFIX);
+        return;
+    }
     const int32_t blk = __ldg(trow + pos / kBlockTokens);
     if (blk < 0 || blk >= p.num_blocks) return;
     for (int t = lane; t < 2 * PIECES; t += 32) {
@@ -159,8 +164,13 @@ __device__ __forceinline__ int new_token_piece(const KParams& p, int s, int kvh,
                                                const int32_t* trow, int lane, uint4& piece,
                                                bool& is_v) {
     constexpr int PIECES = D / 8;                 // 16-byte pieces of one bf16 row
-    if (lane >= 2 * PIECES || __ldg(p.lens + s) != L) return -1;
+    if (__ldg(p.lens + s) != L) return -1;
     const int pos = L - 1;
+    if (pos < p.new_min_pos) {            // inside a shared prefix: every sequence's block
+        if (lane == 0) raise_flag(p.err, PA_DEV_ERR_BAD_PREFIX);
+        return -1;
+    }
+    if (lane >= 2 * PIECES) return -1;
     const int32_t blk = __ldg(trow + pos / kBlockTokens);
     if (blk < 0 || blk >= p.num_blocks) return -1;
     is_v = lane >= PIECES;
@@ -1243,7 +1253,9 @@ decode_reduce_kernel(const KParams p, int num_rows) {
         // and lengths are inputs, so this runs while the kernels before are finishing.
         const int s = row / p.Hq;
         const int nb = p.first_part * p.part_blocks;
-        bool bad = __ldg(p.lens + s) < nb * kBlockTokens;
+        const int len = __ldg(p.lens + s);
+        // (with the step's new rows, a row must also lie past the whole shared prefix)
+        bool bad = len < nb * kBlockTokens || (p.k_new != nullptr && len - 1 < p.new_min_pos);
         for (int b = lane; b < nb; b += 32)
             bad |= __ldg(p.tables + (size_t)s * p.max_blocks + b) != __ldg(p.tables + b);
         if (__any_sync(0xffffffffu, bad) && lane == 0) raise_flag(p.err, PA_DEV_ERR_BAD_PREFIX);
@@ -1598,6 +1610,7 @@ KParams make_params(const DecodeArgs& a) {
                              : nullptr;
     kp.k_new = static_cast<const char*>(a.k_new);
     kp.v_new = static_cast<const char*>(a.v_new);
+    kp.new_min_pos = a.new_min_pos;
     kp.err = a.err;
     kp.Hq = a.num_q_heads;
     kp.Hkv = a.num_kv_heads;

@@ -37,6 +37,8 @@ struct DecodeArgs {
     // written at position context_len - 1 by the decode kernel itself; null otherwise
     const void* k_new = nullptr;
     const void* v_new = nullptr;
+    int new_min_pos = 0;     // a new row below this position (inside a shared prefix) is
+                             // flagged PA_DEV_ERR_BAD_PREFIX and not written
     int num_seqs, num_q_heads, num_kv_heads, head_dim;
     int max_blocks, num_blocks;
     int grid_parts;          // partitions launched per (sequence, kv head)

@@ -155,3 +155,62 @@ def test_append_decode_writes_nothing_while_timeout_is_set():
     assert int(err.item()) == pk.DEV_ERR_TIMEOUT
     assert bool((out.view(torch.int16) == 0x5A5A).all().item())
     assert torch.equal(_bits(a.k), _bits(k0)) and torch.equal(_bits(a.v), _bits(v0))
+
+
+# ---- with a shared prefix (pa_append_decode_attention_shared_prefix) ---------------
+
+@pytest.mark.parametrize("shared,suffixes,hq,hkv,d", [
+    (512, [1, 16, 17, 600, 1], 32, 8, 128),           # one whole shared partition
+    (1024, [1, 100, 513, 2, 77, 1000, 3], 14, 2, 64),  # head_dim 64, 1024-token partitions
+    (528, [1, 30, 700], 8, 1, 128),                    # a prefix past a partition edge
+    (4096, [16, 512, 300, 1, 64, 128, 256, 400, 9, 33, 65], 32, 8, 128),
+    (256, [1, 40, 300], 8, 2, 128),                    # shorter than a partition: fallback
+])
+def test_append_decode_shared_prefix_equals_the_two_calls(shared, suffixes, hq, hkv, d):
+    lens = [shared + n - 1 for n in suffixes]          # the new row goes past the prefix
+    wl = W.make_decode_workload("append_decode_prefix", context_lens=lens, num_q_heads=hq,
+                                num_kv_heads=hkv, head_dim=d, dtype="bf16", seed=shared + hq,
+                                device="cuda", shared_prefix=shared)
+    a, b_k, b_v, (k_new, v_new, start, cu, lens_after) = _pair(wl)
+    ws = pk.decode_workspace(wl.num_seqs, hq, hkv, d, wl.max_blocks)
+    pk.append_kv(a.k, a.v, k_new, v_new, a.tables, start, cu, err_flag=a.err)
+    want = torch.empty_like(wl.q)
+    pk.decode_attention_shared_prefix(want, wl.q, a.k, a.v, a.tables, lens_after, wl.scale, shared,
+                                      workspace=ws, err_flag=a.err)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = torch.empty_like(wl.q)
+    pk.append_decode_attention_shared_prefix(got, wl.q, b_k, b_v, k_new, v_new, a.tables,
+                                             lens_after, wl.scale, shared, workspace=ws,
+                                             err_flag=err)
+    torch.cuda.synchronize()
+    assert int(a.err.item()) == 0 and int(err.item()) == 0
+    assert torch.equal(_bits(a.k), _bits(b_k)) and torch.equal(_bits(a.v), _bits(b_v))
+    assert torch.equal(_bits(want), _bits(got))
+    pairs = _all_pairs(wl)
+    assert_close(wl, as_f64(got).reshape(len(pairs), d),
+                 oracle_contig(wl, pairs, lens_after=lens_after.cpu().numpy()),
+                 f"append+prefix {shared}")
+
+
+@pytest.mark.parametrize("shared", [1024, 256])
+def test_append_decode_shared_prefix_refuses_a_row_inside_the_prefix(shared):
+    # sequence 1's context ends one short of the prefix, so its new row would land on the
+    # prefix's last position, in a block every sequence reads: it is not written, and the
+    # call says so (1024: the shared-prefix kernels; 256: the fallback to the plain path)
+    lens = [shared + 40, shared - 1, shared + 600]     # before the step
+    wl = W.make_decode_workload("append_decode_prefix_bad", context_lens=lens, num_q_heads=8,
+                                num_kv_heads=2, head_dim=128, dtype="bf16", seed=shared,
+                                device="cuda", shared_prefix=shared)
+    a, _, _, (k_new, v_new, start, cu, lens_after) = _pair(wl)
+    k0, v0 = a.k.clone(), a.v.clone()
+    ws = pk.decode_workspace(wl.num_seqs, 8, 2, 128, wl.max_blocks)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(wl.q)
+    pk.append_decode_attention_shared_prefix(out, wl.q, a.k, a.v, k_new, v_new, a.tables,
+                                             lens_after, wl.scale, shared, workspace=ws,
+                                             err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pk.DEV_ERR_BAD_PREFIX
+    # the shared blocks (sequence 0's first shared / 16 table entries) are unchanged
+    pre = a.tables[0, :shared // 16].long()
+    assert torch.equal(_bits(a.k[pre]), _bits(k0[pre])) and torch.equal(_bits(a.v[pre]), _bits(v0[pre]))
