@@ -77,13 +77,10 @@ class Replay:
             n = rw.num_seqs
             # fixed device buffers the captured steps read; host staging in pinned memory
             self.g_tables = torch.full((n, self.max_blocks), -1, dtype=torch.int32, device=device)
-            self.g_start = torch.zeros(n, dtype=torch.int32, device=device)
             self.g_lens = torch.zeros(n, dtype=torch.int32, device=device)
             self.g_seq = torch.zeros(n, dtype=torch.long, device=device)
             self.g_pos = torch.zeros(n, dtype=torch.long, device=device)
-            self.g_cu = torch.arange(n + 1, dtype=torch.int32, device=device)
             self.h_tables = torch.empty_like(self.g_tables, device="cpu").pin_memory()
-            self.h_start = torch.empty_like(self.g_start, device="cpu").pin_memory()
             self.h_lens = torch.empty_like(self.g_lens, device="cpu").pin_memory()
             self.h_seq = torch.empty_like(self.g_seq, device="cpu").pin_memory()
             self.h_pos = torch.empty_like(self.g_pos, device="cpu").pin_memory()
@@ -187,6 +184,11 @@ class Replay:
         out[:] = np.asarray([self.bm.block_table(i, self.max_blocks) for i in ids], np.int32)
         return out
 
+    def _decode_kernels(self, hint: int) -> int:
+        """Kernels of one pa_append_decode_attention call: the main kernel, and the
+        partition merge when a context can span two partitions."""
+        return 1 + (1 if hint > pk.partition_tokens(self.rw.head_dim) else 0)
+
     def _i32(self, a) -> torch.Tensor:
         return torch.tensor(np.asarray(a, np.int32), dtype=torch.int32, device=self.dev)
 
@@ -221,12 +223,12 @@ class Replay:
 
     def _capture(self, S: int):
         """One CUDA graph for an iteration with S running sequences: per layer the
-        gather of the new rows, pa_append_kv and pa_decode_attention, all reading
-        the fixed buffers above."""
+        gather of the new rows and one pa_append_decode_attention (the decode kernel
+        writes the new rows itself), all reading the fixed buffers above."""
         rw = self.rw
         g = torch.cuda.CUDAGraph()
-        tables, start, lens = self.g_tables[:S], self.g_start[:S], self.g_lens[:S]
-        seq, pos, cu = self.g_seq[:S], self.g_pos[:S], self.g_cu[:S + 1]
+        tables, lens = self.g_tables[:S], self.g_lens[:S]
+        seq, pos = self.g_seq[:S], self.g_pos[:S]
         with torch.cuda.graph(g, capture_error_mode="relaxed"):
             outs = []
             for l in range(rw.num_layers):
@@ -234,10 +236,9 @@ class Replay:
                 v_new = rw.v[seq, l, pos]
                 q = rw.q[seq, l, pos]
                 out = torch.empty_like(q)
-                pk.append_kv(self.k[l], self.v[l], k_new, v_new, tables, start, cu,
-                             err_flag=self.err)
-                pk.decode_attention(out, q, self.k[l], self.v[l], tables, lens, rw.scale,
-                                    max_context_len_hint=rw.max_len, err_flag=self.err)
+                pk.append_decode_attention(out, q, self.k[l], self.v[l], k_new, v_new, tables,
+                                           lens, rw.scale, max_context_len_hint=rw.max_len,
+                                           err_flag=self.err)
                 outs.append(out)
         return g, outs
 
@@ -248,9 +249,7 @@ class Replay:
         S = len(run)
         tables = self._i32(self._tables_into([self.bm_id[s] for s in run],
                                              np.empty((S, self.max_blocks), np.int32)))
-        start = self._i32(ctx)
         lens = self._i32(ctx + 1)
-        cu = self._i32(np.arange(S + 1))
         seq_idx = torch.tensor(run, dtype=torch.long, device=self.dev)
         pos_idx = torch.from_numpy(ctx.astype(np.int64)).to(self.dev)
         if prefill:
@@ -261,7 +260,7 @@ class Replay:
             pf_pos = torch.cat([torch.arange(p[2]) for p in prefill]).to(self.dev)
         pairs_t = self._i32(pairs).reshape(-1, 2) if pairs else None
         self.stats.h2d_bytes += sum(t.numel() * t.element_size()
-                                    for t in (tables, start, lens, cu, seq_idx, pos_idx))
+                                    for t in (tables, lens, seq_idx, pos_idx))
 
         ev0 = ev1 = None
         if self.time_gpu:
@@ -282,10 +281,10 @@ class Replay:
             out = torch.empty_like(q)
             if ev0 is not None and l == 0:
                 ev0.record()
-            pk.append_kv(self.k[l], self.v[l], k_new, v_new, tables, start, cu, err_flag=self.err)
-            pk.decode_attention(out, q, self.k[l], self.v[l], tables, lens, rw.scale,
-                                max_context_len_hint=int(ctx.max()) + 1, err_flag=self.err)
-            self.stats.launches += 2
+            hint = int(ctx.max()) + 1
+            pk.append_decode_attention(out, q, self.k[l], self.v[l], k_new, v_new, tables, lens,
+                                       rw.scale, max_context_len_hint=hint, err_flag=self.err)
+            self.stats.launches += self._decode_kernels(hint)
             outs.append(out)
         if ev1 is not None:
             ev1.record()
@@ -302,7 +301,6 @@ class Replay:
         if self.h_free is not None:
             self.h_free.synchronize()
         self._tables_into([self.bm_id[s] for s in run], self.h_tables[:S].numpy())
-        self.h_start[:S].numpy()[:] = ctx
         self.h_lens[:S].numpy()[:] = ctx + 1
         self.h_seq[:S].numpy()[:] = np.asarray(run, np.int64)
         self.h_pos[:S].numpy()[:] = ctx.astype(np.int64)
@@ -332,14 +330,14 @@ class Replay:
                 if pairs_t is not None:
                     pk.copy_block(self.k[l], self.v[l], pairs_t, err_flag=self.err)
                     self.stats.launches += 1
-        for d, h in ((self.g_tables, self.h_tables), (self.g_start, self.h_start),
-                     (self.g_lens, self.h_lens), (self.g_seq, self.h_seq), (self.g_pos, self.h_pos)):
+        for d, h in ((self.g_tables, self.h_tables), (self.g_lens, self.h_lens),
+                     (self.g_seq, self.h_seq), (self.g_pos, self.h_pos)):
             d[:S].copy_(h[:S], non_blocking=True)
             self.stats.h2d_bytes += h[:S].numel() * h.element_size()
         self.h_free = torch.cuda.Event()
         self.h_free.record()
         g.replay()
-        self.stats.launches += 2 * rw.num_layers
+        self.stats.launches += self._decode_kernels(rw.max_len) * rw.num_layers
         if ev1 is not None:
             ev1.record()
             self._timed.append((ev0, ev1))        # read after the run: no wait per iteration
