@@ -373,13 +373,17 @@ def run_ours(args, rank, world, local):
     counter = [0]          # steps issued so far: step i, layer l uses pool (i rot + l) % npools
 
     shared = args.shared_prefix
-    # the bf16 / f32 caches take the step as one call (the decode kernel writes the new
-    # token itself, with or without a shared prefix); the quantised paths append, then decode
-    fused = not quant
+    # the bf16, f32 and FP8 caches take the step as one call (the decode kernel writes the
+    # new token itself, with or without a shared prefix); the FP4 path appends, then decodes
+    fused = quant != "fp4"
 
     def append_decode(q_, kn, vn, tab_, lens_, pool, out=out, strm=stream):
         kp, vp = pools[pool]
-        if shared:
+        if quant == "fp8":
+            pk.append_decode_attention_fp8(out, q_, kp, vp, kn, vn, tab_, lens_, wl.scale,
+                                           workspace=ws, max_context_len_hint=hint, err_flag=err,
+                                           stream=strm)
+        elif shared:
             pk.append_decode_attention_shared_prefix(out, q_, kp, vp, kn, vn, tab_, lens_, wl.scale,
                                                      shared, workspace=ws,
                                                      max_context_len_hint=hint, err_flag=err,
@@ -547,7 +551,8 @@ def run_ours(args, rank, world, local):
                    "context_tokens_after_append": int((wl.context_lens + 1).sum()),
                    "max_context": int(hint),
                    "step": ("%d layers x (" % rot if rot > 1 else "") +
-                           (("pa_append_decode_attention_shared_prefix" if shared else
+                           (("pa_append_decode_attention_fp8" if quant == "fp8" else
+                             "pa_append_decode_attention_shared_prefix" if shared else
                              "pa_append_decode_attention") +
                             " (1 token/seq appended by the decode kernel)"
                             if fused else "pa_append_kv (1 token/seq) + " +
@@ -574,7 +579,9 @@ def run_ours(args, rank, world, local):
             "logical_gbs": round(value * (step_bytes - unique_kv_bytes(wl, wl_shared) +
                                           logical_kv_bytes(wl)) / step_bytes, 1)} if wl_shared else {}),
         "tokens_per_s": round(tokens_per_s, 1),
-        "roofline": {"kernel": ("pa_append_decode_attention_shared_prefix (prefix kernel, suffix kernel "
+        "roofline": {"kernel": ("pa_append_decode_attention_fp8 (main kernel with the quantising append "
+                                "+ partition merge)" if fused and quant == "fp8" else
+                                "pa_append_decode_attention_shared_prefix (prefix kernel, suffix kernel "
                                 "with the append, partition merge)" if fused and shared else
                                 "pa_append_decode_attention (main kernel with the append + partition merge)"
                                 if fused else

@@ -270,6 +270,25 @@ pa_status pa_decode_attention_fp8(void* out, const void* q, const void* k_pool, 
                                   void* stream);
 
 /*
+ * pa_append_decode_attention_fp8 -- one FP8 decode step in one call, as
+ * pa_append_decode_attention is for bf16: the new bf16 rows k_new, v_new
+ * ([num_seqs][num_kv_heads][head_dim], 16-byte aligned) are quantised exactly as
+ * pa_append_kv_fp8 quantises them and written at position context_lens[s] - 1,
+ * then attended over.  Pools and `out` equal those of pa_append_kv_fp8 (one row
+ * per sequence) followed by pa_decode_attention_fp8, bit for bit; flags,
+ * workspace and partitions as pa_decode_attention_fp8.
+ */
+pa_status pa_append_decode_attention_fp8(void* out, const void* q, void* k_pool, void* v_pool,
+                                         const void* k_new, const void* v_new,
+                                         const int32_t* block_tables, const int32_t* context_lens,
+                                         int32_t num_seqs, int32_t num_q_heads,
+                                         int32_t num_kv_heads, int32_t head_dim,
+                                         int32_t max_blocks_per_seq, int32_t max_context_len_hint,
+                                         int32_t num_blocks, float scale, void* workspace,
+                                         size_t workspace_bytes, int32_t* dev_err_flag,
+                                         void* stream);
+
+/*
  * Block-scaled FP4 (MXFP4) KV cache -- a quarter of the bf16 bytes per token
  * (Slipstream, "Companion work": qgemm-mx, a block-scaled FP4 kernel for the same
  * bandwidth-bound decode path).  The format is the microscaling one: E2M1 codes

@@ -9,7 +9,8 @@ from ._native import (  # noqa: F401
     decode_attention, append_decode_attention, decode_attention_shared_prefix,
     append_decode_attention_shared_prefix, decode_workspace,
     decode_workspace_size, lib,
-    pool_shape, fp8_pool_shape, append_kv_fp8, decode_attention_fp8, copy_block_fp8,
+    pool_shape, fp8_pool_shape, append_kv_fp8, decode_attention_fp8, append_decode_attention_fp8,
+    copy_block_fp8,
     fp4_pool_shape, append_kv_fp4, decode_attention_fp4, copy_block_fp4,
     prefill_attention,
     DEV_ERR_BAD_BLOCK, DEV_ERR_BAD_POS, DEV_ERR_HINT, DEV_ERR_BAD_CU, DEV_ERR_TIMEOUT,

@@ -39,6 +39,7 @@ EXPORTED = [
     "pa_decode_workspace_size", "pa_decode_attention", "pa_append_decode_attention",
     "pa_decode_attention_shared_prefix", "pa_append_decode_attention_shared_prefix",
     "pa_decode_attention_noalloc", "pa_append_kv_fp8", "pa_decode_attention_fp8",
+    "pa_append_decode_attention_fp8",
     "pa_append_kv_fp4", "pa_decode_attention_fp4",
     "pa_prefill_attention", "pa_bm_create", "pa_bm_destroy",
     "pa_bm_add_seq", "pa_bm_fork", "pa_bm_free_seq", "pa_bm_blocks_needed",
@@ -99,6 +100,9 @@ def lib() -> ctypes.CDLL:
     L.pa_decode_attention_fp8.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32,
                                           ctypes.c_float, p, sz, p, p]
     L.pa_decode_attention_fp8.restype = ctypes.c_int
+    L.pa_append_decode_attention_fp8.argtypes = [p, p, p, p, p, p, p, p, i32, i32, i32, i32, i32,
+                                                 i32, i32, ctypes.c_float, p, sz, p, p]
+    L.pa_append_decode_attention_fp8.restype = ctypes.c_int
     L.pa_append_kv_fp4.argtypes = [p, p, p, p, p, i32, p, p, i32, i32, i32, i32, i32, p, p]
     L.pa_append_kv_fp4.restype = ctypes.c_int
     L.pa_decode_attention_fp4.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32,
@@ -210,6 +214,26 @@ def decode_attention_fp8(out, q, k_pool, v_pool, block_tables, context_lens, sca
         _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _i32(block_tables, "block_tables"),
         _i32(context_lens, "context_lens"), q.shape[0], q.shape[1], hkv, d, block_tables.shape[1],
         int(max_context_len_hint), nb, float(scale),
+        None if workspace is None else _ptr(workspace), ws_bytes,
+        None if err_flag is None else _i32(err_flag, "err_flag"), _stream(stream)))
+
+
+def append_decode_attention_fp8(out, q, k_pool, v_pool, k_new, v_new, block_tables, context_lens,
+                                scale, workspace=None, max_context_len_hint: int = 0,
+                                err_flag=None, stream=None) -> None:
+    """decode_attention_fp8 with the step's bf16 rows k_new / v_new ([S][Hkv][D]) quantised
+    and written at position context_lens[s] - 1 by the decode kernel itself."""
+    nb, hkv, d = _fp8_dims(k_pool)
+    if q.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
+        raise TypeError("q and out must be bf16")
+    for t, name in ((k_new, "k_new"), (v_new, "v_new")):
+        if tuple(t.shape) != (q.shape[0], hkv, d) or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 [num_seqs][num_kv_heads][head_dim] tensor")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    check("pa_append_decode_attention_fp8", lib().pa_append_decode_attention_fp8(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_new), _ptr(v_new),
+        _i32(block_tables, "block_tables"), _i32(context_lens, "context_lens"), q.shape[0],
+        q.shape[1], hkv, d, block_tables.shape[1], int(max_context_len_hint), nb, float(scale),
         None if workspace is None else _ptr(workspace), ws_bytes,
         None if err_flag is None else _i32(err_flag, "err_flag"), _stream(stream)))
 

@@ -321,13 +321,14 @@ pa_status pa_append_kv_fp8(void* k_pool, void* v_pool, const void* k_new, const 
     return cuda_status(pa::launch_append_fp8(a, static_cast<cudaStream_t>(stream)));
 }
 
-pa_status pa_decode_attention_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,
-                                  const int32_t* block_tables, const int32_t* context_lens,
-                                  int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-                                  int32_t head_dim, int32_t max_blocks_per_seq,
-                                  int32_t max_context_len_hint, int32_t num_blocks, float scale,
-                                  void* workspace, size_t workspace_bytes, int32_t* dev_err_flag,
-                                  void* stream) {
+// pa_decode_attention_fp8, and its one-call form when k_new / v_new are given.
+static pa_status fp8_call(void* out, const void* q, const void* k_pool, const void* v_pool,
+                          const void* k_new, const void* v_new, const int32_t* block_tables,
+                          const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t max_blocks_per_seq,
+                          int32_t max_context_len_hint, int32_t num_blocks, float scale,
+                          void* workspace, size_t workspace_bytes, int32_t* dev_err_flag,
+                          void* stream) {
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
         max_blocks_per_seq <= 0 || !std::isfinite(scale))
         return PA_ERR_INVALID_ARG;
@@ -340,6 +341,8 @@ pa_status pa_decode_attention_fp8(void* out, const void* q, const void* k_pool, 
     if (!out || !q || !k_pool || !v_pool || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
         return PA_ERR_INVALID_ARG;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PA_ERR_INVALID_ARG;
+    if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PA_ERR_INVALID_ARG;
     const size_t need =
         pa::decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
@@ -351,6 +354,8 @@ pa_status pa_decode_attention_fp8(void* out, const void* q, const void* k_pool, 
     a.q = q;
     a.k_pool = k_pool;
     a.v_pool = v_pool;
+    a.k_new = k_new;
+    a.v_new = v_new;
     a.block_tables = block_tables;
     a.context_lens = context_lens;
     a.err = dev_err_flag;
@@ -369,6 +374,33 @@ pa_status pa_decode_attention_fp8(void* out, const void* q, const void* k_pool, 
     a.scale = scale;
     a.dtype = PA_FP8_E4M3;
     return cuda_status(pa::launch_decode_fp8(a, static_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_decode_attention_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                  const int32_t* block_tables, const int32_t* context_lens,
+                                  int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t max_blocks_per_seq,
+                                  int32_t max_context_len_hint, int32_t num_blocks, float scale,
+                                  void* workspace, size_t workspace_bytes, int32_t* dev_err_flag,
+                                  void* stream) {
+    return fp8_call(out, q, k_pool, v_pool, nullptr, nullptr, block_tables, context_lens, num_seqs,
+                    num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, max_context_len_hint,
+                    num_blocks, scale, workspace, workspace_bytes, dev_err_flag, stream);
+}
+
+pa_status pa_append_decode_attention_fp8(void* out, const void* q, void* k_pool, void* v_pool,
+                                         const void* k_new, const void* v_new,
+                                         const int32_t* block_tables, const int32_t* context_lens,
+                                         int32_t num_seqs, int32_t num_q_heads,
+                                         int32_t num_kv_heads, int32_t head_dim,
+                                         int32_t max_blocks_per_seq, int32_t max_context_len_hint,
+                                         int32_t num_blocks, float scale, void* workspace,
+                                         size_t workspace_bytes, int32_t* dev_err_flag,
+                                         void* stream) {
+    if (num_seqs > 0 && (!k_new || !v_new)) return PA_ERR_INVALID_ARG;
+    return fp8_call(out, q, k_pool, v_pool, k_new, v_new, block_tables, context_lens, num_seqs,
+                    num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, max_context_len_hint,
+                    num_blocks, scale, workspace, workspace_bytes, dev_err_flag, stream);
 }
 
 pa_status pa_append_kv_fp4(void* k_pool, void* v_pool, const void* k_new, const void* v_new,

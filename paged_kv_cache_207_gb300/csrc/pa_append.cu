@@ -122,7 +122,6 @@ __global__ void __launch_bounds__(256) append_kernel(const AParams p) {
 // the two scales after the codes.
 template <int D>
 __global__ void __launch_bounds__(256) append_fp8_kernel(const AParams p) {
-    constexpr int VPL = D / 32;   // values per lane: 4 (D = 128) or 2 (D = 64)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -136,58 +135,13 @@ __global__ void __launch_bounds__(256) append_fp8_kernel(const AParams p) {
     const bool ok = wid < (long long)p.total * p.Hkv && locate_row(p, row, lane == 0, s, slot, blk);
     asm volatile("griddepcontrol.wait;" ::: "memory");           // as in append_kernel
     if (!ok) return;                                              // warp-uniform
-    const size_t src = ((size_t)row * p.Hkv + h) * D + (size_t)lane * VPL;
-    float kx[VPL], vx[VPL];
-    if constexpr (VPL == 4) {
-        const uint2 kr = __ldg(reinterpret_cast<const uint2*>(p.k_new) + src / 4);
-        const uint2 vr = __ldg(reinterpret_cast<const uint2*>(p.v_new) + src / 4);
-        kx[0] = __uint_as_float(kr.x << 16); kx[1] = __uint_as_float(kr.x & 0xffff0000u);
-        kx[2] = __uint_as_float(kr.y << 16); kx[3] = __uint_as_float(kr.y & 0xffff0000u);
-        vx[0] = __uint_as_float(vr.x << 16); vx[1] = __uint_as_float(vr.x & 0xffff0000u);
-        vx[2] = __uint_as_float(vr.y << 16); vx[3] = __uint_as_float(vr.y & 0xffff0000u);
-    } else {
-        const uint32_t kr = __ldg(reinterpret_cast<const uint32_t*>(p.k_new) + src / 2);
-        const uint32_t vr = __ldg(reinterpret_cast<const uint32_t*>(p.v_new) + src / 2);
-        kx[0] = __uint_as_float(kr << 16); kx[1] = __uint_as_float(kr & 0xffff0000u);
-        vx[0] = __uint_as_float(vr << 16); vx[1] = __uint_as_float(vr & 0xffff0000u);
-    }
-    float ka = 0.f, va = 0.f;
-#pragma unroll
-    for (int k = 0; k < VPL; ++k) {
-        ka = fmaxf(ka, fabsf(kx[k]));
-        va = fmaxf(va, fabsf(vx[k]));
-    }
-#pragma unroll
-    for (int x = 16; x > 0; x >>= 1) {
-        ka = fmaxf(ka, __shfl_xor_sync(0xffffffffu, ka, x));
-        va = fmaxf(va, __shfl_xor_sync(0xffffffffu, va, x));
-    }
-    const float ks = __fdiv_rn(ka, 448.f), vs = __fdiv_rn(va, 448.f);
+    const size_t src = ((size_t)row * p.Hkv + h) * D * 2;          // bytes of bf16 rows
+    uint32_t kw, vw;
+    float ks, vs;
+    fp8_quantize_rows<D>(p.k_new + src, p.v_new + src, lane, kw, vw, ks, vs);
     const size_t rec = fp8_record_bytes(D);
-    char* krec = p.k_pool + ((size_t)blk * p.Hkv + h) * rec;
-    char* vrec = p.v_pool + ((size_t)blk * p.Hkv + h) * rec;
-    uint8_t kc[VPL], vc[VPL];
-#pragma unroll
-    for (int k = 0; k < VPL; k += 2) {
-        const uint16_t k2 = ks > 0.f ? pack_e4m3x2(__fdiv_rn(kx[k], ks), __fdiv_rn(kx[k + 1], ks)) : 0;
-        const uint16_t v2 = vs > 0.f ? pack_e4m3x2(__fdiv_rn(vx[k], vs), __fdiv_rn(vx[k + 1], vs)) : 0;
-        kc[k] = (uint8_t)(k2 & 0xff); kc[k + 1] = (uint8_t)(k2 >> 8);
-        vc[k] = (uint8_t)(v2 & 0xff); vc[k + 1] = (uint8_t)(v2 >> 8);
-    }
-    // K: dims d = lane*VPL .. +VPL-1 lie in one 16-dim piece
-    const int d0 = lane * VPL;
-    char* kdst = krec + ((size_t)(d0 / 16) * kBlockTokens + slot) * 16 + (d0 % 16);
-    if constexpr (VPL == 4)
-        *reinterpret_cast<uint32_t*>(kdst) = (uint32_t)kc[0] | ((uint32_t)kc[1] << 8) |
-                                             ((uint32_t)kc[2] << 16) | ((uint32_t)kc[3] << 24);
-    else
-        *reinterpret_cast<uint16_t*>(kdst) = (uint16_t)(kc[0] | (kc[1] << 8));
-#pragma unroll
-    for (int k = 0; k < VPL; ++k) vrec[(size_t)(d0 + k) * kBlockTokens + slot] = (char)vc[k];
-    if (lane == 0) {
-        *reinterpret_cast<float*>(krec + (size_t)16 * D + 4 * slot) = ks;
-        *reinterpret_cast<float*>(vrec + (size_t)16 * D + 4 * slot) = vs;
-    }
+    fp8_put_row<D>(p.k_pool + ((size_t)blk * p.Hkv + h) * rec, p.v_pool + ((size_t)blk * p.Hkv + h) * rec,
+                   lane, slot, kw, vw, ks, vs);
 }
 
 // MXFP4 append: one warp per (row, kv head), D / 32 values per lane.  Each block of

@@ -185,6 +185,31 @@ __device__ __forceinline__ int new_token_piece(const KParams& p, int s, int kvh,
     return off;
 }
 
+// Decode with append, FP8 kernel: as new_token_piece, with the row quantised the way the FP8
+// append does it (fp8_quantize_rows, by the whole warp) and written into the pool records
+// (fp8_put_row).  Returns the new row's slot in its block, or -1 (invalid table entry --
+// flagged by the copy issue --, a length past the table, or a row inside a shared prefix).
+template <int D>
+__device__ __forceinline__ int new_token_fp8(const KParams& p, int s, int kvh, int L,
+                                             const int32_t* trow, int lane, uint32_t& kc,
+                                             uint32_t& vc, float& ks, float& vs) {
+    if (__ldg(p.lens + s) != L) return -1;
+    const int pos = L - 1;
+    if (pos < p.new_min_pos) {
+        if (lane == 0) raise_flag(p.err, PA_DEV_ERR_BAD_PREFIX);
+        return -1;
+    }
+    const int32_t blk = __ldg(trow + pos / kBlockTokens);
+    if (blk < 0 || blk >= p.num_blocks) return -1;
+    const size_t src = ((size_t)s * p.Hkv + kvh) * D * 2;
+    fp8_quantize_rows<D>(p.k_new + src, p.v_new + src, lane, kc, vc, ks, vs);
+    const size_t rec = ((size_t)blk * p.Hkv + kvh) * fp8_record_bytes(D);
+    // the pools are writable when k_new is given (the caller's pointers are not const)
+    fp8_put_row<D>(const_cast<char*>(p.k_pool) + rec, const_cast<char*>(p.v_pool) + rec, lane,
+                   pos % kBlockTokens, kc, vc, ks, vs);
+    return pos % kBlockTokens;
+}
+
 // Cross-warp merge of one partition (both element types).  Every warp holds,
 // per padded head g < 8: running max m (log2 units), sum l and unnormalised
 // output row o[g][:] already written to shared memory by the caller.
@@ -546,6 +571,17 @@ decode_fp8_kernel(const KParams p) {
     for (int i = 0; i < NST; ++i)
         if (i < nb_w && issue_blk(first_blk[i], i)) issued |= 1u << i;
 
+    // Decode with append (as in the bf16 kernel): the warp that reads the new row's block
+    // quantises and writes the row while its first records are in flight, and patches it into
+    // its copy of the block at iteration patch_it.
+    uint32_t nkc = 0u, nvc = 0u;
+    float nks = 0.f, nvs = 0.f;
+    int nslot = -1, patch_it = -1;
+    if (p.k_new && L > 0 && j == min(nparts, p.grid_parts) - 1 && warp == (nblk - 1) % NW) {
+        nslot = new_token_fp8<D>(p, s, kvh, L, trow, lane, nkc, nvc, nks, nvs);
+        if (nslot >= 0 && j == nparts - 1) patch_it = (nblk - 1) / NW;
+    }
+
     // query fragments in f16 with the permuted dims: b0 <- dims 16kk+4c, +1; b1 <- +2, +3
     // (loaded while the first records are in flight)
     uint32_t qb[KS][2];
@@ -583,6 +619,15 @@ decode_fp8_kernel(const KParams p) {
             issued &= ~(1u << st);
             const int tok0 = (blk0 + warp + i * NW) * kBlockTokens;
             const uint32_t kt = stage0 + st * 2 * REC, vt = kt + REC;
+            if (i == patch_it) {
+                // the new row's block: its codes and scales as written, whatever the copy read;
+                // the proxy fence orders the stores before the stage's next bulk copy
+                fp8_put_row<D>(reinterpret_cast<char*>(smem) + (kt - smem_u32(smem)),
+                               reinterpret_cast<char*>(smem) + (vt - smem_u32(smem)), lane, nslot,
+                               nkc, nvc, nks, nvs);
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
             const float* kscale = reinterpret_cast<const float*>(smem + (kt - smem_u32(smem)) + 16 * D);
             const float* vscale = reinterpret_cast<const float*>(smem + (vt - smem_u32(smem)) + 16 * D);
             float acc[4] = {0.f, 0.f, 0.f, 0.f};

@@ -8,6 +8,8 @@
 
 #include <cstdint>
 
+#include "pa_internal.h"
+
 namespace pa {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -161,6 +163,75 @@ __device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
     uint16_t r;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// E4M3 quantisation of one (token, kv head) K row and V row (bf16, D values each) by one
+// warp, as the FP8 cache stores them: lane l holds dims l*VPL .. l*VPL + VPL - 1 (VPL = D/32);
+// each row's scale is amax / 448 and each code x / scale (fp32, each step correctly rounded,
+// then E4M3 round to nearest even, saturating).  The lane's VPL K and V codes come back packed
+// (dim l*VPL in bits 0..7).  The rows may come from the previous kernel: plain loads.
+template <int D>
+__device__ __forceinline__ void fp8_quantize_rows(const char* k_row, const char* v_row, int lane,
+                                                  uint32_t& kc, uint32_t& vc, float& ks, float& vs) {
+    constexpr int VPL = D / 32;
+    float kx[VPL], vx[VPL];
+    if constexpr (VPL == 4) {
+        const uint2 kr = *reinterpret_cast<const uint2*>(k_row + (size_t)lane * 8);
+        const uint2 vr = *reinterpret_cast<const uint2*>(v_row + (size_t)lane * 8);
+        kx[0] = bf16_lo_to_f32(kr.x); kx[1] = bf16_hi_to_f32(kr.x);
+        kx[2] = bf16_lo_to_f32(kr.y); kx[3] = bf16_hi_to_f32(kr.y);
+        vx[0] = bf16_lo_to_f32(vr.x); vx[1] = bf16_hi_to_f32(vr.x);
+        vx[2] = bf16_lo_to_f32(vr.y); vx[3] = bf16_hi_to_f32(vr.y);
+    } else {
+        const uint32_t kr = *reinterpret_cast<const uint32_t*>(k_row + (size_t)lane * 4);
+        const uint32_t vr = *reinterpret_cast<const uint32_t*>(v_row + (size_t)lane * 4);
+        kx[0] = bf16_lo_to_f32(kr); kx[1] = bf16_hi_to_f32(kr);
+        vx[0] = bf16_lo_to_f32(vr); vx[1] = bf16_hi_to_f32(vr);
+    }
+    float ka = 0.f, va = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) {
+        ka = fmaxf(ka, fabsf(kx[k]));
+        va = fmaxf(va, fabsf(vx[k]));
+    }
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) {
+        ka = fmaxf(ka, __shfl_xor_sync(0xffffffffu, ka, x));
+        va = fmaxf(va, __shfl_xor_sync(0xffffffffu, va, x));
+    }
+    ks = __fdiv_rn(ka, 448.f);
+    vs = __fdiv_rn(va, 448.f);
+    kc = 0u;
+    vc = 0u;
+#pragma unroll
+    for (int k = 0; k < VPL; k += 2) {
+        const uint32_t k2 = ks > 0.f ? pack_e4m3x2(__fdiv_rn(kx[k], ks), __fdiv_rn(kx[k + 1], ks)) : 0u;
+        const uint32_t v2 = vs > 0.f ? pack_e4m3x2(__fdiv_rn(vx[k], vs), __fdiv_rn(vx[k + 1], vs)) : 0u;
+        kc |= k2 << (8 * k);
+        vc |= v2 << (8 * k);
+    }
+}
+
+// One quantised row into an FP8 (block, kv head) record pair (krec, vrec: pool records in
+// global memory, or a stage's copies of them in shared memory): K codes in the slot's
+// 16-byte piece of each 16 dims, V codes at byte `slot` of each dim's 16-byte row, the two
+// scales after the codes (lane 0).  kc, vc, ks, vs as fp8_quantize_rows gives them.
+template <int D>
+__device__ __forceinline__ void fp8_put_row(char* krec, char* vrec, int lane, int slot,
+                                            uint32_t kc, uint32_t vc, float ks, float vs) {
+    constexpr int VPL = D / 32;
+    const int d0 = lane * VPL;                 // dims d0 .. d0 + VPL - 1 lie in one 16-dim piece
+    char* kdst = krec + ((size_t)(d0 / 16) * kBlockTokens + slot) * 16 + (d0 % 16);
+    if constexpr (VPL == 4)
+        *reinterpret_cast<uint32_t*>(kdst) = kc;
+    else
+        *reinterpret_cast<uint16_t*>(kdst) = (uint16_t)kc;
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) vrec[(size_t)(d0 + k) * kBlockTokens + slot] = (char)(vc >> (8 * k));
+    if (lane == 0) {
+        *reinterpret_cast<float*>(krec + (size_t)16 * D + 4 * slot) = ks;
+        *reinterpret_cast<float*>(vrec + (size_t)16 * D + 4 * slot) = vs;
+    }
 }
 
 // Two E4M3 codes (bits 0..7 and 8..15) -> f16x2 (exact: every E4M3 value is an f16 value).

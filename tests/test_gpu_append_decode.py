@@ -214,3 +214,55 @@ def test_append_decode_shared_prefix_refuses_a_row_inside_the_prefix(shared):
     # the shared blocks (sequence 0's first shared / 16 table entries) are unchanged
     pre = a.tables[0, :shared // 16].long()
     assert torch.equal(_bits(a.k[pre]), _bits(k0[pre])) and torch.equal(_bits(a.v[pre]), _bits(v0[pre]))
+
+
+# ---- FP8 cache (pa_append_decode_attention_fp8) ---------------------------------------
+
+def _fp8_pools(wl):
+    shape = pk.fp8_pool_shape(wl.num_blocks, wl.num_kv_heads, wl.head_dim)
+    kp = torch.zeros(shape, dtype=torch.uint8, device="cuda")
+    vp = torch.zeros(shape, dtype=torch.uint8, device="cuda")
+    tables = torch.from_numpy(wl.block_tables).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if wl.fill:
+        seqs = [f[0] for f in wl.fill]
+        ns = [f[3] for f in wl.fill]
+        first, end = wl.fill[0][2], wl.fill[-1][2] + wl.fill[-1][3]
+        pk.append_kv_fp8(kp, vp, wl.k_rows[first:end].contiguous(), wl.v_rows[first:end].contiguous(),
+                         tables[torch.tensor(seqs, device="cuda")].contiguous(),
+                         torch.tensor([f[1] for f in wl.fill], dtype=torch.int32, device="cuda"),
+                         torch.tensor(np.concatenate([[0], np.cumsum(ns)]), dtype=torch.int32,
+                                      device="cuda"), err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    return kp, vp, tables
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (14, 2, 64), (8, 1, 128)])
+def test_append_decode_fp8_equals_the_two_calls(hq, hkv, d):
+    P = 1024                                            # FP8 partition tokens
+    lens = [0, 15, 16, 17, P - 1, P, P + 1, 2 * P - 1, 2 * P, 3 * P - 50, 37]
+    wl = W.make_decode_workload("append_decode_fp8", context_lens=lens, num_q_heads=hq,
+                                num_kv_heads=hkv, head_dim=d, dtype="bf16", seed=hq + d,
+                                device="cuda", big_key_frac=0.01)
+    ka, va, tables = _fp8_pools(wl)
+    kb, vb = ka.clone(), va.clone()
+    rows = torch.from_numpy(wl.new_rows).cuda()
+    k_new, v_new = wl.k_rows[rows].contiguous(), wl.v_rows[rows].contiguous()
+    start = torch.from_numpy(wl.context_lens.astype(np.int32)).cuda()
+    cu = torch.arange(wl.num_seqs + 1, dtype=torch.int32, device="cuda")
+    ws = pk.decode_workspace(wl.num_seqs, hq, hkv, d, wl.max_blocks)
+    e1 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    e2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pk.append_kv_fp8(ka, va, k_new, v_new, tables, start, cu, err_flag=e1)
+    want = torch.empty_like(wl.q)
+    pk.decode_attention_fp8(want, wl.q, ka, va, tables, start + 1, wl.scale, workspace=ws,
+                            err_flag=e1)
+    got = torch.empty_like(wl.q)
+    pk.append_decode_attention_fp8(got, wl.q, kb, vb, k_new, v_new, tables, start + 1, wl.scale,
+                                   workspace=ws, err_flag=e2)
+    torch.cuda.synchronize()
+    assert int(e1.item()) == 0 and int(e2.item()) == 0
+    assert torch.equal(ka, kb) and torch.equal(va, vb)
+    assert torch.equal(_bits(want), _bits(got))
+    assert bool(torch.isfinite(got.float()).all())
