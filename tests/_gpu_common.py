@@ -87,6 +87,26 @@ class DevicePools:
         pk.append_kv(self.k, self.v, k_new, v_new, self.tables, start, cu, err_flag=self.err)
         return self.decode(lens, q=q, hint=hint)
 
+    def run_step_one_call(self, hint=0, shared=0):
+        """The same step as one pa_append_decode_attention call (with a shared prefix of
+        `shared` tokens, pa_append_decode_attention_shared_prefix): the bench's bf16 step."""
+        wl = self.wl
+        k_new, v_new, start, cu, lens = self.step_inputs()
+        q = wl.q.to(self.k.device).contiguous()
+        out = torch.empty_like(q)
+        ws = pk.decode_workspace(q.shape[0], wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                 self.tables.shape[1], device=self.k.device)
+        if shared:
+            pk.append_decode_attention_shared_prefix(out, q, self.k, self.v, k_new, v_new,
+                                                     self.tables, lens, wl.scale, shared,
+                                                     workspace=ws, max_context_len_hint=hint,
+                                                     err_flag=self.err)
+        else:
+            pk.append_decode_attention(out, q, self.k, self.v, k_new, v_new, self.tables, lens,
+                                       wl.scale, workspace=ws, max_context_len_hint=hint,
+                                       err_flag=self.err)
+        return out
+
     def decode(self, lens, q=None, hint=0, tables=None):
         wl = self.wl
         q = (wl.q if q is None else q).to(self.k.device).contiguous()

@@ -44,6 +44,20 @@ class Fp8Pools:
                          self.tables, start, cu, err_flag=self.err)
         return self.decode(start + 1, hint=hint)
 
+    def step_one_call(self, hint=0):
+        """The same step as one pa_append_decode_attention_fp8 call (the bench's FP8 step)."""
+        wl = self.wl
+        rows = torch.from_numpy(wl.new_rows).cuda()
+        lens = torch.from_numpy(wl.context_lens.astype(np.int32)).cuda() + 1
+        out = torch.empty_like(wl.q)
+        ws = pk.decode_workspace(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                 self.tables.shape[1])
+        pk.append_decode_attention_fp8(out, wl.q, self.k, self.v, wl.k_rows[rows].contiguous(),
+                                       wl.v_rows[rows].contiguous(), self.tables, lens, wl.scale,
+                                       workspace=ws, max_context_len_hint=hint, err_flag=self.err)
+        torch.cuda.synchronize()
+        return out
+
     def decode(self, lens, q=None, tables=None, hint=0):
         wl = self.wl
         q = wl.q if q is None else q
@@ -128,10 +142,13 @@ def test_fp8_copy_block_bit_exact():
     assert torch.equal(kp[1], k0[1]) and torch.equal(vp[5], v0[5])
 
 
-def test_fp8_llama_batch_full_size_sampled():
+@pytest.mark.parametrize("one_call", [False, True])
+def test_fp8_llama_batch_full_size_sampled(one_call):
+    # the 256-sequence workload at full size, as append + decode and as the bench's one call
     wl = W.llama8b_batch(device="cuda")
     fp = Fp8Pools(wl, nan_fill=False)
-    out = fp.step(hint=int(wl.context_lens.max()) + 1)
+    hint = int(wl.context_lens.max()) + 1
+    out = fp.step_one_call(hint=hint) if one_call else fp.step(hint=hint)
     assert int(fp.err.item()) == 0
     rng = np.random.default_rng(8)
     seqs = sorted(set(rng.choice(wl.num_seqs, 12, replace=False).tolist()) |

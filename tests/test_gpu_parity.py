@@ -319,14 +319,20 @@ def _sample_pairs(wl, n, seed):
            [(int(np.argmax(lens)), h) for h in range(wl.num_q_heads)]
 
 
+@pytest.mark.parametrize("one_call", [False, True])
 @pytest.mark.parametrize("name,nsample", [("qwen2.5-0.5b_gqa", 24), ("llama3-8b_batch256", 24),
                                           ("llama3-8b_long_context", 8),
                                           ("llama3-8b_shared_prefix", 16)])
-def test_named_workload_full_size_sampled(name, nsample):
+def test_named_workload_full_size_sampled(name, nsample, one_call):
+    # each workload at full size, as append + decode and as the bench's one call (with the
+    # shared-prefix workload's 4096 shared tokens through the prefix-sharing kernels)
     wl = W.WORKLOADS[name](device="cuda")
     dp = DevicePools(wl, canary=False)
     hint = int(wl.context_lens.max()) + 1
-    out = dp.run_step(hint=hint)
+    if one_call:
+        out = dp.run_step_one_call(hint=hint, shared=4096 if name == "llama3-8b_shared_prefix" else 0)
+    else:
+        out = dp.run_step(hint=hint)
     torch.cuda.synchronize()
     assert int(dp.err.item()) == 0
     pairs = _sample_pairs(wl, nsample, 7)
