@@ -198,3 +198,27 @@ def test_block_manager_rejects_holes_and_unknown_sequences(native):
     L = native.lib()
     h = ctypes.c_void_p()
     assert L.pa_bm_create(0, ctypes.byref(h)) == 1
+
+
+def test_one_call_bindings_check_the_new_rows_on_the_host(native):
+    # the bindings refuse new rows of the wrong shape, type or layout before any call
+    import torch
+    pool = torch.zeros(native.pool_shape(4, 2, 64, torch.bfloat16), dtype=torch.bfloat16)
+    q = torch.zeros(3, 4, 64, dtype=torch.bfloat16)
+    good = torch.zeros(3, 2, 64, dtype=torch.bfloat16)
+    bad = [torch.zeros(3, 2, 32, dtype=torch.bfloat16),        # head_dim
+           torch.zeros(2, 2, 64, dtype=torch.bfloat16),        # sequences
+           torch.zeros(3, 2, 64, dtype=torch.float32),         # type
+           torch.zeros(3, 64, 2, dtype=torch.bfloat16).transpose(1, 2)]   # layout
+    tables = torch.zeros(3, 4, dtype=torch.int32)
+    lens = torch.ones(3, dtype=torch.int32)
+    for b in bad:
+        with pytest.raises(ValueError):
+            native.append_decode_attention(q.clone(), q, pool, pool, b, good, tables, lens, 0.125)
+        with pytest.raises(ValueError):
+            native.append_decode_attention_shared_prefix(q.clone(), q, pool, pool, good, b, tables,
+                                                         lens, 0.125, 512)
+    fp8 = torch.zeros(native.fp8_pool_shape(4, 2, 64), dtype=torch.uint8)
+    for b in bad:
+        with pytest.raises(ValueError):
+            native.append_decode_attention_fp8(q.clone(), q, fp8, fp8, b, good, tables, lens, 0.125)
